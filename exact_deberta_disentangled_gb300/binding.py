@@ -1,0 +1,225 @@
+"""Thin Python binding of libdfattn's C ABI (include/df_attn.h).
+
+Argument marshalling only: tensors are passed to the library as raw device
+pointers and every step of the computation runs in the library's CUDA
+kernels.  PyTorch is used for device memory and streams.  If the library has
+not been built (``exact_deberta_disentangled_gb300.build.build()``), loading
+it raises -- there is no other implementation to fall back on.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdfattn.so")
+
+DF_OK, DF_ERR_INVALID_ARG, DF_ERR_UNSUPPORTED, DF_ERR_WORKSPACE, DF_ERR_CUDA, DF_ERR_TIMEOUT, DF_ERR_DEVICE_ARG = range(7)
+DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+
+EXPORTS = ["df_attn_workspace_size", "df_attn_fwd", "df_attn_bwd", "df_attn_step_host_arena_size",
+           "df_attn_step_host", "df_rel_index_table", "df_get_device_error", "df_status_string", "df_version"]
+
+
+class DfError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+class Params(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("L", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p),
+        ("total_tokens", ctypes.c_int32),
+        ("att_span", ctypes.c_int32),
+        ("position_buckets", ctypes.c_int32),
+        ("max_relative_positions", ctypes.c_int32),
+        ("query_mask", ctypes.c_void_p),
+        ("key_mask", ctypes.c_void_p),
+        ("dropout_p", ctypes.c_float),
+        ("philox_seed", ctypes.c_uint64),
+        ("philox_offset", ctypes.c_uint64),
+        ("softmax_scale", ctypes.c_float),
+        ("dtype", ctypes.c_int),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load():
+    """Load libdfattn.so (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with exact_deberta_disentangled_gb300.build.build()")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            P = ctypes.POINTER(Params)
+            lib.df_attn_workspace_size.restype = sz
+            lib.df_attn_workspace_size.argtypes = [P, ctypes.c_int]
+            lib.df_attn_fwd.restype = ctypes.c_int
+            lib.df_attn_fwd.argtypes = [P] + [vp] * 7 + [vp, sz, vp]
+            lib.df_attn_bwd.restype = ctypes.c_int
+            lib.df_attn_bwd.argtypes = [P] + [vp] * 13 + [vp, sz, vp]
+            lib.df_attn_step_host_arena_size.restype = sz
+            lib.df_attn_step_host_arena_size.argtypes = [P]
+            lib.df_attn_step_host.restype = ctypes.c_int
+            lib.df_attn_step_host.argtypes = [P] + [vp] * 13 + [vp, sz, vp]
+            lib.df_rel_index_table.restype = ctypes.c_int
+            lib.df_rel_index_table.argtypes = [ctypes.c_int32] * 4 + [vp, vp]
+            lib.df_get_device_error.restype = ctypes.c_int
+            lib.df_get_device_error.argtypes = [vp, vp]
+            lib.df_status_string.restype = ctypes.c_char_p
+            lib.df_status_string.argtypes = [ctypes.c_int]
+            lib.df_version.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().df_status_string(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclass
+class Geometry:
+    """Attention call geometry: B sequences of (at most) L tokens."""
+    B: int
+    L: int
+    H: int
+    D: int
+    span: int
+    nb: int
+    mp: int
+    cu_seqlens: Optional[torch.Tensor] = None   # device int32 [B+1] (packed layout)
+    total_tokens: int = 0
+    query_mask: Optional[torch.Tensor] = None   # device uint8 [B*L] (padded layout)
+    key_mask: Optional[torch.Tensor] = None
+    dropout_p: float = 0.0
+    seed: int = 0
+    offset: int = 0
+    scale: float = 0.0
+
+    @property
+    def R(self):
+        return 2 * self.span
+
+    @property
+    def T(self):
+        return self.total_tokens if self.cu_seqlens is not None else self.B * self.L
+
+    def params(self, dtype: torch.dtype) -> Params:
+        p = Params()
+        p.B, p.L, p.H, p.D = self.B, self.L, self.H, self.D
+        p.cu_seqlens = None if self.cu_seqlens is None else self.cu_seqlens.data_ptr()
+        p.total_tokens = self.total_tokens
+        p.att_span, p.position_buckets, p.max_relative_positions = self.span, self.nb, self.mp
+        p.query_mask = None if self.query_mask is None else self.query_mask.data_ptr()
+        p.key_mask = None if self.key_mask is None else self.key_mask.data_ptr()
+        p.dropout_p = self.dropout_p
+        p.philox_seed = self.seed & ((1 << 64) - 1)
+        p.philox_offset = self.offset
+        p.softmax_scale = self.scale
+        p.dtype = DTYPE_CODE[dtype]
+        return p
+
+    def lse_shape(self):
+        return (self.H, self.T) if self.cu_seqlens is not None else (self.B, self.H, self.L)
+
+
+def workspace_size(g: Geometry, dtype: torch.dtype, backward: bool) -> int:
+    p = g.params(dtype)
+    return int(load().df_attn_workspace_size(ctypes.byref(p), 1 if backward else 0))
+
+
+def alloc_workspace(g: Geometry, dtype: torch.dtype, backward: bool, device="cuda") -> torch.Tensor:
+    n = workspace_size(g, dtype, backward)
+    if n == 0:
+        raise DfError(DF_ERR_INVALID_ARG, "df_attn_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def attn_fwd(g: Geometry, q, k, v, qr, kr, out=None, lse=None, workspace=None, stream=None, check=True):
+    """Forward through df_attn_fwd; returns (out, lse, workspace)."""
+    dt = q.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(g.lse_shape(), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(g, dt, False, q.device)
+    p = g.params(dt)
+    rc = load().df_attn_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(out), _ptr(lse),
+                            _ptr(workspace), workspace.numel(), _stream(stream))
+    if check and rc != DF_OK:
+        raise DfError(rc, "df_attn_fwd")
+    return out, lse, workspace
+
+
+def attn_bwd(g: Geometry, q, k, v, qr, kr, out, lse, dout, grads=None, workspace=None, stream=None, check=True):
+    """Backward through df_attn_bwd; returns ((dq, dk, dv, dqr, dkr), workspace)."""
+    dt = q.dtype
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(qr),
+                 torch.empty_like(kr))
+    if workspace is None:
+        workspace = alloc_workspace(g, dt, True, q.device)
+    dq, dk, dv, dqr, dkr = grads
+    p = g.params(dt)
+    rc = load().df_attn_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(out), _ptr(lse),
+                            _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqr), _ptr(dkr), _ptr(workspace),
+                            workspace.numel(), _stream(stream))
+    if check and rc != DF_OK:
+        raise DfError(rc, "df_attn_bwd")
+    return grads, workspace
+
+
+def step_host(g: Geometry, q, k, v, qr, kr, dout, outs, arena, stream=None, host_cu=None, host_qmask=None,
+              host_kmask=None):
+    """One fwd + bwd from pinned host tensors via df_attn_step_host.
+    outs = (out, lse, dq, dk, dv, dqr, dkr) host tensors."""
+    dt = q.dtype
+    g2 = Geometry(**{**g.__dict__})
+    g2.cu_seqlens, g2.query_mask, g2.key_mask = host_cu, host_qmask, host_kmask
+    p = g2.params(dt)
+    out, lse, dq, dk, dv, dqr, dkr = outs
+    rc = load().df_attn_step_host(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(dout),
+                                  _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqr), _ptr(dkr),
+                                  _ptr(arena), arena.numel(), _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_attn_step_host")
+
+
+def step_host_arena_size(g: Geometry, dtype: torch.dtype) -> int:
+    p = g.params(dtype)
+    return int(load().df_attn_step_host_arena_size(ctypes.byref(p)))
+
+
+def rel_index_table(L: int, span: int, nb: int, mp: int, device="cuda", stream=None) -> torch.Tensor:
+    out = torch.empty(2 * L - 1, dtype=torch.int32, device=device)
+    rc = load().df_rel_index_table(L, span, nb, mp, _ptr(out), _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_rel_index_table")
+    return out
+
+
+def device_error(workspace: torch.Tensor, stream=None) -> int:
+    return int(load().df_get_device_error(_ptr(workspace), _stream(stream)))

@@ -1,0 +1,356 @@
+// df_host.cu -- the C ABI of libdfattn (declared in include/df_attn.h):
+// argument validation, workspace carve-up and the launch sequence of the
+// forward and backward passes.  Nothing here allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "df_internal.h"
+
+namespace df {
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Validated problem: fills `out` and returns DF_OK, or an error code.
+df_status resolve(const df_attn_params* a, ProblemDev& out) {
+    if (!a) return DF_ERR_INVALID_ARG;
+    if (a->B < 1 || a->L < 1 || a->H < 1 || a->D < 1 || a->att_span < 1) return DF_ERR_INVALID_ARG;
+    if (a->dtype != DF_BF16 && a->dtype != DF_FP16 && a->dtype != DF_FP32) return DF_ERR_INVALID_ARG;
+    if (!(a->dropout_p >= 0.f && a->dropout_p < 1.f)) return DF_ERR_INVALID_ARG;
+    if (!(a->softmax_scale >= 0.f) || !std::isfinite(a->softmax_scale)) return DF_ERR_INVALID_ARG;
+    if (a->philox_offset >> 32) return DF_ERR_INVALID_ARG;
+    if (a->D != 32 && a->D != 64 && a->D != 128) return DF_ERR_UNSUPPORTED;
+    if (a->L > 8192) return DF_ERR_UNSUPPORTED;
+    if (a->att_span > 512) return DF_ERR_UNSUPPORTED;
+    const bool bucketing = a->position_buckets > 0 && a->max_relative_positions > 0;
+    if (bucketing && (a->position_buckets < 2 || a->max_relative_positions - 1 <= a->position_buckets / 2))
+        return DF_ERR_UNSUPPORTED;
+    long long T;
+    if (a->cu_seqlens) {
+        if (a->query_mask || a->key_mask) return DF_ERR_UNSUPPORTED;  // masks are a padded-layout feature
+        if (a->total_tokens < 1) return DF_ERR_INVALID_ARG;
+        if ((long long)a->total_tokens > (long long)a->B * a->L) return DF_ERR_INVALID_ARG;
+        T = a->total_tokens;
+    } else {
+        T = (long long)a->B * a->L;
+    }
+    if (T * a->H >= (1ll << 31) || (long long)a->B * a->L * a->H >= (1ll << 31)) return DF_ERR_UNSUPPORTED;
+    std::memset(&out, 0, sizeof(out));
+    out.B = a->B;
+    out.L = a->L;
+    out.H = a->H;
+    out.D = a->D;
+    out.span = a->att_span;
+    out.R = 2 * a->att_span;
+    out.nb = bucketing ? a->position_buckets : 0;
+    out.mp = bucketing ? a->max_relative_positions : 0;
+    out.T = (int)T;
+    out.cu = a->cu_seqlens;
+    out.qmask = a->query_mask;
+    out.kmask = a->key_mask;
+    out.scale = a->softmax_scale > 0.f ? a->softmax_scale : (float)(1.0 / std::sqrt(3.0 * a->D));
+    const double p = (double)a->dropout_p;
+    out.dropout = p > 0.0;
+    out.keep_all = p > 0.0 ? 0 : 1;
+    out.drop_scale = p > 0.0 ? (float)(1.0 / (1.0 - p)) : 1.f;
+    if (p > 0.0) {
+        const double t = std::floor((1.0 - p) * 4294967296.0);
+        out.keep_thr = t >= 4294967295.0 ? 0xFFFFFFFFu : (uint32_t)t;
+        if (t >= 4294967296.0) out.keep_all = 1;
+    } else {
+        out.keep_thr = 0xFFFFFFFFu;
+    }
+    out.seed_lo = (uint32_t)a->philox_seed;
+    out.seed_hi = (uint32_t)(a->philox_seed >> 32);
+    out.philox_offset = (uint32_t)a->philox_offset;
+    return DF_OK;
+}
+
+int elem_bytes(df_dtype d) { return d == DF_FP32 ? 4 : 2; }
+
+int rel_chunks(const ProblemDev& p) {
+    // Token chunks of the relative-gradient reduction: enough CTAs to fill
+    // the GPU twice, each chunk at least 512 tokens.
+    const int rb = (p.R + 127) / 128;
+    int c = (2 * 152 + p.H * rb - 1) / (p.H * rb);
+    const int maxc = (p.T + 511) / 512;
+    if (c > maxc) c = maxc;
+    return c < 1 ? 1 : c;
+}
+
+// Carve the workspace; with base == nullptr only the size is computed.
+Workspace carve(const ProblemDev& p, df_dtype dt, bool backward, void* base) {
+    Workspace w;
+    std::memset(&w, 0, sizeof(w));
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char* {
+        char* r = base ? (char*)base + off : nullptr;
+        off += align_up(bytes);
+        return r;
+    };
+    w.err = (int*)take(kAlign);
+    w.dtab = (int32_t*)take(sizeof(int32_t) * (size_t)(2 * p.L - 1));
+    if (dt != DF_FP32) w.relb = (float*)take(sizeof(float) * 4 * (size_t)p.T * p.H);
+    if (backward) {
+        w.rowterm = (float*)take(sizeof(float) * (size_t)p.H * (size_t)p.B * p.L);
+        const size_t g = (size_t)elem_bytes(dt) * (size_t)p.T * p.H * p.R;
+        w.G = take(g);
+        w.Gp = take(g);
+        if (dt != DF_FP32) {
+            w.nchunk = rel_chunks(p);
+            const size_t part = sizeof(float) * (size_t)w.nchunk * p.H * p.R * p.D;
+            w.part_kr = (float*)take(part);
+            w.part_qr = (float*)take(part);
+        }
+    }
+    w.bytes = off;
+    return w;
+}
+
+df_status cuda_status(int e) { return e == 0 ? DF_OK : DF_ERR_CUDA; }
+
+}  // namespace
+
+// ------------------------------------------------------------- TMA encode
+
+int encode_tmap(void* tmap, int dtype_bytes, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box, int swizzle_bytes, const void* base) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    });
+    if (!fn) return 1;
+    CUtensorMapDataType t = dtype_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (swizzle_bytes == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (swizzle_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (swizzle_bytes == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
+    cuuint64_t d[5], s[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i > 0) s[i - 1] = strides_bytes[i - 1];
+    }
+    CUresult r = fn((CUtensorMap*)tmap, t, (cuuint32_t)rank, const_cast<void*>(base), d, s, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : 2;
+}
+
+}  // namespace df
+
+using namespace df;
+
+extern "C" {
+
+const char* df_status_string(df_status s) {
+    switch (s) {
+        case DF_OK: return "DF_OK";
+        case DF_ERR_INVALID_ARG: return "DF_ERR_INVALID_ARG: bad pointer, size, alignment or value";
+        case DF_ERR_UNSUPPORTED: return "DF_ERR_UNSUPPORTED: configuration outside the supported contract";
+        case DF_ERR_WORKSPACE: return "DF_ERR_WORKSPACE: workspace missing or too small";
+        case DF_ERR_CUDA: return "DF_ERR_CUDA: CUDA runtime or launch error";
+        case DF_ERR_TIMEOUT: return "DF_ERR_TIMEOUT: a bounded device wait gave up";
+        case DF_ERR_DEVICE_ARG: return "DF_ERR_DEVICE_ARG: cu_seqlens inconsistent with B, L, total_tokens";
+    }
+    return "unknown df_status";
+}
+
+const char* df_version(void) { return "0.1.0"; }
+
+size_t df_attn_workspace_size(const df_attn_params* a, int backward) {
+    ProblemDev p;
+    if (resolve(a, p) != DF_OK) return 0;
+    return carve(p, a->dtype, backward != 0, nullptr).bytes;
+}
+
+static df_status common_prologue(const df_attn_params* a, ProblemDev& p, Workspace& w, bool backward,
+                                 void* workspace, size_t ws_bytes, cudaStream_t st) {
+    df_status s = resolve(a, p);
+    if (s != DF_OK) return s;
+    if (!workspace || !aligned16(workspace)) return DF_ERR_WORKSPACE;
+    const size_t need = carve(p, a->dtype, backward, nullptr).bytes;
+    if (ws_bytes < need) return DF_ERR_WORKSPACE;
+    w = carve(p, a->dtype, backward, workspace);
+    p.err = w.err;
+    if (launch_clear_error(w.err, st)) return DF_ERR_CUDA;
+    if (launch_delta_table(p.L, p.span, p.nb, p.mp, w.dtab, st)) return DF_ERR_CUDA;
+    if (p.cu && launch_check_cu(p, st)) return DF_ERR_CUDA;
+    return DF_OK;
+}
+
+df_status df_attn_fwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                      const void* kr, void* out, float* lse, void* workspace, size_t ws_bytes, df_stream_t stream) {
+    const void* ptrs[] = {q, k, v, qr, kr, out, lse};
+    for (const void* x : ptrs)
+        if (!x || !aligned16(x)) return DF_ERR_INVALID_ARG;
+    if (a && a->cu_seqlens && ((uintptr_t)a->cu_seqlens & 3u)) return DF_ERR_INVALID_ARG;
+    ProblemDev p;
+    Workspace w;
+    cudaStream_t st = (cudaStream_t)stream;
+    df_status s = common_prologue(a, p, w, false, workspace, ws_bytes, st);
+    if (s != DF_OK) return s;
+    if (a->dtype == DF_FP32)
+        return cuda_status(launch_fwd_f32(p, w, (const float*)q, (const float*)k, (const float*)v, (const float*)qr,
+                                          (const float*)kr, (float*)out, lse, st));
+    if (launch_relbias(p, a->dtype, q, k, qr, kr, w.relb, st)) return DF_ERR_CUDA;
+    return cuda_status(launch_fwd_tc(p, w, a->dtype, q, k, v, qr, kr, out, lse, st));
+}
+
+df_status df_attn_bwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                      const void* kr, const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                      void* dv, void* dqr, void* dkr, void* workspace, size_t ws_bytes, df_stream_t stream) {
+    const void* ptrs[] = {q, k, v, qr, kr, out, lse, dout, dq, dk, dv, dqr, dkr};
+    for (const void* x : ptrs)
+        if (!x || !aligned16(x)) return DF_ERR_INVALID_ARG;
+    if (a && a->cu_seqlens && ((uintptr_t)a->cu_seqlens & 3u)) return DF_ERR_INVALID_ARG;
+    ProblemDev p;
+    Workspace w;
+    cudaStream_t st = (cudaStream_t)stream;
+    df_status s = common_prologue(a, p, w, true, workspace, ws_bytes, st);
+    if (s != DF_OK) return s;
+    if (launch_rowterm(p, a->dtype, out, dout, w.rowterm, st)) return DF_ERR_CUDA;
+    if (a->dtype == DF_FP32)
+        return cuda_status(launch_bwd_f32(p, w, (const float*)q, (const float*)k, (const float*)v,
+                                          (const float*)qr, (const float*)kr, lse, (const float*)dout, (float*)dq,
+                                          (float*)dk, (float*)dv, (float*)dqr, (float*)dkr, st));
+    if (launch_relbias(p, a->dtype, q, k, qr, kr, w.relb, st)) return DF_ERR_CUDA;
+    return cuda_status(launch_bwd_tc(p, w, a->dtype, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st));
+}
+
+// ------------------------------------------------------- host-buffer step
+
+namespace {
+struct Arena {
+    size_t q, k, v, qr, kr, dout, out, lse, dq, dk, dv, dqr, dkr, cu, qm, km, ws, bytes;
+};
+Arena arena_layout(const df_attn_params* a, const ProblemDev& p) {
+    Arena r;
+    size_t off = 0;
+    auto take = [&](size_t b) {
+        size_t o = off;
+        off += align_up(b);
+        return o;
+    };
+    const size_t e = (size_t)elem_bytes(a->dtype);
+    const size_t tok = e * (size_t)p.T * p.H * p.D;
+    const size_t rel = e * (size_t)p.H * p.R * p.D;
+    const size_t lse = sizeof(float) * (size_t)p.H * (p.cu ? (size_t)p.T : (size_t)p.B * p.L);
+    r.q = take(tok);
+    r.k = take(tok);
+    r.v = take(tok);
+    r.qr = take(rel);
+    r.kr = take(rel);
+    r.dout = take(tok);
+    r.out = take(tok);
+    r.lse = take(lse);
+    r.dq = take(tok);
+    r.dk = take(tok);
+    r.dv = take(tok);
+    r.dqr = take(rel);
+    r.dkr = take(rel);
+    r.cu = take(sizeof(int32_t) * (size_t)(p.B + 1));
+    r.qm = take((size_t)p.B * p.L);
+    r.km = take((size_t)p.B * p.L);
+    const size_t wf = carve(p, a->dtype, false, nullptr).bytes, wb = carve(p, a->dtype, true, nullptr).bytes;
+    r.ws = take(wf > wb ? wf : wb);
+    r.bytes = off;
+    return r;
+}
+}  // namespace
+
+size_t df_attn_step_host_arena_size(const df_attn_params* a) {
+    ProblemDev p;
+    if (resolve(a, p) != DF_OK) return 0;
+    return arena_layout(a, p).bytes;
+}
+
+df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                            const void* kr, const void* dout, void* out, float* lse, void* dq, void* dk, void* dv,
+                            void* dqr, void* dkr, void* arena, size_t arena_bytes, df_stream_t stream) {
+    const void* ptrs[] = {q, k, v, qr, kr, dout, out, lse, dq, dk, dv, dqr, dkr};
+    for (const void* x : ptrs)
+        if (!x) return DF_ERR_INVALID_ARG;
+    ProblemDev p;
+    df_status s = resolve(a, p);
+    if (s != DF_OK) return s;
+    if (!arena || !aligned16(arena)) return DF_ERR_WORKSPACE;
+    const Arena L = arena_layout(a, p);
+    if (arena_bytes < L.bytes) return DF_ERR_WORKSPACE;
+    char* base = (char*)arena;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t e = (size_t)elem_bytes(a->dtype);
+    const size_t tok = e * (size_t)p.T * p.H * p.D;
+    const size_t rel = e * (size_t)p.H * p.R * p.D;
+    const size_t lseb = sizeof(float) * (size_t)p.H * (p.cu ? (size_t)p.T : (size_t)p.B * p.L);
+    auto h2d = [&](size_t off, const void* src, size_t n) {
+        return cudaMemcpyAsync(base + off, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    };
+    auto d2h = [&](void* dst, size_t off, size_t n) {
+        return cudaMemcpyAsync(dst, base + off, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    };
+    df_attn_params dp = *a;
+    bool ok = h2d(L.q, q, tok) && h2d(L.k, k, tok) && h2d(L.v, v, tok) && h2d(L.qr, qr, rel) &&
+              h2d(L.kr, kr, rel) && h2d(L.dout, dout, tok);
+    if (ok && a->cu_seqlens) {
+        ok = h2d(L.cu, a->cu_seqlens, sizeof(int32_t) * (size_t)(p.B + 1));
+        dp.cu_seqlens = (const int32_t*)(base + L.cu);
+    }
+    if (ok && a->query_mask) {
+        ok = h2d(L.qm, a->query_mask, (size_t)p.B * p.L);
+        dp.query_mask = (const uint8_t*)(base + L.qm);
+    }
+    if (ok && a->key_mask) {
+        ok = h2d(L.km, a->key_mask, (size_t)p.B * p.L);
+        dp.key_mask = (const uint8_t*)(base + L.km);
+    }
+    if (!ok) return DF_ERR_CUDA;
+    const size_t wsb = arena_bytes - L.ws;
+    s = df_attn_fwd(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
+                    (float*)(base + L.lse), base + L.ws, wsb, stream);
+    if (s != DF_OK) return s;
+    s = df_attn_bwd(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
+                    (const float*)(base + L.lse), base + L.dout, base + L.dq, base + L.dk, base + L.dv,
+                    base + L.dqr, base + L.dkr, base + L.ws, wsb, stream);
+    if (s != DF_OK) return s;
+    ok = d2h(out, L.out, tok) && d2h(lse, L.lse, lseb) && d2h(dq, L.dq, tok) && d2h(dk, L.dk, tok) &&
+         d2h(dv, L.dv, tok) && d2h(dqr, L.dqr, rel) && d2h(dkr, L.dkr, rel);
+    if (!ok) return DF_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DF_ERR_CUDA;
+    return df_get_device_error(base + L.ws, stream);
+}
+
+df_status df_rel_index_table(int32_t L, int32_t att_span, int32_t nb, int32_t mp, int32_t* out_dev,
+                             df_stream_t stream) {
+    if (L < 1 || L > 8192 || att_span < 1 || att_span > 512 || !out_dev) return DF_ERR_INVALID_ARG;
+    const bool bucketing = nb > 0 && mp > 0;
+    if (bucketing && (nb < 2 || mp - 1 <= nb / 2)) return DF_ERR_UNSUPPORTED;
+    return cuda_status(
+        launch_delta_table(L, att_span, bucketing ? nb : 0, bucketing ? mp : 0, out_dev, (cudaStream_t)stream));
+}
+
+df_status df_get_device_error(const void* workspace, df_stream_t stream) {
+    if (!workspace) return DF_ERR_WORKSPACE;
+    int word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream) !=
+        cudaSuccess)
+        return DF_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DF_ERR_CUDA;
+    return (df_status)word;
+}
+
+}  // extern "C"

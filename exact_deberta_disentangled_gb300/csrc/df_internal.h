@@ -1,0 +1,73 @@
+// df_internal.h -- structures shared by the host side of libdfattn and its
+// kernels (not part of the public ABI).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#include "../../include/df_attn.h"
+
+namespace df {
+
+// Everything a kernel needs to know about one attention call.
+struct ProblemDev {
+    int B, L, H, D, R, span, nb, mp;
+    int T;                    // total tokens (B * L when padded)
+    const int32_t* cu;        // device cu_seqlens or nullptr (padded)
+    const uint8_t* qmask;     // padded only, [B * L] or nullptr
+    const uint8_t* kmask;
+    float scale;              // c
+    float drop_scale;         // 1 / (1 - p)
+    uint32_t keep_thr;        // keep iff philox word < keep_thr (unless keep_all)
+    int keep_all;             // 1 when p == 0
+    int dropout;              // p > 0
+    uint32_t seed_lo, seed_hi, philox_offset;
+    int* err;                 // device error word (workspace)
+};
+
+// Workspace carve-up (device pointers, all 256-byte aligned).
+struct Workspace {
+    int* err;                 // error word
+    int32_t* dtab;            // [2L - 1] delta(r) at r + L - 1
+    float* relb;              // [T, H, 4]: c*log2e * (Q.Kr[0], Q.Kr[R-1], K.Qr[0], K.Qr[R-1])
+    float* rowterm;           // [H, T] Dl_i (backward)
+    void* G;                  // [T, H, R] diagonal sums of dZ by row (backward)
+    void* Gp;                 // [T, H, R] diagonal sums of dZ by column (backward)
+    float* part_kr;           // [nchunk, H, R, D] partial dKr (backward)
+    float* part_qr;           // [nchunk, H, R, D] partial dQr (backward)
+    int nchunk;
+    size_t bytes;
+};
+
+// Launch helpers implemented in the .cu files.  Each returns a cudaError_t
+// as int (0 = success).
+int launch_delta_table(int L, int span, int nb, int mp, int32_t* out, cudaStream_t st);
+int launch_check_cu(const ProblemDev& p, cudaStream_t st);
+int launch_clear_error(int* err, cudaStream_t st);
+int launch_relbias(const ProblemDev& p, df_dtype dt, const void* q, const void* k, const void* qr, const void* kr,
+                   float* relb, cudaStream_t st);
+int launch_rowterm(const ProblemDev& p, df_dtype dt, const void* out, const void* dout, float* rowterm,
+                   cudaStream_t st);
+
+// strict fp32 path
+int launch_fwd_f32(const ProblemDev& p, const Workspace& ws, const float* q, const float* k, const float* v,
+                   const float* qr, const float* kr, float* out, float* lse, cudaStream_t st);
+int launch_bwd_f32(const ProblemDev& p, const Workspace& ws, const float* q, const float* k, const float* v,
+                   const float* qr, const float* kr, const float* lse, const float* dout, float* dq, float* dk,
+                   float* dv, float* dqr, float* dkr, cudaStream_t st);
+
+// tensor-core path (bf16 / fp16)
+int launch_fwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
+                  const void* v, const void* qr, const void* kr, void* out, float* lse, cudaStream_t st);
+int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
+                  const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
+                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st);
+
+// Encode a 2-D or 3-D tiled TMA descriptor (innermost dimension first).
+// Returns 0 on success.
+int encode_tmap(void* tmap, int dtype_bytes, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box, int swizzle_bytes, const void* base);
+
+}  // namespace df

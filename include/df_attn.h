@@ -1,0 +1,188 @@
+/*
+ * df_attn.h -- C ABI of the GB300 (sm_103a) exact DeBERTa-v2/v3 disentangled
+ * self-attention library (libdfattn.so): forward and fused backward, computed
+ * without ever storing the [B, H, L, L] score matrix.
+ *
+ * The operation (per sequence, per head h; tokens i, j counted inside the
+ * sequence; R = 2 * att_span):
+ *
+ *   delta(i, j) = clamp(bucket(i - j) + att_span, 0, R - 1)
+ *   S[i, j]     = c * (Q_i.K_j + Q_i.Kr[delta] + K_j.Qr[delta])     c = 1/sqrt(3D)
+ *   P           = softmax_j(S) with -inf for masked queries / keys
+ *   O           = (P * keep / (1 - p)) V ;   LSE_i = log sum_j exp(S[i, j])
+ *
+ * bucket() is DeBERTa's log bucketing: |r| <= nb/2 keeps r, larger |r| maps
+ * to sign(r) * (nb/2 + ceil(ln(|r| / (nb/2)) / ln((mp - 1) / (nb/2)) * (nb/2 - 1)))
+ * (nb = position_buckets, mp = max_relative_positions; no bucketing when
+ * either is <= 0).
+ *
+ * Passages this follows -- "DisentangledFlash" (pypi disentangled-flash
+ * 1.1.1): section "Status" (exact C2P/P2C DeBERTa-v2/v3 attention without the
+ * [B, H, L, L] matrix, FP16 / BF16 / strict FP32, head dims 32/64/128,
+ * factorised 2-D padding masks, lengths up to 8192, packed cu_seqlens
+ * training, Philox dropout regenerated in backward); section "Hugging Face
+ * usage" (an LSE-producing training forward, a dQ kernel and a dK/dV kernel);
+ * section "Performance" (the relative-position products over R rows and the
+ * relative-position gradients counted in the FLOP formula).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense and contiguous; the caller owns every buffer.
+ *     No entry point allocates device memory; scratch comes from the
+ *     caller's workspace (size from df_attn_workspace_size).
+ *   - Device pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *   - Argument errors return a status before anything is enqueued and
+ *     nothing is written.  There is no fallback path: an unsupported
+ *     configuration returns DF_ERR_UNSUPPORTED.  No C++ exception crosses
+ *     this boundary.
+ *   - Errors found on the device (inconsistent cu_seqlens, a bounded wait
+ *     that gave up) are recorded in the workspace and reported by
+ *     df_get_device_error.
+ */
+#ifndef DF_ATTN_H
+#define DF_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same type as cudaStream_t). */
+typedef struct CUstream_st *df_stream_t;
+
+typedef enum {
+    DF_OK = 0,
+    DF_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or value      */
+    DF_ERR_UNSUPPORTED = 2,   /* valid but outside the supported contract   */
+    DF_ERR_WORKSPACE = 3,     /* workspace missing or too small             */
+    DF_ERR_CUDA = 4,          /* a CUDA runtime / launch error              */
+    DF_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up         */
+    DF_ERR_DEVICE_ARG = 6     /* the device found inconsistent cu_seqlens   */
+} df_status;
+
+typedef enum {
+    DF_BF16 = 0,              /* bf16 storage, fp32 accumulation (tensor cores) */
+    DF_FP16 = 1,              /* fp16 storage, fp32 accumulation (tensor cores) */
+    DF_FP32 = 2               /* strict fp32 (CUDA-core fp32 arithmetic)        */
+} df_dtype;
+
+/*
+ * Problem description.
+ *   Padded layout (cu_seqlens == NULL): B sequences of L tokens; Q, K, V, O,
+ *     dO, dQ, dK, dV are [B, L, H, D]; LSE is fp32 [B, H, L].
+ *   Packed layout (cu_seqlens != NULL): B sequences back to back,
+ *     cu_seqlens[0] = 0, cu_seqlens[b+1] - cu_seqlens[b] = length of
+ *     sequence b (1 <= length <= L, L = the longest length),
+ *     cu_seqlens[B] = total_tokens; tensors are [total_tokens, H, D]; LSE is
+ *     fp32 [H, total_tokens].  No padding token is computed.
+ *   Qr, Kr, dQr, dKr are [H, R, D] with R = 2 * att_span.
+ *   query_mask / key_mask: padded layout only, [B, L] bytes (0 = masked),
+ *     or NULL.  The 2-D mask is query_mask (x) key_mask.  A row with no
+ *     attendable key (masked query, or all keys masked) gets O = 0,
+ *     LSE = +inf and zero gradients.
+ *   Dropout of the attention probabilities (dropout_p in [0, 1)): keep[i,j]
+ *     is word (j & 3) of Philox4x32-10(counter = (j >> 2, i, b*H + h,
+ *     philox_offset), key = (seed low 32 bits, seed high 32 bits)) compared
+ *     with floor((1 - dropout_p) * 2^32); i, j are positions inside the
+ *     sequence.  The mask is regenerated in the backward, never stored.
+ *     philox_offset must be < 2^32.
+ *   softmax_scale: c; 0 selects 1/sqrt(3D).
+ */
+typedef struct {
+    int32_t B, L, H, D;
+    const int32_t *cu_seqlens;     /* device [B+1] int32, or NULL (padded)   */
+    int32_t total_tokens;          /* packed layout only                      */
+    int32_t att_span;              /* R = 2 * att_span relative rows          */
+    int32_t position_buckets;      /* nb (<= 0: no log bucketing)             */
+    int32_t max_relative_positions;/* mp (<= 0: no log bucketing)             */
+    const uint8_t *query_mask;     /* device [B, L] or NULL (padded only)     */
+    const uint8_t *key_mask;       /* device [B, L] or NULL (padded only)     */
+    float dropout_p;
+    uint64_t philox_seed;
+    uint64_t philox_offset;
+    float softmax_scale;
+    df_dtype dtype;
+} df_attn_params;
+
+/*
+ * Supported contract: D in {32, 64, 128}; 1 <= L <= 8192; 1 <= att_span <=
+ * 512; B, H >= 1 and B * L * H < 2^31 (padded) or total_tokens * H < 2^31
+ * (packed); when log bucketing is on, position_buckets >= 2 and
+ * max_relative_positions - 1 > position_buckets / 2.
+ */
+
+/* Bytes of device workspace that df_attn_fwd (backward = 0) or df_attn_bwd
+ * (backward != 0) needs for these parameters; 0 if the parameters are
+ * invalid.  The workspace holds the relative-index table, per-token
+ * relative-position dot products, the device error word and, for the
+ * backward, the row terms Dl_i, the diagonal sums of dZ used for the
+ * relative-position gradients ([T, H, R] twice, in the input dtype for bf16 /
+ * fp16 and fp32 for strict fp32) and fp32 partial sums of dQr / dKr. */
+size_t df_attn_workspace_size(const df_attn_params *p, int backward);
+
+/*
+ * Forward.  Writes out (same dtype and layout as q) and lse (fp32, natural
+ * log, layout above; +inf for rows with no attendable key).
+ * q, k, v: [B, L, H, D] or [T, H, D] in p->dtype; qr, kr: [H, R, D].
+ */
+df_status df_attn_fwd(const df_attn_params *p, const void *q, const void *k, const void *v, const void *qr,
+                      const void *kr, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                      df_stream_t stream);
+
+/*
+ * Backward.  Takes the forward's inputs, its out and lse, and dout (layout of
+ * out); writes dq, dk, dv (layout of q) and dqr, dkr ([H, R, D], summed over
+ * the batch, overwritten).  All gradients are deterministic: the same call
+ * gives bitwise the same results (no floating-point atomics; relative-
+ * position gradients are reduced in a fixed order).
+ */
+df_status df_attn_bwd(const df_attn_params *p, const void *q, const void *k, const void *v, const void *qr,
+                      const void *kr, const void *out, const float *lse, const void *dout, void *dq, void *dk,
+                      void *dv, void *dqr, void *dkr, void *workspace, size_t workspace_bytes,
+                      df_stream_t stream);
+
+/*
+ * One training step of the layer from HOST buffers: copies q, k, v, qr, kr,
+ * dout from host memory to the device arena, runs the forward and the
+ * backward, and copies out, lse, dq, dk, dv, dqr, dkr back to host memory,
+ * all on `stream`; returns after the stream has finished.  In this call
+ * p->cu_seqlens, p->query_mask and p->key_mask are HOST pointers (copied
+ * too).  Host buffers should be pinned for full copy bandwidth.  The device
+ * arena (caller-owned, df_attn_step_host_arena_size bytes) holds the device
+ * copies and the workspace.
+ */
+size_t df_attn_step_host_arena_size(const df_attn_params *p);
+df_status df_attn_step_host(const df_attn_params *p, const void *q, const void *k, const void *v, const void *qr,
+                            const void *kr, const void *dout, void *out, float *lse, void *dq, void *dk, void *dv,
+                            void *dqr, void *dkr, void *device_arena, size_t arena_bytes, df_stream_t stream);
+
+/*
+ * The relative-position index table delta(r) for r = -(L-1) .. L-1, written
+ * as int32 to out_dev[r + L - 1] (device, 2L - 1 entries), computed on the
+ * device exactly as the attention kernels use it.  For bit-exact checks.
+ */
+df_status df_rel_index_table(int32_t L, int32_t att_span, int32_t position_buckets,
+                             int32_t max_relative_positions, int32_t *out_dev, df_stream_t stream);
+
+/*
+ * Synchronises `stream` and reads the device error word of a workspace that
+ * was passed to df_attn_fwd / df_attn_bwd: DF_OK, DF_ERR_DEVICE_ARG
+ * (cu_seqlens inconsistent with B, L, total_tokens) or DF_ERR_TIMEOUT (a
+ * bounded device wait gave up; the affected outputs are unspecified).  The
+ * word is cleared at the start of every df_attn_fwd / df_attn_bwd call.
+ */
+df_status df_get_device_error(const void *workspace, df_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *df_status_string(df_status s);
+
+/* Library version, "major.minor.patch". */
+const char *df_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DF_ATTN_H */

@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+exports every symbol its header declares, and argument validation returns
+the documented status codes before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from exact_deberta_disentangled_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "df_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return B.load()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(df_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_symbols_are_exported(lib):
+    names = header_functions()
+    assert "df_attn_fwd" in names and "df_attn_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(B.EXPORTS) | set(names)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = B.status_string(code)
+        assert s.startswith("DF_")
+    assert lib.df_version().decode().count(".") == 2
+
+
+def geom(**kw):
+    base = dict(B=2, L=512, H=12, D=64, span=256, nb=256, mp=512)
+    base.update(kw)
+    return B.Geometry(**base)
+
+
+def test_workspace_sizes(lib):
+    import torch
+    f = B.workspace_size(geom(), torch.bfloat16, False)
+    b = B.workspace_size(geom(), torch.bfloat16, True)
+    assert 0 < f < b
+    assert B.workspace_size(geom(D=48), torch.bfloat16, False) == 0
+    assert B.workspace_size(geom(L=8193), torch.bfloat16, False) == 0
+    assert B.workspace_size(geom(span=0), torch.bfloat16, False) == 0
+    # backward scratch holds the two [T, H, R] diagonal-sum buffers
+    T, H, R = 2 * 512, 12, 512
+    assert b - f >= 2 * 2 * T * H * R
+
+
+class FakeTensor:
+    """An aligned non-null address that is never dereferenced (validation
+    fails before any device work)."""
+
+    def __init__(self, addr=0x10000):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
+def call_fwd(g, dtype_code=0, ws_bytes=1 << 30, ptr=0x10000, ws_ptr=0x20000):
+    import torch
+    lib = B.load()
+    p = g.params(torch.bfloat16)
+    p.dtype = dtype_code
+    vp = [ctypes.c_void_p(ptr)] * 7
+    return lib.df_attn_fwd(ctypes.byref(p), *vp, ctypes.c_void_p(ws_ptr), ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=48), B.DF_ERR_UNSUPPORTED),
+    (dict(D=256), B.DF_ERR_UNSUPPORTED),
+    (dict(L=8193), B.DF_ERR_UNSUPPORTED),
+    (dict(span=600), B.DF_ERR_UNSUPPORTED),
+    (dict(nb=256, mp=100), B.DF_ERR_UNSUPPORTED),
+    (dict(B=0), B.DF_ERR_INVALID_ARG),
+    (dict(H=0), B.DF_ERR_INVALID_ARG),
+    (dict(span=0), B.DF_ERR_INVALID_ARG),
+    (dict(dropout_p=1.0), B.DF_ERR_INVALID_ARG),
+    (dict(dropout_p=-0.1), B.DF_ERR_INVALID_ARG),
+    (dict(offset=1 << 32), B.DF_ERR_INVALID_ARG),
+    (dict(scale=-1.0), B.DF_ERR_INVALID_ARG),
+])
+def test_validation_codes(lib, kw, code):
+    assert call_fwd(geom(**kw)) == code
+
+
+def test_pointer_and_workspace_checks(lib):
+    g = geom()
+    assert call_fwd(g, ptr=0) == B.DF_ERR_INVALID_ARG           # null tensor
+    assert call_fwd(g, ptr=0x10008) == B.DF_ERR_INVALID_ARG     # not 16-byte aligned
+    assert call_fwd(g, ws_bytes=1024) == B.DF_ERR_WORKSPACE      # too small
+    assert call_fwd(g, ws_ptr=0) == B.DF_ERR_WORKSPACE           # missing
+    assert call_fwd(g, dtype_code=7) == B.DF_ERR_INVALID_ARG     # unknown dtype
+
+
+def test_packed_layout_rules(lib):
+    g = geom(cu_seqlens=FakeTensor(), total_tokens=600)
+    g.query_mask = FakeTensor()
+    assert call_fwd(g) == B.DF_ERR_UNSUPPORTED                  # masks only in the padded layout
+    g = geom(cu_seqlens=FakeTensor(), total_tokens=0)
+    assert call_fwd(g) == B.DF_ERR_INVALID_ARG
+    g = geom(cu_seqlens=FakeTensor(), total_tokens=2 * 512 + 1)
+    assert call_fwd(g) == B.DF_ERR_INVALID_ARG                  # more tokens than B*L

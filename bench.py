@@ -1,0 +1,340 @@
+"""Benchmark: exact disentangled attention forward + backward through the C ABI.
+
+One step = df_attn_fwd + df_attn_bwd over one batch of the L=8192 length-sweep
+workload (B=2, H=12, D=64, bf16, att_span 256 -> R=512, buckets 256 / max
+relative positions 512, 16,384 tokens, N(0,1) synthetic inputs).  Throughput
+is counted with the pages' FLOP formula: BH(4L^2 D + 4LRD) forward plus
+BH(10L^2 D + 12LRD) backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torchrun, one rank per GPU, each rank its own batch (weak
+scaling, no collective on the data path: the batch shards into independent
+sequences).  `--impl reference` times the fp64 CPU oracle on host cores on a
+bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "sweep_L8192"
+PHASES = ("fwd", "dq", "dkv", "rel")
+
+
+def flops_fwd(B, H, L, D, R):
+    return B * H * (4 * L * L * D + 4 * L * R * D)
+
+
+def flops_bwd(B, H, L, D, R):
+    return B * H * (10 * L * L * D + 12 * L * R * D)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(target_s: float, seed_offset: int = 0):
+    """Time the fp64 oracle (as it stands) on a row sample of the workload:
+    query rows [0, r) of one (sequence, head) pair per host thread.  Returns
+    (TFLOP/s by the pages' count, description, threads)."""
+    import numpy as np
+
+    from exact_deberta_disentangled_gb300 import synth
+    from oracle import oracle
+
+    w = synth.WORKLOADS[WORKLOAD]
+    x = synth.make_inputs(w)
+    prob = oracle.Problem(x.cu_seqlens.numpy(), w.H, w.D, w.span, w.nb, w.mp)
+    f64 = lambda a: a.double().numpy()
+    args = [f64(a) for a in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    nthr = oracle.max_threads()
+    pairs = [(p // w.H % x.B, p % w.H) for p in range(nthr)]
+    # calibrate on a few rows, then size the sample to the time target
+    t = time.perf_counter()
+    oracle.step_rows_sample(prob, pairs, 0, 8, *args, nthreads=nthr)
+    per_row = max((time.perf_counter() - t) / 8, 1e-4)
+    rows = int(max(8, min(w.L, target_s / per_row)))
+    t = time.perf_counter()
+    oracle.step_rows_sample(prob, pairs, 0, rows, *args, nthreads=nthr)
+    dt = time.perf_counter() - t
+    L, D, R = w.L, w.D, w.R
+    per_row_flops = (4 * L * D + 4 * R * D) + (10 * L * D + 12 * R * D)
+    flops = per_row_flops * rows * len(pairs)
+    desc = (f"fp64 oracle fwd+bwd of query rows 0..{rows - 1} of {len(pairs)} (sequence, head) pairs of the "
+            f"L={L} workload, one pair per thread; pages' FLOP count per row")
+    return flops / dt / 1e12, desc, nthr, dt
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    vals = []
+    desc, nthr = "", 0
+    for i in range(args.warmup + args.steps):
+        v, desc, nthr, _ = oracle_sample(args.ref_seconds)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "length sweep L=8192: B=2, H=12, D=64, att_span=256 (R=512), buckets 256, "
+                               "max_rel 512, 16384 tokens", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthr, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "disentangled attn fwd+bwd TFLOP/s (pages' FLOP count) at L=8192 bf16, % roofline"
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from exact_deberta_disentangled_gb300 import binding as Bd
+    from exact_deberta_disentangled_gb300 import build as build_mod
+    from exact_deberta_disentangled_gb300 import synth
+
+    if not os.path.exists(Bd.LIB_PATH):
+        if rank == 0:
+            build_mod.build()
+        if world > 1:
+            dist.barrier()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[WORKLOAD]
+    x = synth.make_inputs(w, seed=w.seed + rank)
+    B, L, H, D, R = x.B, x.L, w.H, w.D, w.R
+    g = Bd.Geometry(B=B, L=L, H=H, D=D, span=w.span, nb=w.nb, mp=w.mp)
+    q, k, v, qr, kr, do = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    out = torch.empty_like(q)
+    lse = torch.empty(g.lse_shape(), dtype=torch.float32, device=dev)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(qr),
+             torch.empty_like(kr))
+    wsf = Bd.alloc_workspace(g, q.dtype, False, dev)
+    wsb = Bd.alloc_workspace(g, q.dtype, True, dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 2x L2
+    stream = torch.cuda.current_stream()
+
+    def step():
+        Bd.attn_fwd(g, q, k, v, qr, kr, out=out, lse=lse, workspace=wsf)
+        Bd.attn_bwd(g, q, k, v, qr, kr, out, lse, do, grads=grads, workspace=wsb)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert Bd.device_error(wsf) == 0 and Bd.device_error(wsb) == 0
+
+    # per-kernel timing hooks (CUDA events recorded by the library on this stream)
+    ev_ph = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(PHASES))]
+    for e in ev_ph:
+        e.record(stream)
+    torch.cuda.synchronize()
+    phase_ms = {p: [] for p in PHASES}
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    Bd.set_profile_events(ev_ph)
+    try:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+            torch.cuda.synchronize()
+            for pi, p in enumerate(PHASES):
+                phase_ms[p].append(ev_ph[2 * pi].elapsed_time(ev_ph[2 * pi + 1]))
+    finally:
+        Bd.set_profile_events(None)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    fl_f, fl_b = flops_fwd(B, H, L, D, R), flops_bwd(B, H, L, D, R)
+    step_flops = fl_f + fl_b
+    value = world * step_flops / (ms * 1e-3) / 1e12
+
+    # end-to-end through df_attn_step_host: pinned host buffers, copies inside the timed region
+    hq, hk, hv, hqr, hkr, hdo = [t.pin_memory() for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    houts = (torch.empty_like(hq).pin_memory(), torch.empty(g.lse_shape(), dtype=torch.float32).pin_memory(),
+             torch.empty_like(hq).pin_memory(), torch.empty_like(hk).pin_memory(),
+             torch.empty_like(hv).pin_memory(), torch.empty_like(hqr).pin_memory(),
+             torch.empty_like(hkr).pin_memory())
+    arena = torch.empty(Bd.step_host_arena_size(g, q.dtype), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqr, hkr, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in houts)
+    for _ in range(max(1, args.warmup // 2)):
+        Bd.step_host(g, hq, hk, hv, hqr, hkr, hdo, houts, arena)
+    e2e_steps = max(3, args.steps // 2)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        Bd.step_host(g, hq, hk, hv, hqr, hkr, hdo, houts, arena)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * step_flops / e2e_s / 1e12
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    avg = {p: sum(v) / len(v) for p, v in phase_ms.items()}
+    dominant = max(PHASES, key=lambda p: avg[p])
+    # algorithmic tensor FLOPs of each kernel by the pages' count:
+    #   fwd kernel  4 L^2 D + 4 L R D (all of the forward count)
+    #   dK/dV kernel  S^T, dP^T, dV, dK products: 8 L^2 D
+    #   dQ kernel     dQ product: 2 L^2 D (its recomputed S, dP are not credited)
+    #   rel kernels   the relative-position gradient products: 8 L R D
+    kflops = {"fwd": fl_f, "dkv": B * H * 8 * L * L * D, "dq": B * H * 2 * L * L * D,
+              "rel": B * H * 8 * L * R * D}
+    peak = peaks.get("bf16_tflops", 1900.0)
+    achieved = kflops[dominant] / (avg[dominant] * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get(dominant)
+        except Exception:
+            traffic = None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v_cpu, desc, nthr, _ = oracle_sample(args.ref_seconds)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": nthr, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "length sweep L=8192: B=2, H=12, D=64, att_span=256 (R=512), buckets 256, "
+                               "max_rel 512, 16384 tokens per GPU, N(0,1) inputs", "global_batch": B * world,
+                   "seq_len": L, "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "flushed before every timed step (512 MB write)",
+                   "flops_per_step": step_flops, "fwd_flops": fl_f, "bwd_flops": fl_b,
+                   "pct_of_bf16_peak": 100.0 * (value / world) / peak},
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "kernel_ms": avg, "kernel_flops": kflops},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps * 13,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--ref-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

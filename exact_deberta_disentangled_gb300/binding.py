@@ -23,7 +23,8 @@ DF_OK, DF_ERR_INVALID_ARG, DF_ERR_UNSUPPORTED, DF_ERR_WORKSPACE, DF_ERR_CUDA, DF
 DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 
 EXPORTS = ["df_attn_workspace_size", "df_attn_fwd", "df_attn_bwd", "df_attn_step_host_arena_size",
-           "df_attn_step_host", "df_rel_index_table", "df_get_device_error", "df_status_string", "df_version"]
+           "df_attn_step_host", "df_rel_index_table", "df_get_device_error", "df_status_string", "df_version",
+           "df_attn_set_profile_events"]
 
 
 class DfError(RuntimeError):
@@ -81,6 +82,8 @@ def load():
             lib.df_status_string.restype = ctypes.c_char_p
             lib.df_status_string.argtypes = [ctypes.c_int]
             lib.df_version.restype = ctypes.c_char_p
+            lib.df_attn_set_profile_events.restype = ctypes.c_int
+            lib.df_attn_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -223,3 +226,19 @@ def rel_index_table(L: int, span: int, nb: int, mp: int, device="cuda", stream=N
 
 def device_error(workspace: torch.Tensor, stream=None) -> int:
     return int(load().df_get_device_error(_ptr(workspace), _stream(stream)))
+
+
+PROFILE_PHASES = ("fwd", "dq", "dkv", "rel")
+
+
+def set_profile_events(events):
+    """Install (list of 8 torch.cuda.Event, begin/end per phase) or clear
+    (None) the library's per-phase timing hooks."""
+    lib = load()
+    if events is None:
+        rc = lib.df_attn_set_profile_events(None, 0)
+    else:
+        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        rc = lib.df_attn_set_profile_events(arr, len(events))
+    if rc != DF_OK:
+        raise DfError(rc, "df_attn_set_profile_events")

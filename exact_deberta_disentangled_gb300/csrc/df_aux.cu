@@ -57,7 +57,7 @@ DF_DEV float warp_sum(float x) {
     return x;
 }
 
-// Per (token t, head h): the four dot products Q_t.Kr[0], Q_t.Kr[R-1],
+// Per (token t, head h): the four dot products, stored [H, 4, T]: Q_t.Kr[0], Q_t.Kr[R-1],
 // K_t.Qr[0], K_t.Qr[R-1], pre-multiplied by c*log2(e) (the kernels work in
 // base-2 exponent units).  A masked key gets -inf in its two K terms, which
 // is how the key mask enters saturated tiles.  One warp per (t, h).
@@ -91,12 +91,11 @@ __global__ void relbias_kernel(ProblemDev p, const T* __restrict__ q, const T* _
         const float sc = p.scale * 1.4426950408889634f;
         bool kvalid = true;
         if (p.kmask) kvalid = p.kmask[t] != 0;
-        float4 o;
-        o.x = a0 * sc;
-        o.y = a1 * sc;
-        o.z = kvalid ? b0 * sc : -INFINITY;
-        o.w = kvalid ? b1 * sc : -INFINITY;
-        reinterpret_cast<float4*>(relb)[(size_t)t * p.H + h] = o;
+        const size_t T = (size_t)p.T, base = (size_t)h * 4 * T + t;
+        relb[base] = a0 * sc;
+        relb[base + T] = a1 * sc;
+        relb[base + 2 * T] = kvalid ? b0 * sc : -INFINITY;
+        relb[base + 3 * T] = kvalid ? b1 * sc : -INFINITY;
     }
 }
 

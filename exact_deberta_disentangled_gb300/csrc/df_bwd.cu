@@ -1,9 +1,572 @@
-// df_bwd.cu -- tensor-core backward (placeholder until the tcgen05 kernels land).
-#include "df_common.cuh"
+// df_bwd.cu -- tensor-core backward of exact disentangled attention.
+//
+// "DisentangledFlash" (section "Hugging Face usage") splits the fused
+// backward into a dQ kernel and a dK/dV kernel; section "Performance" counts
+// the relative-position gradients.  Here both attention kernels are one
+// template, mirrored by SIGMA:
+//
+//   SIGMA = +1 (dQ kernel):   rows = 128 queries, columns = key tiles
+//        S = Q K^T, dPd = dO V^T, dZ = c P (dP - Dl),  dQ += dZ K
+//        G[i, r]  = sum_{j: delta(i-j) = r} dZ[i, j]
+//   SIGMA = -1 (dK/dV kernel): rows = 128 keys, columns = query tiles
+//        S^T = K Q^T, dPd^T = V dO^T,  dV += Pd^T dO,  dK += dZ^T Q
+//        G'[j, r] = sum_{i: delta(i-j) = r} dZ[i, j]
+//
+// P is recomputed from the forward's LSE (never stored) and the dropout mask
+// is regenerated from the same Philox stream.  Every output row has exactly
+// one owner CTA and every sum runs in a fixed order, so the result is
+// bitwise reproducible with no floating-point atomics.
+//
+// G / G' ([T, H, Rp] in the input dtype) feed the relative-position
+// gradients (df_rel.cu):  dQ += G Kr,  dK += G' Qr,  dKr = sum G^T Q,
+// dQr = sum G'^T K.  A band tile adds its diagonal sums with a TMA
+// reduce-add of a [128 x band] box; every element receives at most two
+// non-zero additions that way (neighbouring tiles share at most one relative
+// row), so the order of the additions cannot change the result.  The two
+// clamped rows (delta 0 and R-1), which collect the far field, are summed in
+// registers and added once at the end.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "df_tile.cuh"
+
 namespace df {
-int launch_bwd_tc(const ProblemDev&, const Workspace&, df_dtype, const void*, const void*, const void*,
-                  const void*, const void*, const float*, const void*, void*, void*, void*, void*, void*,
-                  cudaStream_t) {
-    return (int)cudaErrorNotSupported;
+namespace {
+
+constexpr uint32_t kAcc1 = 0, kAcc2 = 128, kSCol = 256, kPCol = 384, kTCol = 256;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdSmem {
+    using G = Geo<D>;
+    static constexpr int GBOXW = G::BN == 128 ? 136 : 104;   // two boxes cover band + 8-alignment slack
+    static constexpr int R1 = 0;
+    static constexpr int RB = G::BM * D * 2;
+    static constexpr int R2 = R1 + RB;
+    static constexpr int CB = G::BN * D * 2;
+    static constexpr int C1 = R2 + RB;                       // [2] stages
+    static constexpr int C2 = C1 + 2 * CB;                   // [2] stages
+    static constexpr int BAND = C2 + 2 * CB;
+    static constexpr int BANDB = G::NBAND * G::CW * 2;
+    static constexpr int STG = BAND + BANDB;                 // own | cross, aliased by the G boxes
+    static constexpr int OWNB = G::BM * G::OWN_S * 2;
+    static constexpr int CROSS = STG + (OWNB + 15) / 16 * 16;
+    static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
+    static constexpr int GSB = 2 * G::BM * GBOXW * 2;
+    static constexpr int STGB = (CROSS - STG) + CROSSB > GSB ? (CROSS - STG) + CROSSB : GSB;
+    static constexpr int DWIN = (STG + STGB + 15) / 16 * 16;
+    static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // colb, clse, cdl
+    static constexpr int MISC = COLV + 3 * G::BN * 4;
+    static constexpr int BYTES = MISC + 256;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
+struct BwdBars {
+    uint64_t row_full;
+    uint64_t c_full[2], c_empty[2];
+    uint64_t band_full, band_empty;
+    uint64_t t_full, t_empty;
+    uint64_t s_full, z_full, mma3_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int cross_base[4];
+};
+
+DF_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+DF_DEV void tma_reduce_add_2d(const CUtensorMap* m, const void* smem_src, int x, int y) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            (uint64_t)m),
+        "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+        : "memory");
 }
+DF_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+DF_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+DF_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+template <bool BF16>
+DF_DEV uint16_t f2h16(float v) {
+    return (uint16_t)(pack2<BF16>(v, 0.f) & 0xFFFFu);
+}
+template <bool BF16>
+DF_DEV float h16f(uint16_t v) {
+    return BF16 ? __uint_as_float((uint32_t)v << 16) : h2f(v);
+}
+
+template <int D, bool BF16, int SIGMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
+                  const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmC2,
+                  const __grid_constant__ CUtensorMap tmXr, const __grid_constant__ CUtensorMap tmYr,
+                  const __grid_constant__ CUtensorMap tmG, const ProblemDev p, const int32_t* __restrict__ dtab,
+                  const float* __restrict__ relb, const float* __restrict__ lse, const float* __restrict__ rowterm,
+                  float* __restrict__ acc1_out, void* __restrict__ acc2_out, void* __restrict__ Gbuf, int Rp) {
+    using G = Geo<D>;
+    using S = BwdSmem<D>;
+    using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+    constexpr int BM = G::BM, BN = G::BN;
+    constexpr bool ROWQ = SIGMA > 0;   // rows are queries
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + S::MISC);
+    int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
+    float* colb = reinterpret_cast<float*>(smem + S::COLV);
+    float* clse = colb + BN;
+    float* cdl = clse + BN;
+    uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::STG);
+    uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
+    uint16_t* gstage = reinterpret_cast<uint16_t*>(smem + S::STG);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y, b = blockIdx.z;
+    int t0, n;
+    seq_ok(p, b, t0, n);
+    const int r0 = blockIdx.x * BM;   // first row token (query or key) of this CTA
+    if (r0 >= n) return;
+    const int ntiles = (n + BN - 1) / BN;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->row_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->c_full[s], 1);
+            mbar_init(&bars->c_empty[s], 1);
+        }
+        mbar_init(&bars->band_full, 1);
+        mbar_init(&bars->band_empty, 1);
+        mbar_init(&bars->t_full, 1);
+        mbar_init(&bars->t_empty, 4);
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->z_full, 4);
+        mbar_init(&bars->mma3_done, 1);
+        bars->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc_alloc(&bars->tmem_base, 512);
+        tc_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    volatile int* abort_flag = &bars->abort_flag;
+    int* err = p.err;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars->row_full, 2 * S::RB);
+            for (int c = 0; c < G::NCH; ++c) {
+                tma_load_2d(smem + S::R1 + c * BM * G::CW * 2, &tmR1, h * D + c * G::CW, t0 + r0, &bars->row_full);
+                tma_load_2d(smem + S::R2 + c * BM * G::CW * 2, &tmR2, h * D + c * G::CW, t0 + r0, &bars->row_full);
+            }
+            int band_loads = 0;
+            for (int it = 0; it < ntiles; ++it) {
+                const int s = it & 1, use = it >> 1;
+                const int c0 = it * BN;
+                if (use > 0 && !mbar_wait(&bars->c_empty[s], (use - 1) & 1, err, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars->c_full[s], 2 * S::CB);
+                for (int c = 0; c < G::NCH; ++c) {
+                    tma_load_2d(smem + S::C1 + s * S::CB + c * BN * G::CW * 2, &tmC1, h * D + c * G::CW, t0 + c0,
+                                &bars->c_full[s]);
+                    tma_load_2d(smem + S::C2 + s * S::CB + c * BN * G::CW * 2, &tmC2, h * D + c * G::CW, t0 + c0,
+                                &bars->c_full[s]);
+                }
+                const int base = ROWQ ? r0 - c0 : c0 - r0;
+                const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, base);
+                if (tk.uniform) continue;
+                bool ok = true;
+                for (int pass = 0; pass < 2 && ok; ++pass) {
+                    for (int c = 0; c < G::NCH; ++c) {
+                        if (band_loads > 0 &&
+                            !mbar_wait(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars->band_full, S::BANDB);
+                        tma_load_2d(smem + S::BAND, pass == 0 ? &tmXr : &tmYr, c * G::CW, h * p.R + tk.dlo,
+                                    &bars->band_full);
+                        ++band_loads;
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t sR1 = smem_u32(smem + S::R1), sR2 = smem_u32(smem + S::R2);
+            const uint32_t sBand = smem_u32(smem + S::BAND);
+            constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
+            constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
+            constexpr uint32_t idA = idesc_f16(128, D, BF16, false, true);
+            bool ok = mbar_wait(&bars->row_full, 0, err, abort_flag);
+            int band_used = 0, t_uses = 0;
+            for (int it = 0; it < ntiles && ok; ++it) {
+                const int s = it & 1, use = it >> 1;
+                const int c0 = it * BN;
+                const uint32_t sC1 = smem_u32(smem + S::C1 + s * S::CB), sC2 = smem_u32(smem + S::C2 + s * S::CB);
+                const int base = ROWQ ? r0 - c0 : c0 - r0;
+                const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, base);
+                // the band products and S / dP overwrite the previous tile's P / dZ operands
+                if (it > 0 && !(ok = mbar_wait(&bars->mma3_done, (it - 1) & 1, err, abort_flag))) break;
+                tc_fence_after();
+                if (!tk.uniform) {
+                    for (int pass = 0; pass < 2 && ok; ++pass) {
+                        if (pass == 1 && !(ok = mbar_wait(&bars->c_full[s], use & 1, err, abort_flag))) break;
+                        if (t_uses > 0 && !(ok = mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)))
+                            break;
+                        const uint32_t sA = pass == 0 ? sR1 : sC1;
+                        const int arows = pass == 0 ? BM : BN;
+                        for (int c = 0; c < G::NCH && ok; ++c) {
+                            if (!(ok = mbar_wait(&bars->band_full, band_used & 1, err, abort_flag))) break;
+                            tc_fence_after();
+                            for (int k = 0; k < G::CW / 16; ++k)
+                                tc_mma_ss(tmem + kTCol, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
+                                          desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
+                            tc_commit(&bars->band_empty);
+                            ++band_used;
+                        }
+                        if (!ok) break;
+                        tc_commit(&bars->t_full);
+                        ++t_uses;
+                    }
+                    if (!ok) break;
+                    // S / dP reuse the band columns: wait until the cross window was copied out
+                    if (!(ok = mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))) break;
+                } else {
+                    if (!(ok = mbar_wait(&bars->c_full[s], use & 1, err, abort_flag))) break;
+                }
+                tc_fence_after();
+                for (int k = 0; k < D / 16; ++k) {
+                    tc_mma_ss(tmem + kSCol, desc_k<G>(sR1, BM, k), desc_k<G>(sC1, BN, k), idS, k != 0);
+                    tc_mma_ss(tmem + kPCol, desc_k<G>(sR2, BM, k), desc_k<G>(sC2, BN, k), idS, k != 0);
+                }
+                tc_commit(&bars->s_full);
+                if (!(ok = mbar_wait(&bars->z_full, it & 1, err, abort_flag))) break;
+                tc_fence_after();
+                for (int k = 0; k < BN / 16; ++k) {
+                    // acc1 += dZ . C1   (dQ += dZ K  |  dK += dZ^T Q)
+                    tc_mma_ts(tmem + kAcc1, tmem + kPCol + k * 8, desc_mn<G>(sC1, BN, k), idA, (it | k) != 0);
+                    // dV += Pd^T dO
+                    if (!ROWQ)
+                        tc_mma_ts(tmem + kAcc2, tmem + kSCol + k * 8, desc_mn<G>(sC2, BN, k), idA, (it | k) != 0);
+                }
+                tc_commit(&bars->c_empty[s]);
+                tc_commit(&bars->mma3_done);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax / gradient warpgroup
+        const int w4 = warp & 3;
+        const int row = 32 * w4 + lane;
+        const int tid = threadIdx.x - 64;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
+        const int rt = r0 + row;              // row token position in the sequence
+        const bool row_in = rt < n;
+        const size_t T = (size_t)p.T;
+        const float* relb_h = relb + (size_t)h * 4 * T;
+        const float kscale = p.scale * kLog2e;
+        // per-row constants
+        float rb0 = -INFINITY, rb1 = -INFINITY, lse2 = INFINITY, dl = 0.f;
+        if (row_in) {
+            const bool rvalid = ROWQ ? (!p.qmask || p.qmask[t0 + rt]) : (!p.kmask || p.kmask[t0 + rt]);
+            if (rvalid) {
+                rb0 = relb_h[(ROWQ ? 0 : 2) * T + t0 + rt];
+                rb1 = relb_h[(ROWQ ? 1 : 3) * T + t0 + rt];
+            }
+            if (ROWQ) {
+                lse2 = lse[lse_index(p, b, h, t0, rt)] * kLog2e;
+                dl = rowterm[lse_index(p, b, h, t0, rt)];
+            }
+        }
+        const bool rvalid = rb0 != -INFINITY;
+        float g_lo = 0.f, g_hi = 0.f;     // diagonal sums at delta 0 and R-1
+        int t_uses = 0;
+        bool ok = true;
+        uint16_t* own_row = own + row * G::OWN_S;
+        for (int it = 0; it < ntiles && ok; ++it) {
+            const int c0 = it * BN;
+            const int base = ROWQ ? r0 - c0 : c0 - r0;
+            const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, base);
+            if (tid == 0) bulk_wait_read0();   // the previous G box left shared memory
+            named_bar_sync(1, 128);
+            if (tid < BN) {
+                const int ct = c0 + tid;
+                float cb = -INFINITY, cl = INFINITY, cd = 0.f;
+                if (ct < n) {
+                    const bool cvalid = ROWQ ? (!p.kmask || p.kmask[t0 + ct]) : (!p.qmask || p.qmask[t0 + ct]);
+                    if (cvalid) cb = tk.uniform ? relb_h[((ROWQ ? 2 : 0) + tk.which) * T + t0 + ct] : 0.f;
+                    if (!ROWQ) {
+                        cl = lse[lse_index(p, b, h, t0, ct)] * kLog2e;
+                        cd = rowterm[lse_index(p, b, h, t0, ct)];
+                    }
+                }
+                colb[tid] = cb;
+                clse[tid] = cl;
+                cdl[tid] = cd;
+            }
+            int own_a = 0;
+            if (!tk.uniform) {
+                fill_dwin<BM, BN, SIGMA>(p, dtab, base, tk.dlo, dwin, tid, 128);
+                int lo, hi;
+                if (!(ok = mbar_wait(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                tc_fence_after();
+                own_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
+                own_a = copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_empty);
+                ++t_uses;
+                if (!(ok = mbar_wait(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                tc_fence_after();
+                if (32 * w4 < BN) {
+                    cross_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
+                    const int ca = copy_band_window(lane_base + kTCol, lo, hi, cross + row * G::CROSS_S, kscale);
+                    if (lane == 0) bars->cross_base[w4] = ca;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_empty);
+                ++t_uses;
+            }
+            named_bar_sync(1, 128);
+            if (!(ok = mbar_wait(&bars->s_full, it & 1, err, abort_flag))) break;
+            tc_fence_after();
+            const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
+            int cb4[4] = {0, 0, 0, 0};
+            if (!tk.uniform)
+                for (int u = 0; u < 4; ++u) cb4[u] = bars->cross_base[u];
+            float dz[BN];
+            float rowsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t sr[32], pr[32];
+                tc_ld32(lane_base + kSCol + 32 * c, sr);
+                tc_ld32(lane_base + kPCol + 32 * c, pr);
+                tc_wait_ld();
+                uint32_t kb = 0xFFFFFFFFu;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 32 * c + e;   // column within the tile
+                    float x = fmaf(__uint_as_float(sr[e]), kscale, colb[j]) + rb;
+                    if (!tk.uniform) {
+                        const int m = dwin[ROWQ ? row - j + BN - 1 : j - row + BM - 1];
+                        x += h2f(own_row[m - own_a]) + h2f(cross[j * G::CROSS_S + m - cb4[j >> 5]]);
+                    }
+                    const float lsej = ROWQ ? lse2 : clse[j];
+                    const float pr_ = ex2(x - lsej);
+                    float keep = 1.f;
+                    if (p.dropout) {
+                        if (ROWQ) {
+                            if ((e & 3) == 0) kb = keep_bits4(p, b, h, rt, (c0 + j) >> 2);
+                            keep = ((kb >> (e & 3)) & 1u) ? p.drop_scale : 0.f;
+                        } else {
+                            const uint32_t k4 = keep_bits4(p, b, h, c0 + j, rt >> 2);
+                            keep = ((k4 >> (rt & 3)) & 1u) ? p.drop_scale : 0.f;
+                        }
+                    }
+                    const float dlj = ROWQ ? dl : cdl[j];
+                    const float z = p.scale * pr_ * (__uint_as_float(pr[e]) * keep - dlj);
+                    dz[j] = z;
+                    rowsum += z;
+                    sr[e] = __float_as_uint(pr_ * keep);
+                }
+                uint32_t zp[16], pp[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    zp[e] = pack2<BF16>(dz[32 * c + 2 * e], dz[32 * c + 2 * e + 1]);
+                    pp[e] = pack2<BF16>(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+                }
+                tc_st16(lane_base + kPCol + 16 * c, zp);
+                if (!ROWQ) tc_st16(lane_base + kSCol + 16 * c, pp);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->z_full);
+            // ---- diagonal sums of dZ for this tile
+            if (tk.uniform) {
+                if (tk.which) g_hi += rowsum; else g_lo += rowsum;
+            } else {
+                named_bar_sync(1, 128);   // everyone finished reading own / cross
+                uint32_t* g32a = reinterpret_cast<uint32_t*>(gstage + (size_t)row * S::GBOXW);
+                uint32_t* g32b = reinterpret_cast<uint32_t*>(gstage + (size_t)(BM + row) * S::GBOXW);
+                for (int x = 0; x < S::GBOXW / 2; ++x) {
+                    g32a[x] = 0u;
+                    g32b[x] = 0u;
+                }
+                const int dlo8 = tk.dlo & ~7, off = tk.dlo - dlo8;
+                int run_m = dwin[ROWQ ? row + BN - 1 : BM - 1 - row];
+                float acc = 0.f;
+                auto flush = [&](int m, float v) {
+                    const int r = tk.dlo + m;
+                    if (r == 0) {
+                        g_lo += v;
+                    } else if (r == p.R - 1) {
+                        g_hi += v;
+                    } else {
+                        const int xx = m + off;
+                        uint16_t* dst = xx < S::GBOXW ? gstage + (size_t)row * S::GBOXW + xx
+                                                      : gstage + (size_t)(BM + row) * S::GBOXW + (xx - S::GBOXW);
+                        *dst = f2h16<BF16>(v);
+                    }
+                };
+#pragma unroll
+                for (int j = 0; j < BN; ++j) {
+                    const int m = dwin[ROWQ ? row - j + BN - 1 : j - row + BM - 1];
+                    if (m != run_m) {
+                        flush(run_m, acc);
+                        run_m = m;
+                        acc = 0.f;
+                    }
+                    acc += dz[j];
+                }
+                flush(run_m, acc);
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (tid == 0) {
+                    const int x0 = h * Rp + dlo8;
+                    tma_reduce_add_2d(&tmG, gstage, x0, t0 + r0);
+                    tma_reduce_add_2d(&tmG, gstage + (size_t)BM * S::GBOXW, x0 + S::GBOXW, t0 + r0);
+                    bulk_commit();
+                }
+            }
+        }
+        if (tid == 0) bulk_wait0();
+        // ------------------------------------------------------------ epilogue
+        if (ok) ok = mbar_wait(&bars->mma3_done, (ntiles - 1) & 1, err, abort_flag);
+        tc_fence_after();
+        if (ok) {
+            float* a1 = acc1_out + ((size_t)(t0 + rt) * p.H + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tc_ld32(lane_base + kAcc1 + 32 * c, r);
+                tc_wait_ld();
+                if (row_in) {
+                    float4* dst = reinterpret_cast<float4*>(a1 + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                             __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                }
+            }
+            if (!ROWQ) {
+                T16* a2 = reinterpret_cast<T16*>(acc2_out) + ((size_t)(t0 + rt) * p.H + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tc_ld32(lane_base + kAcc2 + 32 * c, r);
+                    tc_wait_ld();
+                    if (row_in) {
+                        uint4* dst = reinterpret_cast<uint4*>(a2 + 32 * c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w;
+                            w.x = pack2<BF16>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                            w.y = pack2<BF16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                            w.z = pack2<BF16>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                            w.w = pack2<BF16>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                            dst[v] = w;
+                        }
+                    }
+                }
+            }
+            // the far-field diagonal sums; concurrent box additions to these
+            // two entries only ever add zero
+            if (row_in) {
+                uint16_t* grow = reinterpret_cast<uint16_t*>(Gbuf) + ((size_t)(t0 + rt) * p.H + h) * Rp;
+                if (g_lo != 0.f) grow[0] = f2h16<BF16>(h16f<BF16>(grow[0]) + g_lo);
+                if (g_hi != 0.f) grow[p.R - 1] = f2h16<BF16>(h16f<BF16>(grow[p.R - 1]) + g_hi);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tc_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool BF16, int SIGMA>
+int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const void* r2, const void* c1,
+               const void* c2, const void* xr, const void* yr, void* Gbuf, int Rp, float* acc1, void* acc2,
+               const float* lse, cudaStream_t st) {
+    using G = Geo<D>;
+    using S = BwdSmem<D>;
+    CUtensorMap m1, m2, m3, m4, m5, m6, mg;
+    const uint64_t tok_dims[2] = {(uint64_t)p.H * D, (uint64_t)p.T};
+    const uint64_t tok_str[1] = {(uint64_t)p.H * D * 2};
+    const uint64_t rel_dims[2] = {(uint64_t)D, (uint64_t)p.H * p.R};
+    const uint64_t rel_str[1] = {(uint64_t)D * 2};
+    const uint64_t g_dims[2] = {(uint64_t)p.H * Rp, (uint64_t)p.T};
+    const uint64_t g_str[1] = {(uint64_t)p.H * Rp * 2};
+    const uint32_t boxr[2] = {(uint32_t)G::CW, (uint32_t)G::BM};
+    const uint32_t boxc[2] = {(uint32_t)G::CW, (uint32_t)G::BN};
+    const uint32_t boxb[2] = {(uint32_t)G::CW, (uint32_t)G::NBAND};
+    const uint32_t boxg[2] = {(uint32_t)S::GBOXW, (uint32_t)G::BM};
+    const int code = BF16 ? 0 : 1;
+    if (encode_tmap(&m1, code, 2, tok_dims, tok_str, boxr, G::SWZB, r1) ||
+        encode_tmap(&m2, code, 2, tok_dims, tok_str, boxr, G::SWZB, r2) ||
+        encode_tmap(&m3, code, 2, tok_dims, tok_str, boxc, G::SWZB, c1) ||
+        encode_tmap(&m4, code, 2, tok_dims, tok_str, boxc, G::SWZB, c2) ||
+        encode_tmap(&m5, code, 2, rel_dims, rel_str, boxb, G::SWZB, xr) ||
+        encode_tmap(&m6, code, 2, rel_dims, rel_str, boxb, G::SWZB, yr) ||
+        encode_tmap(&mg, code, 2, g_dims, g_str, boxg, 0, Gbuf))
+        return (int)cudaErrorInvalidValue;
+    auto kern = bwd_tc_kernel<D, BF16, SIGMA>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+    if (e != cudaSuccess) return (int)e;
+    dim3 grid((p.L + G::BM - 1) / G::BM, p.H, p.B);
+    const int phase = SIGMA > 0 ? kProfDq : kProfDkv;
+    prof_record(phase, 0, st);
+    kern<<<grid, kThreads, S::ALLOC, st>>>(m1, m2, m3, m4, m5, m6, mg, p, ws.dtab, ws.relb, lse, ws.rowterm, acc1,
+                                           acc2, Gbuf, Rp);
+    prof_record(phase, 1, st);
+    return (int)cudaGetLastError();
+}
+
+template <int D, bool BF16>
+int launch_bwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, const void* k, const void* v,
+                    const void* qr, const void* kr, const float* lse, const void* dout, void* dq, void* dk,
+                    void* dv, void* dqr, void* dkr, cudaStream_t st) {
+    const int Rp = ws.Rp;
+    const size_t gbytes = (size_t)p.T * p.H * Rp * 2;
+    cudaError_t ce = cudaMemsetAsync(ws.G, 0, gbytes, st);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(ws.Gp, 0, gbytes, st);
+    if (ce != cudaSuccess) return (int)ce;
+    // dQ kernel: rows = queries (Q, dO), columns = keys (K, V); own band Kr, cross Qr
+    int e = launch_one<D, BF16, 1>(p, ws, q, dout, k, v, kr, qr, ws.G, Rp, ws.acc32a, nullptr, lse, st);
+    if (e) return e;
+    // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO); own band Qr, cross Kr
+    e = launch_one<D, BF16, -1>(p, ws, k, v, q, dout, qr, kr, ws.Gp, Rp, ws.acc32b, dv, lse, st);
+    if (e) return e;
+    return launch_rel_tc(p, ws, BF16 ? DF_BF16 : DF_FP16, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st);
+}
+
+}  // namespace
+
+int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
+                  const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
+                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st) {
+    const bool bf = dt == DF_BF16;
+    switch (p.D) {
+        case 32: return bf ? launch_bwd_impl<32, true>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st)
+                           : launch_bwd_impl<32, false>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st);
+        case 64: return bf ? launch_bwd_impl<64, true>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st)
+                           : launch_bwd_impl<64, false>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st);
+        case 128:
+            return bf ? launch_bwd_impl<128, true>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st)
+                      : launch_bwd_impl<128, false>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st);
+    }
+    return (int)cudaErrorInvalidValue;
+}
+
 }  // namespace df

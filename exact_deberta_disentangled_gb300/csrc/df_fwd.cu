@@ -1,8 +1,446 @@
-// df_fwd.cu -- tensor-core forward (placeholder until the tcgen05 kernel lands).
-#include "df_common.cuh"
+// df_fwd.cu -- tensor-core forward of exact disentangled attention (bf16 /
+// fp16 storage, fp32 accumulation) for sm_103a.
+//
+// One CTA owns 128 query rows of one (sequence, head) and walks the key
+// tiles of the sequence, keeping the running max / sum of an online softmax
+// ("DisentangledFlash", section "Hugging Face usage": an LSE-producing
+// forward; section "Status": the [B, H, L, L] matrix is never stored).
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q once, K/V tiles into a 2-stage ring, and for
+//               band tiles the Kr / Qr band rows.
+//   warp 1      tcgen05 issuer (one thread) and TMEM owner.
+//   warps 2..5  softmax warpgroup: thread = query row = TMEM lane.
+// Tensor memory (512 columns): O [0, 128), S / P [128, 256), band products
+// [256, 512).  P (16-bit) is written over the first half of S and feeds the
+// P.V product straight from tensor memory.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "df_tile.cuh"
+
 namespace df {
-int launch_fwd_tc(const ProblemDev&, const Workspace&, df_dtype, const void*, const void*, const void*,
-                  const void*, const void*, void*, float*, cudaStream_t) {
-    return (int)cudaErrorNotSupported;
+namespace {
+
+constexpr uint32_t kOCol = 0, kSCol = 128, kTCol = 256;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleSlack = 8.f;   // keep a stale max while the new one exceeds it by <= 8 (2^8 headroom)
+
+template <int D>
+struct FwdSmem {
+    using G = Geo<D>;
+    static constexpr int kStages = 2;
+    static constexpr int Q = 0;
+    static constexpr int QB = G::BM * D * 2;
+    static constexpr int KVB = G::BN * D * 2;
+    static constexpr int K0 = Q + QB;
+    static constexpr int V0 = K0 + kStages * KVB;
+    static constexpr int BAND = V0 + kStages * KVB;
+    static constexpr int BANDB = G::NBAND * G::CW * 2;
+    static constexpr int OWN = BAND + BANDB;
+    static constexpr int OWNB = G::BM * G::OWN_S * 2;
+    static constexpr int CROSS = (OWN + OWNB + 15) / 16 * 16;
+    static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
+    static constexpr int DWIN = CROSS + CROSSB;
+    static constexpr int COLB = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;
+    static constexpr int MISC = COLB + G::BN * 4;
+    static constexpr int BYTES = MISC + 256;
+    static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+};
+
+struct FwdBars {
+    uint64_t q_full;
+    uint64_t kv_full[2], kv_empty[2];
+    uint64_t band_full, band_empty;
+    uint64_t t_full, t_empty;
+    uint64_t s_full, p_full, pv_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int cross_base[4];
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKr,
+                  const __grid_constant__ CUtensorMap tmQr, const ProblemDev p, const int32_t* __restrict__ dtab,
+                  const float* __restrict__ relb, void* __restrict__ out_, float* __restrict__ lse) {
+    using G = Geo<D>;
+    using S = FwdSmem<D>;
+    constexpr int BM = G::BM, BN = G::BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    FwdBars* bars = reinterpret_cast<FwdBars*>(smem + S::MISC);
+    int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
+    float* colb = reinterpret_cast<float*>(smem + S::COLB);
+    uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::OWN);
+    uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y, b = blockIdx.z;
+    int t0, n;
+    seq_ok(p, b, t0, n);
+    const int i0 = blockIdx.x * BM;
+    if (i0 >= n) return;
+    const int ntiles = (n + BN - 1) / BN;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
+        mbar_init(&bars->band_full, 1);
+        mbar_init(&bars->band_empty, 1);
+        mbar_init(&bars->t_full, 1);
+        mbar_init(&bars->t_empty, 4);
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->p_full, 4);
+        mbar_init(&bars->pv_done, 1);
+        bars->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc_alloc(&bars->tmem_base, 512);
+        tc_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    volatile int* abort_flag = &bars->abort_flag;
+    int* err = p.err;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(&bars->q_full, S::QB);
+            for (int c = 0; c < G::NCH; ++c)
+                tma_load_2d(smem + S::Q + c * BM * G::CW * 2, &tmQ, h * D + c * G::CW, t0 + i0, &bars->q_full);
+            int band_loads = 0;
+            for (int it = 0; it < ntiles; ++it) {
+                const int s = it & 1, use = it >> 1;
+                const int j0 = it * BN;
+                if (use > 0 && !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, err, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars->kv_full[s], 2 * S::KVB);
+                for (int c = 0; c < G::NCH; ++c) {
+                    tma_load_2d(smem + S::K0 + s * S::KVB + c * BN * G::CW * 2, &tmK, h * D + c * G::CW, t0 + j0,
+                                &bars->kv_full[s]);
+                    tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
+                                &bars->kv_full[s]);
+                }
+                const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - j0);
+                if (tk.uniform) continue;
+                bool ok = true;
+                for (int pass = 0; pass < 2 && ok; ++pass) {
+                    for (int c = 0; c < G::NCH; ++c) {
+                        if (band_loads > 0 &&
+                            !mbar_wait(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars->band_full, S::BANDB);
+                        tma_load_2d(smem + S::BAND, pass == 0 ? &tmKr : &tmQr, c * G::CW, h * p.R + tk.dlo,
+                                    &bars->band_full);
+                        ++band_loads;
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t sQ = smem_u32(smem + S::Q), sBand = smem_u32(smem + S::BAND);
+            constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
+            constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
+            constexpr uint32_t idO = idesc_f16(128, D, BF16, false, true);
+            bool ok = mbar_wait(&bars->q_full, 0, err, abort_flag);
+            int band_used = 0, t_uses = 0;
+            for (int it = 0; it < ntiles && ok; ++it) {
+                const int s = it & 1, use = it >> 1;
+                const int j0 = it * BN;
+                const uint32_t sK = smem_u32(smem + S::K0 + s * S::KVB), sV = smem_u32(smem + S::V0 + s * S::KVB);
+                const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - j0);
+                if (!tk.uniform) {
+                    // Town = Q . Kr[band]^T
+                    if (t_uses > 0 && !(ok = mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))) break;
+                    for (int c = 0; c < G::NCH && ok; ++c) {
+                        if (!(ok = mbar_wait(&bars->band_full, band_used & 1, err, abort_flag))) break;
+                        tc_fence_after();
+                        for (int k = 0; k < G::CW / 16; ++k)
+                            tc_mma_ss(tmem + kTCol, desc_k<G>(sQ, BM, c * (G::CW / 16) + k),
+                                      desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
+                        tc_commit(&bars->band_empty);
+                        ++band_used;
+                    }
+                    if (!ok) break;
+                    tc_commit(&bars->t_full);
+                    ++t_uses;
+                    // Tcross = K . Qr[band]^T (lanes = keys)
+                    if (!(ok = mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))) break;
+                    for (int c = 0; c < G::NCH && ok; ++c) {
+                        if (!(ok = mbar_wait(&bars->band_full, band_used & 1, err, abort_flag))) break;
+                        tc_fence_after();
+                        for (int k = 0; k < G::CW / 16; ++k)
+                            tc_mma_ss(tmem + kTCol, desc_k<G>(sK, BN, c * (G::CW / 16) + k),
+                                      desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
+                        tc_commit(&bars->band_empty);
+                        ++band_used;
+                    }
+                    if (!ok) break;
+                    tc_commit(&bars->t_full);
+                    ++t_uses;
+                } else {
+                    if (!(ok = mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag))) break;
+                }
+                tc_fence_after();
+                // S and P share columns: the previous P.V must have consumed P.
+                if (it > 0 && !(ok = mbar_wait(&bars->pv_done, (it - 1) & 1, err, abort_flag))) break;
+                tc_fence_after();
+                for (int k = 0; k < D / 16; ++k)
+                    tc_mma_ss(tmem + kSCol, desc_k<G>(sQ, BM, k), desc_k<G>(sK, BN, k), idS, k != 0);
+                tc_commit(&bars->s_full);
+                if (!(ok = mbar_wait(&bars->p_full, it & 1, err, abort_flag))) break;
+                tc_fence_after();
+                for (int k = 0; k < BN / 16; ++k)
+                    tc_mma_ts(tmem + kOCol, tmem + kSCol + k * 8, desc_mn<G>(sV, BN, k), idO, (it | k) != 0);
+                tc_commit(&bars->kv_empty[s]);
+                tc_commit(&bars->pv_done);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int w4 = warp & 3;
+        const int row = 32 * w4 + lane;           // query row in the tile == TMEM lane
+        const int tid = threadIdx.x - 64;         // 0..127
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
+        const int i = i0 + row;
+        const bool row_in = i < n;
+        const bool row_valid = row_in && (!p.qmask || p.qmask[t0 + i]);
+        const size_t T = (size_t)p.T;
+        const float* relb_h = relb + (size_t)h * 4 * T;
+        const float a0 = row_in ? relb_h[t0 + i] : 0.f;
+        const float a1 = row_in ? relb_h[T + t0 + i] : 0.f;
+        const float kscale = p.scale * kLog2e;
+        float m_run = -INFINITY, l_run = 0.f;
+        int t_uses = 0;
+        bool ok = true;
+        uint16_t* own_row = own + row * G::OWN_S;
+        for (int it = 0; it < ntiles && ok; ++it) {
+            const int j0 = it * BN;
+            const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - j0);
+            named_bar_sync(1, 128);
+            if (tid < BN) {
+                const int j = j0 + tid;
+                float cb = -INFINITY;
+                if (j < n) {
+                    if (tk.uniform)
+                        cb = relb_h[(2 + tk.which) * T + t0 + j];
+                    else
+                        cb = (p.kmask && !p.kmask[t0 + j]) ? -INFINITY : 0.f;
+                }
+                colb[tid] = cb;
+            }
+            int own_a = 0;
+            if (!tk.uniform) {
+                fill_dwin<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, dwin, tid, 128);
+                int lo, hi;
+                if (!(ok = mbar_wait(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                tc_fence_after();
+                own_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
+                own_a = copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_empty);
+                ++t_uses;
+                if (!(ok = mbar_wait(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                tc_fence_after();
+                if (32 * w4 < BN) {
+                    cross_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
+                    const int ca = copy_band_window(lane_base + kTCol, lo, hi, cross + row * G::CROSS_S, kscale);
+                    if (lane == 0) bars->cross_base[w4] = ca;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_empty);
+                ++t_uses;
+            }
+            named_bar_sync(1, 128);
+            if (!(ok = mbar_wait(&bars->s_full, it & 1, err, abort_flag))) break;
+            tc_fence_after();
+            float x[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tc_ld32(lane_base + kSCol + 32 * c, r);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[32 * c + e] = fmaf(__uint_as_float(r[e]), kscale, colb[32 * c + e]);
+            }
+            float rb = tk.uniform ? (tk.which ? a1 : a0) : 0.f;
+            if (!row_valid) rb = -INFINITY;
+            if (!tk.uniform) {
+                const int cb[4] = {bars->cross_base[0], bars->cross_base[1], bars->cross_base[2],
+                                   bars->cross_base[3]};
+#pragma unroll
+                for (int j = 0; j < BN; ++j) {
+                    const int m = dwin[row - j + BN - 1];
+                    x[j] += h2f(own_row[m - own_a]) + h2f(cross[j * G::CROSS_S + m - cb[j >> 5]]);
+                }
+            }
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < BN; ++j) tmax = fmaxf(tmax, x[j]);
+            tmax += rb;
+            // online softmax in base-2 units; the max is only moved when it
+            // grows by more than kRescaleSlack
+            if (tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY)) {
+                const float alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
+                l_run *= alpha;
+                if (it > 0) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tc_ld32(lane_base + kOCol + 32 * c, r);
+                        tc_wait_ld();
+                        uint32_t o16a[16], o16b[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            o16a[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                            o16b[e] = __float_as_uint(__uint_as_float(r[16 + e]) * alpha);
+                        }
+                        tc_st16(lane_base + kOCol + 32 * c, o16a);
+                        tc_st16(lane_base + kOCol + 32 * c + 16, o16b);
+                    }
+                }
+                m_run = tmax;
+            }
+            const float mm = m_run - rb;
+            float sum = 0.f;
+            uint32_t pk[BN / 2];
+            if (m_run == -INFINITY || rb == -INFINITY) {
+#pragma unroll
+                for (int e = 0; e < BN / 2; ++e) pk[e] = 0u;
+            } else {
+                uint32_t kb = 0xFFFFFFFFu;
+#pragma unroll
+                for (int e = 0; e < BN / 2; ++e) {
+                    const float p0 = ex2(x[2 * e] - mm), p1 = ex2(x[2 * e + 1] - mm);
+                    sum += p0 + p1;
+                    float d0 = p0, d1 = p1;
+                    if (p.dropout) {
+                        if ((e & 1) == 0) kb = keep_bits4(p, b, h, i, (j0 + 2 * e) >> 2);
+                        const int sh = (2 * e) & 3;
+                        d0 = ((kb >> sh) & 1u) ? p0 * p.drop_scale : 0.f;
+                        d1 = ((kb >> (sh + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
+                    }
+                    pk[e] = pack2<BF16>(d0, d1);
+                }
+            }
+            l_run += sum;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r16[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r16[e] = pk[16 * c + e];
+                tc_st16(lane_base + kSCol + 16 * c, r16);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full);
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok) ok = mbar_wait(&bars->pv_done, (ntiles - 1) & 1, err, abort_flag);
+        tc_fence_after();
+        if (ok) {
+            const bool any = row_valid && l_run > 0.f;
+            const float inv = any ? 1.f / l_run : 0.f;
+            using OutT = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+            OutT* orow = reinterpret_cast<OutT*>(out_) + ((size_t)(t0 + i) * p.H + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tc_ld32(lane_base + kOCol + 32 * c, r);
+                tc_wait_ld();
+                if (row_in) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack2<BF16>(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+                        w.y = pack2<BF16>(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+                        w.z = pack2<BF16>(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+                        w.w = pack2<BF16>(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                        dst[v] = w;
+                    }
+                }
+            }
+            if (row_in) lse[lse_index(p, b, h, t0, i)] = any ? (m_run + log2f(l_run)) * kLn2 : INFINITY;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tc_dealloc(tmem, 512);
+    }
 }
+
+template <int D, bool BF16>
+int launch_fwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, const void* k, const void* v,
+                    const void* qr, const void* kr, void* out, float* lse, cudaStream_t st) {
+    using G = Geo<D>;
+    using S = FwdSmem<D>;
+    CUtensorMap mq, mk, mv, mkr, mqr;
+    const uint64_t tok_dims[2] = {(uint64_t)p.H * D, (uint64_t)p.T};
+    const uint64_t tok_str[1] = {(uint64_t)p.H * D * 2};
+    const uint64_t rel_dims[2] = {(uint64_t)D, (uint64_t)p.H * p.R};
+    const uint64_t rel_str[1] = {(uint64_t)D * 2};
+    const uint32_t boxq[2] = {(uint32_t)G::CW, (uint32_t)G::BM};
+    const uint32_t boxk[2] = {(uint32_t)G::CW, (uint32_t)G::BN};
+    const uint32_t boxr[2] = {(uint32_t)G::CW, (uint32_t)G::NBAND};
+    const int code = BF16 ? 0 : 1;
+    if (encode_tmap(&mq, code, 2, tok_dims, tok_str, boxq, G::SWZB, q) ||
+        encode_tmap(&mk, code, 2, tok_dims, tok_str, boxk, G::SWZB, k) ||
+        encode_tmap(&mv, code, 2, tok_dims, tok_str, boxk, G::SWZB, v) ||
+        encode_tmap(&mkr, code, 2, rel_dims, rel_str, boxr, G::SWZB, kr) ||
+        encode_tmap(&mqr, code, 2, rel_dims, rel_str, boxr, G::SWZB, qr))
+        return (int)cudaErrorInvalidValue;
+    auto kern = fwd_tc_kernel<D, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+    if (e != cudaSuccess) return (int)e;
+    dim3 grid((p.L + G::BM - 1) / G::BM, p.H, p.B);
+    prof_record(kProfFwd, 0, st);
+    kern<<<grid, kThreads, S::ALLOC, st>>>(mq, mk, mv, mkr, mqr, p, ws.dtab, ws.relb, out, lse);
+    prof_record(kProfFwd, 1, st);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_fwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
+                  const void* v, const void* qr, const void* kr, void* out, float* lse, cudaStream_t st) {
+    const bool bf = dt == DF_BF16;
+    switch (p.D) {
+        case 32: return bf ? launch_fwd_impl<32, true>(p, ws, q, k, v, qr, kr, out, lse, st)
+                           : launch_fwd_impl<32, false>(p, ws, q, k, v, qr, kr, out, lse, st);
+        case 64: return bf ? launch_fwd_impl<64, true>(p, ws, q, k, v, qr, kr, out, lse, st)
+                           : launch_fwd_impl<64, false>(p, ws, q, k, v, qr, kr, out, lse, st);
+        case 128: return bf ? launch_fwd_impl<128, true>(p, ws, q, k, v, qr, kr, out, lse, st)
+                            : launch_fwd_impl<128, false>(p, ws, q, k, v, qr, kr, out, lse, st);
+    }
+    return (int)cudaErrorInvalidValue;
+}
+
 }  // namespace df

@@ -97,9 +97,10 @@ Workspace carve(const ProblemDev& p, df_dtype dt, bool backward, void* base) {
     w.err = (int*)take(kAlign);
     w.dtab = (int32_t*)take(sizeof(int32_t) * (size_t)(2 * p.L - 1));
     if (dt != DF_FP32) w.relb = (float*)take(sizeof(float) * 4 * (size_t)p.T * p.H);
+    w.Rp = dt == DF_FP32 ? p.R : (p.R + 63) / 64 * 64;
     if (backward) {
         w.rowterm = (float*)take(sizeof(float) * (size_t)p.H * (size_t)p.B * p.L);
-        const size_t g = (size_t)elem_bytes(dt) * (size_t)p.T * p.H * p.R;
+        const size_t g = (size_t)elem_bytes(dt) * (size_t)p.T * p.H * w.Rp;
         w.G = take(g);
         w.Gp = take(g);
         if (dt != DF_FP32) {
@@ -107,6 +108,9 @@ Workspace carve(const ProblemDev& p, df_dtype dt, bool backward, void* base) {
             const size_t part = sizeof(float) * (size_t)w.nchunk * p.H * p.R * p.D;
             w.part_kr = (float*)take(part);
             w.part_qr = (float*)take(part);
+            const size_t a = sizeof(float) * (size_t)p.T * p.H * p.D;
+            w.acc32a = (float*)take(a);
+            w.acc32b = (float*)take(a);
         }
     }
     w.bytes = off;
@@ -115,11 +119,18 @@ Workspace carve(const ProblemDev& p, df_dtype dt, bool backward, void* base) {
 
 df_status cuda_status(int e) { return e == 0 ? DF_OK : DF_ERR_CUDA; }
 
+cudaEvent_t g_prof[2 * kProfPhases];
+int g_prof_on = 0;
+
 }  // namespace
+
+void prof_record(int phase, int end, cudaStream_t st) {
+    if (g_prof_on && phase >= 0 && phase < kProfPhases) cudaEventRecord(g_prof[2 * phase + (end ? 1 : 0)], st);
+}
 
 // ------------------------------------------------------------- TMA encode
 
-int encode_tmap(void* tmap, int dtype_bytes, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+int encode_tmap(void* tmap, int dtype_code, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                 const uint32_t* box, int swizzle_bytes, const void* base) {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -132,7 +143,9 @@ int encode_tmap(void* tmap, int dtype_bytes, int rank, const uint64_t* dims, con
             fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
     });
     if (!fn) return 1;
-    CUtensorMapDataType t = dtype_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUtensorMapDataType t = dtype_code == 0   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                            : dtype_code == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
     if (swizzle_bytes == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
     if (swizzle_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
@@ -171,6 +184,20 @@ const char* df_status_string(df_status s) {
 }
 
 const char* df_version(void) { return "0.1.0"; }
+
+df_status df_attn_set_profile_events(void* const* events, int n) {
+    if (!events || n == 0) {
+        g_prof_on = 0;
+        return DF_OK;
+    }
+    if (n != 2 * kProfPhases) return DF_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        if (!events[i]) return DF_ERR_INVALID_ARG;
+        g_prof[i] = (cudaEvent_t)events[i];
+    }
+    g_prof_on = 1;
+    return DF_OK;
+}
 
 size_t df_attn_workspace_size(const df_attn_params* a, int backward) {
     ProblemDev p;

@@ -31,13 +31,16 @@ struct ProblemDev {
 struct Workspace {
     int* err;                 // error word
     int32_t* dtab;            // [2L - 1] delta(r) at r + L - 1
-    float* relb;              // [T, H, 4]: c*log2e * (Q.Kr[0], Q.Kr[R-1], K.Qr[0], K.Qr[R-1])
+    float* relb;              // [H, 4, T]: c*log2e * (Q.Kr[0], Q.Kr[R-1], K.Qr[0], K.Qr[R-1])
     float* rowterm;           // [H, T] Dl_i (backward)
     void* G;                  // [T, H, R] diagonal sums of dZ by row (backward)
     void* Gp;                 // [T, H, R] diagonal sums of dZ by column (backward)
     float* part_kr;           // [nchunk, H, R, D] partial dKr (backward)
     float* part_qr;           // [nchunk, H, R, D] partial dQr (backward)
+    float* acc32a;            // [T, H, D] fp32 dQ before the relative term (backward)
+    float* acc32b;            // [T, H, D] fp32 dK before the relative term (backward)
     int nchunk;
+    int Rp;                   // row length of G / G' (R, or R rounded up to 64 on the tensor-core path)
     size_t bytes;
 };
 
@@ -65,9 +68,17 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
                   const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
                   void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st);
 
-// Encode a 2-D or 3-D tiled TMA descriptor (innermost dimension first).
-// Returns 0 on success.
-int encode_tmap(void* tmap, int dtype_bytes, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, const void* q, const void* k,
+                  const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st);
+
+// Optional benchmark timing hooks (df_attn_set_profile_events): record the
+// begin / end event of a kernel phase on the launching stream.
+enum ProfPhase { kProfFwd = 0, kProfDq = 1, kProfDkv = 2, kProfRel = 3, kProfPhases = 4 };
+void prof_record(int phase, int end, cudaStream_t st);
+
+// Encode a 2-D or 3-D tiled TMA descriptor (innermost dimension first);
+// dtype_code 0 = bf16, 1 = fp16, 2 = fp32.  Returns 0 on success.
+int encode_tmap(void* tmap, int dtype_code, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                 const uint32_t* box, int swizzle_bytes, const void* base);
 
 }  // namespace df

@@ -1,0 +1,138 @@
+// df_tile.cuh -- tile geometry and the relative-position machinery shared by
+// the tensor-core forward and backward kernels.
+//
+// A tile pairs NR "row" tokens (the tokens a thread of the softmax warpgroup
+// owns: queries in the forward and dQ kernels, keys in the dK/dV kernel)
+// with NC "column" tokens.  Its relative positions are
+//     r = base + SIGMA * (row - col),   base = i0 - j0,
+// SIGMA = +1 when rows are queries and -1 when rows are keys.
+//
+// Uniform tiles: every r maps to delta = 0 or every r to delta = R - 1 (the
+// clamped far field).  There C2P / P2C collapse to one value per query and
+// one per key, taken from the per-token table of df_aux.cu.
+//
+// Band tiles: the tile reaches at most NR + NC - 1 consecutive relative rows
+// [dlo, dlo + NBAND).  Two tensor-core products give every value the tile
+// can need:  Town = Rows . Xr[band]^T   (lanes = rows)
+//            Tcross = Cols . Yr[band]^T  (lanes = columns)
+// (Xr = Kr, Yr = Qr when rows are queries; swapped when rows are keys).  Each
+// is copied from tensor memory to shared memory, scaled by c*log2(e) and
+// rounded to fp16, and the softmax gathers  Town[row][delta(r) - dlo] +
+// Tcross[col][delta(r) - dlo]  per element.  The own window is private to its
+// thread; the cross window is shared by the warpgroup.
+#pragma once
+
+#include "df_common.cuh"
+
+namespace df {
+
+template <int D_>
+struct Geo {
+    static constexpr int D = D_;
+    static constexpr int BM = 128;                      // rows per tile (TMEM lanes)
+    static constexpr int BN = D == 128 ? 64 : 128;      // columns per tile
+    static constexpr int CW = D == 32 ? 32 : 64;        // elements per swizzled row chunk
+    static constexpr int NCH = D / CW;                  // chunks per head-dim row
+    static constexpr uint32_t SWZ = D == 32 ? 4u : 2u;  // descriptor swizzle code (64B / 128B)
+    static constexpr int SWZB = CW * 2;                 // TMA swizzle span in bytes
+    static constexpr int NBAND = BM + BN - 1 <= 192 ? 192 : 256;
+    static constexpr int OWN_S = BN == 64 ? 114 : 178;  // own window stride (halves), >= 16*ceil((BN+46)/16)
+    static constexpr int CROSS_S = 176;                                // cross window stride (halves)
+};
+
+DF_DEV int dclamp(const ProblemDev& p, const int32_t* __restrict__ dtab, int r) {
+    r = r > p.L - 1 ? p.L - 1 : r;
+    r = r < -(p.L - 1) ? -(p.L - 1) : r;
+    return __ldg(dtab + r + p.L - 1);
+}
+
+// K-major operand: `rows` rows of a [rows x D] tile stored as D/CW regions of
+// [rows x CW] (TMA swizzle), k-step of 16 elements.
+template <class G>
+DF_DEV uint64_t desc_k(uint32_t base, int rows, int kstep) {
+    constexpr int per = G::CW / 16;
+    const int region = kstep / per, within = kstep % per;
+    return sdesc(base + (uint32_t)(region * rows * G::CW * 2 + within * 32), 16, 8 * G::CW * 2, G::SWZ);
+}
+
+// MN-major B operand: N = head dim (D/CW regions of [rows x CW]), K = rows,
+// k-step of 16 rows.
+template <class G>
+DF_DEV uint64_t desc_mn(uint32_t base, int rows, int kstep) {
+    return sdesc(base + (uint32_t)(kstep * 16 * G::CW * 2), (uint32_t)(rows * G::CW * 2), 8 * G::CW * 2, G::SWZ);
+}
+
+struct TileKind {
+    int dlo, dhi;
+    int uniform;   // 1: every element has delta == dlo, and dlo is 0 or R-1
+    int which;     // uniform tiles: 0 -> delta 0, 1 -> delta R-1
+};
+
+template <int NR, int NC, int SIGMA>
+DF_DEV TileKind classify(const ProblemDev& p, const int32_t* __restrict__ dtab, int base) {
+    const int rlo = SIGMA > 0 ? base - (NC - 1) : base - (NR - 1);
+    const int rhi = SIGMA > 0 ? base + (NR - 1) : base + (NC - 1);
+    TileKind k;
+    k.dlo = dclamp(p, dtab, rlo);
+    k.dhi = dclamp(p, dtab, rhi);
+    k.uniform = k.dlo == k.dhi && (k.dlo == 0 || k.dlo == p.R - 1);
+    k.which = k.dlo == 0 ? 0 : 1;
+    return k;
+}
+
+// dwin[x] = delta(r) - dlo for the tile, x = SIGMA*(row - col) + (SIGMA > 0 ? NC - 1 : NR - 1).
+template <int NR, int NC, int SIGMA>
+DF_DEV void fill_dwin(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int dlo, int16_t* dwin,
+                      int tid, int nthreads) {
+    for (int x = tid; x < NR + NC - 1; x += nthreads) {
+        const int r = SIGMA > 0 ? base + x - (NC - 1) : base - (x - (NR - 1));
+        dwin[x] = (int16_t)(dclamp(p, dtab, r) - dlo);
+    }
+}
+
+// Copy the columns of a band product that a warp needs (`lo` .. `hi`, band
+// coordinates) from tensor memory to the thread's shared-memory row, scaled
+// to base-2 exponent units and rounded to fp16.  Returns the band coordinate
+// of dst[0] (warp-uniform, a multiple of 16).
+DF_DEV int copy_band_window(uint32_t t_lane_col0, int lo, int hi, uint16_t* dst, float scale) {
+    const int a = lo & ~15;
+    const int nch = ((hi - a) >> 4) + 1;
+    for (int c = 0; c < nch; ++c) {
+        uint32_t r[16];
+        tc_ld16(t_lane_col0 + (uint32_t)(a + 16 * c), r);
+        tc_wait_ld();
+        uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + 16 * c);
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+            d32[x] = pack2<false>(__uint_as_float(r[2 * x]) * scale, __uint_as_float(r[2 * x + 1]) * scale);
+    }
+    return a;
+}
+
+// Band window of the own product for the warp holding rows [32w, 32w + 32).
+template <int NR, int NC, int SIGMA>
+DF_DEV void own_range(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int dlo, int w, int& lo,
+                      int& hi) {
+    const int rmin = SIGMA > 0 ? base + 32 * w - (NC - 1) : base - (32 * w + 31);
+    const int rmax = SIGMA > 0 ? base + 32 * w + 31 : base - 32 * w + (NC - 1);
+    lo = dclamp(p, dtab, rmin) - dlo;
+    hi = dclamp(p, dtab, rmax) - dlo;
+}
+
+// Band window of the cross product for the warp holding columns [32u, 32u + 32).
+template <int NR, int NC, int SIGMA>
+DF_DEV void cross_range(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int dlo, int u, int& lo,
+                        int& hi) {
+    const int rmin = SIGMA > 0 ? base - (32 * u + 31) : base + 32 * u - (NR - 1);
+    const int rmax = SIGMA > 0 ? base + (NR - 1) - 32 * u : base + 32 * u + 31;
+    lo = dclamp(p, dtab, rmin) - dlo;
+    hi = dclamp(p, dtab, rmax) - dlo;
+}
+
+DF_DEV float h2f(uint16_t h) {
+    float f;
+    asm("{ .reg .f16 t; mov.b16 t, %1; cvt.f32.f16 %0, t; }" : "=f"(f) : "h"(h));
+    return f;
+}
+
+}  // namespace df

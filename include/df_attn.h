@@ -175,6 +175,17 @@ df_status df_rel_index_table(int32_t L, int32_t att_span, int32_t position_bucke
  */
 df_status df_get_device_error(const void *workspace, df_stream_t stream);
 
+/*
+ * Benchmark timing hooks.  `events` holds 8 CUDA event handles (cudaEvent_t,
+ * created by the caller, on the device the calls run on): while set, every
+ * df_attn_fwd / df_attn_bwd records events[2k] just before and events[2k+1]
+ * just after kernel phase k on the call's stream -- k = 0 the forward
+ * attention kernel, 1 the dQ kernel, 2 the dK/dV kernel, 3 the relative-
+ * position gradient kernels.  Pass NULL / 0 to switch the hooks off.  The
+ * setting is process-wide and not thread-safe; it exists for measurement only.
+ */
+df_status df_attn_set_profile_events(void *const *events, int n);
+
 /* Static, human-readable name of a status code. */
 const char *df_status_string(df_status s);
 

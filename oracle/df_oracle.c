@@ -372,6 +372,165 @@ int orc_backward(const orc_cfg *c, const double *q, const double *k, const doubl
     return err ? -1 : 0;
 }
 
+/* Sampled backward of one (s, h) pair for full-size checks: dQ of the rows
+ * listed in rows[] and dK, dV of the keys listed in cols[] (positions inside
+ * the sequence), each computed from the plain definition.  The per-row
+ * constants LSE_i and Dl_i that the key gradients need are computed for every
+ * row (rows in parallel).  Outputs: dq_rows [nrows, D], dk_cols, dv_cols
+ * [ncols, D]. */
+int orc_backward_sample(const orc_cfg *c, int s, int h, const double *q, const double *k, const double *v,
+                        const double *qr, const double *kr, const double *dout, int nrows, const int *rows,
+                        int ncols, const int *cols, double *dq_rows, double *dk_cols, double *dv_cols)
+{
+    const int H = c->H, D = c->D, R = 2 * c->span;
+    const int t0 = c->cu[s], n = c->cu[s + 1] - t0;
+    const double cs = scale_of(c);
+    const uint64_t thr = orc_keep_threshold(c->p_drop);
+    const double dscale = c->p_drop > 0.0 ? 1.0 / (1.0 - c->p_drop) : 1.0;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * 2);
+    if (!lse) return -2;
+    double *dl = lse + n;
+    int err = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : err)
+#endif
+    for (int i = 0; i < n; ++i) {
+        double *srow = (double *)malloc(sizeof(double) * (size_t)n);
+        if (!srow) { err |= 1; continue; }
+        int any = score_row(c, s, h, i, q, k, qr, kr, srow);
+        lse[i] = any ? row_lse(srow, n) : INFINITY;
+        double acc = 0.0;
+        if (any) {
+            const double *doi = dout + ((size_t)(t0 + i) * H + h) * D;
+            for (int j = 0; j < n; ++j) {
+                double p = exp(srow[j] - lse[i]);
+                if (p == 0.0) continue;
+                double keep = 1.0;
+                if (c->p_drop > 0.0) keep = keep_bit(c, s, h, i, j, thr) ? dscale : 0.0;
+                acc += p * dot(doi, v + ((size_t)(t0 + j) * H + h) * D, D) * keep;
+            }
+        }
+        dl[i] = acc;
+        free(srow);
+    }
+    if (err) { free(lse); return -2; }
+    double *srow = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    for (int ri = 0; ri < nrows; ++ri) {
+        const int i = rows[ri];
+        double *o = dq_rows + (size_t)ri * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (i < 0 || i >= n || lse[i] == INFINITY) continue;
+        score_row(c, s, h, i, q, k, qr, kr, srow);
+        const double *doi = dout + ((size_t)(t0 + i) * H + h) * D;
+        for (int j = 0; j < n; ++j) {
+            double p = exp(srow[j] - lse[i]);
+            if (p == 0.0) continue;
+            double keep = 1.0;
+            if (c->p_drop > 0.0) keep = keep_bit(c, s, h, i, j, thr) ? dscale : 0.0;
+            const double *kj = k + ((size_t)(t0 + j) * H + h) * D;
+            double g = cs * p * (dot(doi, v + ((size_t)(t0 + j) * H + h) * D, D) * keep - dl[i]);
+            long dd = orc_delta((long)i - (long)j, c->span, c->nb, c->mp);
+            const double *krd = kr + ((size_t)h * R + dd) * D;
+            for (int d = 0; d < D; ++d) o[d] += g * (kj[d] + krd[d]);
+        }
+    }
+    for (int cj = 0; cj < ncols; ++cj) {
+        const int j = cols[cj];
+        double *ok = dk_cols + (size_t)cj * D, *ov = dv_cols + (size_t)cj * D;
+        for (int d = 0; d < D; ++d) { ok[d] = 0.0; ov[d] = 0.0; }
+        if (j < 0 || j >= n) continue;
+        if (c->kmask && !c->kmask[t0 + j]) continue;
+        const double *kj = k + ((size_t)(t0 + j) * H + h) * D;
+        const double *vj = v + ((size_t)(t0 + j) * H + h) * D;
+        for (int i = 0; i < n; ++i) {
+            if (lse[i] == INFINITY) continue;
+            if (c->qmask && !c->qmask[t0 + i]) continue;
+            const double *qi = q + ((size_t)(t0 + i) * H + h) * D;
+            const double *doi = dout + ((size_t)(t0 + i) * H + h) * D;
+            long dd = orc_delta((long)i - (long)j, c->span, c->nb, c->mp);
+            const double *krd = kr + ((size_t)h * R + dd) * D;
+            const double *qrd = qr + ((size_t)h * R + dd) * D;
+            double z = dot(qi, kj, D) + dot(qi, krd, D) + dot(kj, qrd, D);
+            double p = exp(cs * z - lse[i]);
+            double keep = 1.0;
+            if (c->p_drop > 0.0) keep = keep_bit(c, s, h, i, j, thr) ? dscale : 0.0;
+            double g = cs * p * (dot(doi, vj, D) * keep - dl[i]);
+            for (int d = 0; d < D; ++d) {
+                ov[d] += p * keep * doi[d];
+                ok[d] += g * (qi[d] + qrd[d]);
+            }
+        }
+    }
+    free(srow);
+    free(lse);
+    return 0;
+}
+
+/* Forward and backward work of the query rows [r0, r1) of `npairs` (s, h)
+ * pairs (one pair per OpenMP thread), exactly as orc_forward_pair /
+ * orc_backward_pair do it row by row, with private accumulators.  Used to
+ * time the oracle on a bounded sample of a large workload.  Returns a
+ * checksum of the outputs (so the work cannot be skipped). */
+double orc_step_rows_sample(const orc_cfg *c, int npairs, const int *pairs, int r0, int r1, const double *q,
+                            const double *k, const double *v, const double *qr, const double *kr,
+                            const double *dout, int nthreads)
+{
+    double total = 0.0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : total)
+#endif
+    for (int x = 0; x < npairs; ++x) {
+        const int s = pairs[2 * x], h = pairs[2 * x + 1];
+        const int H = c->H, D = c->D, R = 2 * c->span;
+        const int t0 = c->cu[s], n = c->cu[s + 1] - t0;
+        const double cs = scale_of(c);
+        const uint64_t thr = orc_keep_threshold(c->p_drop);
+        const double dscale = c->p_drop > 0.0 ? 1.0 / (1.0 - c->p_drop) : 1.0;
+        double *buf = (double *)calloc((size_t)3 * n + (size_t)2 * n * D + (size_t)2 * R * D + 2 * (size_t)D, sizeof(double));
+        if (!buf) continue;
+        double *srow = buf, *prow = srow + n, *dzrow = prow + n;
+        double *dk = dzrow + n, *dv = dk + (size_t)n * D, *dkr = dv + (size_t)n * D, *dqr = dkr + (size_t)R * D;
+        double *o = dqr + (size_t)R * D, *dq = o + D;
+        for (int i = r0; i < r1 && i < n; ++i) {
+            const double *qi = q + ((size_t)(t0 + i) * H + h) * D;
+            const double *doi = dout + ((size_t)(t0 + i) * H + h) * D;
+            if (!score_row(c, s, h, i, q, k, qr, kr, srow)) continue;
+            const double L = row_lse(srow, n);
+            for (int d = 0; d < D; ++d) { o[d] = 0.0; dq[d] = 0.0; }
+            double dl = 0.0;
+            for (int j = 0; j < n; ++j) {
+                const double p = exp(srow[j] - L);
+                prow[j] = p;
+                double keep = 1.0;
+                if (c->p_drop > 0.0) keep = keep_bit(c, s, h, i, j, thr) ? dscale : 0.0;
+                const double *vj = v + ((size_t)(t0 + j) * H + h) * D;
+                for (int d = 0; d < D; ++d) o[d] += p * keep * vj[d];
+                for (int d = 0; d < D; ++d) dv[(size_t)j * D + d] += p * keep * doi[d];
+                dzrow[j] = dot(doi, vj, D) * keep;
+                dl += p * dzrow[j];
+            }
+            for (int j = 0; j < n; ++j) {
+                const double g = cs * prow[j] * (dzrow[j] - dl);
+                const double *kj = k + ((size_t)(t0 + j) * H + h) * D;
+                const long dd = orc_delta((long)i - (long)j, c->span, c->nb, c->mp);
+                const double *krd = kr + ((size_t)h * R + dd) * D;
+                const double *qrd = qr + ((size_t)h * R + dd) * D;
+                for (int d = 0; d < D; ++d) {
+                    dq[d] += g * (kj[d] + krd[d]);
+                    dk[(size_t)j * D + d] += g * (qi[d] + qrd[d]);
+                    dkr[(size_t)dd * D + d] += g * qi[d];
+                    dqr[(size_t)dd * D + d] += g * kj[d];
+                }
+            }
+            for (int d = 0; d < D; ++d) total += o[d] + dq[d];
+        }
+        for (size_t x2 = 0; x2 < (size_t)2 * n * D + (size_t)2 * R * D; ++x2) total += dk[x2];
+        free(buf);
+    }
+    return total;
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP

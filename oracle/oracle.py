@@ -76,6 +76,11 @@ def _load():
             lib.orc_forward.argtypes = [cp] + [dp] * 7 + [ctypes.c_int]
             lib.orc_backward_pair.argtypes = [cp, ctypes.c_int, ctypes.c_int] + [dp] * 11
             lib.orc_backward.argtypes = [cp] + [dp] * 11 + [ctypes.c_int]
+            lib.orc_backward_sample.argtypes = [cp, ctypes.c_int, ctypes.c_int] + [dp] * 6 + [
+                ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.POINTER(ctypes.c_int), dp, dp, dp]
+            lib.orc_step_rows_sample.restype = ctypes.c_double
+            lib.orc_step_rows_sample.argtypes = [cp, ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int,
+                                                 ctypes.c_int] + [dp] * 6 + [ctypes.c_int]
             lib.orc_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -226,3 +231,33 @@ def backward_pair(prob: Problem, s: int, h: int, q, k, v, qr, kr, dout):
         raise RuntimeError("oracle backward_pair failed")
     t0, t1 = int(prob.cu[s]), int(prob.cu[s + 1])
     return dq[t0:t1, h].copy(), dk[t0:t1, h].copy(), dv[t0:t1, h].copy(), pq, pk
+
+
+def backward_sample(prob: Problem, s: int, h: int, rows, cols, q, k, v, qr, kr, dout):
+    """dQ of selected rows and dK, dV of selected keys of one (sequence,
+    head) pair (positions inside the sequence)."""
+    q, k, v, qr, kr, dout = map(_f64, (q, k, v, qr, kr, dout))
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int32))
+    dq = np.zeros((len(rows), prob.D))
+    dk = np.zeros((len(cols), prob.D))
+    dv = np.zeros((len(cols), prob.D))
+    c = prob._cfg()
+    ip = ctypes.POINTER(ctypes.c_int)
+    rc = _load().orc_backward_sample(ctypes.byref(c), int(s), int(h), _dp(q), _dp(k), _dp(v), _dp(qr), _dp(kr),
+                                     _dp(dout), len(rows), rows.ctypes.data_as(ip), len(cols),
+                                     cols.ctypes.data_as(ip), _dp(dq), _dp(dk), _dp(dv))
+    if rc != 0:
+        raise RuntimeError("oracle backward_sample failed")
+    return dq, dk, dv
+
+
+def step_rows_sample(prob: Problem, pairs, r0: int, r1: int, q, k, v, qr, kr, dout, nthreads: int = 0) -> float:
+    """Forward + backward work of query rows [r0, r1) of the listed (s, h)
+    pairs, one pair per thread; returns a checksum."""
+    q, k, v, qr, kr, dout = map(_f64, (q, k, v, qr, kr, dout))
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1))
+    c = prob._cfg()
+    return float(_load().orc_step_rows_sample(ctypes.byref(c), len(pr) // 2, pr.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                              int(r0), int(r1), _dp(q), _dp(k), _dp(v), _dp(qr), _dp(kr), _dp(dout),
+                                              int(nthreads)))

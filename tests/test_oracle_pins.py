@@ -428,3 +428,27 @@ def test_philox_output_words_are_uniform_and_key_sensitive():
         x = O.philox4x32_10(ctr, key) ^ base
         flips = sum(bin(int(w)).count("1") for w in x)
         assert 40 < flips < 88
+
+
+def test_sampled_backward_matches_full_backward():
+    """The sampled-row routine used for full-size checks agrees with the full
+    oracle backward (masks and dropout included)."""
+    cu = np.array([0, 40, 90])
+    H, D, span = 2, 8, 6
+    m = np.ones(90, np.uint8)
+    m[33:40] = 0
+    prob = O.Problem(cu, H, D, span, 8, 16, qmask=m, kmask=m, p_drop=0.2, seed=77, offset=2)
+    q, k, v, qr, kr, do = _problem_inputs(cu, H, D, span, 31)
+    dq, dk, dv, _, _ = O.backward(prob, q, k, v, qr, kr, do)
+    rows = [0, 5, 33, 39]
+    cols = [1, 20, 35, 49]
+    for s in range(2):
+        for h in range(H):
+            t0 = cu[s]
+            n = cu[s + 1] - t0
+            rr = [r for r in rows if r < n]
+            cc = [c for c in cols if c < n]
+            sq, sk, sv = O.backward_sample(prob, s, h, rr, cc, q, k, v, qr, kr, do)
+            np.testing.assert_allclose(sq, dq[t0 + np.array(rr), h], rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(sk, dk[t0 + np.array(cc), h], rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(sv, dv[t0 + np.array(cc), h], rtol=1e-10, atol=1e-12)

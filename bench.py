@@ -39,6 +39,27 @@ def flops_bwd(B, H, L, D, R):
     return B * H * (10 * L * L * D + 12 * L * R * D)
 
 
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling: independent sequences)."""
+    return base_seed + rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Slowest rank's value (the job's time is the slowest replica's)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, step_flops: float, seconds_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank processed step_flops per step."""
+    return world * step_flops / seconds_per_step / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -174,7 +195,7 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[WORKLOAD]
-    x = synth.make_inputs(w, seed=w.seed + rank)
+    x = synth.make_inputs(w, seed=rank_seed(w.seed, rank))
     B, L, H, D, R = x.B, x.L, w.H, w.D, w.R
     g = Bd.Geometry(B=B, L=L, H=H, D=D, span=w.span, nb=w.nb, mp=w.mp)
     q, k, v, qr, kr, do = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
@@ -229,13 +250,10 @@ def run_gpu(args, rank, world, local_rank):
     clk = clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     fl_f, fl_b = flops_fwd(B, H, L, D, R), flops_bwd(B, H, L, D, R)
     step_flops = fl_f + fl_b
-    value = world * step_flops / (ms * 1e-3) / 1e12
+    value = job_throughput(world, step_flops, ms * 1e-3)
 
     # end-to-end through df_attn_step_host: pinned host buffers, copies inside the timed region
     hq, hk, hv, hqr, hkr, hdo = [t.pin_memory() for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
@@ -254,11 +272,8 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(e2e_steps):
         Bd.step_host(g, hq, hk, hv, hqr, hkr, hdo, houts, arena)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * step_flops / e2e_s / 1e12
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    e2e_value = job_throughput(world, step_flops, e2e_s)
 
     if rank != 0:
         return

@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!tk.uniform) {
                 fill_dwin<BM, BN, SIGMA>(p, dtab, base, tk.dlo, dwin, tid, 128);
                 int lo, hi;
-                if (!(ok = mbar_wait(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
                 tc_fence_after();
                 own_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
                 own_a = copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->t_empty);
                 ++t_uses;
-                if (!(ok = mbar_wait(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
                 tc_fence_after();
                 if (32 * w4 < BN) {
                     cross_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++t_uses;
             }
             named_bar_sync(1, 128);
-            if (!(ok = mbar_wait(&bars->s_full, it & 1, err, abort_flag))) break;
+            if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
             int cb4[4] = {0, 0, 0, 0};
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tid == 0) bulk_wait0();
         // ------------------------------------------------------------ epilogue
-        if (ok) ok = mbar_wait(&bars->mma3_done, (ntiles - 1) & 1, err, abort_flag);
+        if (ok) ok = mbar_wait_warp(&bars->mma3_done, (ntiles - 1) & 1, err, abort_flag);
         tc_fence_after();
         if (ok) {
             float* a1 = acc1_out + ((size_t)(t0 + rt) * p.H + h) * D;

@@ -156,6 +156,12 @@ DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err_word, volatile in
     }
 }
 
+// mbar_wait taken by a whole warp with one outcome for every lane, so that
+// warp-collective tcgen05 instructions after it never run divergent.
+DF_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err_word, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, err_word, abort_flag));
+}
+
 // Named barrier among `nthreads` threads (a multiple of 32).
 DF_DEV void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!tk.uniform) {
                 fill_dwin<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, dwin, tid, 128);
                 int lo, hi;
-                if (!(ok = mbar_wait(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
                 tc_fence_after();
                 own_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
                 own_a = copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->t_empty);
                 ++t_uses;
-                if (!(ok = mbar_wait(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
                 tc_fence_after();
                 if (32 * w4 < BN) {
                     cross_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++t_uses;
             }
             named_bar_sync(1, 128);
-            if (!(ok = mbar_wait(&bars->s_full, it & 1, err, abort_flag))) break;
+            if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
             tc_fence_after();
             float x[BN];
 #pragma unroll
@@ -304,10 +304,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmax += rb;
             // online softmax in base-2 units; the max is only moved when it
             // grows by more than kRescaleSlack
-            if (tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY)) {
-                const float alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
+            const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
+            float alpha = 1.f;
+            if (need) {
+                alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
                 l_run *= alpha;
-                if (it > 0) {
+                m_run = tmax;
+            }
+            // the O accumulator is rescaled by the whole warp (tcgen05.ld / st
+            // are warp-collective); rows that keep their max use alpha = 1
+            if (__any_sync(0xffffffffu, need) && it > 0) {
+                {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
@@ -323,7 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_st16(lane_base + kOCol + 32 * c + 16, o16b);
                     }
                 }
-                m_run = tmax;
             }
             const float mm = m_run - rb;
             float sum = 0.f;
@@ -361,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bars->p_full);
         }
         // ------------------------------------------------------------ epilogue
-        if (ok) ok = mbar_wait(&bars->pv_done, (ntiles - 1) & 1, err, abort_flag);
+        if (ok) ok = mbar_wait_warp(&bars->pv_done, (ntiles - 1) & 1, err, abort_flag);
         tc_fence_after();
         if (ok) {
             const bool any = row_valid && l_run > 0.f;

@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kRelThreads, 1)
         tc_commit(&bars->done);
     }
     __syncthreads();
-    if (ok) ok = mbar_wait(&bars->done, 0, p.err, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) ok = mbar_wait_warp(&bars->done, 0, p.err, abort_flag);
     tc_fence_after();
     const int row = 32 * warp + lane, tok = tok0 + row;
     using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
@@ -212,7 +213,8 @@ __global__ void __launch_bounds__(kRelThreads, 1)
         tc_commit(&bars->done);
     }
     __syncthreads();
-    if (nk > 0 && ok) ok = mbar_wait(&bars->done, 0, p.err, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (nk > 0 && ok) ok = mbar_wait_warp(&bars->done, 0, p.err, abort_flag);
     tc_fence_after();
     const int r = 128 * rb + 32 * warp + lane;
     float* dst = part + (((size_t)ch * p.H + h) * p.R + r) * D;

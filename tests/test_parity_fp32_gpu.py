@@ -99,9 +99,8 @@ def test_inconsistent_cu_seqlens_are_reported_not_faulted():
     w = synth.WORKLOADS["varlen"]
     x = synth.make_inputs(w, H=2, total_tokens=300, dtype="fp32")
     dev = torch.device(DEV)
-    cu = x.cu_seqlens.clone()
-    cu[1] = cu[2] + 5            # non-monotone offsets
-    g = B.Geometry(B=x.B, L=x.L, H=2, D=w.D, span=w.span, nb=w.nb, mp=w.mp, cu_seqlens=cu.to(dev),
+    cu = torch.tensor([0, 205, 100, 300], dtype=torch.int32)   # non-monotone offsets
+    g = B.Geometry(B=3, L=205, H=2, D=w.D, span=w.span, nb=w.nb, mp=w.mp, cu_seqlens=cu.to(dev),
                    total_tokens=300)
     t = [a.to(dev) for a in (x.q, x.k, x.v, x.qr, x.kr)]
     out, lse, ws = B.attn_fwd(g, *t)

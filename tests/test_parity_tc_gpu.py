@@ -57,8 +57,6 @@ def check_against_oracle(x, w, H, p_drop=0.0, seed=0, offset=0, backward=True):
     assert max_abs(out, o_ref) <= OUT_MAX, max_abs(out, o_ref)
     lse_got = lse_to_oracle_layout(lse, x.packed, x.B, H, x.L)
     fin = np.isfinite(lse_ref)
-    if not x.packed:
-        valid = np.ones_like(fin)
     assert np.array_equal(np.isfinite(lse_got), fin)
     assert rel_l2(lse_got[fin], lse_ref[fin]) <= OUT_TOL
     assert max_abs(lse_got[fin], lse_ref[fin]) <= OUT_MAX

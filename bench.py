@@ -323,6 +323,31 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args, local_rank):
+    """Small case for kernel profiling (ncu): the sweep shape at L=4096,
+    B=2, H=12 (8,192 tokens; inputs + diagonal-sum buffers > L2).  Runs
+    warmup + steps fwd+bwd iterations without timing."""
+    import torch
+
+    from exact_deberta_disentangled_gb300 import binding as Bd
+    from exact_deberta_disentangled_gb300 import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS["sweep_L4096"]
+    x = synth.make_inputs(w, B=2)
+    g = Bd.Geometry(B=x.B, L=x.L, H=w.H, D=w.D, span=w.span, nb=w.nb, mp=w.mp)
+    q, k, v, qr, kr, do = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    out, lse, wsf = Bd.attn_fwd(g, q, k, v, qr, kr)
+    grads, wsb = Bd.attn_bwd(g, q, k, v, qr, kr, out, lse, do)
+    for _ in range(args.warmup + args.steps - 1):
+        Bd.attn_fwd(g, q, k, v, qr, kr, out=out, lse=lse, workspace=wsf)
+        Bd.attn_bwd(g, q, k, v, qr, kr, out, lse, do, grads=grads, workspace=wsb)
+    torch.cuda.synchronize()
+    assert Bd.device_error(wsf) == 0 and Bd.device_error(wsb) == 0
+    print("profile case done", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -331,12 +356,17 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="run the small profiling case (L=4096, B=2) without timing")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.profile_run:
+        run_profile_case(args, local_rank)
         return
     if world > 1:
         import torch

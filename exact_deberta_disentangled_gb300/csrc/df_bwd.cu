@@ -412,6 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         g_hi += v;
                     } else {
                         const int xx = m + off;
+                        if (xx < 0 || xx >= 2 * S::GBOXW) {
+                            raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
+                            return;
+                        }
                         uint16_t* dst = xx < S::GBOXW ? gstage + (size_t)row * S::GBOXW + xx
                                                       : gstage + (size_t)(BM + row) * S::GBOXW + (xx - S::GBOXW);
                         *dst = f2h16<BF16>(v);

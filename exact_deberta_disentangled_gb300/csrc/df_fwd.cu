@@ -11,9 +11,12 @@
 //               band tiles the Kr / Qr band rows.
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.
 //   warps 2..5  softmax warpgroup: thread = query row = TMEM lane.
-// Tensor memory (512 columns): O [0, 128), S / P [128, 256), band products
-// [256, 512).  P (16-bit) is written over the first half of S and feeds the
-// P.V product straight from tensor memory.
+// Tensor memory (512 columns): O [0, 128), two S / P buffers [128, 256) and
+// [256, 384), band products [256, 512) (they share columns with the second
+// S buffer, so band tiles wait for it).  Tile n uses S buffer n & 1: the
+// issuer computes S for tile n + 1 while the softmax works on tile n.  P
+// (16-bit) is written over the first half of S and feeds the P.V product
+// straight from tensor memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -24,7 +27,10 @@
 namespace df {
 namespace {
 
-constexpr uint32_t kOCol = 0, kSCol = 128, kTCol = 256;
+constexpr uint32_t kOCol = 0, kSCol0 = 128, kTCol = 256;
+
+// S / P buffer of tile `it`
+__device__ __forceinline__ uint32_t s_col(int it) { return kSCol0 + 128u * (uint32_t)(it & 1); }
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -57,7 +63,7 @@ struct FwdBars {
     uint64_t kv_full[2], kv_empty[2];
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
-    uint64_t s_full, p_full, pv_done;
+    uint64_t s_full[2], p_full, pv_done[2];
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -98,9 +104,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->band_empty, 1);
         mbar_init(&bars->t_full, 1);
         mbar_init(&bars->t_empty, 4);
-        mbar_init(&bars->s_full, 1);
+        for (int s2 = 0; s2 < 2; ++s2) {
+            mbar_init(&bars->s_full[s2], 1);
+            mbar_init(&bars->pv_done[s2], 1);
+        }
         mbar_init(&bars->p_full, 4);
-        mbar_init(&bars->pv_done, 1);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -164,57 +172,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idO = idesc_f16(128, D, BF16, false, true);
             bool ok = mbar_wait(&bars->q_full, 0, err, abort_flag);
             int band_used = 0, t_uses = 0;
-            for (int it = 0; it < ntiles && ok; ++it) {
-                const int s = it & 1, use = it >> 1;
-                const int j0 = it * BN;
-                const uint32_t sK = smem_u32(smem + S::K0 + s * S::KVB), sV = smem_u32(smem + S::V0 + s * S::KVB);
-                const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - j0);
+            int pv_cnt[2] = {0, 0};   // P.V products issued per S buffer
+            // S (and, for band tiles, the two band products) of tile m into buffer m & 1
+            auto issue_s = [&](int m) -> bool {
+                const int s = m & 1, use = m >> 1, b = m & 1;
+                const uint32_t sK = smem_u32(smem + S::K0 + s * S::KVB);
+                const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - m * BN);
                 if (!tk.uniform) {
-                    // Town = Q . Kr[band]^T
-                    if (t_uses > 0 && !(ok = mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))) break;
-                    for (int c = 0; c < G::NCH && ok; ++c) {
-                        if (!(ok = mbar_wait(&bars->band_full, band_used & 1, err, abort_flag))) break;
-                        tc_fence_after();
-                        for (int k = 0; k < G::CW / 16; ++k)
-                            tc_mma_ss(tmem + kTCol, desc_k<G>(sQ, BM, c * (G::CW / 16) + k),
-                                      desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
-                        tc_commit(&bars->band_empty);
-                        ++band_used;
+                    // the band columns overlap S buffer 1: its last P must have been consumed
+                    if (pv_cnt[1] > 0 && !mbar_wait(&bars->pv_done[1], (pv_cnt[1] - 1) & 1, err, abort_flag))
+                        return false;
+                    for (int pass = 0; pass < 2; ++pass) {
+                        if (pass == 1 && !mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag)) return false;
+                        if (t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                            return false;
+                        const uint32_t sA = pass == 0 ? sQ : sK;
+                        const int arows = pass == 0 ? BM : BN;
+                        for (int c = 0; c < G::NCH; ++c) {
+                            if (!mbar_wait(&bars->band_full, band_used & 1, err, abort_flag)) return false;
+                            tc_fence_after();
+                            for (int k = 0; k < G::CW / 16; ++k)
+                                tc_mma_ss(tmem + kTCol, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
+                                          desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
+                            tc_commit(&bars->band_empty);
+                            ++band_used;
+                        }
+                        tc_commit(&bars->t_full);
+                        ++t_uses;
                     }
-                    if (!ok) break;
-                    tc_commit(&bars->t_full);
-                    ++t_uses;
-                    // Tcross = K . Qr[band]^T (lanes = keys)
-                    if (!(ok = mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag))) break;
-                    if (!(ok = mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))) break;
-                    for (int c = 0; c < G::NCH && ok; ++c) {
-                        if (!(ok = mbar_wait(&bars->band_full, band_used & 1, err, abort_flag))) break;
-                        tc_fence_after();
-                        for (int k = 0; k < G::CW / 16; ++k)
-                            tc_mma_ss(tmem + kTCol, desc_k<G>(sK, BN, c * (G::CW / 16) + k),
-                                      desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
-                        tc_commit(&bars->band_empty);
-                        ++band_used;
-                    }
-                    if (!ok) break;
-                    tc_commit(&bars->t_full);
-                    ++t_uses;
-                } else {
-                    if (!(ok = mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag))) break;
+                } else if (!mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag)) {
+                    return false;
                 }
-                tc_fence_after();
-                // S and P share columns: the previous P.V must have consumed P.
-                if (it > 0 && !(ok = mbar_wait(&bars->pv_done, (it - 1) & 1, err, abort_flag))) break;
+                // buffer b free: its previous P consumed; buffer 1 also holds band columns
+                if (pv_cnt[b] > 0 && !mbar_wait(&bars->pv_done[b], (pv_cnt[b] - 1) & 1, err, abort_flag))
+                    return false;
+                if (b == 1 && t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                    return false;
                 tc_fence_after();
                 for (int k = 0; k < D / 16; ++k)
-                    tc_mma_ss(tmem + kSCol, desc_k<G>(sQ, BM, k), desc_k<G>(sK, BN, k), idS, k != 0);
-                tc_commit(&bars->s_full);
+                    tc_mma_ss(tmem + s_col(m), desc_k<G>(sQ, BM, k), desc_k<G>(sK, BN, k), idS, k != 0);
+                tc_commit(&bars->s_full[b]);
+                return true;
+            };
+            auto is_band = [&](int m) { return !classify<BM, BN, 1>(p, dtab, i0 - m * BN).uniform; };
+            if (ok) ok = issue_s(0);
+            for (int it = 0; it < ntiles && ok; ++it) {
+                const int s = it & 1;
+                const uint32_t sV = smem_u32(smem + S::V0 + s * S::KVB);
+                // uniform next tile: compute its S while the softmax works on this one
+                const bool next = it + 1 < ntiles;
+                const bool next_band = next && is_band(it + 1);
+                if (next && !next_band && !(ok = issue_s(it + 1))) break;
                 if (!(ok = mbar_wait(&bars->p_full, it & 1, err, abort_flag))) break;
                 tc_fence_after();
                 for (int k = 0; k < BN / 16; ++k)
-                    tc_mma_ts(tmem + kOCol, tmem + kSCol + k * 8, desc_mn<G>(sV, BN, k), idO, (it | k) != 0);
+                    tc_mma_ts(tmem + kOCol, tmem + s_col(it) + k * 8, desc_mn<G>(sV, BN, k), idO, (it | k) != 0);
                 tc_commit(&bars->kv_empty[s]);
-                tc_commit(&bars->pv_done);
+                tc_commit(&bars->pv_done[it & 1]);
+                ++pv_cnt[it & 1];
+                if (next_band && !(ok = issue_s(it + 1))) break;
             }
         }
         __syncwarp();
@@ -276,17 +292,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++t_uses;
             }
             named_bar_sync(1, 128);
-            if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
+            if (!(ok = mbar_wait_warp(&bars->s_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
             tc_fence_after();
+            const uint32_t scol = s_col(it);
             float x[BN];
+            {
+                uint32_t* xr = reinterpret_cast<uint32_t*>(x);
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tc_ld32(lane_base + kSCol + 32 * c, r);
+                for (int c = 0; c < BN / 32; ++c) tc_ld32p(lane_base + scol + 32 * c, xr + 32 * c);
                 tc_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[32 * c + e] = fmaf(__uint_as_float(r[e]), kscale, colb[32 * c + e]);
             }
+#pragma unroll
+            for (int j = 0; j < BN; ++j) x[j] = fmaf(__uint_as_float(__float_as_uint(x[j])), kscale, colb[j]);
             float rb = tk.uniform ? (tk.which ? a1 : a0) : 0.f;
             if (!row_valid) rb = -INFINITY;
             if (!tk.uniform) {
@@ -314,6 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the O accumulator is rescaled by the whole warp (tcgen05.ld / st
             // are warp-collective); rows that keep their max use alpha = 1
             if (__any_sync(0xffffffffu, need) && it > 0) {
+                // P.V of the previous tile must have landed in O first
+                if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err, abort_flag)))
+                    break;
+                tc_fence_after();
                 {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -359,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r16[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) r16[e] = pk[16 * c + e];
-                tc_st16(lane_base + kSCol + 16 * c, r16);
+                tc_st16(lane_base + scol + 16 * c, r16);
             }
             tc_wait_st();
             tc_fence_before();
@@ -367,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bars->p_full);
         }
         // ------------------------------------------------------------ epilogue
-        if (ok) ok = mbar_wait_warp(&bars->pv_done, (ntiles - 1) & 1, err, abort_flag);
+        if (ok) ok = mbar_wait_warp(&bars->pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, err, abort_flag);
         tc_fence_after();
         if (ok) {
             const bool any = row_valid && l_run > 0.f;

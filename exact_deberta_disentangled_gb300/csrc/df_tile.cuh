@@ -85,7 +85,7 @@ template <int NR, int NC, int SIGMA>
 DF_DEV void fill_dwin(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int dlo, int16_t* dwin,
                       int tid, int nthreads) {
     for (int x = tid; x < NR + NC - 1; x += nthreads) {
-        const int r = SIGMA > 0 ? base + x - (NC - 1) : base - (x - (NR - 1));
+        const int r = base + x - (SIGMA > 0 ? NC - 1 : NR - 1);
         dwin[x] = (int16_t)(dclamp(p, dtab, r) - dlo);
     }
 }

@@ -69,7 +69,7 @@ struct BwdBars {
     uint64_t c_full[2], c_empty[2];
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
-    uint64_t s_full, z_full, mma3_done;
+    uint64_t s_full, z_full, zread, mma3_done;
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->t_empty, 4);
         mbar_init(&bars->s_full, 1);
         mbar_init(&bars->z_full, 4);
+        mbar_init(&bars->zread, 4);
         mbar_init(&bars->mma3_done, 1);
         bars->abort_flag = 0;
         fence_barrier_init();
@@ -212,8 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sC1 = smem_u32(smem + S::C1 + s * S::CB), sC2 = smem_u32(smem + S::C2 + s * S::CB);
                 const int base = ROWQ ? r0 - c0 : c0 - r0;
                 const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, base);
-                // the band products and S / dP overwrite the previous tile's P / dZ operands
+                // the band products and S / dP overwrite the previous tile's P / dZ
+                // (operands of its dQ / dK / dV products, and read back for the
+                // diagonal sums)
                 if (it > 0 && !(ok = mbar_wait(&bars->mma3_done, (it - 1) & 1, err, abort_flag))) break;
+                if (it > 0 && !(ok = mbar_wait(&bars->zread, (it - 1) & 1, err, abort_flag))) break;
                 tc_fence_after();
                 if (!tk.uniform) {
                     for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -339,48 +343,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
-            int cb4[4] = {0, 0, 0, 0};
-            if (!tk.uniform)
-                for (int u = 0; u < 4; ++u) cb4[u] = bars->cross_base[u];
-            float dz[BN];
+            const bool band = !tk.uniform;
             float rowsum = 0.f;
-#pragma unroll
+            // rolled loop over 32-column chunks: S, dP -> P, dZ (and Pd for the dK/dV kernel)
+#pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t sr[32], pr[32];
                 tc_ld32(lane_base + kSCol + 32 * c, sr);
                 tc_ld32(lane_base + kPCol + 32 * c, pr);
                 tc_wait_ld();
-                uint32_t kb = 0xFFFFFFFFu;
+                uint32_t keep = 0xFFFFFFFFu;
+                if (p.dropout)
+                    keep = ROWQ ? keep_bits32_row(p, b, h, rt, c0 + 32 * c) : keep_bits32_col(p, b, h, c0 + 32 * c, rt);
+                const float* cbp = colb + 32 * c;
+                const float* clp = clse + 32 * c;
+                const float* cdp = cdl + 32 * c;
+                if (band) {
+                    const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
+                    const uint16_t* orow = own_row - own_a;
+                    const int16_t* dw = ROWQ ? dwin + row - 32 * c + BN - 1 : dwin + 32 * c - row + BM - 1;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int m = ROWQ ? dw[-e] : dw[e];
+                        sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cbp[e]) + h2f(orow[m]) +
+                                                h2f(crow[e * G::CROSS_S + m]));
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cbp[e]));
+                }
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int j = 32 * c + e;   // column within the tile
-                    float x = fmaf(__uint_as_float(sr[e]), kscale, colb[j]) + rb;
-                    if (!tk.uniform) {
-                        const int m = dwin[ROWQ ? row - j + BN - 1 : j - row + BM - 1];
-                        x += h2f(own_row[m - own_a]) + h2f(cross[j * G::CROSS_S + m - cb4[j >> 5]]);
-                    }
-                    const float lsej = ROWQ ? lse2 : clse[j];
-                    const float pr_ = ex2(x - lsej);
-                    float keep = 1.f;
-                    if (p.dropout) {
-                        if (ROWQ) {
-                            if ((e & 3) == 0) kb = keep_bits4(p, b, h, rt, (c0 + j) >> 2);
-                            keep = ((kb >> (e & 3)) & 1u) ? p.drop_scale : 0.f;
-                        } else {
-                            const uint32_t k4 = keep_bits4(p, b, h, c0 + j, rt >> 2);
-                            keep = ((k4 >> (rt & 3)) & 1u) ? p.drop_scale : 0.f;
-                        }
-                    }
-                    const float dlj = ROWQ ? dl : cdl[j];
-                    const float z = p.scale * pr_ * (__uint_as_float(pr[e]) * keep - dlj);
-                    dz[j] = z;
+                    const float lsej = ROWQ ? lse2 : clp[e];
+                    const float pr_ = ex2(__uint_as_float(sr[e]) + rb - lsej);
+                    const float kp = p.dropout ? (((keep >> e) & 1u) ? p.drop_scale : 0.f) : 1.f;
+                    const float dlj = ROWQ ? dl : cdp[e];
+                    const float z = p.scale * pr_ * (__uint_as_float(pr[e]) * kp - dlj);
                     rowsum += z;
-                    sr[e] = __float_as_uint(pr_ * keep);
+                    pr[e] = __float_as_uint(z);
+                    sr[e] = __float_as_uint(pr_ * kp);
                 }
                 uint32_t zp[16], pp[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    zp[e] = pack2<BF16>(dz[32 * c + 2 * e], dz[32 * c + 2 * e + 1]);
+                    zp[e] = pack2<BF16>(__uint_as_float(pr[2 * e]), __uint_as_float(pr[2 * e + 1]));
                     pp[e] = pack2<BF16>(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
                 }
                 tc_st16(lane_base + kPCol + 16 * c, zp);
@@ -391,47 +397,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->z_full);
             // ---- diagonal sums of dZ for this tile
-            if (tk.uniform) {
+            if (!band) {
                 if (tk.which) g_hi += rowsum; else g_lo += rowsum;
+                if (lane == 0) mbar_arrive(&bars->zread);
             } else {
                 named_bar_sync(1, 128);   // everyone finished reading own / cross
-                uint32_t* g32a = reinterpret_cast<uint32_t*>(gstage + (size_t)row * S::GBOXW);
-                uint32_t* g32b = reinterpret_cast<uint32_t*>(gstage + (size_t)(BM + row) * S::GBOXW);
+                uint16_t* g0 = gstage + (size_t)row * S::GBOXW;
+                uint16_t* g1 = gstage + (size_t)(BM + row) * S::GBOXW;
+#pragma unroll 4
                 for (int x = 0; x < S::GBOXW / 2; ++x) {
-                    g32a[x] = 0u;
-                    g32b[x] = 0u;
+                    reinterpret_cast<uint32_t*>(g0)[x] = 0u;
+                    reinterpret_cast<uint32_t*>(g1)[x] = 0u;
                 }
                 const int dlo8 = tk.dlo & ~7, off = tk.dlo - dlo8;
+                bool bad = false;
+                auto gstore = [&](int m, float v) {
+                    const int xx = m + off;
+                    bad |= xx < 0 || xx >= 2 * S::GBOXW;
+                    if (xx >= 0 && xx < S::GBOXW)
+                        g0[xx] = f2h16<BF16>(v);
+                    else if (xx >= S::GBOXW && xx < 2 * S::GBOXW)
+                        g1[xx - S::GBOXW] = f2h16<BF16>(v);
+                };
+                // runs of equal relative index along the row; dZ comes back from
+                // tensor memory (16-bit, as the dQ / dK products use it)
                 int run_m = dwin[ROWQ ? row + BN - 1 : BM - 1 - row];
                 float acc = 0.f;
-                auto flush = [&](int m, float v) {
-                    const int r = tk.dlo + m;
-                    if (r == 0) {
-                        g_lo += v;
-                    } else if (r == p.R - 1) {
-                        g_hi += v;
-                    } else {
-                        const int xx = m + off;
-                        if (xx < 0 || xx >= 2 * S::GBOXW) {
-                            raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
-                            return;
-                        }
-                        uint16_t* dst = xx < S::GBOXW ? gstage + (size_t)row * S::GBOXW + xx
-                                                      : gstage + (size_t)(BM + row) * S::GBOXW + (xx - S::GBOXW);
-                        *dst = f2h16<BF16>(v);
-                    }
-                };
+#pragma unroll 1
+                for (int c2 = 0; c2 < BN / 64; ++c2) {
+                    uint32_t zr[32];
+                    tc_ld32(lane_base + kPCol + 32 * c2, zr);
+                    tc_wait_ld();
+                    const int16_t* dw = ROWQ ? dwin + row - 64 * c2 + BN - 1 : dwin + 64 * c2 - row + BM - 1;
 #pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                    const int m = dwin[ROWQ ? row - j + BN - 1 : j - row + BM - 1];
-                    if (m != run_m) {
-                        flush(run_m, acc);
-                        run_m = m;
-                        acc = 0.f;
+                    for (int e = 0; e < 64; ++e) {
+                        const int m = ROWQ ? dw[-e] : dw[e];
+                        const float v = h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
+                        if (m != run_m) {
+                            gstore(run_m, acc);
+                            run_m = m;
+                            acc = 0.f;
+                        }
+                        acc += v;
                     }
-                    acc += dz[j];
                 }
-                flush(run_m, acc);
+                gstore(run_m, acc);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->zread);
+                if (bad) raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
+                // the clamped relative rows (far field) are summed in registers
+                if (tk.dlo == 0 && off < S::GBOXW) {
+                    g_lo += h16f<BF16>(g0[off]);
+                    g0[off] = 0;
+                }
+                if (tk.dhi == p.R - 1) {
+                    const int xx = p.R - 1 - tk.dlo + off;
+                    if (xx >= 0 && xx < S::GBOXW) {
+                        g_hi += h16f<BF16>(g0[xx]);
+                        g0[xx] = 0;
+                    } else if (xx >= S::GBOXW && xx < 2 * S::GBOXW) {
+                        g_hi += h16f<BF16>(g1[xx - S::GBOXW]);
+                        g1[xx - S::GBOXW] = 0;
+                    }
+                }
                 fence_proxy_async_smem();
                 named_bar_sync(1, 128);
                 if (tid == 0) {

@@ -288,6 +288,35 @@ DF_DEV void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
         : "memory");
 }
 
+DF_DEV void tc_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Keep bits of the 32 keys j0 .. j0+31 (j0 a multiple of 4) for query i, as
+// bits 0..31; one Philox call per 4 keys, in a rolled loop.
+DF_DEV uint32_t keep_bits32_row(const ProblemDev& p, int b, int h, int i, int j0) {
+    uint32_t k = 0;
+#pragma unroll 1
+    for (int q = 0; q < 8; ++q) k |= keep_bits4(p, b, h, i, (j0 >> 2) + q) << (4 * q);
+    return k;
+}
+
+// Keep bits of the 32 queries i0 .. i0+31 for key j, as bits 0..31 (one
+// Philox call per query).
+DF_DEV uint32_t keep_bits32_col(const ProblemDev& p, int b, int h, int i0, int j) {
+    uint32_t k = 0;
+#pragma unroll 1
+    for (int q = 0; q < 32; ++q) k |= ((keep_bits4(p, b, h, i0 + q, j >> 2) >> (j & 3)) & 1u) << q;
+    return k;
+}
+
 // Pack two fp32 into one 32-bit word of 16-bit values: `lo` in bits 0..15.
 template <bool BF16>
 DF_DEV uint32_t pack2(float lo, float hi) {

@@ -295,29 +295,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait_warp(&bars->s_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
             tc_fence_after();
             const uint32_t scol = s_col(it);
-            float x[BN];
-            {
-                uint32_t* xr = reinterpret_cast<uint32_t*>(x);
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) tc_ld32p(lane_base + scol + 32 * c, xr + 32 * c);
-                tc_wait_ld();
-            }
-#pragma unroll
-            for (int j = 0; j < BN; ++j) x[j] = fmaf(__uint_as_float(__float_as_uint(x[j])), kscale, colb[j]);
             float rb = tk.uniform ? (tk.which ? a1 : a0) : 0.f;
             if (!row_valid) rb = -INFINITY;
-            if (!tk.uniform) {
-                const int cb[4] = {bars->cross_base[0], bars->cross_base[1], bars->cross_base[2],
-                                   bars->cross_base[3]};
+            const bool band = !tk.uniform;
+            // pass 1: biased logits (band tiles write them back over S) and the tile max
+            float tmax = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tc_ld32(lane_base + scol + 32 * c, r);
+                tc_wait_ld();
+                const float* cbp = colb + 32 * c;
+                if (band) {
+                    const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
+                    const int16_t* dw = dwin + row - 32 * c + BN - 1;
+                    const uint16_t* orow = own_row - own_a;
 #pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                    const int m = dwin[row - j + BN - 1];
-                    x[j] += h2f(own_row[m - own_a]) + h2f(cross[j * G::CROSS_S + m - cb[j >> 5]]);
+                    for (int e = 0; e < 32; ++e) {
+                        const int m = dw[-e];
+                        const float x = fmaf(__uint_as_float(r[e]), kscale, cbp[e]) + h2f(orow[m]) +
+                                        h2f(crow[e * G::CROSS_S + m]);
+                        tmax = fmaxf(tmax, x);
+                        r[e] = __float_as_uint(x);
+                    }
+                    tc_st32(lane_base + scol + 32 * c, r);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, fmaf(__uint_as_float(r[e]), kscale, cbp[e]));
                 }
             }
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < BN; ++j) tmax = fmaxf(tmax, x[j]);
+            if (band) tc_wait_st();
             tmax += rb;
             // online softmax in base-2 units; the max is only moved when it
             // grows by more than kRescaleSlack
@@ -352,36 +359,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // pass 2: probabilities, written as 16-bit P over the first half of S
             const float mm = m_run - rb;
+            const bool dead = m_run == -INFINITY || rb == -INFINITY;
             float sum = 0.f;
-            uint32_t pk[BN / 2];
-            if (m_run == -INFINITY || rb == -INFINITY) {
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tc_ld32(lane_base + scol + 32 * c, r);
+                tc_wait_ld();
+                const uint32_t keep = p.dropout ? keep_bits32_row(p, b, h, i, j0 + 32 * c) : 0xFFFFFFFFu;
+                const float* cbp = colb + 32 * c;
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < BN / 2; ++e) pk[e] = 0u;
-            } else {
-                uint32_t kb = 0xFFFFFFFFu;
-#pragma unroll
-                for (int e = 0; e < BN / 2; ++e) {
-                    const float p0 = ex2(x[2 * e] - mm), p1 = ex2(x[2 * e + 1] - mm);
+                for (int e = 0; e < 16; ++e) {
+                    const float x0 = band ? __uint_as_float(r[2 * e]) : fmaf(__uint_as_float(r[2 * e]), kscale, cbp[2 * e]);
+                    const float x1 =
+                        band ? __uint_as_float(r[2 * e + 1]) : fmaf(__uint_as_float(r[2 * e + 1]), kscale, cbp[2 * e + 1]);
+                    const float p0 = dead ? 0.f : ex2(x0 - mm), p1 = dead ? 0.f : ex2(x1 - mm);
                     sum += p0 + p1;
                     float d0 = p0, d1 = p1;
                     if (p.dropout) {
-                        if ((e & 1) == 0) kb = keep_bits4(p, b, h, i, (j0 + 2 * e) >> 2);
-                        const int sh = (2 * e) & 3;
-                        d0 = ((kb >> sh) & 1u) ? p0 * p.drop_scale : 0.f;
-                        d1 = ((kb >> (sh + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
+                        d0 = ((keep >> (2 * e)) & 1u) ? p0 * p.drop_scale : 0.f;
+                        d1 = ((keep >> (2 * e + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
                     }
                     pk[e] = pack2<BF16>(d0, d1);
                 }
+                tc_st16(lane_base + scol + 16 * c, pk);
             }
             l_run += sum;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r16[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) r16[e] = pk[16 * c + e];
-                tc_st16(lane_base + scol + 16 * c, r16);
-            }
             tc_wait_st();
             tc_fence_before();
             __syncwarp();

@@ -24,7 +24,7 @@ DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 
 EXPORTS = ["df_attn_workspace_size", "df_attn_fwd", "df_attn_bwd", "df_attn_step_host_arena_size",
            "df_attn_step_host", "df_rel_index_table", "df_get_device_error", "df_status_string", "df_version",
-           "df_attn_set_profile_events"]
+           "df_attn_set_profile_events", "df_attn_fwd_noalloc"]
 
 
 class DfError(RuntimeError):
@@ -82,6 +82,8 @@ def load():
             lib.df_status_string.restype = ctypes.c_char_p
             lib.df_status_string.argtypes = [ctypes.c_int]
             lib.df_version.restype = ctypes.c_char_p
+            lib.df_attn_fwd_noalloc.restype = ctypes.c_int
+            lib.df_attn_fwd_noalloc.argtypes = [P] + [vp] * 7 + [vp]
             lib.df_attn_set_profile_events.restype = ctypes.c_int
             lib.df_attn_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
             _lib = lib
@@ -242,3 +244,14 @@ def set_profile_events(events):
         rc = lib.df_attn_set_profile_events(arr, len(events))
     if rc != DF_OK:
         raise DfError(rc, "df_attn_set_profile_events")
+
+
+def attn_fwd_noalloc(g: Geometry, q, k, v, qr, kr, out, lse, stream=None, check=True):
+    """Forward through df_attn_fwd_noalloc (no workspace: the library's
+    static device scratch); the caller passes the outputs."""
+    p = g.params(q.dtype)
+    rc = load().df_attn_fwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(out),
+                                    _ptr(lse), _stream(stream))
+    if check and rc != DF_OK:
+        raise DfError(rc, "df_attn_fwd_noalloc")
+    return rc

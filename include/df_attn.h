@@ -159,6 +159,28 @@ df_status df_attn_step_host(const df_attn_params *p, const void *q, const void *
                             void *dqr, void *dkr, void *device_arena, size_t arena_bytes, df_stream_t stream);
 
 /*
+ * Forward that allocates nothing (the paper has no counterpart; this is a
+ * deployment convenience).  For callers that cannot allocate device memory
+ * -- code inside a host framework that owns all device memory (a plugin or
+ * custom operator whose allocator it may not grow), or latency-critical
+ * loops where cudaMalloc's implicit synchronisation is not acceptable.  Same
+ * arguments and results as df_attn_fwd minus the workspace: the scratch lives
+ * in a file-scope device array of 8 MiB that every GPU loading this library
+ * holds until the process exits.  The caller still passes inputs and outputs.
+ *   - Limit: df_attn_workspace_size(p, 0) <= 8 MiB, i.e. about
+ *     16 * total_tokens * H + 8 * L bytes (e.g. 16,384 tokens x 24 heads);
+ *     larger problems return DF_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race and give undefined results; serialise them.
+ *   - Device-side errors (inconsistent cu_seqlens, a give-up) are not
+ *     reported by this entry point; outputs of such a call are unspecified.
+ */
+df_status df_attn_fwd_noalloc(const df_attn_params *p, const void *q, const void *k, const void *v,
+                              const void *qr, const void *kr, void *out, float *lse, df_stream_t stream);
+
+/*
  * The relative-position index table delta(r) for r = -(L-1) .. L-1, written
  * as int32 to out_dev[r + L - 1] (device, 2L - 1 entries), computed on the
  * device exactly as the attention kernels use it.  For bit-exact checks.

@@ -36,7 +36,7 @@ namespace df {
 namespace {
 
 constexpr uint32_t kAcc1 = 0, kAcc2 = 128, kSCol = 256, kPCol = 384, kTCol = 256;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -59,7 +59,8 @@ struct BwdSmem {
     static constexpr int STGB = (CROSS - STG) + CROSSB > GSB ? (CROSS - STG) + CROSSB : GSB;
     static constexpr int DWIN = (STG + STGB + 15) / 16 * 16;
     static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // colb, clse, cdl
-    static constexpr int MISC = COLV + 3 * G::BN * 4;
+    static constexpr int XCH = COLV + 3 * G::BN * 4;       // [4][BM] floats: the far-field sums of the two halves
+    static constexpr int MISC = XCH + 4 * G::BM * 4;
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;
 };
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* colb = reinterpret_cast<float*>(smem + S::COLV);
     float* clse = colb + BN;
     float* cdl = clse + BN;
+    float* xch = reinterpret_cast<float*>(smem + S::XCH);
     uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::STG);
     uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
     uint16_t* gstage = reinterpret_cast<uint16_t*>(smem + S::STG);
@@ -140,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->t_full, 1);
         mbar_init(&bars->t_empty, 4);
         mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->z_full, 4);
-        mbar_init(&bars->zread, 4);
+        mbar_init(&bars->z_full, 8);
+        mbar_init(&bars->zread, 8);
         mbar_init(&bars->mma3_done, 1);
         bars->abort_flag = 0;
         fence_barrier_init();
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
             constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
             constexpr uint32_t idA = idesc_f16(128, D, BF16, false, true);
+            constexpr uint32_t kHOff = BN / 4;   // 16-bit dZ / Pd start a quarter into their buffers
             bool ok = mbar_wait(&bars->row_full, 0, err, abort_flag);
             int band_used = 0, t_uses = 0;
             for (int it = 0; it < ntiles && ok; ++it) {
@@ -255,10 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int k = 0; k < BN / 16; ++k) {
                     // acc1 += dZ . C1   (dQ += dZ K  |  dK += dZ^T Q)
-                    tc_mma_ts(tmem + kAcc1, tmem + kPCol + k * 8, desc_mn<G>(sC1, BN, k), idA, (it | k) != 0);
+                    tc_mma_ts(tmem + kAcc1, tmem + kPCol + kHOff + k * 8, desc_mn<G>(sC1, BN, k), idA,
+                              (it | k) != 0);
                     // dV += Pd^T dO
                     if (!ROWQ)
-                        tc_mma_ts(tmem + kAcc2, tmem + kSCol + k * 8, desc_mn<G>(sC2, BN, k), idA, (it | k) != 0);
+                        tc_mma_ts(tmem + kAcc2, tmem + kSCol + kHOff + k * 8, desc_mn<G>(sC2, BN, k), idA,
+                                  (it | k) != 0);
                 }
                 tc_commit(&bars->c_empty[s]);
                 tc_commit(&bars->mma3_done);
@@ -266,11 +271,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax / gradient warpgroup
+        // ------------------------------------------------------------ softmax / gradient warps
+        // Eight warps: warp w owns TMEM lanes 32 (w & 3) .. +31 (rows) and
+        // column half hf = (w - 2) / 4 of every tile.  The first-half warps
+        // copy the band windows and form the diagonal sums of band tiles;
+        // every warp takes the same bounded waits.
         const int w4 = warp & 3;
+        const int hf = (warp - 2) >> 2;
         const int row = 32 * w4 + lane;
-        const int tid = threadIdx.x - 64;
+        const int tid = threadIdx.x - 64;     // 0..255
+        const int pair_bar = 2 + w4;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
+        constexpr int NCT = BN / 64;          // 32-column chunks per thread
+        const int cbeg = hf * NCT;
+        // 16-bit dZ / Pd of chunk c go to TMEM columns BN/4 + 16 c of the dP / S
+        // buffers: inside the columns this warp has already read, because the
+        // first half walks its chunks backwards and the second half forwards
+        constexpr uint32_t kHOff = BN / 4;
         const int rt = r0 + row;              // row token position in the sequence
         const bool row_in = rt < n;
         const size_t T = (size_t)p.T;
@@ -290,98 +307,151 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         const bool rvalid = rb0 != -INFINITY;
-        float g_lo = 0.f, g_hi = 0.f;     // diagonal sums at delta 0 and R-1
+        float g_lo = 0.f, g_hi = 0.f;     // this thread's share of the diagonal sums at delta 0 and R-1
         int t_uses = 0;
         bool ok = true;
         uint16_t* own_row = own + row * G::OWN_S;
+        // per-column terms of a tile, fetched one tile ahead:
+        //   cv0 = column bias (P2C of keys / C2P of queries in uniform tiles,
+        //         0 in band tiles, -inf for masked or missing columns), minus the
+        //         column's LSE (base 2) when the columns are queries;
+        //   cv1 = c * Dl of the column (dK/dV kernel only)
+        auto colterms = [&](int ct_tile, const TileKind& k, float& v0, float& v1) {
+            v0 = -INFINITY;
+            v1 = 0.f;
+            const int ct = ct_tile * BN + tid;
+            if (tid >= BN || ct >= n) return;
+            const bool cvalid = ROWQ ? (!p.kmask || p.kmask[t0 + ct]) : (!p.qmask || p.qmask[t0 + ct]);
+            if (!cvalid) return;
+            float cb = k.uniform ? relb_h[((ROWQ ? 2 : 0) + k.which) * T + t0 + ct] : 0.f;
+            if (!ROWQ) {
+                cb -= lse[lse_index(p, b, h, t0, ct)] * kLog2e;
+                v1 = p.scale * rowterm[lse_index(p, b, h, t0, ct)];
+            }
+            v0 = cb;
+        };
+        TileKind tk_next = classify<BM, BN, SIGMA>(p, dtab, ROWQ ? r0 : -r0);
+        float cv0_next, cv1_next;
+        colterms(0, tk_next, cv0_next, cv1_next);
         for (int it = 0; it < ntiles && ok; ++it) {
             const int c0 = it * BN;
             const int base = ROWQ ? r0 - c0 : c0 - r0;
-            const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, base);
+            const TileKind tk = tk_next;
+            const float cv0 = cv0_next, cv1 = cv1_next;
             if (tid == 0) bulk_wait_read0();   // the previous G box left shared memory
-            named_bar_sync(1, 128);
+            named_bar_sync(1, 256);
             if (tid < BN) {
-                const int ct = c0 + tid;
-                float cb = -INFINITY, cl = INFINITY, cd = 0.f;
-                if (ct < n) {
-                    const bool cvalid = ROWQ ? (!p.kmask || p.kmask[t0 + ct]) : (!p.qmask || p.qmask[t0 + ct]);
-                    if (cvalid) cb = tk.uniform ? relb_h[((ROWQ ? 2 : 0) + tk.which) * T + t0 + ct] : 0.f;
-                    if (!ROWQ) {
-                        cl = lse[lse_index(p, b, h, t0, ct)] * kLog2e;
-                        cd = rowterm[lse_index(p, b, h, t0, ct)];
-                    }
-                }
-                colb[tid] = cb;
-                clse[tid] = cl;
-                cdl[tid] = cd;
+                colb[tid] = cv0;
+                cdl[tid] = cv1;
+            }
+            if (it + 1 < ntiles) {
+                const int nb2 = ROWQ ? r0 - c0 - BN : c0 + BN - r0;
+                tk_next = classify<BM, BN, SIGMA>(p, dtab, nb2);
+                colterms(it + 1, tk_next, cv0_next, cv1_next);
             }
             int own_a = 0;
             if (!tk.uniform) {
-                fill_dwin<BM, BN, SIGMA>(p, dtab, base, tk.dlo, dwin, tid, 128);
+                fill_dwin<BM, BN, SIGMA>(p, dtab, base, tk.dlo, dwin, tid, 256);
                 int lo, hi;
-                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
-                tc_fence_after();
                 own_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
-                own_a = copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
-                ++t_uses;
+                own_a = lo & ~15;
                 if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
-                tc_fence_after();
-                if (32 * w4 < BN) {
-                    cross_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
-                    const int ca = copy_band_window(lane_base + kTCol, lo, hi, cross + row * G::CROSS_S, kscale);
-                    if (lane == 0) bars->cross_base[w4] = ca;
+                if (hf == 0) {
+                    tc_fence_after();
+                    copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->t_empty);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
-                ++t_uses;
+                if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
+                if (hf == 0) {
+                    tc_fence_after();
+                    if (32 * w4 < BN) {
+                        cross_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
+                        const int ca = copy_band_window(lane_base + kTCol, lo, hi, cross + row * G::CROSS_S, kscale);
+                        if (lane == 0) bars->cross_base[w4] = ca;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->t_empty);
+                }
+                t_uses += 2;
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(1, 256);
             if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
             const bool band = !tk.uniform;
-            float rowsum = 0.f;
-            // rolled loop over 32-column chunks: S, dP -> P, dZ (and Pd for the dK/dV kernel)
+            // per-row constant of the exponent (base 2): row bias, minus the row LSE for query rows
+            const float rowc = ROWQ ? rb - lse2 : rb;
+            const float dls_row = p.scale * dl;
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
+            // this thread's 32-column chunks: S, dP -> P, dZ (and Pd for the dK/dV kernel)
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int cc = 0; cc < NCT; ++cc) {
+                const int c = hf ? cbeg + cc : cbeg + NCT - 1 - cc;
                 uint32_t sr[32], pr[32];
                 tc_ld32(lane_base + kSCol + 32 * c, sr);
                 tc_ld32(lane_base + kPCol + 32 * c, pr);
                 tc_wait_ld();
-                uint32_t keep = 0xFFFFFFFFu;
-                if (p.dropout)
-                    keep = ROWQ ? keep_bits32_row(p, b, h, rt, c0 + 32 * c) : keep_bits32_col(p, b, h, c0 + 32 * c, rt);
-                const float* cbp = colb + 32 * c;
-                const float* clp = clse + 32 * c;
-                const float* cdp = cdl + 32 * c;
+                const float4* cv0p = reinterpret_cast<const float4*>(colb + 32 * c);
                 if (band) {
                     const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
                     const uint16_t* orow = own_row - own_a;
                     const int16_t* dw = ROWQ ? dwin + row - 32 * c + BN - 1 : dwin + 32 * c - row + BM - 1;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int m = ROWQ ? dw[-e] : dw[e];
-                        sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cbp[e]) + h2f(orow[m]) +
-                                                h2f(crow[e * G::CROSS_S + m]));
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 cv = cv0p[q];
+                        const float cvs[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int e = 4 * q + t;
+                            const int m = ROWQ ? dw[-e] : dw[e];
+                            sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cvs[t]) + rowc +
+                                                    (h2f(orow[m]) + h2f(crow[e * G::CROSS_S + m])));
+                        }
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cbp[e]));
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 cv = cv0p[q];
+                        sr[4 * q + 0] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 0]), kscale, cv.x) + rowc);
+                        sr[4 * q + 1] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 1]), kscale, cv.y) + rowc);
+                        sr[4 * q + 2] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 2]), kscale, cv.z) + rowc);
+                        sr[4 * q + 3] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 3]), kscale, cv.w) + rowc);
+                    }
                 }
+                const uint32_t keep = !p.dropout ? 0xFFFFFFFFu
+                                      : ROWQ     ? keep_bits32_row(p, b, h, rt, c0 + 32 * c)
+                                                 : keep_bits32_col(p, b, h, c0 + 32 * c, rt);
+                const float4* cv1p = reinterpret_cast<const float4*>(cdl + 32 * c);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float lsej = ROWQ ? lse2 : clp[e];
-                    const float pr_ = ex2(__uint_as_float(sr[e]) + rb - lsej);
-                    const float kp = p.dropout ? (((keep >> e) & 1u) ? p.drop_scale : 0.f) : 1.f;
-                    const float dlj = ROWQ ? dl : cdp[e];
-                    const float z = p.scale * pr_ * (__uint_as_float(pr[e]) * kp - dlj);
-                    rowsum += z;
-                    pr[e] = __float_as_uint(z);
-                    sr[e] = __float_as_uint(pr_ * kp);
+                for (int q = 0; q < 8; ++q) {
+                    float dlq[4] = {dls_row, dls_row, dls_row, dls_row};
+                    if (!ROWQ) {
+                        const float4 d4 = cv1p[q];
+                        dlq[0] = d4.x;
+                        dlq[1] = d4.y;
+                        dlq[2] = d4.z;
+                        dlq[3] = d4.w;
+                    }
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int e = 4 * q + t;
+                        const float pr_ = ex2(__uint_as_float(sr[e]));
+                        float z, pd;
+                        if (p.dropout) {
+                            const float kp = ((keep >> e) & 1u) ? p.drop_scale : 0.f;
+                            z = pr_ * fmaf(__uint_as_float(pr[e]), p.scale * kp, -dlq[t]);
+                            pd = pr_ * kp;
+                        } else {
+                            z = pr_ * fmaf(__uint_as_float(pr[e]), p.scale, -dlq[t]);
+                            pd = pr_;
+                        }
+                        rs[t] += z;
+                        pr[e] = __float_as_uint(z);
+                        sr[e] = __float_as_uint(pd);
+                    }
                 }
                 uint32_t zp[16], pp[16];
 #pragma unroll
@@ -389,9 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     zp[e] = pack2<BF16>(__uint_as_float(pr[2 * e]), __uint_as_float(pr[2 * e + 1]));
                     pp[e] = pack2<BF16>(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
                 }
-                tc_st16(lane_base + kPCol + 16 * c, zp);
-                if (!ROWQ) tc_st16(lane_base + kSCol + 16 * c, pp);
+                tc_st16(lane_base + kPCol + kHOff + 16 * c, zp);
+                if (!ROWQ) tc_st16(lane_base + kSCol + kHOff + 16 * c, pp);
             }
+            const float rowsum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -401,70 +472,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (tk.which) g_hi += rowsum; else g_lo += rowsum;
                 if (lane == 0) mbar_arrive(&bars->zread);
             } else {
-                named_bar_sync(1, 128);   // everyone finished reading own / cross
-                uint16_t* g0 = gstage + (size_t)row * S::GBOXW;
-                uint16_t* g1 = gstage + (size_t)(BM + row) * S::GBOXW;
+                named_bar_sync(1, 256);   // own / cross no longer read; every dZ is in tensor memory
+                tc_fence_after();
+                if (hf == 0) {
+                    uint16_t* g0 = gstage + (size_t)row * S::GBOXW;
+                    uint16_t* g1 = gstage + (size_t)(BM + row) * S::GBOXW;
 #pragma unroll 4
-                for (int x = 0; x < S::GBOXW / 2; ++x) {
-                    reinterpret_cast<uint32_t*>(g0)[x] = 0u;
-                    reinterpret_cast<uint32_t*>(g1)[x] = 0u;
-                }
-                const int dlo8 = tk.dlo & ~7, off = tk.dlo - dlo8;
-                bool bad = false;
-                auto gstore = [&](int m, float v) {
-                    const int xx = m + off;
-                    bad |= xx < 0 || xx >= 2 * S::GBOXW;
-                    if (xx >= 0 && xx < S::GBOXW)
-                        g0[xx] = f2h16<BF16>(v);
-                    else if (xx >= S::GBOXW && xx < 2 * S::GBOXW)
-                        g1[xx - S::GBOXW] = f2h16<BF16>(v);
-                };
-                // runs of equal relative index along the row; dZ comes back from
-                // tensor memory (16-bit, as the dQ / dK products use it)
-                int run_m = dwin[ROWQ ? row + BN - 1 : BM - 1 - row];
-                float acc = 0.f;
-#pragma unroll 1
-                for (int c2 = 0; c2 < BN / 64; ++c2) {
-                    uint32_t zr[32];
-                    tc_ld32(lane_base + kPCol + 32 * c2, zr);
-                    tc_wait_ld();
-                    const int16_t* dw = ROWQ ? dwin + row - 64 * c2 + BN - 1 : dwin + 64 * c2 - row + BM - 1;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        const int m = ROWQ ? dw[-e] : dw[e];
-                        const float v = h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
-                        if (m != run_m) {
-                            gstore(run_m, acc);
-                            run_m = m;
-                            acc = 0.f;
-                        }
-                        acc += v;
+                    for (int x = 0; x < S::GBOXW / 2; ++x) {
+                        reinterpret_cast<uint32_t*>(g0)[x] = 0u;
+                        reinterpret_cast<uint32_t*>(g1)[x] = 0u;
                     }
+                    const int dlo8 = tk.dlo & ~7, off = tk.dlo - dlo8;
+                    bool bad = false;
+                    auto gstore = [&](int m, float v) {
+                        const int xx = m + off;
+                        bad |= xx < 0 || xx >= 2 * S::GBOXW;
+                        if (xx >= 0 && xx < S::GBOXW)
+                            g0[xx] = f2h16<BF16>(v);
+                        else if (xx >= S::GBOXW && xx < 2 * S::GBOXW)
+                            g1[xx - S::GBOXW] = f2h16<BF16>(v);
+                    };
+                    // runs of equal relative index along the row; dZ comes back from
+                    // tensor memory (16-bit, as the dQ / dK products use it)
+                    int run_m = dwin[ROWQ ? row + BN - 1 : BM - 1 - row];
+                    float acc = 0.f;
+#pragma unroll 1
+                    for (int c2 = 0; c2 < BN / 64; ++c2) {
+                        uint32_t zr[32];
+                        tc_ld32(lane_base + kPCol + kHOff + 32 * c2, zr);
+                        tc_wait_ld();
+                        const int16_t* dw = ROWQ ? dwin + row - 64 * c2 + BN - 1 : dwin + 64 * c2 - row + BM - 1;
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) {
+                            const int m = ROWQ ? dw[-e] : dw[e];
+                            const float v = h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
+                            if (m != run_m) {
+                                gstore(run_m, acc);
+                                run_m = m;
+                                acc = 0.f;
+                            }
+                            acc += v;
+                        }
+                    }
+                    gstore(run_m, acc);
+                    if (bad) raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
+                    // the clamped relative rows (far field) are summed in registers
+                    if (tk.dlo == 0 && off < S::GBOXW) {
+                        g_lo += h16f<BF16>(g0[off]);
+                        g0[off] = 0;
+                    }
+                    if (tk.dhi == p.R - 1) {
+                        const int xx = p.R - 1 - tk.dlo + off;
+                        if (xx >= 0 && xx < S::GBOXW) {
+                            g_hi += h16f<BF16>(g0[xx]);
+                            g0[xx] = 0;
+                        } else if (xx >= S::GBOXW && xx < 2 * S::GBOXW) {
+                            g_hi += h16f<BF16>(g1[xx - S::GBOXW]);
+                            g1[xx - S::GBOXW] = 0;
+                        }
+                    }
+                    fence_proxy_async_smem();
                 }
-                gstore(run_m, acc);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->zread);
-                if (bad) raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
-                // the clamped relative rows (far field) are summed in registers
-                if (tk.dlo == 0 && off < S::GBOXW) {
-                    g_lo += h16f<BF16>(g0[off]);
-                    g0[off] = 0;
-                }
-                if (tk.dhi == p.R - 1) {
-                    const int xx = p.R - 1 - tk.dlo + off;
-                    if (xx >= 0 && xx < S::GBOXW) {
-                        g_hi += h16f<BF16>(g0[xx]);
-                        g0[xx] = 0;
-                    } else if (xx >= S::GBOXW && xx < 2 * S::GBOXW) {
-                        g_hi += h16f<BF16>(g1[xx - S::GBOXW]);
-                        g1[xx - S::GBOXW] = 0;
-                    }
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
+                named_bar_sync(1, 256);
                 if (tid == 0) {
-                    const int x0 = h * Rp + dlo8;
+                    const int x0 = h * Rp + (tk.dlo & ~7);
                     tma_reduce_add_2d(&tmG, gstage, x0, t0 + r0);
                     tma_reduce_add_2d(&tmG, gstage + (size_t)BM * S::GBOXW, x0 + S::GBOXW, t0 + r0);
                     bulk_commit();
@@ -476,31 +550,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = mbar_wait_warp(&bars->mma3_done, (ntiles - 1) & 1, err, abort_flag);
         tc_fence_after();
         if (ok) {
-            float* a1 = acc1_out + ((size_t)(t0 + rt) * p.H + h) * D;
+            // accumulator columns [hf D/2, (hf+1) D/2), 16 at a time
+            float* a1 = acc1_out + ((size_t)(t0 + rt) * p.H + h) * D + hf * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tc_ld32(lane_base + kAcc1 + 32 * c, r);
+                uint32_t r[16];
+                tc_ld16(lane_base + kAcc1 + hf * (D / 2) + 16 * c, r);
                 tc_wait_ld();
                 if (row_in) {
-                    float4* dst = reinterpret_cast<float4*>(a1 + 32 * c);
+                    float4* dst = reinterpret_cast<float4*>(a1 + 16 * c);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
+                    for (int v = 0; v < 4; ++v)
                         dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
                 }
             }
             if (!ROWQ) {
-                T16* a2 = reinterpret_cast<T16*>(acc2_out) + ((size_t)(t0 + rt) * p.H + h) * D;
+                T16* a2 = reinterpret_cast<T16*>(acc2_out) + ((size_t)(t0 + rt) * p.H + h) * D + hf * (D / 2);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tc_ld32(lane_base + kAcc2 + 32 * c, r);
+                    uint32_t r[16];
+                    tc_ld16(lane_base + kAcc2 + hf * (D / 2) + 16 * c, r);
                     tc_wait_ld();
                     if (row_in) {
-                        uint4* dst = reinterpret_cast<uint4*>(a2 + 32 * c);
+                        uint4* dst = reinterpret_cast<uint4*>(a2 + 16 * c);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
+                        for (int v = 0; v < 2; ++v) {
                             uint4 w;
                             w.x = pack2<BF16>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
                             w.y = pack2<BF16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
@@ -511,12 +586,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // the far-field diagonal sums; concurrent box additions to these
-            // two entries only ever add zero
-            if (row_in) {
+            // the far-field diagonal sums: the two halves' shares, added once;
+            // concurrent box additions to these two entries only ever add zero
+            xch[hf * BM + row] = g_lo;
+            xch[2 * BM + hf * BM + row] = g_hi;
+            named_bar_sync(pair_bar, 64);
+            if (row_in && hf == 0) {
+                const float glo = xch[row] + xch[BM + row];
+                const float ghi = xch[2 * BM + row] + xch[3 * BM + row];
                 uint16_t* grow = reinterpret_cast<uint16_t*>(Gbuf) + ((size_t)(t0 + rt) * p.H + h) * Rp;
-                if (g_lo != 0.f) grow[0] = f2h16<BF16>(h16f<BF16>(grow[0]) + g_lo);
-                if (g_hi != 0.f) grow[p.R - 1] = f2h16<BF16>(h16f<BF16>(grow[p.R - 1]) + g_hi);
+                if (glo != 0.f) grow[0] = f2h16<BF16>(h16f<BF16>(grow[0]) + glo);
+                if (ghi != 0.f) grow[p.R - 1] = f2h16<BF16>(h16f<BF16>(grow[p.R - 1]) + ghi);
             }
         }
     }

@@ -123,14 +123,18 @@ DF_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
                  : "memory");
 }
 
+// One bounded probe of an mbarrier phase.  The suspend-time hint lets the
+// waiting thread sleep (instead of re-issuing the probe) until the phase
+// completes or about 20 us have passed, leaving issue slots to the warps that
+// share its SM sub-partition.
 DF_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
         : "memory");
     return ok != 0;
 }
@@ -145,7 +149,7 @@ DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err_word, volatile in
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if ((it & 7u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 raise_error(err_word, DF_ERR_TIMEOUT);

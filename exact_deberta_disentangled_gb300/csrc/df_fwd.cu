@@ -6,17 +6,21 @@
 // ("DisentangledFlash", section "Hugging Face usage": an LSE-producing
 // forward; section "Status": the [B, H, L, L] matrix is never stored).
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer: Q once, K/V tiles into a 2-stage ring, and for
 //               band tiles the Kr / Qr band rows.
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.
-//   warps 2..5  softmax warpgroup: thread = query row = TMEM lane.
+//   warps 2..9  softmax: a thread owns one query row (= TMEM lane) and one
+//               half of the columns of every key tile.
 // Tensor memory (512 columns): O [0, 128), two S / P buffers [128, 256) and
 // [256, 384), band products [256, 512) (they share columns with the second
 // S buffer, so band tiles wait for it).  Tile n uses S buffer n & 1: the
 // issuer computes S for tile n + 1 while the softmax works on tile n.  P
-// (16-bit) is written over the first half of S and feeds the P.V product
-// straight from tensor memory.
+// (16-bit) is written over the middle half of S, columns [BN/4, 3 BN/4),
+// and feeds the P.V product straight from tensor memory.  Each column half of
+// a row is owned by one warp; P of that half lands inside the S columns the
+// same warp has already read (the first half walks its chunks backwards), so
+// the two warps of a row never overwrite each other's unread logits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -31,7 +35,7 @@ constexpr uint32_t kOCol = 0, kSCol0 = 128, kTCol = 256;
 
 // S / P buffer of tile `it`
 __device__ __forceinline__ uint32_t s_col(int it) { return kSCol0 + 128u * (uint32_t)(it & 1); }
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;   // keep a stale max while the new one exceeds it by <= 8 (2^8 headroom)
@@ -53,7 +57,8 @@ struct FwdSmem {
     static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
     static constexpr int DWIN = CROSS + CROSSB;
     static constexpr int COLB = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;
-    static constexpr int MISC = COLB + G::BN * 4;
+    static constexpr int XCH = COLB + G::BN * 4;          // [4][BM] floats: partial maxima, partial sums
+    static constexpr int MISC = XCH + 4 * G::BM * 4;
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
 };
@@ -83,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     FwdBars* bars = reinterpret_cast<FwdBars*>(smem + S::MISC);
     int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
     float* colb = reinterpret_cast<float*>(smem + S::COLB);
+    float* xch = reinterpret_cast<float*>(smem + S::XCH);
     uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::OWN);
     uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
 
@@ -108,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->s_full[s2], 1);
             mbar_init(&bars->pv_done[s2], 1);
         }
-        mbar_init(&bars->p_full, 4);
+        mbar_init(&bars->p_full, 8);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -170,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
             constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
             constexpr uint32_t idO = idesc_f16(128, D, BF16, false, true);
+            constexpr uint32_t kPOff = BN / 4;   // P starts a quarter into its S buffer
             bool ok = mbar_wait(&bars->q_full, 0, err, abort_flag);
             int band_used = 0, t_uses = 0;
             int pv_cnt[2] = {0, 0};   // P.V products issued per S buffer
@@ -226,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait(&bars->p_full, it & 1, err, abort_flag))) break;
                 tc_fence_after();
                 for (int k = 0; k < BN / 16; ++k)
-                    tc_mma_ts(tmem + kOCol, tmem + s_col(it) + k * 8, desc_mn<G>(sV, BN, k), idO, (it | k) != 0);
+                    tc_mma_ts(tmem + kOCol, tmem + s_col(it) + kPOff + k * 8, desc_mn<G>(sV, BN, k), idO,
+                              (it | k) != 0);
                 tc_commit(&bars->kv_empty[s]);
                 tc_commit(&bars->pv_done[it & 1]);
                 ++pv_cnt[it & 1];
@@ -236,10 +244,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
+        // Eight warps: warp w owns TMEM lanes 32 (w & 3) .. +31 (query rows)
+        // and column half hf = (w - 2) / 4 of every key tile, so two warps
+        // share each SM sub-partition.  The two threads of a row exchange
+        // their partial maxima (per tile) and sums (at the end) through shared
+        // memory, synchronised by a 64-thread barrier per lane quarter.
         const int w4 = warp & 3;
+        const int hf = (warp - 2) >> 2;
         const int row = 32 * w4 + lane;           // query row in the tile == TMEM lane
-        const int tid = threadIdx.x - 64;         // 0..127
+        const int tid = threadIdx.x - 64;         // 0..255
+        const int pair_bar = 2 + w4;              // named barrier of this row's two warps
         const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
+        constexpr int NCT = BN / 64;              // 32-column chunks per thread
+        const int cbeg = hf * NCT;
+        // chunk order: backwards in the first half, so that the 16-bit result of
+        // chunk c (TMEM columns BN/4 + 16 c ..) only covers chunks already read
+        auto chunk = [&](int cc) { return hf ? cbeg + cc : cbeg + NCT - 1 - cc; };
+        constexpr uint32_t kPOff = BN / 4;
         const int i = i0 + row;
         const bool row_in = i < n;
         const bool row_valid = row_in && (!p.qmask || p.qmask[t0 + i]);
@@ -248,65 +269,176 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float a0 = row_in ? relb_h[t0 + i] : 0.f;
         const float a1 = row_in ? relb_h[T + t0 + i] : 0.f;
         const float kscale = p.scale * kLog2e;
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_run = -INFINITY, l_part = 0.f;
         int t_uses = 0;
         bool ok = true;
         uint16_t* own_row = own + row * G::OWN_S;
+        // O columns of this thread: [hf D/2, (hf+1) D/2), 16 at a time
+        auto rescale_o = [&](float alpha) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[16];
+                tc_ld16(lane_base + kOCol + hf * (D / 2) + 16 * c, r);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                tc_st16(lane_base + kOCol + hf * (D / 2) + 16 * c, r);
+            }
+        };
+        // per-key column term of a tile (P2C scalar of uniform tiles, key mask,
+        // sequence end); fetched one tile ahead so the load latency overlaps work
+        auto colterm = [&](int jt, const TileKind& k) -> float {
+            const int j = jt * BN + tid;
+            if (tid >= BN || j >= n) return -INFINITY;
+            if (k.uniform) return relb_h[(2 + k.which) * T + t0 + j];
+            return (p.kmask && !p.kmask[t0 + j]) ? -INFINITY : 0.f;
+        };
+        TileKind tk_next = classify<BM, BN, 1>(p, dtab, i0);
+        float cb_next = colterm(0, tk_next);
         for (int it = 0; it < ntiles && ok; ++it) {
             const int j0 = it * BN;
-            const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - j0);
-            named_bar_sync(1, 128);
-            if (tid < BN) {
-                const int j = j0 + tid;
-                float cb = -INFINITY;
-                if (j < n) {
-                    if (tk.uniform)
-                        cb = relb_h[(2 + tk.which) * T + t0 + j];
-                    else
-                        cb = (p.kmask && !p.kmask[t0 + j]) ? -INFINITY : 0.f;
-                }
-                colb[tid] = cb;
+            const TileKind tk = tk_next;
+            const float cb_cur = cb_next;
+            named_bar_sync(1, 256);
+            if (tid < BN) colb[tid] = cb_cur;
+            if (it + 1 < ntiles) {
+                tk_next = classify<BM, BN, 1>(p, dtab, i0 - j0 - BN);
+                cb_next = colterm(it + 1, tk_next);
             }
             int own_a = 0;
             if (!tk.uniform) {
-                fill_dwin<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, dwin, tid, 128);
+                fill_dwin<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, dwin, tid, 256);
                 int lo, hi;
-                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
-                tc_fence_after();
                 own_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
-                own_a = copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
-                ++t_uses;
+                own_a = lo & ~15;
+                // The first-half warps copy the band windows; every softmax warp
+                // takes the same bounded waits so that a give-up is symmetric.
                 if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
-                tc_fence_after();
-                if (32 * w4 < BN) {
-                    cross_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
-                    const int ca = copy_band_window(lane_base + kTCol, lo, hi, cross + row * G::CROSS_S, kscale);
-                    if (lane == 0) bars->cross_base[w4] = ca;
+                if (hf == 0) {
+                    tc_fence_after();
+                    copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->t_empty);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
-                ++t_uses;
+                if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
+                if (hf == 0) {
+                    tc_fence_after();
+                    if (32 * w4 < BN) {
+                        cross_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
+                        const int ca = copy_band_window(lane_base + kTCol, lo, hi, cross + row * G::CROSS_S, kscale);
+                        if (lane == 0) bars->cross_base[w4] = ca;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->t_empty);
+                }
+                t_uses += 2;
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(1, 256);
             if (!(ok = mbar_wait_warp(&bars->s_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
             tc_fence_after();
             const uint32_t scol = s_col(it);
             float rb = tk.uniform ? (tk.which ? a1 : a0) : 0.f;
             if (!row_valid) rb = -INFINITY;
             const bool band = !tk.uniform;
-            // pass 1: biased logits (band tiles write them back over S) and the tile max
-            float tmax = -INFINITY;
+            // row maximum of the tile from the two halves
+            auto full_max = [&](float part) -> float {
+                xch[hf * BM + row] = part;
+                named_bar_sync(pair_bar, 64);
+                return fmaxf(xch[row], xch[BM + row]);
+            };
+            float sum = 0.f;
+            if (!band) {
+                // Uniform tile, one pass: probabilities against the running max,
+                // kept in registers; redone (rarely) when the tile max moves the
+                // running max by more than kRescaleSlack.
+                uint32_t pk[16 * NCT];
+                const float m_old = m_run;
+                const bool attempted = m_old != -INFINITY && rb != -INFINITY;
+                float mm = attempted ? m_old - rb : INFINITY;
+                bool dead = !attempted;
+                for (int pass = 0; pass < 2; ++pass) {
+                    float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int cc = 0; cc < NCT; ++cc) {
+                        const int c = cbeg + cc;
+                        uint32_t r[32];
+                        tc_ld32(lane_base + scol + 32 * c, r);
+                        tc_wait_ld();
+                        const uint32_t keep = p.dropout ? keep_bits32_row(p, b, h, i, j0 + 32 * c) : 0xFFFFFFFFu;
+                        const float4* cb4 = reinterpret_cast<const float4*>(colb + 32 * c);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 cv = cb4[q];
+                            const float x0 = fmaf(__uint_as_float(r[4 * q + 0]), kscale, cv.x);
+                            const float x1 = fmaf(__uint_as_float(r[4 * q + 1]), kscale, cv.y);
+                            const float x2 = fmaf(__uint_as_float(r[4 * q + 2]), kscale, cv.z);
+                            const float x3 = fmaf(__uint_as_float(r[4 * q + 3]), kscale, cv.w);
+                            tm[0] = fmaxf(tm[0], x0);
+                            tm[1] = fmaxf(tm[1], x1);
+                            tm[2] = fmaxf(tm[2], x2);
+                            tm[3] = fmaxf(tm[3], x3);
+                            float p0 = dead ? 0.f : ex2(x0 - mm), p1 = dead ? 0.f : ex2(x1 - mm);
+                            float p2 = dead ? 0.f : ex2(x2 - mm), p3 = dead ? 0.f : ex2(x3 - mm);
+                            sm[0] += p0;
+                            sm[1] += p1;
+                            sm[2] += p2;
+                            sm[3] += p3;
+                            if (p.dropout) {
+                                const uint32_t kq = keep >> (4 * q);
+                                p0 = (kq & 1u) ? p0 * p.drop_scale : 0.f;
+                                p1 = (kq & 2u) ? p1 * p.drop_scale : 0.f;
+                                p2 = (kq & 4u) ? p2 * p.drop_scale : 0.f;
+                                p3 = (kq & 8u) ? p3 * p.drop_scale : 0.f;
+                            }
+                            pk[16 * cc + 2 * q] = pack2<BF16>(p0, p1);
+                            pk[16 * cc + 2 * q + 1] = pack2<BF16>(p2, p3);
+                        }
+                    }
+                    sum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                    if (pass == 1) break;
+                    const float tmax = full_max(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]))) + rb;
+                    const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
+                        l_part *= alpha;
+                        m_run = tmax;
+                    }
+                    if (__any_sync(0xffffffffu, need) && it > 0) {
+                        // P.V of the previous tile must have landed in O first
+                        if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err,
+                                                  abort_flag)))
+                            break;
+                        tc_fence_after();
+                        rescale_o(alpha);
+                    }
+                    const bool redo = need || (!attempted && m_run != -INFINITY && rb != -INFINITY);
+                    if (!__any_sync(0xffffffffu, redo)) break;
+                    dead = m_run == -INFINITY || rb == -INFINITY;
+                    mm = dead ? INFINITY : m_run - rb;
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int cc = 0; cc < NCT; ++cc) {
+                    uint32_t r16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r16[e] = pk[16 * cc + e];
+                    tc_st16(lane_base + scol + kPOff + 16 * (cbeg + cc), r16);
+                }
+            } else {
+                // ---- band tile: two passes over this thread's 32-column chunks
+                // pass 1: biased logits (written back over S) and the tile max
+                float tm = -INFINITY;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tc_ld32(lane_base + scol + 32 * c, r);
-                tc_wait_ld();
-                const float* cbp = colb + 32 * c;
-                if (band) {
+                for (int cc = 0; cc < NCT; ++cc) {
+                    const int c = cbeg + cc;
+                    uint32_t r[32];
+                    tc_ld32(lane_base + scol + 32 * c, r);
+                    tc_wait_ld();
+                    const float* cbp = colb + 32 * c;
                     const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
                     const int16_t* dw = dwin + row - 32 * c + BN - 1;
                     const uint16_t* orow = own_row - own_a;
@@ -315,79 +447,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int m = dw[-e];
                         const float x = fmaf(__uint_as_float(r[e]), kscale, cbp[e]) + h2f(orow[m]) +
                                         h2f(crow[e * G::CROSS_S + m]);
-                        tmax = fmaxf(tmax, x);
+                        tm = fmaxf(tm, x);
                         r[e] = __float_as_uint(x);
                     }
                     tc_st32(lane_base + scol + 32 * c, r);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, fmaf(__uint_as_float(r[e]), kscale, cbp[e]));
                 }
-            }
-            if (band) tc_wait_st();
-            tmax += rb;
-            // online softmax in base-2 units; the max is only moved when it
-            // grows by more than kRescaleSlack
-            const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
-            float alpha = 1.f;
-            if (need) {
-                alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
-                l_run *= alpha;
-                m_run = tmax;
-            }
-            // the O accumulator is rescaled by the whole warp (tcgen05.ld / st
-            // are warp-collective); rows that keep their max use alpha = 1
-            if (__any_sync(0xffffffffu, need) && it > 0) {
-                // P.V of the previous tile must have landed in O first
-                if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err, abort_flag)))
-                    break;
-                tc_fence_after();
-                {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tc_ld32(lane_base + kOCol + 32 * c, r);
-                        tc_wait_ld();
-                        uint32_t o16a[16], o16b[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            o16a[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                            o16b[e] = __float_as_uint(__uint_as_float(r[16 + e]) * alpha);
-                        }
-                        tc_st16(lane_base + kOCol + 32 * c, o16a);
-                        tc_st16(lane_base + kOCol + 32 * c + 16, o16b);
-                    }
+                tc_wait_st();
+                const float tmax = full_max(tm) + rb;
+                const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
+                float alpha = 1.f;
+                if (need) {
+                    alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
+                    l_part *= alpha;
+                    m_run = tmax;
                 }
-            }
-            // pass 2: probabilities, written as 16-bit P over the first half of S
-            const float mm = m_run - rb;
-            const bool dead = m_run == -INFINITY || rb == -INFINITY;
-            float sum = 0.f;
+                if (__any_sync(0xffffffffu, need) && it > 0) {
+                    if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err, abort_flag)))
+                        break;
+                    tc_fence_after();
+                    rescale_o(alpha);
+                }
+                // pass 2: probabilities, written as 16-bit P over the first half of S
+                const float mm = m_run - rb;
+                const bool dead = m_run == -INFINITY || rb == -INFINITY;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tc_ld32(lane_base + scol + 32 * c, r);
-                tc_wait_ld();
-                const uint32_t keep = p.dropout ? keep_bits32_row(p, b, h, i, j0 + 32 * c) : 0xFFFFFFFFu;
-                const float* cbp = colb + 32 * c;
-                uint32_t pk[16];
+                for (int cc = 0; cc < NCT; ++cc) {
+                    const int c = chunk(cc);
+                    uint32_t r[32];
+                    tc_ld32(lane_base + scol + 32 * c, r);
+                    tc_wait_ld();
+                    const uint32_t keep = p.dropout ? keep_bits32_row(p, b, h, i, j0 + 32 * c) : 0xFFFFFFFFu;
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float x0 = band ? __uint_as_float(r[2 * e]) : fmaf(__uint_as_float(r[2 * e]), kscale, cbp[2 * e]);
-                    const float x1 =
-                        band ? __uint_as_float(r[2 * e + 1]) : fmaf(__uint_as_float(r[2 * e + 1]), kscale, cbp[2 * e + 1]);
-                    const float p0 = dead ? 0.f : ex2(x0 - mm), p1 = dead ? 0.f : ex2(x1 - mm);
-                    sum += p0 + p1;
-                    float d0 = p0, d1 = p1;
-                    if (p.dropout) {
-                        d0 = ((keep >> (2 * e)) & 1u) ? p0 * p.drop_scale : 0.f;
-                        d1 = ((keep >> (2 * e + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = dead ? 0.f : ex2(__uint_as_float(r[2 * e]) - mm);
+                        const float p1 = dead ? 0.f : ex2(__uint_as_float(r[2 * e + 1]) - mm);
+                        sum += p0 + p1;
+                        float d0 = p0, d1 = p1;
+                        if (p.dropout) {
+                            d0 = ((keep >> (2 * e)) & 1u) ? p0 * p.drop_scale : 0.f;
+                            d1 = ((keep >> (2 * e + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
+                        }
+                        pk[e] = pack2<BF16>(d0, d1);
                     }
-                    pk[e] = pack2<BF16>(d0, d1);
+                    tc_st16(lane_base + scol + kPOff + 16 * c, pk);
                 }
-                tc_st16(lane_base + scol + 16 * c, pk);
             }
-            l_run += sum;
+            l_part += sum;
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -397,19 +503,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = mbar_wait_warp(&bars->pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, err, abort_flag);
         tc_fence_after();
         if (ok) {
+            xch[2 * BM + hf * BM + row] = l_part;
+            named_bar_sync(pair_bar, 64);
+            const float l_run = xch[2 * BM + row] + xch[3 * BM + row];
             const bool any = row_valid && l_run > 0.f;
             const float inv = any ? 1.f / l_run : 0.f;
             using OutT = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-            OutT* orow = reinterpret_cast<OutT*>(out_) + ((size_t)(t0 + i) * p.H + h) * D;
+            OutT* orow = reinterpret_cast<OutT*>(out_) + ((size_t)(t0 + i) * p.H + h) * D + hf * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tc_ld32(lane_base + kOCol + 32 * c, r);
+                uint32_t r[16];
+                tc_ld16(lane_base + kOCol + hf * (D / 2) + 16 * c, r);
                 tc_wait_ld();
                 if (row_in) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 16 * c);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int v = 0; v < 2; ++v) {
                         uint4 w;
                         w.x = pack2<BF16>(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
                         w.y = pack2<BF16>(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
@@ -419,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (row_in) lse[lse_index(p, b, h, t0, i)] = any ? (m_run + log2f(l_run)) * kLn2 : INFINITY;
+            if (row_in && hf == 0) lse[lse_index(p, b, h, t0, i)] = any ? (m_run + log2f(l_run)) * kLn2 : INFINITY;
         }
     }
     tc_fence_before();

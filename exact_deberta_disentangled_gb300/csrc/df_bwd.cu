@@ -35,9 +35,25 @@
 namespace df {
 namespace {
 
-constexpr uint32_t kAcc1 = 0, kAcc2 = 128, kSCol = 256, kPCol = 384, kTCol = 256;
 constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Tensor-memory columns (512 per CTA).  The fp32 S and dP of the tile being
+// processed sit in [256, 256 + 2 BN); the band products alias them.  The
+// 16-bit dZ and P~ that feed the dK / dQ / dV products have their own
+// columns, so the issuer can compute the next tile's S / dP as soon as the
+// softmax warps have read this tile's into registers.
+template <int D>
+struct BwdTmem {
+    using G = Geo<D>;
+    static constexpr uint32_t ACC1 = 0, ACC2 = D;                       // fp32 accumulators
+    static constexpr uint32_t S = 256, P = 256 + G::BN;                 // fp32 S, dP
+    static constexpr uint32_t Z = 2 * D + G::BN <= 256 ? 2 * D : 256 + 2 * G::BN;   // 16-bit dZ, then P~
+    static constexpr uint32_t T = 256;                                  // band products
+    static constexpr bool T_OVER_Z = Z >= 256 && T + G::NBAND > Z;      // band products overwrite dZ / P~
+    static_assert(P + G::BN <= 512 && Z + G::BN <= 512 && T + G::NBAND <= 512, "tensor memory");
+    static_assert(Z >= 2 * D && (Z + G::BN <= 256 || Z >= P + G::BN), "overlap");
+};
 
 template <int D>
 struct BwdSmem {
@@ -58,11 +74,13 @@ struct BwdSmem {
     static constexpr int GSB = 2 * G::BM * GBOXW * 2;
     static constexpr int STGB = (CROSS - STG) + CROSSB > GSB ? (CROSS - STG) + CROSSB : GSB;
     static constexpr int DWIN = (STG + STGB + 15) / 16 * 16;
-    static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // colb, clse, cdl
-    static constexpr int XCH = COLV + 3 * G::BN * 4;       // [4][BM] floats: the far-field sums of the two halves
+    static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // [2 tiles][colb | cdl][BN]
+    static constexpr int XCH = COLV + 4 * G::BN * 4;       // [4][BM] floats: exchanges between the two halves
     static constexpr int MISC = XCH + 4 * G::BM * 4;
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;
+    static_assert(ALLOC <= 232448, "shared memory");
+    static_assert(STG % 16 == 0 && (GBOXW * 2) % 16 == 0, "staging rows are zeroed 16 bytes at a time");
 };
 
 struct BwdBars {
@@ -70,7 +88,7 @@ struct BwdBars {
     uint64_t c_full[2], c_empty[2];
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
-    uint64_t s_full, z_full, zread, mma3_done;
+    uint64_t s_full, sread, z_full, zread, mma3_done;
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -108,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float* __restrict__ acc1_out, void* __restrict__ acc2_out, void* __restrict__ Gbuf, int Rp) {
     using G = Geo<D>;
     using S = BwdSmem<D>;
+    using TM = BwdTmem<D>;
     using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     constexpr int BM = G::BM, BN = G::BN;
     constexpr bool ROWQ = SIGMA > 0;   // rows are queries
@@ -115,9 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem + S::MISC);
     int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
-    float* colb = reinterpret_cast<float*>(smem + S::COLV);
-    float* clse = colb + BN;
-    float* cdl = clse + BN;
+    float* colv = reinterpret_cast<float*>(smem + S::COLV);
     float* xch = reinterpret_cast<float*>(smem + S::XCH);
     uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::STG);
     uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
@@ -130,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r0 = blockIdx.x * BM;   // first row token (query or key) of this CTA
     if (r0 >= n) return;
     const int ntiles = (n + BN - 1) / BN;
+    auto tile_base = [&](int m) { return ROWQ ? r0 - m * BN : m * BN - r0; };
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->row_full, 1);
@@ -140,8 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->band_full, 1);
         mbar_init(&bars->band_empty, 1);
         mbar_init(&bars->t_full, 1);
-        mbar_init(&bars->t_empty, 4);
+        mbar_init(&bars->t_empty, 8);
         mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->sread, 8);
         mbar_init(&bars->z_full, 8);
         mbar_init(&bars->zread, 8);
         mbar_init(&bars->mma3_done, 1);
@@ -179,8 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(smem + S::C2 + s * S::CB + c * BN * G::CW * 2, &tmC2, h * D + c * G::CW, t0 + c0,
                                 &bars->c_full[s]);
                 }
-                const int base = ROWQ ? r0 - c0 : c0 - r0;
-                const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, base);
+                const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, tile_base(it));
                 if (tk.uniform) continue;
                 bool ok = true;
                 for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -201,80 +219,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Order per tile m:  S / dP of tile m + 1 (once the softmax warps have
+        // read tile m's into registers), then the dK / dV (dQ) products of tile
+        // m (once its 16-bit dZ / P~ are written).  When the next tile's band
+        // products would overwrite dZ / P~, they wait for tile m to finish.
         if (lane == 0) {
             const uint32_t sR1 = smem_u32(smem + S::R1), sR2 = smem_u32(smem + S::R2);
             const uint32_t sBand = smem_u32(smem + S::BAND);
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
             constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
             constexpr uint32_t idA = idesc_f16(128, D, BF16, false, true);
-            constexpr uint32_t kHOff = BN / 4;   // 16-bit dZ / Pd start a quarter into their buffers
             bool ok = mbar_wait(&bars->row_full, 0, err, abort_flag);
             int band_used = 0, t_uses = 0;
-            for (int it = 0; it < ntiles && ok; ++it) {
-                const int s = it & 1, use = it >> 1;
-                const int c0 = it * BN;
+            auto issue_sdp = [&](int m) -> bool {
+                const int s = m & 1, use = m >> 1;
                 const uint32_t sC1 = smem_u32(smem + S::C1 + s * S::CB), sC2 = smem_u32(smem + S::C2 + s * S::CB);
-                const int base = ROWQ ? r0 - c0 : c0 - r0;
-                const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, base);
-                // the band products and S / dP overwrite the previous tile's P / dZ
-                // (operands of its dQ / dK / dV products, and read back for the
-                // diagonal sums)
-                if (it > 0 && !(ok = mbar_wait(&bars->mma3_done, (it - 1) & 1, err, abort_flag))) break;
-                if (it > 0 && !(ok = mbar_wait(&bars->zread, (it - 1) & 1, err, abort_flag))) break;
-                tc_fence_after();
+                const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, tile_base(m));
                 if (!tk.uniform) {
-                    for (int pass = 0; pass < 2 && ok; ++pass) {
-                        if (pass == 1 && !(ok = mbar_wait(&bars->c_full[s], use & 1, err, abort_flag))) break;
-                        if (t_uses > 0 && !(ok = mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)))
-                            break;
+                    for (int pass = 0; pass < 2; ++pass) {
+                        if (pass == 1 && !mbar_wait(&bars->c_full[s], use & 1, err, abort_flag)) return false;
+                        if (t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                            return false;
                         const uint32_t sA = pass == 0 ? sR1 : sC1;
                         const int arows = pass == 0 ? BM : BN;
-                        for (int c = 0; c < G::NCH && ok; ++c) {
-                            if (!(ok = mbar_wait(&bars->band_full, band_used & 1, err, abort_flag))) break;
+                        for (int c = 0; c < G::NCH; ++c) {
+                            if (!mbar_wait(&bars->band_full, band_used & 1, err, abort_flag)) return false;
                             tc_fence_after();
                             for (int k = 0; k < G::CW / 16; ++k)
-                                tc_mma_ss(tmem + kTCol, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
+                                tc_mma_ss(tmem + TM::T, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
                                           desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
                             tc_commit(&bars->band_empty);
                             ++band_used;
                         }
-                        if (!ok) break;
                         tc_commit(&bars->t_full);
                         ++t_uses;
                     }
-                    if (!ok) break;
                     // S / dP reuse the band columns: wait until the cross window was copied out
-                    if (!(ok = mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))) break;
-                } else {
-                    if (!(ok = mbar_wait(&bars->c_full[s], use & 1, err, abort_flag))) break;
+                    if (!mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)) return false;
+                } else if (!mbar_wait(&bars->c_full[s], use & 1, err, abort_flag)) {
+                    return false;
                 }
                 tc_fence_after();
                 for (int k = 0; k < D / 16; ++k) {
-                    tc_mma_ss(tmem + kSCol, desc_k<G>(sR1, BM, k), desc_k<G>(sC1, BN, k), idS, k != 0);
-                    tc_mma_ss(tmem + kPCol, desc_k<G>(sR2, BM, k), desc_k<G>(sC2, BN, k), idS, k != 0);
+                    tc_mma_ss(tmem + TM::S, desc_k<G>(sR1, BM, k), desc_k<G>(sC1, BN, k), idS, k != 0);
+                    tc_mma_ss(tmem + TM::P, desc_k<G>(sR2, BM, k), desc_k<G>(sC2, BN, k), idS, k != 0);
                 }
                 tc_commit(&bars->s_full);
-                if (!(ok = mbar_wait(&bars->z_full, it & 1, err, abort_flag))) break;
+                return true;
+            };
+            auto issue_acc = [&](int m) -> bool {
+                const int s = m & 1;
+                const uint32_t sC1 = smem_u32(smem + S::C1 + s * S::CB), sC2 = smem_u32(smem + S::C2 + s * S::CB);
+                if (!mbar_wait(&bars->z_full, m & 1, err, abort_flag)) return false;
                 tc_fence_after();
                 for (int k = 0; k < BN / 16; ++k) {
                     // acc1 += dZ . C1   (dQ += dZ K  |  dK += dZ^T Q)
-                    tc_mma_ts(tmem + kAcc1, tmem + kPCol + kHOff + k * 8, desc_mn<G>(sC1, BN, k), idA,
-                              (it | k) != 0);
+                    tc_mma_ts(tmem + TM::ACC1, tmem + TM::Z + k * 8, desc_mn<G>(sC1, BN, k), idA, (m | k) != 0);
                     // dV += Pd^T dO
                     if (!ROWQ)
-                        tc_mma_ts(tmem + kAcc2, tmem + kSCol + kHOff + k * 8, desc_mn<G>(sC2, BN, k), idA,
-                                  (it | k) != 0);
+                        tc_mma_ts(tmem + TM::ACC2, tmem + TM::Z + BN / 2 + k * 8, desc_mn<G>(sC2, BN, k), idA,
+                                  (m | k) != 0);
                 }
                 tc_commit(&bars->c_empty[s]);
                 tc_commit(&bars->mma3_done);
+                return true;
+            };
+            if (ok) ok = issue_sdp(0);
+            for (int it = 0; it < ntiles && ok; ++it) {
+                const bool nxt = it + 1 < ntiles;
+                const bool early =
+                    nxt && (!TM::T_OVER_Z || classify<BM, BN, SIGMA>(p, dtab, tile_base(it + 1)).uniform);
+                if (early) {
+                    if (!(ok = mbar_wait(&bars->sread, it & 1, err, abort_flag))) break;
+                    if (!(ok = issue_sdp(it + 1))) break;
+                }
+                if (!(ok = issue_acc(it))) break;
+                if (nxt && !early) {
+                    // the band products overwrite this tile's dZ / P~: wait until the
+                    // products and the diagonal sums have read them
+                    if (!(ok = mbar_wait(&bars->sread, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait(&bars->mma3_done, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait(&bars->zread, it & 1, err, abort_flag))) break;
+                    if (!(ok = issue_sdp(it + 1))) break;
+                }
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax / gradient warps
         // Eight warps: warp w owns TMEM lanes 32 (w & 3) .. +31 (rows) and
-        // column half hf = (w - 2) / 4 of every tile.  The first-half warps
-        // copy the band windows and form the diagonal sums of band tiles;
+        // column half hf = (w - 2) / 4 of every tile.  Band-window copies and
+        // the diagonal sums of band tiles are split between the two halves;
         // every warp takes the same bounded waits.
         const int w4 = warp & 3;
         const int hf = (warp - 2) >> 2;
@@ -283,11 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pair_bar = 2 + w4;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
         constexpr int NCT = BN / 64;          // 32-column chunks per thread
+        constexpr int HC = BN / 2;            // columns per half
         const int cbeg = hf * NCT;
-        // 16-bit dZ / Pd of chunk c go to TMEM columns BN/4 + 16 c of the dP / S
-        // buffers: inside the columns this warp has already read, because the
-        // first half walks its chunks backwards and the second half forwards
-        constexpr uint32_t kHOff = BN / 4;
         const int rt = r0 + row;              // row token position in the sequence
         const bool row_in = rt < n;
         const size_t T = (size_t)p.T;
@@ -307,15 +339,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         const bool rvalid = rb0 != -INFINITY;
+        const float dls_row = p.scale * dl;
         float g_lo = 0.f, g_hi = 0.f;     // this thread's share of the diagonal sums at delta 0 and R-1
         int t_uses = 0;
         bool ok = true;
         uint16_t* own_row = own + row * G::OWN_S;
-        // per-column terms of a tile, fetched one tile ahead:
+        // per-column terms of a tile:
         //   cv0 = column bias (P2C of keys / C2P of queries in uniform tiles,
         //         0 in band tiles, -inf for masked or missing columns), minus the
         //         column's LSE (base 2) when the columns are queries;
         //   cv1 = c * Dl of the column (dK/dV kernel only)
+        // They go to shared memory one tile ahead (double-buffered) and are
+        // loaded from global memory two tiles ahead.
         auto colterms = [&](int ct_tile, const TileKind& k, float& v0, float& v1) {
             v0 = -INFINITY;
             v1 = 0.f;
@@ -330,24 +365,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             v0 = cb;
         };
-        TileKind tk_next = classify<BM, BN, SIGMA>(p, dtab, ROWQ ? r0 : -r0);
-        float cv0_next, cv1_next;
-        colterms(0, tk_next, cv0_next, cv1_next);
+        auto put_colterms = [&](int slot, float v0, float v1) {
+            if (tid < BN) {
+                colv[slot * 2 * BN + tid] = v0;
+                colv[slot * 2 * BN + BN + tid] = v1;
+            }
+        };
+        TileKind tk_cur = classify<BM, BN, SIGMA>(p, dtab, tile_base(0));
+        TileKind tk_n1 = tk_cur;
+        float cv0_n, cv1_n;   // column terms of the tile two ahead of the one being processed
+        {
+            float v0, v1;
+            colterms(0, tk_cur, v0, v1);
+            put_colterms(0, v0, v1);
+        }
+        if (ntiles > 1) {
+            tk_n1 = classify<BM, BN, SIGMA>(p, dtab, tile_base(1));
+            colterms(1, tk_n1, cv0_n, cv1_n);
+        }
         for (int it = 0; it < ntiles && ok; ++it) {
             const int c0 = it * BN;
-            const int base = ROWQ ? r0 - c0 : c0 - r0;
-            const TileKind tk = tk_next;
-            const float cv0 = cv0_next, cv1 = cv1_next;
+            const int base = tile_base(it);
+            const TileKind tk = tk_cur;
+            const float* colb = colv + (it & 1) * 2 * BN;
+            const float* cdl = colb + BN;
             if (tid == 0) bulk_wait_read0();   // the previous G box left shared memory
             named_bar_sync(1, 256);
-            if (tid < BN) {
-                colb[tid] = cv0;
-                cdl[tid] = cv1;
-            }
             if (it + 1 < ntiles) {
-                const int nb2 = ROWQ ? r0 - c0 - BN : c0 + BN - r0;
-                tk_next = classify<BM, BN, SIGMA>(p, dtab, nb2);
-                colterms(it + 1, tk_next, cv0_next, cv1_next);
+                put_colterms((it + 1) & 1, cv0_n, cv1_n);
+                tk_cur = tk_n1;
+                if (it + 2 < ntiles) {
+                    tk_n1 = classify<BM, BN, SIGMA>(p, dtab, tile_base(it + 2));
+                    colterms(it + 2, tk_n1, cv0_n, cv1_n);
+                }
             }
             int own_a = 0;
             if (!tk.uniform) {
@@ -356,44 +406,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 own_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
                 own_a = lo & ~15;
                 if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
-                if (hf == 0) {
-                    tc_fence_after();
-                    copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->t_empty);
-                }
+                tc_fence_after();
+                copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_empty);
                 if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
-                if (hf == 0) {
-                    tc_fence_after();
-                    if (32 * w4 < BN) {
-                        cross_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
-                        const int ca = copy_band_window(lane_base + kTCol, lo, hi, cross + row * G::CROSS_S, kscale);
-                        if (lane == 0) bars->cross_base[w4] = ca;
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->t_empty);
+                tc_fence_after();
+                if (32 * w4 < BN) {
+                    cross_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
+                    const int ca =
+                        copy_band_window(lane_base + TM::T, lo, hi, cross + row * G::CROSS_S, kscale, hf, 2);
+                    if (lane == 0 && hf == 0) bars->cross_base[w4] = ca;
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_empty);
                 t_uses += 2;
+                named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
-            named_bar_sync(1, 256);
             if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
             const bool band = !tk.uniform;
             // per-row constant of the exponent (base 2): row bias, minus the row LSE for query rows
             const float rowc = ROWQ ? rb - lse2 : rb;
-            const float dls_row = p.scale * dl;
             float rs[4] = {0.f, 0.f, 0.f, 0.f};
             // this thread's 32-column chunks: S, dP -> P, dZ (and Pd for the dK/dV kernel)
 #pragma unroll 1
             for (int cc = 0; cc < NCT; ++cc) {
-                const int c = hf ? cbeg + cc : cbeg + NCT - 1 - cc;
+                const int c = cbeg + cc;
                 uint32_t sr[32], pr[32];
-                tc_ld32(lane_base + kSCol + 32 * c, sr);
-                tc_ld32(lane_base + kPCol + 32 * c, pr);
+                tc_ld32(lane_base + TM::S + 32 * c, sr);
+                tc_ld32(lane_base + TM::P + 32 * c, pr);
                 tc_wait_ld();
+                if (cc == NCT - 1) {
+                    // all of this warp's S / dP columns are in registers
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->sread);
+                }
                 const float4* cv0p = reinterpret_cast<const float4*>(colb + 32 * c);
                 if (band) {
                     const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
@@ -425,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       : ROWQ     ? keep_bits32_row(p, b, h, rt, c0 + 32 * c)
                                                  : keep_bits32_col(p, b, h, c0 + 32 * c, rt);
                 const float4* cv1p = reinterpret_cast<const float4*>(cdl + 32 * c);
+                uint32_t zp[16], pp[16];   // packed as they are formed, so S / dP registers die early
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     float dlq[4] = {dls_row, dls_row, dls_row, dls_row};
@@ -435,33 +488,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dlq[2] = d4.z;
                         dlq[3] = d4.w;
                     }
+                    float z[4], pd[4];
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         const int e = 4 * q + t;
                         const float pr_ = ex2(__uint_as_float(sr[e]));
-                        float z, pd;
                         if (p.dropout) {
                             const float kp = ((keep >> e) & 1u) ? p.drop_scale : 0.f;
-                            z = pr_ * fmaf(__uint_as_float(pr[e]), p.scale * kp, -dlq[t]);
-                            pd = pr_ * kp;
+                            z[t] = pr_ * fmaf(__uint_as_float(pr[e]), p.scale * kp, -dlq[t]);
+                            pd[t] = pr_ * kp;
                         } else {
-                            z = pr_ * fmaf(__uint_as_float(pr[e]), p.scale, -dlq[t]);
-                            pd = pr_;
+                            z[t] = pr_ * fmaf(__uint_as_float(pr[e]), p.scale, -dlq[t]);
+                            pd[t] = pr_;
                         }
-                        rs[t] += z;
-                        pr[e] = __float_as_uint(z);
-                        sr[e] = __float_as_uint(pd);
+                        rs[t] += z[t];
                     }
+                    zp[2 * q] = pack2<BF16>(z[0], z[1]);
+                    zp[2 * q + 1] = pack2<BF16>(z[2], z[3]);
+                    pp[2 * q] = pack2<BF16>(pd[0], pd[1]);
+                    pp[2 * q + 1] = pack2<BF16>(pd[2], pd[3]);
                 }
-                uint32_t zp[16], pp[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    zp[e] = pack2<BF16>(__uint_as_float(pr[2 * e]), __uint_as_float(pr[2 * e + 1]));
-                    pp[e] = pack2<BF16>(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+                if (cc == 0 && it > 0) {
+                    // the previous tile's products must have read their 16-bit operands
+                    if (!(ok = mbar_wait_warp(&bars->mma3_done, (it - 1) & 1, err, abort_flag))) break;
+                    tc_fence_after();
                 }
-                tc_st16(lane_base + kPCol + kHOff + 16 * c, zp);
-                if (!ROWQ) tc_st16(lane_base + kSCol + kHOff + 16 * c, pp);
+                tc_st16(lane_base + TM::Z + 16 * c, zp);
+                if (!ROWQ) tc_st16(lane_base + TM::Z + BN / 2 + 16 * c, pp);
             }
+            if (!ok) break;
             const float rowsum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
             tc_wait_st();
             tc_fence_before();
@@ -474,48 +529,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 named_bar_sync(1, 256);   // own / cross no longer read; every dZ is in tensor memory
                 tc_fence_after();
-                if (hf == 0) {
-                    uint16_t* g0 = gstage + (size_t)row * S::GBOXW;
-                    uint16_t* g1 = gstage + (size_t)(BM + row) * S::GBOXW;
-#pragma unroll 4
-                    for (int x = 0; x < S::GBOXW / 2; ++x) {
-                        reinterpret_cast<uint32_t*>(g0)[x] = 0u;
-                        reinterpret_cast<uint32_t*>(g1)[x] = 0u;
-                    }
-                    const int dlo8 = tk.dlo & ~7, off = tk.dlo - dlo8;
-                    bool bad = false;
-                    auto gstore = [&](int m, float v) {
-                        const int xx = m + off;
-                        bad |= xx < 0 || xx >= 2 * S::GBOXW;
-                        if (xx >= 0 && xx < S::GBOXW)
-                            g0[xx] = f2h16<BF16>(v);
-                        else if (xx >= S::GBOXW && xx < 2 * S::GBOXW)
-                            g1[xx - S::GBOXW] = f2h16<BF16>(v);
-                    };
-                    // runs of equal relative index along the row; dZ comes back from
-                    // tensor memory (16-bit, as the dQ / dK products use it)
-                    int run_m = dwin[ROWQ ? row + BN - 1 : BM - 1 - row];
-                    float acc = 0.f;
-#pragma unroll 1
-                    for (int c2 = 0; c2 < BN / 64; ++c2) {
-                        uint32_t zr[32];
-                        tc_ld32(lane_base + kPCol + kHOff + 32 * c2, zr);
-                        tc_wait_ld();
-                        const int16_t* dw = ROWQ ? dwin + row - 64 * c2 + BN - 1 : dwin + 64 * c2 - row + BM - 1;
+                // staging rows: [BM][GBOXW] low box, then [BM][GBOXW] high box;
+                // half hf clears box hf of its row
+                {
+                    uint4* gz = reinterpret_cast<uint4*>(gstage + (size_t)(hf * BM + row) * S::GBOXW);
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) {
-                            const int m = ROWQ ? dw[-e] : dw[e];
-                            const float v = h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
-                            if (m != run_m) {
-                                gstore(run_m, acc);
-                                run_m = m;
-                                acc = 0.f;
-                            }
-                            acc += v;
-                        }
+                    for (int x = 0; x < S::GBOXW / 8; ++x) gz[x] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                uint16_t* g0 = gstage + (size_t)row * S::GBOXW;
+                uint16_t* g1 = gstage + (size_t)(BM + row) * S::GBOXW;
+                const int dlo8 = tk.dlo & ~7, off = tk.dlo - dlo8;
+                bool bad = false;
+                auto gstore = [&](int m, float v) {
+                    const int xx = m + off;
+                    bad |= xx < 0 || xx >= 2 * S::GBOXW;
+                    if (xx >= 0 && xx < S::GBOXW)
+                        g0[xx] = f2h16<BF16>(v);
+                    else if (xx >= S::GBOXW && xx < 2 * S::GBOXW)
+                        g1[xx - S::GBOXW] = f2h16<BF16>(v);
+                };
+                auto dw_at = [&](int col) -> int {
+                    return ROWQ ? dwin[row - col + BN - 1] : dwin[col - row + BM - 1];
+                };
+                // this half's dZ columns, 16-bit as the products use them
+                uint32_t zr[HC / 2];
+                if constexpr (HC == 64) {
+                    tc_ld32p(lane_base + TM::Z + hf * (HC / 2), zr);
+                } else {
+                    tc_ld16p(lane_base + TM::Z + hf * (HC / 2), zr);
+                }
+                tc_wait_ld();
+                named_bar_sync(pair_bar, 64);   // both boxes of the row are cleared
+                // Runs of equal relative index along the row.  A run that crosses
+                // from the first half into the second is finished by the first
+                // half: the second hands over its partial sum.
+                const int cst = hf * HC;
+                const int m_join = hf ? dw_at(cst - 1) : -1;
+                int run_m = dw_at(cst);
+                bool first_run = true;
+                float acc = 0.f, handoff = 0.f;
+#pragma unroll
+                for (int e = 0; e < HC; ++e) {
+                    const int m = dw_at(cst + e);
+                    const float v = h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
+                    if (m != run_m) {
+                        if (first_run && run_m == m_join) handoff = acc; else gstore(run_m, acc);
+                        first_run = false;
+                        run_m = m;
+                        acc = 0.f;
                     }
-                    gstore(run_m, acc);
-                    if (bad) raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
+                    acc += v;
+                }
+                if (hf) {
+                    if (first_run && run_m == m_join) handoff = acc; else gstore(run_m, acc);
+                    xch[row] = handoff;
+                }
+                named_bar_sync(pair_bar, 64);
+                if (!hf) {
+                    gstore(run_m, acc + xch[row]);
                     // the clamped relative rows (far field) are summed in registers
                     if (tk.dlo == 0 && off < S::GBOXW) {
                         g_lo += h16f<BF16>(g0[off]);
@@ -531,8 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             g1[xx - S::GBOXW] = 0;
                         }
                     }
-                    fence_proxy_async_smem();
                 }
+                if (bad) raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
+                fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->zread);
@@ -555,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[16];
-                tc_ld16(lane_base + kAcc1 + hf * (D / 2) + 16 * c, r);
+                tc_ld16(lane_base + TM::ACC1 + hf * (D / 2) + 16 * c, r);
                 tc_wait_ld();
                 if (row_in) {
                     float4* dst = reinterpret_cast<float4*>(a1 + 16 * c);
@@ -570,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[16];
-                    tc_ld16(lane_base + kAcc2 + hf * (D / 2) + 16 * c, r);
+                    tc_ld16(lane_base + TM::ACC2 + hf * (D / 2) + 16 * c, r);
                     tc_wait_ld();
                     if (row_in) {
                         uint4* dst = reinterpret_cast<uint4*>(a2 + 16 * c);

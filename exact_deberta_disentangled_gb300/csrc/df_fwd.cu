@@ -12,15 +12,18 @@
 //   warp 1      tcgen05 issuer (one thread) and TMEM owner.
 //   warps 2..9  softmax: a thread owns one query row (= TMEM lane) and one
 //               half of the columns of every key tile.
-// Tensor memory (512 columns): O [0, 128), two S / P buffers [128, 256) and
-// [256, 384), band products [256, 512) (they share columns with the second
-// S buffer, so band tiles wait for it).  Tile n uses S buffer n & 1: the
-// issuer computes S for tile n + 1 while the softmax works on tile n.  P
-// (16-bit) is written over the middle half of S, columns [BN/4, 3 BN/4),
-// and feeds the P.V product straight from tensor memory.  Each column half of
-// a row is owned by one warp; P of that half lands inside the S columns the
-// same warp has already read (the first half walks its chunks backwards), so
-// the two warps of a row never overwrite each other's unread logits.
+// The two column halves of a row run independent online softmaxes, each with
+// its own running max and sum and its own output accumulator in tensor
+// memory (O_h += P_h V_h, K = BN/2 per tile); they are merged once, in the
+// epilogue.  So the warps of a row never wait for each other inside the
+// key loop.
+// Tensor memory (512 columns): O_0 and O_1 [0, 2D), two S / P buffers, band
+// products aliasing the second S buffer (band tiles wait for it).  Tile n
+// uses S buffer n & 1: the issuer computes S for tile n + 1 while the softmax
+// works on tile n.  P (16-bit) is written over the middle half of S, columns
+// [BN/4, 3 BN/4), half h's part inside the S columns half h has already read
+// (the first half walks its chunks backwards), and feeds the P.V products
+// straight from tensor memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -31,14 +34,21 @@
 namespace df {
 namespace {
 
-constexpr uint32_t kOCol = 0, kSCol0 = 128, kTCol = 256;
-
-// S / P buffer of tile `it`
-__device__ __forceinline__ uint32_t s_col(int it) { return kSCol0 + 128u * (uint32_t)(it & 1); }
 constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;   // keep a stale max while the new one exceeds it by <= 8 (2^8 headroom)
+
+template <int D>
+struct FwdTmem {
+    using G = Geo<D>;
+    static constexpr uint32_t O0 = 0, O1 = D;                  // output accumulators of the column halves
+    static constexpr uint32_t S0 = 2 * D > 128 ? 2 * D : 128;  // S / P of even tiles
+    static constexpr uint32_t S1 = S0 + G::BN;                 // S / P of odd tiles
+    static constexpr uint32_t T = S1;                          // band products
+    static constexpr uint32_t POFF = G::BN / 4;                // P starts a quarter into its S buffer
+    static_assert(T + G::NBAND <= 512 && S1 + G::BN <= 512, "tensor memory");
+};
 
 template <int D>
 struct FwdSmem {
@@ -56,11 +66,12 @@ struct FwdSmem {
     static constexpr int CROSS = (OWN + OWNB + 15) / 16 * 16;
     static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
     static constexpr int DWIN = CROSS + CROSSB;
-    static constexpr int COLB = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;
-    static constexpr int XCH = COLB + G::BN * 4;          // [4][BM] floats: partial maxima, partial sums
+    static constexpr int COLB = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;   // [2 tiles][BN]
+    static constexpr int XCH = COLB + 2 * G::BN * 4;      // [4][BM] floats: the halves' maxima and sums
     static constexpr int MISC = XCH + 4 * G::BM * 4;
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+    static_assert(ALLOC <= 232448, "shared memory");
 };
 
 struct FwdBars {
@@ -68,7 +79,7 @@ struct FwdBars {
     uint64_t kv_full[2], kv_empty[2];
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
-    uint64_t s_full[2], p_full, pv_done[2];
+    uint64_t s_full[2], p_full[2], pv_done[2];
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -82,12 +93,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float* __restrict__ relb, void* __restrict__ out_, float* __restrict__ lse) {
     using G = Geo<D>;
     using S = FwdSmem<D>;
+    using TM = FwdTmem<D>;
     constexpr int BM = G::BM, BN = G::BN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     FwdBars* bars = reinterpret_cast<FwdBars*>(smem + S::MISC);
     int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
-    float* colb = reinterpret_cast<float*>(smem + S::COLB);
+    float* colv = reinterpret_cast<float*>(smem + S::COLB);
     float* xch = reinterpret_cast<float*>(smem + S::XCH);
     uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::OWN);
     uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
@@ -99,22 +111,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i0 = blockIdx.x * BM;
     if (i0 >= n) return;
     const int ntiles = (n + BN - 1) / BN;
+    auto s_col = [](int it) -> uint32_t { return (it & 1) ? TM::S1 : TM::S0; };
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->kv_full[s], 1);
             mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->pv_done[s], 1);
+            mbar_init(&bars->p_full[s], 4);
         }
         mbar_init(&bars->band_full, 1);
         mbar_init(&bars->band_empty, 1);
         mbar_init(&bars->t_full, 1);
-        mbar_init(&bars->t_empty, 4);
-        for (int s2 = 0; s2 < 2; ++s2) {
-            mbar_init(&bars->s_full[s2], 1);
-            mbar_init(&bars->pv_done[s2], 1);
-        }
-        mbar_init(&bars->p_full, 8);
+        mbar_init(&bars->t_empty, 8);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -176,13 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
             constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
             constexpr uint32_t idO = idesc_f16(128, D, BF16, false, true);
-            constexpr uint32_t kPOff = BN / 4;   // P starts a quarter into its S buffer
             bool ok = mbar_wait(&bars->q_full, 0, err, abort_flag);
             int band_used = 0, t_uses = 0;
-            int pv_cnt[2] = {0, 0};   // P.V products issued per S buffer
+            int pv_cnt[2] = {0, 0};   // P.V rounds issued per S buffer
             // S (and, for band tiles, the two band products) of tile m into buffer m & 1
             auto issue_s = [&](int m) -> bool {
-                const int s = m & 1, use = m >> 1, b = m & 1;
+                const int s = m & 1, use = m >> 1, bf = m & 1;
                 const uint32_t sK = smem_u32(smem + S::K0 + s * S::KVB);
                 const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - m * BN);
                 if (!tk.uniform) {
@@ -199,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!mbar_wait(&bars->band_full, band_used & 1, err, abort_flag)) return false;
                             tc_fence_after();
                             for (int k = 0; k < G::CW / 16; ++k)
-                                tc_mma_ss(tmem + kTCol, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
+                                tc_mma_ss(tmem + TM::T, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
                                           desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
                             tc_commit(&bars->band_empty);
                             ++band_used;
@@ -210,15 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else if (!mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag)) {
                     return false;
                 }
-                // buffer b free: its previous P consumed; buffer 1 also holds band columns
-                if (pv_cnt[b] > 0 && !mbar_wait(&bars->pv_done[b], (pv_cnt[b] - 1) & 1, err, abort_flag))
+                // buffer bf free: its previous P consumed; buffer 1 also holds band columns
+                if (pv_cnt[bf] > 0 && !mbar_wait(&bars->pv_done[bf], (pv_cnt[bf] - 1) & 1, err, abort_flag))
                     return false;
-                if (b == 1 && t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                if (bf == 1 && t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
                     return false;
                 tc_fence_after();
                 for (int k = 0; k < D / 16; ++k)
                     tc_mma_ss(tmem + s_col(m), desc_k<G>(sQ, BM, k), desc_k<G>(sK, BN, k), idS, k != 0);
-                tc_commit(&bars->s_full[b]);
+                tc_commit(&bars->s_full[bf]);
                 return true;
             };
             auto is_band = [&](int m) { return !classify<BM, BN, 1>(p, dtab, i0 - m * BN).uniform; };
@@ -230,11 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool next = it + 1 < ntiles;
                 const bool next_band = next && is_band(it + 1);
                 if (next && !next_band && !(ok = issue_s(it + 1))) break;
-                if (!(ok = mbar_wait(&bars->p_full, it & 1, err, abort_flag))) break;
-                tc_fence_after();
-                for (int k = 0; k < BN / 16; ++k)
-                    tc_mma_ts(tmem + kOCol, tmem + s_col(it) + kPOff + k * 8, desc_mn<G>(sV, BN, k), idO,
-                              (it | k) != 0);
+                // O_h += P_h V_h for the two column halves, each as soon as its P is ready
+                for (int hf = 0; hf < 2 && ok; ++hf) {
+                    if (!(ok = mbar_wait(&bars->p_full[hf], it & 1, err, abort_flag))) break;
+                    tc_fence_after();
+                    for (int k = 0; k < BN / 32; ++k)
+                        tc_mma_ts(tmem + (hf ? TM::O1 : TM::O0), tmem + s_col(it) + TM::POFF + hf * (BN / 4) + k * 8,
+                                  desc_mn<G>(sV, BN, hf * (BN / 32) + k), idO, (it | k) != 0);
+                }
+                if (!ok) break;
                 tc_commit(&bars->kv_empty[s]);
                 tc_commit(&bars->pv_done[it & 1]);
                 ++pv_cnt[it & 1];
@@ -246,21 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ softmax
         // Eight warps: warp w owns TMEM lanes 32 (w & 3) .. +31 (query rows)
         // and column half hf = (w - 2) / 4 of every key tile, so two warps
-        // share each SM sub-partition.  The two threads of a row exchange
-        // their partial maxima (per tile) and sums (at the end) through shared
-        // memory, synchronised by a 64-thread barrier per lane quarter.
+        // share each SM sub-partition.
         const int w4 = warp & 3;
         const int hf = (warp - 2) >> 2;
         const int row = 32 * w4 + lane;           // query row in the tile == TMEM lane
         const int tid = threadIdx.x - 64;         // 0..255
         const int pair_bar = 2 + w4;              // named barrier of this row's two warps
         const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
+        const uint32_t ocol = hf ? TM::O1 : TM::O0;
         constexpr int NCT = BN / 64;              // 32-column chunks per thread
         const int cbeg = hf * NCT;
         // chunk order: backwards in the first half, so that the 16-bit result of
         // chunk c (TMEM columns BN/4 + 16 c ..) only covers chunks already read
         auto chunk = [&](int cc) { return hf ? cbeg + cc : cbeg + NCT - 1 - cc; };
-        constexpr uint32_t kPOff = BN / 4;
         const int i = i0 + row;
         const bool row_in = i < n;
         const bool row_valid = row_in && (!p.qmask || p.qmask[t0 + i]);
@@ -269,41 +281,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float a0 = row_in ? relb_h[t0 + i] : 0.f;
         const float a1 = row_in ? relb_h[T + t0 + i] : 0.f;
         const float kscale = p.scale * kLog2e;
-        float m_run = -INFINITY, l_part = 0.f;
+        float m_run = -INFINITY, l_part = 0.f;   // this half's running max (log2 units) and sum
         int t_uses = 0;
         bool ok = true;
         uint16_t* own_row = own + row * G::OWN_S;
-        // O columns of this thread: [hf D/2, (hf+1) D/2), 16 at a time
+        // this half's output accumulator, all D columns, 16 at a time
         auto rescale_o = [&](float alpha) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 16; ++c) {
                 uint32_t r[16];
-                tc_ld16(lane_base + kOCol + hf * (D / 2) + 16 * c, r);
+                tc_ld16(lane_base + ocol + 16 * c, r);
                 tc_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                tc_st16(lane_base + kOCol + hf * (D / 2) + 16 * c, r);
+                tc_st16(lane_base + ocol + 16 * c, r);
             }
         };
         // per-key column term of a tile (P2C scalar of uniform tiles, key mask,
-        // sequence end); fetched one tile ahead so the load latency overlaps work
+        // sequence end): loaded from global memory two tiles ahead and put into
+        // shared memory (double-buffered) one tile ahead
         auto colterm = [&](int jt, const TileKind& k) -> float {
             const int j = jt * BN + tid;
             if (tid >= BN || j >= n) return -INFINITY;
             if (k.uniform) return relb_h[(2 + k.which) * T + t0 + j];
             return (p.kmask && !p.kmask[t0 + j]) ? -INFINITY : 0.f;
         };
-        TileKind tk_next = classify<BM, BN, 1>(p, dtab, i0);
-        float cb_next = colterm(0, tk_next);
+        TileKind tk_cur = classify<BM, BN, 1>(p, dtab, i0);
+        TileKind tk_n1 = tk_cur;
+        float cb_n = -INFINITY;
+        {
+            const float v = colterm(0, tk_cur);
+            if (tid < BN) colv[tid] = v;
+        }
+        if (ntiles > 1) {
+            tk_n1 = classify<BM, BN, 1>(p, dtab, i0 - BN);
+            cb_n = colterm(1, tk_n1);
+        }
         for (int it = 0; it < ntiles && ok; ++it) {
             const int j0 = it * BN;
-            const TileKind tk = tk_next;
-            const float cb_cur = cb_next;
+            const TileKind tk = tk_cur;
+            const float* colb = colv + (it & 1) * BN;
             named_bar_sync(1, 256);
-            if (tid < BN) colb[tid] = cb_cur;
             if (it + 1 < ntiles) {
-                tk_next = classify<BM, BN, 1>(p, dtab, i0 - j0 - BN);
-                cb_next = colterm(it + 1, tk_next);
+                if (tid < BN) colv[((it + 1) & 1) * BN + tid] = cb_n;
+                tk_cur = tk_n1;
+                if (it + 2 < ntiles) {
+                    tk_n1 = classify<BM, BN, 1>(p, dtab, i0 - j0 - 2 * BN);
+                    cb_n = colterm(it + 2, tk_n1);
+                }
             }
             int own_a = 0;
             if (!tk.uniform) {
@@ -311,42 +336,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int lo, hi;
                 own_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
                 own_a = lo & ~15;
-                // The first-half warps copy the band windows; every softmax warp
-                // takes the same bounded waits so that a give-up is symmetric.
+                // both warps of a lane quarter copy half of each band window
                 if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
-                if (hf == 0) {
-                    tc_fence_after();
-                    copy_band_window(lane_base + kTCol, lo, hi, own_row, kscale);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->t_empty);
-                }
+                tc_fence_after();
+                copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_empty);
                 if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
-                if (hf == 0) {
-                    tc_fence_after();
-                    if (32 * w4 < BN) {
-                        cross_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
-                        const int ca = copy_band_window(lane_base + kTCol, lo, hi, cross + row * G::CROSS_S, kscale);
-                        if (lane == 0) bars->cross_base[w4] = ca;
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->t_empty);
+                tc_fence_after();
+                if (32 * w4 < BN) {
+                    cross_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
+                    const int ca =
+                        copy_band_window(lane_base + TM::T, lo, hi, cross + row * G::CROSS_S, kscale, hf, 2);
+                    if (lane == 0 && hf == 0) bars->cross_base[w4] = ca;
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_empty);
                 t_uses += 2;
+                named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
-            named_bar_sync(1, 256);
             if (!(ok = mbar_wait_warp(&bars->s_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
             tc_fence_after();
             const uint32_t scol = s_col(it);
             float rb = tk.uniform ? (tk.which ? a1 : a0) : 0.f;
             if (!row_valid) rb = -INFINITY;
             const bool band = !tk.uniform;
-            // row maximum of the tile from the two halves
-            auto full_max = [&](float part) -> float {
-                xch[hf * BM + row] = part;
-                named_bar_sync(pair_bar, 64);
-                return fmaxf(xch[row], xch[BM + row]);
+            // a new running max for this half: rescale the sum and (once the
+            // previous tile's P.V has landed) the accumulator
+            auto raise_max = [&](float tmax) -> bool {
+                const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
+                float alpha = 1.f;
+                if (need) {
+                    alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
+                    l_part *= alpha;
+                    m_run = tmax;
+                }
+                if (__any_sync(0xffffffffu, need) && it > 0) {
+                    if (!mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err, abort_flag))
+                        return false;
+                    tc_fence_after();
+                    rescale_o(alpha);
+                }
+                return true;
             };
             float sum = 0.f;
             if (!band) {
@@ -361,21 +394,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int pass = 0; pass < 2; ++pass) {
                     float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                     float sm[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t r[32 * NCT];
+#pragma unroll
+                    for (int cc = 0; cc < NCT; ++cc) tc_ld32p(lane_base + scol + 32 * (cbeg + cc), r + 32 * cc);
+                    tc_wait_ld();
 #pragma unroll
                     for (int cc = 0; cc < NCT; ++cc) {
                         const int c = cbeg + cc;
-                        uint32_t r[32];
-                        tc_ld32(lane_base + scol + 32 * c, r);
-                        tc_wait_ld();
                         const uint32_t keep = p.dropout ? keep_bits32_row(p, b, h, i, j0 + 32 * c) : 0xFFFFFFFFu;
                         const float4* cb4 = reinterpret_cast<const float4*>(colb + 32 * c);
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             const float4 cv = cb4[q];
-                            const float x0 = fmaf(__uint_as_float(r[4 * q + 0]), kscale, cv.x);
-                            const float x1 = fmaf(__uint_as_float(r[4 * q + 1]), kscale, cv.y);
-                            const float x2 = fmaf(__uint_as_float(r[4 * q + 2]), kscale, cv.z);
-                            const float x3 = fmaf(__uint_as_float(r[4 * q + 3]), kscale, cv.w);
+                            const float x0 = fmaf(__uint_as_float(r[32 * cc + 4 * q + 0]), kscale, cv.x);
+                            const float x1 = fmaf(__uint_as_float(r[32 * cc + 4 * q + 1]), kscale, cv.y);
+                            const float x2 = fmaf(__uint_as_float(r[32 * cc + 4 * q + 2]), kscale, cv.z);
+                            const float x3 = fmaf(__uint_as_float(r[32 * cc + 4 * q + 3]), kscale, cv.w);
                             tm[0] = fmaxf(tm[0], x0);
                             tm[1] = fmaxf(tm[1], x1);
                             tm[2] = fmaxf(tm[2], x2);
@@ -399,22 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     sum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
                     if (pass == 1) break;
-                    const float tmax = full_max(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]))) + rb;
+                    const float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) + rb;
                     const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
-                    float alpha = 1.f;
-                    if (need) {
-                        alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
-                        l_part *= alpha;
-                        m_run = tmax;
-                    }
-                    if (__any_sync(0xffffffffu, need) && it > 0) {
-                        // P.V of the previous tile must have landed in O first
-                        if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err,
-                                                  abort_flag)))
-                            break;
-                        tc_fence_after();
-                        rescale_o(alpha);
-                    }
+                    if (!(ok = raise_max(tmax))) break;
                     const bool redo = need || (!attempted && m_run != -INFINITY && rb != -INFINITY);
                     if (!__any_sync(0xffffffffu, redo)) break;
                     dead = m_run == -INFINITY || rb == -INFINITY;
@@ -426,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r16[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) r16[e] = pk[16 * cc + e];
-                    tc_st16(lane_base + scol + kPOff + 16 * (cbeg + cc), r16);
+                    tc_st16(lane_base + scol + TM::POFF + 16 * (cbeg + cc), r16);
                 }
             } else {
                 // ---- band tile: two passes over this thread's 32-column chunks
@@ -453,21 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_st32(lane_base + scol + 32 * c, r);
                 }
                 tc_wait_st();
-                const float tmax = full_max(tm) + rb;
-                const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
-                float alpha = 1.f;
-                if (need) {
-                    alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
-                    l_part *= alpha;
-                    m_run = tmax;
-                }
-                if (__any_sync(0xffffffffu, need) && it > 0) {
-                    if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err, abort_flag)))
-                        break;
-                    tc_fence_after();
-                    rescale_o(alpha);
-                }
-                // pass 2: probabilities, written as 16-bit P over the first half of S
+                if (!(ok = raise_max(tm + rb))) break;
+                // pass 2: probabilities, written as 16-bit P over the middle half of S
                 const float mm = m_run - rb;
                 const bool dead = m_run == -INFINITY || rb == -INFINITY;
 #pragma unroll 1
@@ -490,45 +498,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         pk[e] = pack2<BF16>(d0, d1);
                     }
-                    tc_st16(lane_base + scol + kPOff + 16 * c, pk);
+                    tc_st16(lane_base + scol + TM::POFF + 16 * c, pk);
                 }
             }
             l_part += sum;
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full);
+            if (lane == 0) mbar_arrive(&bars->p_full[hf]);
         }
         // ------------------------------------------------------------ epilogue
+        // merge the two halves: m = max(m_0, m_1), l = sum_h l_h 2^(m_h - m),
+        // O = sum_h O_h 2^(m_h - m) / l
         if (ok) ok = mbar_wait_warp(&bars->pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, err, abort_flag);
         tc_fence_after();
         if (ok) {
+            xch[hf * BM + row] = m_run;
             xch[2 * BM + hf * BM + row] = l_part;
             named_bar_sync(pair_bar, 64);
-            const float l_run = xch[2 * BM + row] + xch[3 * BM + row];
+            const float m0 = xch[row], m1 = xch[BM + row];
+            const float mx = fmaxf(m0, m1);
+            const float s0 = m0 == -INFINITY ? 0.f : ex2(m0 - mx);
+            const float s1 = m1 == -INFINITY ? 0.f : ex2(m1 - mx);
+            const float l_run = xch[2 * BM + row] * s0 + xch[3 * BM + row] * s1;
             const bool any = row_valid && l_run > 0.f;
             const float inv = any ? 1.f / l_run : 0.f;
+            const float f0 = s0 * inv, f1 = s1 * inv;
             using OutT = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
             OutT* orow = reinterpret_cast<OutT*>(out_) + ((size_t)(t0 + i) * p.H + h) * D + hf * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[16];
-                tc_ld16(lane_base + kOCol + hf * (D / 2) + 16 * c, r);
+                uint32_t r0[16], r1[16];
+                tc_ld16(lane_base + TM::O0 + hf * (D / 2) + 16 * c, r0);
+                tc_ld16(lane_base + TM::O1 + hf * (D / 2) + 16 * c, r1);
                 tc_wait_ld();
                 if (row_in) {
+                    float o[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = fmaf(__uint_as_float(r0[e]), f0, __uint_as_float(r1[e]) * f1);
                     uint4* dst = reinterpret_cast<uint4*>(orow + 16 * c);
 #pragma unroll
                     for (int v = 0; v < 2; ++v) {
                         uint4 w;
-                        w.x = pack2<BF16>(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-                        w.y = pack2<BF16>(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-                        w.z = pack2<BF16>(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-                        w.w = pack2<BF16>(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                        w.x = pack2<BF16>(o[8 * v + 0], o[8 * v + 1]);
+                        w.y = pack2<BF16>(o[8 * v + 2], o[8 * v + 3]);
+                        w.z = pack2<BF16>(o[8 * v + 4], o[8 * v + 5]);
+                        w.w = pack2<BF16>(o[8 * v + 6], o[8 * v + 7]);
                         dst[v] = w;
                     }
                 }
             }
-            if (row_in && hf == 0) lse[lse_index(p, b, h, t0, i)] = any ? (m_run + log2f(l_run)) * kLn2 : INFINITY;
+            if (row_in && hf == 0) lse[lse_index(p, b, h, t0, i)] = any ? (mx + log2f(l_run)) * kLn2 : INFINITY;
         }
     }
     tc_fence_before();

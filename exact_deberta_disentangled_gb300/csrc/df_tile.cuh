@@ -90,21 +90,34 @@ DF_DEV void fill_dwin(const ProblemDev& p, const int32_t* __restrict__ dtab, int
     }
 }
 
-// Copy the columns of a band product that a warp needs (`lo` .. `hi`, band
-// coordinates) from tensor memory to the thread's shared-memory row, scaled
-// to base-2 exponent units and rounded to fp16.  Returns the band coordinate
+// Copy the columns of a band product that a lane quarter needs (`lo` ..
+// `hi`, band coordinates) from tensor memory to the thread's shared-memory
+// row, scaled to base-2 exponent units and rounded to fp16.  The window is cut
+// into 16-column chunks; the warp copies chunks part, part + nparts, ... (the
+// two warps of a lane quarter share the work).  Returns the band coordinate
 // of dst[0] (warp-uniform, a multiple of 16).
-DF_DEV int copy_band_window(uint32_t t_lane_col0, int lo, int hi, uint16_t* dst, float scale) {
+DF_DEV int copy_band_window(uint32_t t_lane_col0, int lo, int hi, uint16_t* dst, float scale, int part = 0,
+                            int nparts = 1) {
     const int a = lo & ~15;
     const int nch = ((hi - a) >> 4) + 1;
-    for (int c = 0; c < nch; ++c) {
-        uint32_t r[16];
-        tc_ld16(t_lane_col0 + (uint32_t)(a + 16 * c), r);
+    for (int c = part; c < nch; c += 2 * nparts) {
+        // two chunks per tensor-memory round trip
+        const bool two = c + nparts < nch;
+        uint32_t r[32];
+        tc_ld16p(t_lane_col0 + (uint32_t)(a + 16 * c), r);
+        if (two) tc_ld16p(t_lane_col0 + (uint32_t)(a + 16 * (c + nparts)), r + 16);
         tc_wait_ld();
         uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + 16 * c);
 #pragma unroll
         for (int x = 0; x < 8; ++x)
             d32[x] = pack2<false>(__uint_as_float(r[2 * x]) * scale, __uint_as_float(r[2 * x + 1]) * scale);
+        if (two) {
+            uint32_t* e32 = reinterpret_cast<uint32_t*>(dst + 16 * (c + nparts));
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                e32[x] = pack2<false>(__uint_as_float(r[16 + 2 * x]) * scale,
+                                      __uint_as_float(r[16 + 2 * x + 1]) * scale);
+        }
     }
     return a;
 }

@@ -60,6 +60,41 @@ def job_throughput(world: int, step_flops: float, seconds_per_step: float) -> fl
     return world * step_flops / seconds_per_step / 1e12
 
 
+# DRAM traffic of one launch of each attention kernel at this workload, from the
+# committed ncu summary of that kernel; reported only while the kernel's sources
+# are the ones the counters were taken on (else null)
+PROFILE_FILES = {
+    "fwd": ("fwd_tc_kernel_L8192_B1_H12_D64.md", ["df_fwd.cu", "df_tile.cuh", "df_common.cuh"]),
+    "dkv": ("bwd_tc_kernel_dkv_L8192_B1_H12_D64.md",
+            ["df_bwd_kernel.cuh", "df_bwd_dkv.cu", "df_tile.cuh", "df_common.cuh"]),
+    "dq": ("bwd_tc_kernel_dq_L8192_B1_H12_D64.md",
+           ["df_bwd_kernel.cuh", "df_bwd_dq.cu", "df_tile.cuh", "df_common.cuh"]),
+}
+
+
+def kernel_traffic(kernel: str):
+    import hashlib
+    if kernel not in PROFILE_FILES:
+        return None
+    md, srcs = PROFILE_FILES[kernel]
+    try:
+        fields = {}
+        with open(os.path.join(ROOT, "profiles", md)) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip().split()[0] if v.strip() else ""
+        h = hashlib.sha256()
+        for name in srcs:
+            with open(os.path.join(ROOT, "exact_deberta_disentangled_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if fields.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
+            return None
+        return int(fields["traffic_bytes_per_launch_L8192_B2"])
+    except Exception:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -289,13 +324,7 @@ def run_gpu(args, rank, world, local_rank):
               "rel": B * H * 8 * L * R * D}
     peak = peaks.get("bf16_tflops", 1900.0)
     achieved = kflops[dominant] / (avg[dominant] * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get(dominant)
-        except Exception:
-            traffic = None
+    traffic = kernel_traffic(dominant)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         v_cpu, desc, nthr, _ = oracle_sample(args.ref_seconds)
@@ -317,16 +346,19 @@ def run_gpu(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
-        "gpu_launches": args.steps * 13,
+        # per step: delta table x2, relative scalars x2, fwd, Dl, dQ, dK/dV,
+        # relative-gradient row / column / reduce kernels x2 each
+        "gpu_launches": args.steps * 14,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
 
 
 def run_profile_case(args, local_rank):
-    """Small case for kernel profiling (ncu): the sweep shape at L=4096,
-    B=2, H=12 (8,192 tokens; inputs + diagonal-sum buffers > L2).  Runs
-    warmup + steps fwd+bwd iterations without timing."""
+    """Small case for kernel profiling (ncu): one sequence of the L=8192
+    workload (B=1, H=12, 8,192 tokens: the same tile mix as the timed
+    workload at half its size; inputs + diagonal-sum buffers ~330 MB > L2).
+    Runs warmup + steps fwd+bwd iterations without timing."""
     import torch
 
     from exact_deberta_disentangled_gb300 import binding as Bd
@@ -334,8 +366,8 @@ def run_profile_case(args, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = synth.WORKLOADS["sweep_L4096"]
-    x = synth.make_inputs(w, B=2)
+    w = synth.WORKLOADS["sweep_L8192"]
+    x = synth.make_inputs(w, B=1)
     g = Bd.Geometry(B=x.B, L=x.L, H=w.H, D=w.D, span=w.span, nb=w.nb, mp=w.mp)
     q, k, v, qr, kr, do = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
     out, lse, wsf = Bd.attn_fwd(g, q, k, v, qr, kr)
@@ -344,7 +376,9 @@ def run_profile_case(args, local_rank):
         Bd.attn_fwd(g, q, k, v, qr, kr, out=out, lse=lse, workspace=wsf)
         Bd.attn_bwd(g, q, k, v, qr, kr, out, lse, do, grads=grads, workspace=wsb)
     torch.cuda.synchronize()
-    assert Bd.device_error(wsf) == 0 and Bd.device_error(wsb) == 0
+    ef, eb = Bd.device_error(wsf), Bd.device_error(wsb)
+    if ef or eb:
+        raise SystemExit(f"device error word: forward {ef}, backward {eb}")
     print("profile case done", flush=True)
 
 
@@ -357,7 +391,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-run", action="store_true",
-                    help="run the small profiling case (L=4096, B=2) without timing")
+                    help="run the small profiling case (L=8192, B=1) without timing")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -1,757 +1,30 @@
-// df_bwd.cu -- tensor-core backward of exact disentangled attention.
+// df_bwd.cu -- the backward pass: clears the diagonal-sum buffers G / G',
+// runs the dQ kernel and the dK/dV kernel (df_bwd_kernel.cuh) and then the
+// relative-position gradients (df_rel.cu).
 //
 // "DisentangledFlash" (section "Hugging Face usage") splits the fused
 // backward into a dQ kernel and a dK/dV kernel; section "Performance" counts
-// the relative-position gradients.  Here both attention kernels are one
-// template, mirrored by SIGMA:
-//
-//   SIGMA = +1 (dQ kernel):   rows = 128 queries, columns = key tiles
-//        S = Q K^T, dPd = dO V^T, dZ = c P (dP - Dl),  dQ += dZ K
-//        G[i, r]  = sum_{j: delta(i-j) = r} dZ[i, j]
-//   SIGMA = -1 (dK/dV kernel): rows = 128 keys, columns = query tiles
-//        S^T = K Q^T, dPd^T = V dO^T,  dV += Pd^T dO,  dK += dZ^T Q
-//        G'[j, r] = sum_{i: delta(i-j) = r} dZ[i, j]
-//
-// P is recomputed from the forward's LSE (never stored) and the dropout mask
-// is regenerated from the same Philox stream.  Every output row has exactly
-// one owner CTA and every sum runs in a fixed order, so the result is
-// bitwise reproducible with no floating-point atomics.
-//
-// G / G' ([T, H, Rp] in the input dtype) feed the relative-position
-// gradients (df_rel.cu):  dQ += G Kr,  dK += G' Qr,  dKr = sum G^T Q,
-// dQr = sum G'^T K.  A band tile adds its diagonal sums with a TMA
-// reduce-add of a [128 x band] box; every element receives at most two
-// non-zero additions that way (neighbouring tiles share at most one relative
-// row), so the order of the additions cannot change the result.  The two
-// clamped rows (delta 0 and R-1), which collect the far field, are summed in
-// registers and added once at the end.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include <type_traits>
-
-#include "df_tile.cuh"
+// the relative-position gradients.
+#include "df_internal.h"
 
 namespace df {
-namespace {
 
-constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
-constexpr float kLog2e = 1.4426950408889634f;
-
-// Tensor-memory columns (512 per CTA).  The fp32 S and dP of the tile being
-// processed sit in [256, 256 + 2 BN); the band products alias them.  The
-// 16-bit dZ and P~ that feed the dK / dQ / dV products have their own
-// columns, so the issuer can compute the next tile's S / dP as soon as the
-// softmax warps have read this tile's into registers.
-template <int D>
-struct BwdTmem {
-    using G = Geo<D>;
-    static constexpr uint32_t ACC1 = 0, ACC2 = D;                       // fp32 accumulators
-    static constexpr uint32_t S = 256, P = 256 + G::BN;                 // fp32 S, dP
-    static constexpr uint32_t Z = 2 * D + G::BN <= 256 ? 2 * D : 256 + 2 * G::BN;   // 16-bit dZ, then P~
-    static constexpr uint32_t T = 256;                                  // band products
-    static constexpr bool T_OVER_Z = Z >= 256 && T + G::NBAND > Z;      // band products overwrite dZ / P~
-    static_assert(P + G::BN <= 512 && Z + G::BN <= 512 && T + G::NBAND <= 512, "tensor memory");
-    static_assert(Z >= 2 * D && (Z + G::BN <= 256 || Z >= P + G::BN), "overlap");
-};
-
-template <int D>
-struct BwdSmem {
-    using G = Geo<D>;
-    static constexpr int GBOXW = G::BN == 128 ? 136 : 104;   // two boxes cover band + 8-alignment slack
-    static constexpr int R1 = 0;
-    static constexpr int RB = G::BM * D * 2;
-    static constexpr int R2 = R1 + RB;
-    static constexpr int CB = G::BN * D * 2;
-    static constexpr int C1 = R2 + RB;                       // [2] stages
-    static constexpr int C2 = C1 + 2 * CB;                   // [2] stages
-    static constexpr int BAND = C2 + 2 * CB;
-    static constexpr int BANDB = G::NBAND * G::CW * 2;
-    static constexpr int STG = BAND + BANDB;                 // own | cross, aliased by the G boxes
-    static constexpr int OWNB = G::BM * G::OWN_S * 2;
-    static constexpr int CROSS = STG + (OWNB + 15) / 16 * 16;
-    static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
-    static constexpr int GSB = 2 * G::BM * GBOXW * 2;
-    static constexpr int STGB = (CROSS - STG) + CROSSB > GSB ? (CROSS - STG) + CROSSB : GSB;
-    static constexpr int DWIN = (STG + STGB + 15) / 16 * 16;
-    static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // [2 tiles][colb | cdl][BN]
-    static constexpr int XCH = COLV + 4 * G::BN * 4;       // [4][BM] floats: exchanges between the two halves
-    static constexpr int MISC = XCH + 4 * G::BM * 4;
-    static constexpr int BYTES = MISC + 256;
-    static constexpr int ALLOC = BYTES + 1024;
-    static_assert(ALLOC <= 232448, "shared memory");
-    static_assert(STG % 16 == 0 && (GBOXW * 2) % 16 == 0, "staging rows are zeroed 16 bytes at a time");
-};
-
-struct BwdBars {
-    uint64_t row_full;
-    uint64_t c_full[2], c_empty[2];
-    uint64_t band_full, band_empty;
-    uint64_t t_full, t_empty;
-    uint64_t s_full, sread, z_full, zread, mma3_done;
-    uint32_t tmem_base;
-    int abort_flag;
-    int cross_base[4];
-};
-
-DF_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-DF_DEV void tma_reduce_add_2d(const CUtensorMap* m, const void* smem_src, int x, int y) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            (uint64_t)m),
-        "r"(smem_u32(smem_src)), "r"(x), "r"(y)
-        : "memory");
-}
-DF_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-DF_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-DF_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-template <bool BF16>
-DF_DEV uint16_t f2h16(float v) {
-    return (uint16_t)(pack2<BF16>(v, 0.f) & 0xFFFFu);
-}
-template <bool BF16>
-DF_DEV float h16f(uint16_t v) {
-    return BF16 ? __uint_as_float((uint32_t)v << 16) : h2f(v);
-}
-
-template <int D, bool BF16, int SIGMA>
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
-                  const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmC2,
-                  const __grid_constant__ CUtensorMap tmXr, const __grid_constant__ CUtensorMap tmYr,
-                  const __grid_constant__ CUtensorMap tmG, const ProblemDev p, const int32_t* __restrict__ dtab,
-                  const float* __restrict__ relb, const float* __restrict__ lse, const float* __restrict__ rowterm,
-                  float* __restrict__ acc1_out, void* __restrict__ acc2_out, void* __restrict__ Gbuf, int Rp) {
-    using G = Geo<D>;
-    using S = BwdSmem<D>;
-    using TM = BwdTmem<D>;
-    using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-    constexpr int BM = G::BM, BN = G::BN;
-    constexpr bool ROWQ = SIGMA > 0;   // rows are queries
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    BwdBars* bars = reinterpret_cast<BwdBars*>(smem + S::MISC);
-    int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
-    float* colv = reinterpret_cast<float*>(smem + S::COLV);
-    float* xch = reinterpret_cast<float*>(smem + S::XCH);
-    uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::STG);
-    uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
-    uint16_t* gstage = reinterpret_cast<uint16_t*>(smem + S::STG);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y, b = blockIdx.z;
-    int t0, n;
-    seq_ok(p, b, t0, n);
-    const int r0 = blockIdx.x * BM;   // first row token (query or key) of this CTA
-    if (r0 >= n) return;
-    const int ntiles = (n + BN - 1) / BN;
-    auto tile_base = [&](int m) { return ROWQ ? r0 - m * BN : m * BN - r0; };
-
-    if (threadIdx.x == 0) {
-        mbar_init(&bars->row_full, 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->c_full[s], 1);
-            mbar_init(&bars->c_empty[s], 1);
-        }
-        mbar_init(&bars->band_full, 1);
-        mbar_init(&bars->band_empty, 1);
-        mbar_init(&bars->t_full, 1);
-        mbar_init(&bars->t_empty, 8);
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->sread, 8);
-        mbar_init(&bars->z_full, 8);
-        mbar_init(&bars->zread, 8);
-        mbar_init(&bars->mma3_done, 1);
-        bars->abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        tc_alloc(&bars->tmem_base, 512);
-        tc_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
-    volatile int* abort_flag = &bars->abort_flag;
-    int* err = p.err;
-
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars->row_full, 2 * S::RB);
-            for (int c = 0; c < G::NCH; ++c) {
-                tma_load_2d(smem + S::R1 + c * BM * G::CW * 2, &tmR1, h * D + c * G::CW, t0 + r0, &bars->row_full);
-                tma_load_2d(smem + S::R2 + c * BM * G::CW * 2, &tmR2, h * D + c * G::CW, t0 + r0, &bars->row_full);
-            }
-            int band_loads = 0;
-            for (int it = 0; it < ntiles; ++it) {
-                const int s = it & 1, use = it >> 1;
-                const int c0 = it * BN;
-                if (use > 0 && !mbar_wait(&bars->c_empty[s], (use - 1) & 1, err, abort_flag)) break;
-                mbar_arrive_expect_tx(&bars->c_full[s], 2 * S::CB);
-                for (int c = 0; c < G::NCH; ++c) {
-                    tma_load_2d(smem + S::C1 + s * S::CB + c * BN * G::CW * 2, &tmC1, h * D + c * G::CW, t0 + c0,
-                                &bars->c_full[s]);
-                    tma_load_2d(smem + S::C2 + s * S::CB + c * BN * G::CW * 2, &tmC2, h * D + c * G::CW, t0 + c0,
-                                &bars->c_full[s]);
-                }
-                const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, tile_base(it));
-                if (tk.uniform) continue;
-                bool ok = true;
-                for (int pass = 0; pass < 2 && ok; ++pass) {
-                    for (int c = 0; c < G::NCH; ++c) {
-                        if (band_loads > 0 &&
-                            !mbar_wait(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&bars->band_full, S::BANDB);
-                        tma_load_2d(smem + S::BAND, pass == 0 ? &tmXr : &tmYr, c * G::CW, h * p.R + tk.dlo,
-                                    &bars->band_full);
-                        ++band_loads;
-                    }
-                }
-                if (!ok) break;
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Order per tile m:  S / dP of tile m + 1 (once the softmax warps have
-        // read tile m's into registers), then the dK / dV (dQ) products of tile
-        // m (once its 16-bit dZ / P~ are written).  When the next tile's band
-        // products would overwrite dZ / P~, they wait for tile m to finish.
-        if (lane == 0) {
-            const uint32_t sR1 = smem_u32(smem + S::R1), sR2 = smem_u32(smem + S::R2);
-            const uint32_t sBand = smem_u32(smem + S::BAND);
-            constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
-            constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
-            constexpr uint32_t idA = idesc_f16(128, D, BF16, false, true);
-            bool ok = mbar_wait(&bars->row_full, 0, err, abort_flag);
-            int band_used = 0, t_uses = 0;
-            auto issue_sdp = [&](int m) -> bool {
-                const int s = m & 1, use = m >> 1;
-                const uint32_t sC1 = smem_u32(smem + S::C1 + s * S::CB), sC2 = smem_u32(smem + S::C2 + s * S::CB);
-                const TileKind tk = classify<BM, BN, SIGMA>(p, dtab, tile_base(m));
-                if (!tk.uniform) {
-                    for (int pass = 0; pass < 2; ++pass) {
-                        if (pass == 1 && !mbar_wait(&bars->c_full[s], use & 1, err, abort_flag)) return false;
-                        if (t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
-                            return false;
-                        const uint32_t sA = pass == 0 ? sR1 : sC1;
-                        const int arows = pass == 0 ? BM : BN;
-                        for (int c = 0; c < G::NCH; ++c) {
-                            if (!mbar_wait(&bars->band_full, band_used & 1, err, abort_flag)) return false;
-                            tc_fence_after();
-                            for (int k = 0; k < G::CW / 16; ++k)
-                                tc_mma_ss(tmem + TM::T, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
-                                          desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
-                            tc_commit(&bars->band_empty);
-                            ++band_used;
-                        }
-                        tc_commit(&bars->t_full);
-                        ++t_uses;
-                    }
-                    // S / dP reuse the band columns: wait until the cross window was copied out
-                    if (!mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)) return false;
-                } else if (!mbar_wait(&bars->c_full[s], use & 1, err, abort_flag)) {
-                    return false;
-                }
-                tc_fence_after();
-                for (int k = 0; k < D / 16; ++k) {
-                    tc_mma_ss(tmem + TM::S, desc_k<G>(sR1, BM, k), desc_k<G>(sC1, BN, k), idS, k != 0);
-                    tc_mma_ss(tmem + TM::P, desc_k<G>(sR2, BM, k), desc_k<G>(sC2, BN, k), idS, k != 0);
-                }
-                tc_commit(&bars->s_full);
-                return true;
-            };
-            auto issue_acc = [&](int m) -> bool {
-                const int s = m & 1;
-                const uint32_t sC1 = smem_u32(smem + S::C1 + s * S::CB), sC2 = smem_u32(smem + S::C2 + s * S::CB);
-                if (!mbar_wait(&bars->z_full, m & 1, err, abort_flag)) return false;
-                tc_fence_after();
-                for (int k = 0; k < BN / 16; ++k) {
-                    // acc1 += dZ . C1   (dQ += dZ K  |  dK += dZ^T Q)
-                    tc_mma_ts(tmem + TM::ACC1, tmem + TM::Z + k * 8, desc_mn<G>(sC1, BN, k), idA, (m | k) != 0);
-                    // dV += Pd^T dO
-                    if (!ROWQ)
-                        tc_mma_ts(tmem + TM::ACC2, tmem + TM::Z + BN / 2 + k * 8, desc_mn<G>(sC2, BN, k), idA,
-                                  (m | k) != 0);
-                }
-                tc_commit(&bars->c_empty[s]);
-                tc_commit(&bars->mma3_done);
-                return true;
-            };
-            if (ok) ok = issue_sdp(0);
-            for (int it = 0; it < ntiles && ok; ++it) {
-                const bool nxt = it + 1 < ntiles;
-                const bool early =
-                    nxt && (!TM::T_OVER_Z || classify<BM, BN, SIGMA>(p, dtab, tile_base(it + 1)).uniform);
-                if (early) {
-                    if (!(ok = mbar_wait(&bars->sread, it & 1, err, abort_flag))) break;
-                    if (!(ok = issue_sdp(it + 1))) break;
-                }
-                if (!(ok = issue_acc(it))) break;
-                if (nxt && !early) {
-                    // the band products overwrite this tile's dZ / P~: wait until the
-                    // products and the diagonal sums have read them
-                    if (!(ok = mbar_wait(&bars->sread, it & 1, err, abort_flag))) break;
-                    if (!(ok = mbar_wait(&bars->mma3_done, it & 1, err, abort_flag))) break;
-                    if (!(ok = mbar_wait(&bars->zread, it & 1, err, abort_flag))) break;
-                    if (!(ok = issue_sdp(it + 1))) break;
-                }
-            }
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax / gradient warps
-        // Eight warps: warp w owns TMEM lanes 32 (w & 3) .. +31 (rows) and
-        // column half hf = (w - 2) / 4 of every tile.  Band-window copies and
-        // the diagonal sums of band tiles are split between the two halves;
-        // every warp takes the same bounded waits.
-        const int w4 = warp & 3;
-        const int hf = (warp - 2) >> 2;
-        const int row = 32 * w4 + lane;
-        const int tid = threadIdx.x - 64;     // 0..255
-        const int pair_bar = 2 + w4;
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * w4) << 16);
-        constexpr int NCT = BN / 64;          // 32-column chunks per thread
-        constexpr int HC = BN / 2;            // columns per half
-        const int cbeg = hf * NCT;
-        const int rt = r0 + row;              // row token position in the sequence
-        const bool row_in = rt < n;
-        const size_t T = (size_t)p.T;
-        const float* relb_h = relb + (size_t)h * 4 * T;
-        const float kscale = p.scale * kLog2e;
-        // per-row constants
-        float rb0 = -INFINITY, rb1 = -INFINITY, lse2 = INFINITY, dl = 0.f;
-        if (row_in) {
-            const bool rvalid = ROWQ ? (!p.qmask || p.qmask[t0 + rt]) : (!p.kmask || p.kmask[t0 + rt]);
-            if (rvalid) {
-                rb0 = relb_h[(ROWQ ? 0 : 2) * T + t0 + rt];
-                rb1 = relb_h[(ROWQ ? 1 : 3) * T + t0 + rt];
-            }
-            if (ROWQ) {
-                lse2 = lse[lse_index(p, b, h, t0, rt)] * kLog2e;
-                dl = rowterm[lse_index(p, b, h, t0, rt)];
-            }
-        }
-        const bool rvalid = rb0 != -INFINITY;
-        const float dls_row = p.scale * dl;
-        float g_lo = 0.f, g_hi = 0.f;     // this thread's share of the diagonal sums at delta 0 and R-1
-        int t_uses = 0;
-        bool ok = true;
-        uint16_t* own_row = own + row * G::OWN_S;
-        // per-column terms of a tile:
-        //   cv0 = column bias (P2C of keys / C2P of queries in uniform tiles,
-        //         0 in band tiles, -inf for masked or missing columns), minus the
-        //         column's LSE (base 2) when the columns are queries;
-        //   cv1 = c * Dl of the column (dK/dV kernel only)
-        // They go to shared memory one tile ahead (double-buffered) and are
-        // loaded from global memory two tiles ahead.
-        auto colterms = [&](int ct_tile, const TileKind& k, float& v0, float& v1) {
-            v0 = -INFINITY;
-            v1 = 0.f;
-            const int ct = ct_tile * BN + tid;
-            if (tid >= BN || ct >= n) return;
-            const bool cvalid = ROWQ ? (!p.kmask || p.kmask[t0 + ct]) : (!p.qmask || p.qmask[t0 + ct]);
-            if (!cvalid) return;
-            float cb = k.uniform ? relb_h[((ROWQ ? 2 : 0) + k.which) * T + t0 + ct] : 0.f;
-            if (!ROWQ) {
-                cb -= lse[lse_index(p, b, h, t0, ct)] * kLog2e;
-                v1 = p.scale * rowterm[lse_index(p, b, h, t0, ct)];
-            }
-            v0 = cb;
-        };
-        auto put_colterms = [&](int slot, float v0, float v1) {
-            if (tid < BN) {
-                colv[slot * 2 * BN + tid] = v0;
-                colv[slot * 2 * BN + BN + tid] = v1;
-            }
-        };
-        TileKind tk_cur = classify<BM, BN, SIGMA>(p, dtab, tile_base(0));
-        TileKind tk_n1 = tk_cur;
-        float cv0_n, cv1_n;   // column terms of the tile two ahead of the one being processed
-        {
-            float v0, v1;
-            colterms(0, tk_cur, v0, v1);
-            put_colterms(0, v0, v1);
-        }
-        if (ntiles > 1) {
-            tk_n1 = classify<BM, BN, SIGMA>(p, dtab, tile_base(1));
-            colterms(1, tk_n1, cv0_n, cv1_n);
-        }
-        for (int it = 0; it < ntiles && ok; ++it) {
-            const int c0 = it * BN;
-            const int base = tile_base(it);
-            const TileKind tk = tk_cur;
-            const float* colb = colv + (it & 1) * 2 * BN;
-            const float* cdl = colb + BN;
-            if (tid == 0) bulk_wait_read0();   // the previous G box left shared memory
-            named_bar_sync(1, 256);
-            if (it + 1 < ntiles) {
-                put_colterms((it + 1) & 1, cv0_n, cv1_n);
-                tk_cur = tk_n1;
-                if (it + 2 < ntiles) {
-                    tk_n1 = classify<BM, BN, SIGMA>(p, dtab, tile_base(it + 2));
-                    colterms(it + 2, tk_n1, cv0_n, cv1_n);
-                }
-            }
-            int own_a = 0;
-            if (!tk.uniform) {
-                fill_dwin<BM, BN, SIGMA>(p, dtab, base, tk.dlo, dwin, tid, 256);
-                int lo, hi;
-                own_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
-                own_a = lo & ~15;
-                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
-                tc_fence_after();
-                copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
-                if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
-                tc_fence_after();
-                if (32 * w4 < BN) {
-                    cross_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
-                    const int ca =
-                        copy_band_window(lane_base + TM::T, lo, hi, cross + row * G::CROSS_S, kscale, hf, 2);
-                    if (lane == 0 && hf == 0) bars->cross_base[w4] = ca;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
-                t_uses += 2;
-                named_bar_sync(1, 256);   // dwin, own / cross windows complete
-            }
-            if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
-            tc_fence_after();
-            const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
-            const bool band = !tk.uniform;
-            // per-row constant of the exponent (base 2): row bias, minus the row LSE for query rows
-            const float rowc = ROWQ ? rb - lse2 : rb;
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
-            // this thread's 32-column chunks: S, dP -> P, dZ (and Pd for the dK/dV kernel)
-#pragma unroll 1
-            for (int cc = 0; cc < NCT; ++cc) {
-                const int c = cbeg + cc;
-                uint32_t sr[32], pr[32];
-                tc_ld32(lane_base + TM::S + 32 * c, sr);
-                tc_ld32(lane_base + TM::P + 32 * c, pr);
-                tc_wait_ld();
-                if (cc == NCT - 1) {
-                    // all of this warp's S / dP columns are in registers
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->sread);
-                }
-                const float4* cv0p = reinterpret_cast<const float4*>(colb + 32 * c);
-                if (band) {
-                    const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
-                    const uint16_t* orow = own_row - own_a;
-                    const int16_t* dw = ROWQ ? dwin + row - 32 * c + BN - 1 : dwin + 32 * c - row + BM - 1;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 cv = cv0p[q];
-                        const float cvs[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const int e = 4 * q + t;
-                            const int m = ROWQ ? dw[-e] : dw[e];
-                            sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cvs[t]) + rowc +
-                                                    (h2f(orow[m]) + h2f(crow[e * G::CROSS_S + m])));
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 cv = cv0p[q];
-                        sr[4 * q + 0] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 0]), kscale, cv.x) + rowc);
-                        sr[4 * q + 1] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 1]), kscale, cv.y) + rowc);
-                        sr[4 * q + 2] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 2]), kscale, cv.z) + rowc);
-                        sr[4 * q + 3] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 3]), kscale, cv.w) + rowc);
-                    }
-                }
-                const uint32_t keep = !p.dropout ? 0xFFFFFFFFu
-                                      : ROWQ     ? keep_bits32_row(p, b, h, rt, c0 + 32 * c)
-                                                 : keep_bits32_col(p, b, h, c0 + 32 * c, rt);
-                const float4* cv1p = reinterpret_cast<const float4*>(cdl + 32 * c);
-                uint32_t zp[16], pp[16];   // packed as they are formed, so S / dP registers die early
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float dlq[4] = {dls_row, dls_row, dls_row, dls_row};
-                    if (!ROWQ) {
-                        const float4 d4 = cv1p[q];
-                        dlq[0] = d4.x;
-                        dlq[1] = d4.y;
-                        dlq[2] = d4.z;
-                        dlq[3] = d4.w;
-                    }
-                    float z[4], pd[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int e = 4 * q + t;
-                        const float pr_ = ex2(__uint_as_float(sr[e]));
-                        if (p.dropout) {
-                            const float kp = ((keep >> e) & 1u) ? p.drop_scale : 0.f;
-                            z[t] = pr_ * fmaf(__uint_as_float(pr[e]), p.scale * kp, -dlq[t]);
-                            pd[t] = pr_ * kp;
-                        } else {
-                            z[t] = pr_ * fmaf(__uint_as_float(pr[e]), p.scale, -dlq[t]);
-                            pd[t] = pr_;
-                        }
-                        rs[t] += z[t];
-                    }
-                    zp[2 * q] = pack2<BF16>(z[0], z[1]);
-                    zp[2 * q + 1] = pack2<BF16>(z[2], z[3]);
-                    pp[2 * q] = pack2<BF16>(pd[0], pd[1]);
-                    pp[2 * q + 1] = pack2<BF16>(pd[2], pd[3]);
-                }
-                if (cc == 0 && it > 0) {
-                    // the previous tile's products must have read their 16-bit operands
-                    if (!(ok = mbar_wait_warp(&bars->mma3_done, (it - 1) & 1, err, abort_flag))) break;
-                    tc_fence_after();
-                }
-                tc_st16(lane_base + TM::Z + 16 * c, zp);
-                if (!ROWQ) tc_st16(lane_base + TM::Z + BN / 2 + 16 * c, pp);
-            }
-            if (!ok) break;
-            const float rowsum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->z_full);
-            // ---- diagonal sums of dZ for this tile
-            if (!band) {
-                if (tk.which) g_hi += rowsum; else g_lo += rowsum;
-                if (lane == 0) mbar_arrive(&bars->zread);
-            } else {
-                named_bar_sync(1, 256);   // own / cross no longer read; every dZ is in tensor memory
-                tc_fence_after();
-                // staging rows: [BM][GBOXW] low box, then [BM][GBOXW] high box;
-                // half hf clears box hf of its row
-                {
-                    uint4* gz = reinterpret_cast<uint4*>(gstage + (size_t)(hf * BM + row) * S::GBOXW);
-#pragma unroll
-                    for (int x = 0; x < S::GBOXW / 8; ++x) gz[x] = make_uint4(0u, 0u, 0u, 0u);
-                }
-                uint16_t* g0 = gstage + (size_t)row * S::GBOXW;
-                uint16_t* g1 = gstage + (size_t)(BM + row) * S::GBOXW;
-                const int dlo8 = tk.dlo & ~7, off = tk.dlo - dlo8;
-                bool bad = false;
-                auto gstore = [&](int m, float v) {
-                    const int xx = m + off;
-                    bad |= xx < 0 || xx >= 2 * S::GBOXW;
-                    if (xx >= 0 && xx < S::GBOXW)
-                        g0[xx] = f2h16<BF16>(v);
-                    else if (xx >= S::GBOXW && xx < 2 * S::GBOXW)
-                        g1[xx - S::GBOXW] = f2h16<BF16>(v);
-                };
-                auto dw_at = [&](int col) -> int {
-                    return ROWQ ? dwin[row - col + BN - 1] : dwin[col - row + BM - 1];
-                };
-                // this half's dZ columns, 16-bit as the products use them
-                uint32_t zr[HC / 2];
-                if constexpr (HC == 64) {
-                    tc_ld32p(lane_base + TM::Z + hf * (HC / 2), zr);
-                } else {
-                    tc_ld16p(lane_base + TM::Z + hf * (HC / 2), zr);
-                }
-                tc_wait_ld();
-                named_bar_sync(pair_bar, 64);   // both boxes of the row are cleared
-                // Runs of equal relative index along the row.  A run that crosses
-                // from the first half into the second is finished by the first
-                // half: the second hands over its partial sum.
-                const int cst = hf * HC;
-                const int m_join = hf ? dw_at(cst - 1) : -1;
-                int run_m = dw_at(cst);
-                bool first_run = true;
-                float acc = 0.f, handoff = 0.f;
-#pragma unroll
-                for (int e = 0; e < HC; ++e) {
-                    const int m = dw_at(cst + e);
-                    const float v = h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
-                    if (m != run_m) {
-                        if (first_run && run_m == m_join) handoff = acc; else gstore(run_m, acc);
-                        first_run = false;
-                        run_m = m;
-                        acc = 0.f;
-                    }
-                    acc += v;
-                }
-                if (hf) {
-                    if (first_run && run_m == m_join) handoff = acc; else gstore(run_m, acc);
-                    xch[row] = handoff;
-                }
-                named_bar_sync(pair_bar, 64);
-                if (!hf) {
-                    gstore(run_m, acc + xch[row]);
-                    // the clamped relative rows (far field) are summed in registers
-                    if (tk.dlo == 0 && off < S::GBOXW) {
-                        g_lo += h16f<BF16>(g0[off]);
-                        g0[off] = 0;
-                    }
-                    if (tk.dhi == p.R - 1) {
-                        const int xx = p.R - 1 - tk.dlo + off;
-                        if (xx >= 0 && xx < S::GBOXW) {
-                            g_hi += h16f<BF16>(g0[xx]);
-                            g0[xx] = 0;
-                        } else if (xx >= S::GBOXW && xx < 2 * S::GBOXW) {
-                            g_hi += h16f<BF16>(g1[xx - S::GBOXW]);
-                            g1[xx - S::GBOXW] = 0;
-                        }
-                    }
-                }
-                if (bad) raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->zread);
-                named_bar_sync(1, 256);
-                if (tid == 0) {
-                    const int x0 = h * Rp + (tk.dlo & ~7);
-                    tma_reduce_add_2d(&tmG, gstage, x0, t0 + r0);
-                    tma_reduce_add_2d(&tmG, gstage + (size_t)BM * S::GBOXW, x0 + S::GBOXW, t0 + r0);
-                    bulk_commit();
-                }
-            }
-        }
-        if (tid == 0) bulk_wait0();
-        // ------------------------------------------------------------ epilogue
-        if (ok) ok = mbar_wait_warp(&bars->mma3_done, (ntiles - 1) & 1, err, abort_flag);
-        tc_fence_after();
-        if (ok) {
-            // accumulator columns [hf D/2, (hf+1) D/2), 16 at a time
-            float* a1 = acc1_out + ((size_t)(t0 + rt) * p.H + h) * D + hf * (D / 2);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[16];
-                tc_ld16(lane_base + TM::ACC1 + hf * (D / 2) + 16 * c, r);
-                tc_wait_ld();
-                if (row_in) {
-                    float4* dst = reinterpret_cast<float4*>(a1 + 16 * c);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                             __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                }
-            }
-            if (!ROWQ) {
-                T16* a2 = reinterpret_cast<T16*>(acc2_out) + ((size_t)(t0 + rt) * p.H + h) * D + hf * (D / 2);
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[16];
-                    tc_ld16(lane_base + TM::ACC2 + hf * (D / 2) + 16 * c, r);
-                    tc_wait_ld();
-                    if (row_in) {
-                        uint4* dst = reinterpret_cast<uint4*>(a2 + 16 * c);
-#pragma unroll
-                        for (int v = 0; v < 2; ++v) {
-                            uint4 w;
-                            w.x = pack2<BF16>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                            w.y = pack2<BF16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                            w.z = pack2<BF16>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                            w.w = pack2<BF16>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                            dst[v] = w;
-                        }
-                    }
-                }
-            }
-            // the far-field diagonal sums: the two halves' shares, added once;
-            // concurrent box additions to these two entries only ever add zero
-            xch[hf * BM + row] = g_lo;
-            xch[2 * BM + hf * BM + row] = g_hi;
-            named_bar_sync(pair_bar, 64);
-            if (row_in && hf == 0) {
-                const float glo = xch[row] + xch[BM + row];
-                const float ghi = xch[2 * BM + row] + xch[3 * BM + row];
-                uint16_t* grow = reinterpret_cast<uint16_t*>(Gbuf) + ((size_t)(t0 + rt) * p.H + h) * Rp;
-                if (glo != 0.f) grow[0] = f2h16<BF16>(h16f<BF16>(grow[0]) + glo);
-                if (ghi != 0.f) grow[p.R - 1] = f2h16<BF16>(h16f<BF16>(grow[p.R - 1]) + ghi);
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tc_dealloc(tmem, 512);
-    }
-}
-
-template <int D, bool BF16, int SIGMA>
-int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const void* r2, const void* c1,
-               const void* c2, const void* xr, const void* yr, void* Gbuf, int Rp, float* acc1, void* acc2,
-               const float* lse, cudaStream_t st) {
-    using G = Geo<D>;
-    using S = BwdSmem<D>;
-    CUtensorMap m1, m2, m3, m4, m5, m6, mg;
-    const uint64_t tok_dims[2] = {(uint64_t)p.H * D, (uint64_t)p.T};
-    const uint64_t tok_str[1] = {(uint64_t)p.H * D * 2};
-    const uint64_t rel_dims[2] = {(uint64_t)D, (uint64_t)p.H * p.R};
-    const uint64_t rel_str[1] = {(uint64_t)D * 2};
-    const uint64_t g_dims[2] = {(uint64_t)p.H * Rp, (uint64_t)p.T};
-    const uint64_t g_str[1] = {(uint64_t)p.H * Rp * 2};
-    const uint32_t boxr[2] = {(uint32_t)G::CW, (uint32_t)G::BM};
-    const uint32_t boxc[2] = {(uint32_t)G::CW, (uint32_t)G::BN};
-    const uint32_t boxb[2] = {(uint32_t)G::CW, (uint32_t)G::NBAND};
-    const uint32_t boxg[2] = {(uint32_t)S::GBOXW, (uint32_t)G::BM};
-    const int code = BF16 ? 0 : 1;
-    if (encode_tmap(&m1, code, 2, tok_dims, tok_str, boxr, G::SWZB, r1) ||
-        encode_tmap(&m2, code, 2, tok_dims, tok_str, boxr, G::SWZB, r2) ||
-        encode_tmap(&m3, code, 2, tok_dims, tok_str, boxc, G::SWZB, c1) ||
-        encode_tmap(&m4, code, 2, tok_dims, tok_str, boxc, G::SWZB, c2) ||
-        encode_tmap(&m5, code, 2, rel_dims, rel_str, boxb, G::SWZB, xr) ||
-        encode_tmap(&m6, code, 2, rel_dims, rel_str, boxb, G::SWZB, yr) ||
-        encode_tmap(&mg, code, 2, g_dims, g_str, boxg, 0, Gbuf))
-        return (int)cudaErrorInvalidValue;
-    auto kern = bwd_tc_kernel<D, BF16, SIGMA>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
-    if (e != cudaSuccess) return (int)e;
-    dim3 grid((p.L + G::BM - 1) / G::BM, p.H, p.B);
-    const int phase = SIGMA > 0 ? kProfDq : kProfDkv;
-    prof_record(phase, 0, st);
-    kern<<<grid, kThreads, S::ALLOC, st>>>(m1, m2, m3, m4, m5, m6, mg, p, ws.dtab, ws.relb, lse, ws.rowterm, acc1,
-                                           acc2, Gbuf, Rp);
-    prof_record(phase, 1, st);
-    return (int)cudaGetLastError();
-}
-
-template <int D, bool BF16>
-int launch_bwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, const void* k, const void* v,
-                    const void* qr, const void* kr, const float* lse, const void* dout, void* dq, void* dk,
-                    void* dv, void* dqr, void* dkr, cudaStream_t st) {
+int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
+                  const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
+                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st) {
+    if (p.D != 32 && p.D != 64 && p.D != 128) return (int)cudaErrorInvalidValue;
     const int Rp = ws.Rp;
     const size_t gbytes = (size_t)p.T * p.H * Rp * 2;
     cudaError_t ce = cudaMemsetAsync(ws.G, 0, gbytes, st);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(ws.Gp, 0, gbytes, st);
     if (ce != cudaSuccess) return (int)ce;
     // dQ kernel: rows = queries (Q, dO), columns = keys (K, V); own band Kr, cross Qr
-    int e = launch_one<D, BF16, 1>(p, ws, q, dout, k, v, kr, qr, ws.G, Rp, ws.acc32a, nullptr, lse, st);
+    int e = launch_bwd_dq(p, ws, dt, q, dout, k, v, kr, qr, ws.G, Rp, ws.acc32a, nullptr, lse, st);
     if (e) return e;
     // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO); own band Qr, cross Kr
-    e = launch_one<D, BF16, -1>(p, ws, k, v, q, dout, qr, kr, ws.Gp, Rp, ws.acc32b, dv, lse, st);
+    e = launch_bwd_dkv(p, ws, dt, k, v, q, dout, qr, kr, ws.Gp, Rp, ws.acc32b, dv, lse, st);
     if (e) return e;
-    return launch_rel_tc(p, ws, BF16 ? DF_BF16 : DF_FP16, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st);
-}
-
-}  // namespace
-
-int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
-                  const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
-                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st) {
-    const bool bf = dt == DF_BF16;
-    switch (p.D) {
-        case 32: return bf ? launch_bwd_impl<32, true>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st)
-                           : launch_bwd_impl<32, false>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st);
-        case 64: return bf ? launch_bwd_impl<64, true>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st)
-                           : launch_bwd_impl<64, false>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st);
-        case 128:
-            return bf ? launch_bwd_impl<128, true>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st)
-                      : launch_bwd_impl<128, false>(p, ws, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st);
-    }
-    return (int)cudaErrorInvalidValue;
+    return launch_rel_tc(p, ws, dt, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st);
 }
 
 }  // namespace df

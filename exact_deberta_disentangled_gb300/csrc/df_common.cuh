@@ -139,10 +139,15 @@ DF_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitNs.  On
-// give-up the device error word records DF_ERR_TIMEOUT and the CTA-wide abort
-// flag is set, so that every other role of the CTA stops waiting too.
+// Wait for phase `parity` of an mbarrier, giving up once BOTH kWaitLimitNs
+// have passed on the global timer AND kWaitMinProbes probes have failed (a
+// jump of the global timer alone, as a profiler's clock resynchronisation can
+// cause, does not end a wait that is about to succeed; a real hang still ends,
+// after at most max(2 s, 2^20 probes of <= 20 us)).  On give-up the device
+// error word records DF_ERR_TIMEOUT and the CTA-wide abort flag is set, so
+// that every other role of the CTA stops waiting too.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kWaitMinProbes = 1u << 20;
 
 DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err_word, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -151,7 +156,7 @@ DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err_word, volatile in
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 7u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (it >= kWaitMinProbes && globaltimer_ns() - t0 > kWaitLimitNs) {
                 raise_error(err_word, DF_ERR_TIMEOUT);
                 *abort_flag = 1;
                 return false;

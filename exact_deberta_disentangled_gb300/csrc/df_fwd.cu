@@ -85,7 +85,7 @@ struct FwdBars {
     int cross_base[4];
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKr,
@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < G::NCH; ++c)
                 tma_load_2d(smem + S::Q + c * BM * G::CW * 2, &tmQ, h * D + c * G::CW, t0 + i0, &bars->q_full);
             int band_loads = 0;
+            KindRaw kr = kind_fetch<BM, BN, 1>(p, dtab, i0);   // kind of the next tile, in flight
             for (int it = 0; it < ntiles; ++it) {
                 const int s = it & 1, use = it >> 1;
                 const int j0 = it * BN;
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
                                 &bars->kv_full[s]);
                 }
-                const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - j0);
+                const TileKind tk = kind_finish(p, kr);
+                kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - j0 - BN);
                 if (tk.uniform) continue;
                 bool ok = true;
                 for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -191,10 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int band_used = 0, t_uses = 0;
             int pv_cnt[2] = {0, 0};   // P.V rounds issued per S buffer
             // S (and, for band tiles, the two band products) of tile m into buffer m & 1
-            auto issue_s = [&](int m) -> bool {
+            auto issue_s = [&](int m, const TileKind& tk) -> bool {
                 const int s = m & 1, use = m >> 1, bf = m & 1;
                 const uint32_t sK = smem_u32(smem + S::K0 + s * S::KVB);
-                const TileKind tk = classify<BM, BN, 1>(p, dtab, i0 - m * BN);
                 if (!tk.uniform) {
                     // the band columns overlap S buffer 1: its last P must have been consumed
                     if (pv_cnt[1] > 0 && !mbar_wait(&bars->pv_done[1], (pv_cnt[1] - 1) & 1, err, abort_flag))
@@ -231,15 +232,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(&bars->s_full[bf]);
                 return true;
             };
-            auto is_band = [&](int m) { return !classify<BM, BN, 1>(p, dtab, i0 - m * BN).uniform; };
-            if (ok) ok = issue_s(0);
+            // the kind of tile it + 1 is fetched while tile it is handled
+            KindRaw kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - BN);
+            if (ok) ok = issue_s(0, classify<BM, BN, 1>(p, dtab, i0));
             for (int it = 0; it < ntiles && ok; ++it) {
                 const int s = it & 1;
                 const uint32_t sV = smem_u32(smem + S::V0 + s * S::KVB);
+                const TileKind kn = kind_finish(p, kr);
+                kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - (it + 2) * BN);
                 // uniform next tile: compute its S while the softmax works on this one
                 const bool next = it + 1 < ntiles;
-                const bool next_band = next && is_band(it + 1);
-                if (next && !next_band && !(ok = issue_s(it + 1))) break;
+                const bool next_band = next && !kn.uniform;
+                if (next && !next_band && !(ok = issue_s(it + 1, kn))) break;
                 // O_h += P_h V_h for the two column halves, each as soon as its P is ready
                 for (int hf = 0; hf < 2 && ok; ++hf) {
                     if (!(ok = mbar_wait(&bars->p_full[hf], it & 1, err, abort_flag))) break;
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(&bars->kv_empty[s]);
                 tc_commit(&bars->pv_done[it & 1]);
                 ++pv_cnt[it & 1];
-                if (next_band && !(ok = issue_s(it + 1))) break;
+                if (next_band && !(ok = issue_s(it + 1, kn))) break;
             }
         }
         __syncwarp();
@@ -297,38 +301,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_st16(lane_base + ocol + 16 * c, r);
             }
         };
-        // per-key column term of a tile (P2C scalar of uniform tiles, key mask,
-        // sequence end): loaded from global memory two tiles ahead and put into
-        // shared memory (double-buffered) one tile ahead
-        auto colterm = [&](int jt, const TileKind& k) -> float {
-            const int j = jt * BN + tid;
-            if (tid >= BN || j >= n) return -INFINITY;
-            if (k.uniform) return relb_h[(2 + k.which) * T + t0 + j];
-            return (p.kmask && !p.kmask[t0 + j]) ? -INFINITY : 0.f;
+        // per-key column term of a tile (P2C scalar of uniform tiles, with the
+        // key mask folded in; key mask of band tiles; -inf past the sequence
+        // end).  Its loads are issued two tiles ahead (col_fetch) and used one
+        // tile ahead (col_finish), when it goes to shared memory
+        // (double-buffered); tile kinds are fetched three tiles ahead.
+        struct ColRaw {
+            float cb;
+            int ok, mk;
         };
-        TileKind tk_cur = classify<BM, BN, 1>(p, dtab, i0);
-        TileKind tk_n1 = tk_cur;
-        float cb_n = -INFINITY;
-        {
-            const float v = colterm(0, tk_cur);
-            if (tid < BN) colv[tid] = v;
-        }
-        if (ntiles > 1) {
-            tk_n1 = classify<BM, BN, 1>(p, dtab, i0 - BN);
-            cb_n = colterm(1, tk_n1);
-        }
+        auto col_fetch = [&](int jt, const TileKind& k) -> ColRaw {
+            ColRaw c;
+            const int j = jt * BN + tid;
+            c.ok = tid < BN && j < n;
+            const int js = c.ok ? j : 0;   // an index that is safe to load
+            c.cb = k.uniform ? relb_h[(2 + k.which) * T + t0 + js] : 0.f;
+            c.mk = (!k.uniform && p.kmask) ? p.kmask[t0 + js] : 1;
+            return c;
+        };
+        auto put_colterm = [&](int slot, const ColRaw& c) {
+            if (tid < BN) colv[slot * BN + tid] = (c.ok && c.mk != 0) ? c.cb : -INFINITY;
+        };
+        const TileKind tk0 = classify<BM, BN, 1>(p, dtab, i0);
+        const TileKind tk1 = classify<BM, BN, 1>(p, dtab, i0 - BN);
+        put_colterm(0, col_fetch(0, tk0));
+        ColRaw cr = col_fetch(1, tk1);                                  // tile it + 1
+        KindRaw kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - 2 * BN);       // tile it + 2
+        uint32_t kc = pack_kind(tk0), kn = pack_kind(tk1);              // tiles it, it + 1
         for (int it = 0; it < ntiles && ok; ++it) {
             const int j0 = it * BN;
-            const TileKind tk = tk_cur;
+            const TileKind tk = unpack_kind(kc);
             const float* colb = colv + (it & 1) * BN;
             named_bar_sync(1, 256);
-            if (it + 1 < ntiles) {
-                if (tid < BN) colv[((it + 1) & 1) * BN + tid] = cb_n;
-                tk_cur = tk_n1;
-                if (it + 2 < ntiles) {
-                    tk_n1 = classify<BM, BN, 1>(p, dtab, i0 - j0 - 2 * BN);
-                    cb_n = colterm(it + 2, tk_n1);
-                }
+            put_colterm((it + 1) & 1, cr);
+            {
+                const TileKind k2 = kind_finish(p, kr);
+                cr = col_fetch(it + 2, k2);
+                kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - j0 - 3 * BN);
+                kc = kn;
+                kn = pack_kind(k2);
             }
             int own_a = 0;
             if (!tk.uniform) {
@@ -363,95 +374,126 @@ __global__ void __launch_bounds__(kThreads, 1)
             float rb = tk.uniform ? (tk.which ? a1 : a0) : 0.f;
             if (!row_valid) rb = -INFINITY;
             const bool band = !tk.uniform;
-            // a new running max for this half: rescale the sum and (once the
-            // previous tile's P.V has landed) the accumulator
-            auto raise_max = [&](float tmax) -> bool {
+            // a new running max for this half: rescale the sum now and the
+            // accumulator after this tile's P is stored (fewer live registers),
+            // once the previous tile's P.V has landed
+            float alpha = 1.f;
+            bool resc = false;
+            auto raise_max = [&](float tmax) {
                 const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
-                float alpha = 1.f;
                 if (need) {
-                    alpha = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
-                    l_part *= alpha;
+                    const float a = m_run == -INFINITY ? 0.f : ex2(m_run - tmax);
+                    alpha *= a;
+                    l_part *= a;
                     m_run = tmax;
                 }
-                if (__any_sync(0xffffffffu, need) && it > 0) {
-                    if (!mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err, abort_flag))
-                        return false;
-                    tc_fence_after();
-                    rescale_o(alpha);
+                resc |= need;
+            };
+            // Probabilities of this thread's chunks against the running max,
+            // written as 16-bit P over the middle half of S, chunk by chunk in
+            // chunk() order.  RAW: S holds Q.K^T (uniform tile: scale and column
+            // term applied here); otherwise band pass 1 left the biased logits.
+            auto p_pass = [&](auto raw_tag) -> float {
+                constexpr bool RAW = decltype(raw_tag)::value;
+                const float mm = (m_run == -INFINITY || rb == -INFINITY) ? INFINITY : m_run - rb;
+                float sm = 0.f;
+#pragma unroll 1
+                for (int cc = 0; cc < NCT; ++cc) {
+                    const int c = chunk(cc);
+                    uint32_t r[32];
+                    tc_ld32(lane_base + scol + 32 * c, r);
+                    tc_wait_ld();
+                    uint32_t keep = 0xFFFFFFFFu;
+                    if constexpr (DROP) keep = keep_bits32_row(p, b, h, i, j0 + 32 * c);
+                    const float* cbp = colb + 32 * c;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
+                        if constexpr (RAW) {
+                            x0 = fmaf(x0, kscale, cbp[2 * e]);
+                            x1 = fmaf(x1, kscale, cbp[2 * e + 1]);
+                        }
+                        const float p0 = ex2(x0 - mm);
+                        const float p1 = ex2(x1 - mm);
+                        sm += p0 + p1;
+                        float d0 = p0, d1 = p1;
+                        if constexpr (DROP) {
+                            d0 = ((keep >> (2 * e)) & 1u) ? p0 * p.drop_scale : 0.f;
+                            d1 = ((keep >> (2 * e + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
+                        }
+                        pk[e] = pack2<BF16>(d0, d1);
+                    }
+                    tc_st16(lane_base + scol + TM::POFF + 16 * c, pk);
                 }
-                return true;
+                return sm;
             };
             float sum = 0.f;
             if (!band) {
-                // Uniform tile, one pass: probabilities against the running max,
-                // kept in registers; redone (rarely) when the tile max moves the
-                // running max by more than kRescaleSlack.
+                // Uniform tile, one pass against the running max (+inf for a dead
+                // row or before the first max: every probability 0), kept in
+                // registers.  When the tile moves the running max by more than
+                // kRescaleSlack (and on the first tile) the warp recomputes P
+                // with p_pass instead.
                 uint32_t pk[16 * NCT];
-                const float m_old = m_run;
-                const bool attempted = m_old != -INFINITY && rb != -INFINITY;
-                float mm = attempted ? m_old - rb : INFINITY;
-                bool dead = !attempted;
-                for (int pass = 0; pass < 2; ++pass) {
-                    float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                    float sm[4] = {0.f, 0.f, 0.f, 0.f};
-                    uint32_t r[32 * NCT];
-#pragma unroll
-                    for (int cc = 0; cc < NCT; ++cc) tc_ld32p(lane_base + scol + 32 * (cbeg + cc), r + 32 * cc);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int cc = 0; cc < NCT; ++cc) {
-                        const int c = cbeg + cc;
-                        const uint32_t keep = p.dropout ? keep_bits32_row(p, b, h, i, j0 + 32 * c) : 0xFFFFFFFFu;
-                        const float4* cb4 = reinterpret_cast<const float4*>(colb + 32 * c);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 cv = cb4[q];
-                            const float x0 = fmaf(__uint_as_float(r[32 * cc + 4 * q + 0]), kscale, cv.x);
-                            const float x1 = fmaf(__uint_as_float(r[32 * cc + 4 * q + 1]), kscale, cv.y);
-                            const float x2 = fmaf(__uint_as_float(r[32 * cc + 4 * q + 2]), kscale, cv.z);
-                            const float x3 = fmaf(__uint_as_float(r[32 * cc + 4 * q + 3]), kscale, cv.w);
-                            tm[0] = fmaxf(tm[0], x0);
-                            tm[1] = fmaxf(tm[1], x1);
-                            tm[2] = fmaxf(tm[2], x2);
-                            tm[3] = fmaxf(tm[3], x3);
-                            float p0 = dead ? 0.f : ex2(x0 - mm), p1 = dead ? 0.f : ex2(x1 - mm);
-                            float p2 = dead ? 0.f : ex2(x2 - mm), p3 = dead ? 0.f : ex2(x3 - mm);
-                            sm[0] += p0;
-                            sm[1] += p1;
-                            sm[2] += p2;
-                            sm[3] += p3;
-                            if (p.dropout) {
-                                const uint32_t kq = keep >> (4 * q);
-                                p0 = (kq & 1u) ? p0 * p.drop_scale : 0.f;
-                                p1 = (kq & 2u) ? p1 * p.drop_scale : 0.f;
-                                p2 = (kq & 4u) ? p2 * p.drop_scale : 0.f;
-                                p3 = (kq & 8u) ? p3 * p.drop_scale : 0.f;
-                            }
-                            pk[16 * cc + 2 * q] = pack2<BF16>(p0, p1);
-                            pk[16 * cc + 2 * q + 1] = pack2<BF16>(p2, p3);
-                        }
-                    }
-                    sum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-                    if (pass == 1) break;
-                    const float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) + rb;
-                    const bool need = tmax > m_run + kRescaleSlack || (m_run == -INFINITY && tmax > -INFINITY);
-                    if (!(ok = raise_max(tmax))) break;
-                    const bool redo = need || (!attempted && m_run != -INFINITY && rb != -INFINITY);
-                    if (!__any_sync(0xffffffffu, redo)) break;
-                    dead = m_run == -INFINITY || rb == -INFINITY;
-                    mm = dead ? INFINITY : m_run - rb;
-                }
-                if (!ok) break;
+                const bool attempted = m_run != -INFINITY && rb != -INFINITY;
+                const float mm = attempted ? m_run - rb : INFINITY;
+                float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int cc = 0; cc < NCT; ++cc) {
-                    uint32_t r16[16];
+                    const int c = cbeg + cc;
+                    uint32_t r[32];
+                    tc_ld32(lane_base + scol + 32 * c, r);
+                    tc_wait_ld();
+                    uint32_t keep = 0xFFFFFFFFu;
+                    if constexpr (DROP) keep = keep_bits32_row(p, b, h, i, j0 + 32 * c);
+                    const float4* cb4 = reinterpret_cast<const float4*>(colb + 32 * c);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) r16[e] = pk[16 * cc + e];
-                    tc_st16(lane_base + scol + TM::POFF + 16 * (cbeg + cc), r16);
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 cv = cb4[q];
+                        const float x0 = fmaf(__uint_as_float(r[4 * q + 0]), kscale, cv.x);
+                        const float x1 = fmaf(__uint_as_float(r[4 * q + 1]), kscale, cv.y);
+                        const float x2 = fmaf(__uint_as_float(r[4 * q + 2]), kscale, cv.z);
+                        const float x3 = fmaf(__uint_as_float(r[4 * q + 3]), kscale, cv.w);
+                        tm[0] = fmaxf(tm[0], x0);
+                        tm[1] = fmaxf(tm[1], x1);
+                        tm[2] = fmaxf(tm[2], x2);
+                        tm[3] = fmaxf(tm[3], x3);
+                        float p0 = ex2(x0 - mm), p1 = ex2(x1 - mm);
+                        float p2 = ex2(x2 - mm), p3 = ex2(x3 - mm);
+                        sm[0] += p0;
+                        sm[1] += p1;
+                        sm[2] += p2;
+                        sm[3] += p3;
+                        if constexpr (DROP) {
+                            const uint32_t kq = keep >> (4 * q);
+                            p0 = (kq & 1u) ? p0 * p.drop_scale : 0.f;
+                            p1 = (kq & 2u) ? p1 * p.drop_scale : 0.f;
+                            p2 = (kq & 4u) ? p2 * p.drop_scale : 0.f;
+                            p3 = (kq & 8u) ? p3 * p.drop_scale : 0.f;
+                        }
+                        pk[16 * cc + 2 * q] = pack2<BF16>(p0, p1);
+                        pk[16 * cc + 2 * q + 1] = pack2<BF16>(p2, p3);
+                    }
+                }
+                sum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                raise_max(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) + rb);
+                const bool redo = resc || (!attempted && m_run != -INFINITY && rb != -INFINITY);
+                if (__any_sync(0xffffffffu, redo)) {
+                    sum = p_pass(std::true_type{});
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < NCT; ++cc) {
+                        uint32_t r16[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) r16[e] = pk[16 * cc + e];
+                        tc_st16(lane_base + scol + TM::POFF + 16 * (cbeg + cc), r16);
+                    }
                 }
             } else {
-                // ---- band tile: two passes over this thread's 32-column chunks
-                // pass 1: biased logits (written back over S) and the tile max
+                // ---- band tile, pass 1: biased logits (written back over S) and
+                // the tile max; pass 2 (p_pass): probabilities
                 float tm = -INFINITY;
 #pragma unroll 1
                 for (int cc = 0; cc < NCT; ++cc) {
@@ -474,34 +516,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_st32(lane_base + scol + 32 * c, r);
                 }
                 tc_wait_st();
-                if (!(ok = raise_max(tm + rb))) break;
-                // pass 2: probabilities, written as 16-bit P over the middle half of S
-                const float mm = m_run - rb;
-                const bool dead = m_run == -INFINITY || rb == -INFINITY;
-#pragma unroll 1
-                for (int cc = 0; cc < NCT; ++cc) {
-                    const int c = chunk(cc);
-                    uint32_t r[32];
-                    tc_ld32(lane_base + scol + 32 * c, r);
-                    tc_wait_ld();
-                    const uint32_t keep = p.dropout ? keep_bits32_row(p, b, h, i, j0 + 32 * c) : 0xFFFFFFFFu;
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = dead ? 0.f : ex2(__uint_as_float(r[2 * e]) - mm);
-                        const float p1 = dead ? 0.f : ex2(__uint_as_float(r[2 * e + 1]) - mm);
-                        sum += p0 + p1;
-                        float d0 = p0, d1 = p1;
-                        if (p.dropout) {
-                            d0 = ((keep >> (2 * e)) & 1u) ? p0 * p.drop_scale : 0.f;
-                            d1 = ((keep >> (2 * e + 1)) & 1u) ? p1 * p.drop_scale : 0.f;
-                        }
-                        pk[e] = pack2<BF16>(d0, d1);
-                    }
-                    tc_st16(lane_base + scol + TM::POFF + 16 * c, pk);
-                }
+                raise_max(tm + rb);
+                sum = p_pass(std::false_type{});
             }
             l_part += sum;
+            if (__any_sync(0xffffffffu, resc) && it > 0) {
+                if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err, abort_flag))) break;
+                tc_fence_after();
+                rescale_o(alpha);
+            }
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -560,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP>
 int launch_fwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, const void* k, const void* v,
                     const void* qr, const void* kr, void* out, float* lse, cudaStream_t st) {
     using G = Geo<D>;
@@ -580,7 +603,7 @@ int launch_fwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, con
         encode_tmap(&mkr, code, 2, rel_dims, rel_str, boxr, G::SWZB, kr) ||
         encode_tmap(&mqr, code, 2, rel_dims, rel_str, boxr, G::SWZB, qr))
         return (int)cudaErrorInvalidValue;
-    auto kern = fwd_tc_kernel<D, BF16>;
+    auto kern = fwd_tc_kernel<D, BF16, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
     if (e != cudaSuccess) return (int)e;
     dim3 grid((p.L + G::BM - 1) / G::BM, p.H, p.B);
@@ -594,15 +617,17 @@ int launch_fwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, con
 
 int launch_fwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
                   const void* v, const void* qr, const void* kr, void* out, float* lse, cudaStream_t st) {
-    const bool bf = dt == DF_BF16;
+#define DF_ONE(D_, BF_, DR_) launch_fwd_impl<D_, BF_, DR_>(p, ws, q, k, v, qr, kr, out, lse, st)
+#define DF_DT(D_, DR_) (dt == DF_BF16 ? DF_ONE(D_, true, DR_) : DF_ONE(D_, false, DR_))
+#define DF_DROP(D_) (p.dropout ? DF_DT(D_, true) : DF_DT(D_, false))
     switch (p.D) {
-        case 32: return bf ? launch_fwd_impl<32, true>(p, ws, q, k, v, qr, kr, out, lse, st)
-                           : launch_fwd_impl<32, false>(p, ws, q, k, v, qr, kr, out, lse, st);
-        case 64: return bf ? launch_fwd_impl<64, true>(p, ws, q, k, v, qr, kr, out, lse, st)
-                           : launch_fwd_impl<64, false>(p, ws, q, k, v, qr, kr, out, lse, st);
-        case 128: return bf ? launch_fwd_impl<128, true>(p, ws, q, k, v, qr, kr, out, lse, st)
-                            : launch_fwd_impl<128, false>(p, ws, q, k, v, qr, kr, out, lse, st);
+        case 32: return DF_DROP(32);
+        case 64: return DF_DROP(64);
+        case 128: return DF_DROP(128);
     }
+#undef DF_DROP
+#undef DF_DT
+#undef DF_ONE
     return (int)cudaErrorInvalidValue;
 }
 

@@ -68,6 +68,14 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
                   const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
                   void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st);
 
+// the two attention-backward kernels (df_bwd_dq.cu, df_bwd_dkv.cu): rows r1 / r2,
+// columns c1 / c2, own band rows xr, cross band rows yr
+int launch_bwd_dq(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* r1, const void* r2,
+                  const void* c1, const void* c2, const void* xr, const void* yr, void* Gbuf, int Rp, float* acc1,
+                  void* acc2, const float* lse, cudaStream_t st);
+int launch_bwd_dkv(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* r1, const void* r2,
+                   const void* c1, const void* c2, const void* xr, const void* yr, void* Gbuf, int Rp, float* acc1,
+                   void* acc2, const float* lse, cudaStream_t st);
 int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, const void* q, const void* k,
                   const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st);
 

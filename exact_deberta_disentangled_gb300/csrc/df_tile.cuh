@@ -68,16 +68,49 @@ struct TileKind {
     int which;     // uniform tiles: 0 -> delta 0, 1 -> delta R-1
 };
 
+// A TileKind in one register (dlo, dhi < R <= 1024), so that the kind of a
+// tile can be fetched a few tiles ahead: classify reads the relative-index
+// table from global memory, and using its result at once stalls the thread.
+DF_DEV uint32_t pack_kind(const TileKind& k) {
+    return (uint32_t)k.dlo | ((uint32_t)k.dhi << 14) | ((uint32_t)k.uniform << 28) | ((uint32_t)k.which << 29);
+}
+DF_DEV TileKind unpack_kind(uint32_t v) {
+    TileKind k;
+    k.dlo = (int)(v & 0x3FFFu);
+    k.dhi = (int)((v >> 14) & 0x3FFFu);
+    k.uniform = (int)((v >> 28) & 1u);
+    k.which = (int)((v >> 29) & 1u);
+    return k;
+}
+
+// The two relative indices that decide a tile's kind, as loaded: kind_fetch
+// only issues the loads, kind_finish (a tile later) uses them.
+struct KindRaw {
+    int dlo, dhi;
+};
+
 template <int NR, int NC, int SIGMA>
-DF_DEV TileKind classify(const ProblemDev& p, const int32_t* __restrict__ dtab, int base) {
+DF_DEV KindRaw kind_fetch(const ProblemDev& p, const int32_t* __restrict__ dtab, int base) {
     const int rlo = SIGMA > 0 ? base - (NC - 1) : base - (NR - 1);
     const int rhi = SIGMA > 0 ? base + (NR - 1) : base + (NC - 1);
+    KindRaw r;
+    r.dlo = dclamp(p, dtab, rlo);
+    r.dhi = dclamp(p, dtab, rhi);
+    return r;
+}
+
+DF_DEV TileKind kind_finish(const ProblemDev& p, const KindRaw& r) {
     TileKind k;
-    k.dlo = dclamp(p, dtab, rlo);
-    k.dhi = dclamp(p, dtab, rhi);
+    k.dlo = r.dlo;
+    k.dhi = r.dhi;
     k.uniform = k.dlo == k.dhi && (k.dlo == 0 || k.dlo == p.R - 1);
     k.which = k.dlo == 0 ? 0 : 1;
     return k;
+}
+
+template <int NR, int NC, int SIGMA>
+DF_DEV TileKind classify(const ProblemDev& p, const int32_t* __restrict__ dtab, int base) {
+    return kind_finish(p, kind_fetch<NR, NC, SIGMA>(p, dtab, base));
 }
 
 // dwin[x] = delta(r) - dlo for the tile, x = SIGMA*(row - col) + (SIGMA > 0 ? NC - 1 : NR - 1).

@@ -18,14 +18,14 @@ def geo(D):
     nband = 192 if BM + BN - 1 <= 192 else 256
     own_s = 114 if BN == 64 else 178
     cross_s = 176
-    gboxw = 136 if BN == 128 else 104
-    return BN, nband, own_s, cross_s, gboxw
+    gw = 320 if BN == 128 else 256        # staging row width (16-bit sums)
+    return BN, nband, own_s, cross_s, gw
 
 
 def check_kernel(L, span, nb, mp, D, sigma, n=None):
     """All (row tile, column tile) pairs of one sequence of length n <= L."""
     n = L if n is None else n
-    BN, NBAND, OWN_S, CROSS_S, GBOXW = geo(D)
+    BN, NBAND, OWN_S, CROSS_S, GW = geo(D)
     NR, NC = BM, BN
     R = 2 * span
     tab = oracle.delta_table(L, span, nb, mp)
@@ -76,11 +76,14 @@ def check_kernel(L, span, nb, mp, D, sigma, n=None):
                 assert a >= 0 and a + 16 * nch <= NBAND and 16 * nch <= CROSS_S
                 mu = m[:, 32 * u:32 * u + 32]
                 assert mu.min() >= lo and mu.max() <= hi
-            # backward: staged diagonal sums and the TMA box coordinates
-            off = dlo - (dlo & ~7)
+            # backward: staged diagonal sums (one row of GW sums per tile row,
+            # relative rows from dlo & ~63) and the far-field entries
+            off = dlo & 63
             xx = m + off
-            assert xx.min() >= 0 and xx.max() < 2 * GBOXW
-            assert (dlo & ~7) % 8 == 0 and (GBOXW * 2) % 16 == 0
+            assert xx.min() >= 0 and xx.max() < GW and GW % 64 == 0
+            for far in (0, R - 1):
+                if dlo <= far <= dhi:
+                    assert 0 <= far - dlo + off < GW
     return nband_tiles
 
 

@@ -61,8 +61,12 @@ struct BwdTmem {
 template <int D>
 struct BwdSmem {
     using G = Geo<D>;
+    static constexpr int kMaxTiles = 8192 / G::BN;          // L <= 8192
     // diagonal-sum staging: one row of GW 16-bit sums per tile row, covering
-    // relative rows [dlo & ~63, (dlo & ~63) + GW); a tile reaches at most
+    // relative rows [dlo & ~63, (dlo & ~63) + GW), stored as GW / 64 segments of
+    // 128 bytes with the TMA 128-byte swizzle (16-byte chunk c of segment s at
+    // position c ^ (s & 7)), so that the 32 rows of a warp do not all hit the
+    // same bank; a tile reaches at most
     // BM + BN - 1 of them, starting at most 63 in
     static constexpr int GW = G::BN == 128 ? 320 : 256;
     static constexpr int R1 = 0;
@@ -82,11 +86,12 @@ struct BwdSmem {
     static constexpr int DWIN = (STG + STGB + 15) / 16 * 16;
     static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // [2 tiles][colb | cdl][BN]
     static constexpr int XCH = COLV + 4 * G::BN * 4;       // [4][BM] floats: exchanges between the two halves
-    static constexpr int MISC = XCH + 4 * G::BM * 4;
+    static constexpr int KINDS = XCH + 4 * G::BM * 4;        // packed TileKind of every column tile
+    static constexpr int MISC = KINDS + kMaxTiles * 4;
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory");
-    static_assert(STG % 16 == 0 && GW % 64 == 0 && GW >= 63 + G::BM + G::BN - 1, "staging rows");
+    static_assert(STG % 1024 == 0 && GW % 64 == 0 && GW >= 63 + G::BM + G::BN - 1, "staging rows");
 };
 
 struct BwdBars {
@@ -145,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::STG);
     uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
     uint16_t* gstage = reinterpret_cast<uint16_t*>(smem + S::STG);
+    uint32_t* kinds = reinterpret_cast<uint32_t*>(smem + S::KINDS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, b = blockIdx.z;
@@ -173,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bars->abort_flag = 0;
         fence_barrier_init();
     }
+    // the kind of every column tile (two relative-index loads each), once
+    for (int t = threadIdx.x; t < ntiles; t += kThreads)
+        kinds[t] = pack_kind(classify<BM, BN, SIGMA>(p, dtab, tile_base(t)));
     if (warp == 1) {
         tc_alloc(&bars->tmem_base, 512);
         tc_relinquish();
@@ -193,7 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem + S::R2 + c * BM * G::CW * 2, &tmR2, h * D + c * G::CW, t0 + r0, &bars->row_full);
             }
             int band_loads = 0;
-            KindRaw kr = kind_fetch<BM, BN, SIGMA>(p, dtab, tile_base(0));   // kind of the next tile, in flight
             for (int it = 0; it < ntiles; ++it) {
                 const int s = it & 1, use = it >> 1;
                 const int c0 = it * BN;
@@ -205,8 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(smem + S::C2 + s * S::CB + c * BN * G::CW * 2, &tmC2, h * D + c * G::CW, t0 + c0,
                                 &bars->c_full[s]);
                 }
-                const TileKind tk = kind_finish(p, kr);
-                kr = kind_fetch<BM, BN, SIGMA>(p, dtab, tile_base(it + 1));
+                const TileKind tk = unpack_kind(kinds[it]);
                 if (tk.uniform) continue;
                 bool ok = true;
                 for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -231,90 +238,100 @@ __global__ void __launch_bounds__(kThreads, 1)
         // read tile m's into registers), then the dK / dV (dQ) products of tile
         // m (once its 16-bit dZ / P~ are written).  When the next tile's band
         // products would overwrite dZ / P~, they wait for tile m to finish.
-        if (lane == 0) {
+        // The whole warp walks the issue loop (its control flow warp-uniform);
+        // the MMAs and commits are the elect.sync forms, issued by one lane.
+        // Operand descriptors are built once (per CTA or per ring stage) and
+        // advanced per k-step by a constant.
+        {
             const uint32_t sR1 = smem_u32(smem + S::R1), sR2 = smem_u32(smem + S::R2);
             const uint32_t sBand = smem_u32(smem + S::BAND);
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
             constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
             constexpr uint32_t idA = idesc_f16(128, D, BF16, false, true);
-            bool ok = mbar_wait(&bars->row_full, 0, err, abort_flag);
+            const uint64_t dR1 = desc_k<G>(sR1, BM, 0), dR2 = desc_k<G>(sR2, BM, 0);
+            const uint64_t dBand = desc_k<G>(sBand, G::NBAND, 0);
+            // column operands, K-major and MN-major, of ring stages 0 and 1
+            const uint32_t sC10 = smem_u32(smem + S::C1), sC20 = smem_u32(smem + S::C2);
+            const uint64_t dC1k0 = desc_k<G>(sC10, BN, 0), dC1k1 = dadd(dC1k0, S::CB);
+            const uint64_t dC2k0 = desc_k<G>(sC20, BN, 0), dC2k1 = dadd(dC2k0, S::CB);
+            const uint64_t dC1m0 = desc_mn<G>(sC10, BN, 0), dC1m1 = dadd(dC1m0, S::CB);
+            const uint64_t dC2m0 = desc_mn<G>(sC20, BN, 0), dC2m1 = dadd(dC2m0, S::CB);
+            bool ok = mbar_wait_warp(&bars->row_full, 0, err, abort_flag);
             int band_used = 0, t_uses = 0;
             auto issue_sdp = [&](int m, const TileKind& tk) -> bool {
                 const int s = m & 1, use = m >> 1;
-                const uint32_t sC1 = smem_u32(smem + S::C1 + s * S::CB), sC2 = smem_u32(smem + S::C2 + s * S::CB);
                 if (!tk.uniform) {
                     for (int pass = 0; pass < 2; ++pass) {
-                        if (pass == 1 && !mbar_wait(&bars->c_full[s], use & 1, err, abort_flag)) return false;
-                        if (t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                        if (pass == 1 && !mbar_wait_warp(&bars->c_full[s], use & 1, err, abort_flag)) return false;
+                        if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
                             return false;
-                        const uint32_t sA = pass == 0 ? sR1 : sC1;
+                        const uint64_t dA = pass == 0 ? dR1 : s ? dC1k1 : dC1k0;
                         const int arows = pass == 0 ? BM : BN;
                         for (int c = 0; c < G::NCH; ++c) {
-                            if (!mbar_wait(&bars->band_full, band_used & 1, err, abort_flag)) return false;
+                            if (!mbar_wait_warp(&bars->band_full, band_used & 1, err, abort_flag)) return false;
                             tc_fence_after();
                             for (int k = 0; k < G::CW / 16; ++k)
-                                tc_mma_ss(tmem + TM::T, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
-                                          desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
-                            tc_commit(&bars->band_empty);
+                                tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, c * (G::CW / 16) + k)),
+                                            dadd(dBand, kofs<G>(G::NBAND, k)), idT, (c | k) != 0);
+                            tc_commit_w(&bars->band_empty);
                             ++band_used;
                         }
-                        tc_commit(&bars->t_full);
+                        tc_commit_w(&bars->t_full);
                         ++t_uses;
                     }
                     // S / dP reuse the band columns: wait until the cross window was copied out
-                    if (!mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)) return false;
-                } else if (!mbar_wait(&bars->c_full[s], use & 1, err, abort_flag)) {
+                    if (!mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)) return false;
+                } else if (!mbar_wait_warp(&bars->c_full[s], use & 1, err, abort_flag)) {
                     return false;
                 }
                 tc_fence_after();
+                const uint64_t dS = s ? dC1k1 : dC1k0, dP = s ? dC2k1 : dC2k0;
+#pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    tc_mma_ss(tmem + TM::S, desc_k<G>(sR1, BM, k), desc_k<G>(sC1, BN, k), idS, k != 0);
-                    tc_mma_ss(tmem + TM::P, desc_k<G>(sR2, BM, k), desc_k<G>(sC2, BN, k), idS, k != 0);
+                    tc_mma_ss_w(tmem + TM::S, dadd(dR1, kofs<G>(BM, k)), dadd(dS, kofs<G>(BN, k)), idS, k != 0);
+                    tc_mma_ss_w(tmem + TM::P, dadd(dR2, kofs<G>(BM, k)), dadd(dP, kofs<G>(BN, k)), idS, k != 0);
                 }
-                tc_commit(&bars->s_full);
+                tc_commit_w(&bars->s_full);
                 return true;
             };
             auto issue_acc = [&](int m) -> bool {
                 const int s = m & 1;
-                const uint32_t sC1 = smem_u32(smem + S::C1 + s * S::CB), sC2 = smem_u32(smem + S::C2 + s * S::CB);
-                if (!mbar_wait(&bars->z_full, m & 1, err, abort_flag)) return false;
+                if (!mbar_wait_warp(&bars->z_full, m & 1, err, abort_flag)) return false;
                 tc_fence_after();
+                const uint64_t d1 = s ? dC1m1 : dC1m0, d2 = s ? dC2m1 : dC2m0;
+#pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     // acc1 += dZ . C1   (dQ += dZ K  |  dK += dZ^T Q)
-                    tc_mma_ts(tmem + TM::ACC1, tmem + TM::Z + k * 8, desc_mn<G>(sC1, BN, k), idA, (m | k) != 0);
+                    tc_mma_ts_w(tmem + TM::ACC1, tmem + TM::Z + k * 8, dadd(d1, mnofs<G>(k)), idA, (m | k) != 0);
                     // dV += Pd^T dO
                     if (!ROWQ)
-                        tc_mma_ts(tmem + TM::ACC2, tmem + TM::Z + BN / 2 + k * 8, desc_mn<G>(sC2, BN, k), idA,
-                                  (m | k) != 0);
+                        tc_mma_ts_w(tmem + TM::ACC2, tmem + TM::Z + BN / 2 + k * 8, dadd(d2, mnofs<G>(k)), idA,
+                                    (m | k) != 0);
                 }
-                tc_commit(&bars->c_empty[s]);
-                tc_commit(&bars->mma3_done);
+                tc_commit_w(&bars->c_empty[s]);
+                tc_commit_w(&bars->mma3_done);
                 return true;
             };
-            // the kind of tile it + 1 is fetched while tile it is handled
-            KindRaw kr = kind_fetch<BM, BN, SIGMA>(p, dtab, tile_base(1));
-            if (ok) ok = issue_sdp(0, classify<BM, BN, SIGMA>(p, dtab, tile_base(0)));
+            if (ok) ok = issue_sdp(0, unpack_kind(kinds[0]));
             for (int it = 0; it < ntiles && ok; ++it) {
                 const bool nxt = it + 1 < ntiles;
-                const TileKind kn = kind_finish(p, kr);
-                kr = kind_fetch<BM, BN, SIGMA>(p, dtab, tile_base(it + 2));
+                const TileKind kn = unpack_kind(kinds[nxt ? it + 1 : it]);
                 const bool early = nxt && (!TM::T_OVER_Z || kn.uniform);
                 if (early) {
-                    if (!(ok = mbar_wait(&bars->sread, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, err, abort_flag))) break;
                     if (!(ok = issue_sdp(it + 1, kn))) break;
                 }
                 if (!(ok = issue_acc(it))) break;
                 if (nxt && !early) {
                     // the band products overwrite this tile's dZ / P~: wait until the
                     // products and the diagonal sums have read them
-                    if (!(ok = mbar_wait(&bars->sread, it & 1, err, abort_flag))) break;
-                    if (!(ok = mbar_wait(&bars->mma3_done, it & 1, err, abort_flag))) break;
-                    if (!(ok = mbar_wait(&bars->zread, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->mma3_done, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->zread, it & 1, err, abort_flag))) break;
                     if (!(ok = issue_sdp(it + 1, kn))) break;
                 }
             }
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax / gradient warps
         // Eight warps: warp w owns TMEM lanes 32 (w & 3) .. +31 (rows) and
@@ -360,9 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         //         column's LSE (base 2) when the columns are queries;
         //   cv1 = c * Dl of the column (dK/dV kernel only).
         // Their loads are issued two tiles ahead (col_fetch) and used one tile
-        // ahead (col_finish), when they go to shared memory (double-buffered);
-        // tile kinds are fetched three tiles ahead.  No loaded value is used
-        // in the tile that loads it.
+        // ahead, when they go to shared memory (double-buffered).  No loaded
+        // value is used in the tile that loads it.
         struct ColRaw {
             float cb, ls, rt;
             int ok, mk;
@@ -383,35 +399,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return c;
         };
-        auto put_colterms = [&](int slot, const ColRaw& c) {
+        auto put_colterms = [&](int slot, ColRaw c) {
+            pin(c.cb);
+            pin(c.ls);
+            pin(c.rt);
+            pin(c.ok);
+            pin(c.mk);
             if (tid < BN) {
                 const bool valid = c.ok && c.mk != 0;
                 colv[slot * 2 * BN + tid] = !valid ? -INFINITY : ROWQ ? c.cb : c.cb - c.ls * kLog2e;
                 colv[slot * 2 * BN + BN + tid] = valid && !ROWQ ? p.scale * c.rt : 0.f;
             }
         };
-        const TileKind tk0 = classify<BM, BN, SIGMA>(p, dtab, tile_base(0));
-        const TileKind tk1 = classify<BM, BN, SIGMA>(p, dtab, tile_base(1));
-        put_colterms(0, col_fetch(0, tk0));
-        ColRaw cr = col_fetch(1, tk1);                                     // tile it + 1
-        KindRaw kr = kind_fetch<BM, BN, SIGMA>(p, dtab, tile_base(2));     // tile it + 2
-        uint32_t kc = pack_kind(tk0), kn = pack_kind(tk1);                 // tiles it, it + 1
+        auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
+        put_colterms(0, col_fetch(0, kind_of(0)));
+        ColRaw cr = col_fetch(1, kind_of(1));                              // tile it + 1
         for (int it = 0; it < ntiles && ok; ++it) {
             const int c0 = it * BN;
             const int base = tile_base(it);
-            const TileKind tk = unpack_kind(kc);
+            const TileKind tk = kind_of(it);
             const float* colb = colv + (it & 1) * 2 * BN;
             const float* cdl = colb + BN;
             if (tid == 0) bulk_wait_read0();   // the previous G box left shared memory
             named_bar_sync(1, 256);
             put_colterms((it + 1) & 1, cr);
-            {
-                const TileKind k2 = kind_finish(p, kr);
-                cr = col_fetch(it + 2, k2);
-                kr = kind_fetch<BM, BN, SIGMA>(p, dtab, tile_base(it + 3));
-                kc = kn;
-                kn = pack_kind(k2);
-            }
+            cr = col_fetch(it + 2, kind_of(it + 2));
             int own_a = 0;
             if (!tk.uniform) {
                 fill_dwin<BM, BN, SIGMA>(p, dtab, base, tk.dlo, dwin, tid, 256);
@@ -545,6 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // staging row of this tile row: GW 16-bit sums, relative rows from
                 // (dlo & ~63); half hf clears half of it
                 uint16_t* grow = gstage + (size_t)row * S::GW;
+                // element xx of this row in the swizzled staging
+                auto gat = [&](int xx) -> uint16_t& {
+                    const int sg = row * (S::GW / 64) + (xx >> 6), x = xx & 63;
+                    return gstage[sg * 64 + ((((x >> 3) ^ (sg & 7)) << 3) | (x & 7))];
+                };
                 {
                     uint4* gz = reinterpret_cast<uint4*>(grow) + hf * (S::GW / 16);
 #pragma unroll
@@ -556,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int xx = m + off;
                     const bool in = (unsigned)xx < (unsigned)S::GW;
                     bad |= !in;
-                    if (in) grow[xx] = f2h16<BF16>(v);
+                    if (in) gat(xx) = f2h16<BF16>(v);
                 };
                 auto dw_at = [&](int col) -> int {
                     return ROWQ ? dwin[row - col + BN - 1] : dwin[col - row + BM - 1];
@@ -599,14 +616,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     gput(run_m, acc + xch[row]);
                     // the clamped relative rows (far field) are summed in registers
                     if (tk.dlo == 0) {
-                        g_lo += h16f<BF16>(grow[off]);
-                        grow[off] = 0;
+                        g_lo += h16f<BF16>(gat(off));
+                        gat(off) = 0;
                     }
                     if (tk.dhi == p.R - 1) {
                         const int xx = p.R - 1 - tk.dlo + off;
                         if ((unsigned)xx < (unsigned)S::GW) {
-                            g_hi += h16f<BF16>(grow[xx]);
-                            grow[xx] = 0;
+                            g_hi += h16f<BF16>(gat(xx));
+                            gat(xx) = 0;
                         }
                     }
                 }
@@ -711,7 +728,7 @@ int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const v
         encode_tmap(&m4, code, 2, tok_dims, tok_str, boxc, G::SWZB, c2) ||
         encode_tmap(&m5, code, 2, rel_dims, rel_str, boxb, G::SWZB, xr) ||
         encode_tmap(&m6, code, 2, rel_dims, rel_str, boxb, G::SWZB, yr) ||
-        encode_tmap(&mg, code, 3, g_dims, g_str, boxg, 0, Gbuf))
+        encode_tmap(&mg, code, 3, g_dims, g_str, boxg, 128, Gbuf))
         return (int)cudaErrorInvalidValue;
     auto kern = bwd_tc_kernel<D, BF16, SIGMA, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);

@@ -171,6 +171,12 @@ DF_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err_word, volati
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, err_word, abort_flag));
 }
 
+// Pin a register value at this point of the program: the empty volatile asm
+// "redefines" it, so arithmetic on a value loaded early cannot be hoisted
+// above (and stall right after) the load.  Emits no instruction.
+DF_DEV void pin(float& x) { asm volatile("" : "+f"(x)); }
+DF_DEV void pin(int& x) { asm volatile("" : "+r"(x)); }
+
 // Named barrier among `nthreads` threads (a multiple of 32).
 DF_DEV void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -241,6 +247,31 @@ DF_DEV void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-collective forms: the whole warp executes them (its control flow
+// warp-uniform) and elect.sync picks the one lane that issues the MMA or the
+// commit.  Issued this way an MMA costs about its tensor-pipe time (64 cycles
+// for 128 x 128 x 16); issued from a single-lane branch it cost 2-4x more.
+DF_DEV void tc_mma_ss_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+DF_DEV void tc_mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+DF_DEV void tc_commit_w(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
         : "memory");
 }
 

@@ -68,7 +68,9 @@ struct FwdSmem {
     static constexpr int DWIN = CROSS + CROSSB;
     static constexpr int COLB = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;   // [2 tiles][BN]
     static constexpr int XCH = COLB + 2 * G::BN * 4;      // [4][BM] floats: the halves' maxima and sums
-    static constexpr int MISC = XCH + 4 * G::BM * 4;
+    static constexpr int kMaxTiles = 8192 / G::BN;        // L <= 8192
+    static constexpr int KINDS = XCH + 4 * G::BM * 4;     // packed TileKind of every key tile
+    static constexpr int MISC = KINDS + kMaxTiles * 4;
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
     static_assert(ALLOC <= 232448, "shared memory");
@@ -103,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xch = reinterpret_cast<float*>(smem + S::XCH);
     uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::OWN);
     uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
+    uint32_t* kinds = reinterpret_cast<uint32_t*>(smem + S::KINDS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, b = blockIdx.z;
@@ -129,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bars->abort_flag = 0;
         fence_barrier_init();
     }
+    // the kind of every key tile (two relative-index loads each), once
+    for (int t = threadIdx.x; t < ntiles; t += kThreads) kinds[t] = pack_kind(classify<BM, BN, 1>(p, dtab, i0 - t * BN));
     if (warp == 1) {
         tc_alloc(&bars->tmem_base, 512);
         tc_relinquish();
@@ -150,7 +155,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < G::NCH; ++c)
                 tma_load_2d(smem + S::Q + c * BM * G::CW * 2, &tmQ, h * D + c * G::CW, t0 + i0, &bars->q_full);
             int band_loads = 0;
-            KindRaw kr = kind_fetch<BM, BN, 1>(p, dtab, i0);   // kind of the next tile, in flight
             for (int it = 0; it < ntiles; ++it) {
                 const int s = it & 1, use = it >> 1;
                 const int j0 = it * BN;
@@ -162,8 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
                                 &bars->kv_full[s]);
                 }
-                const TileKind tk = kind_finish(p, kr);
-                kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - j0 - BN);
+                const TileKind tk = unpack_kind(kinds[it]);
                 if (tk.uniform) continue;
                 bool ok = true;
                 for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -184,82 +187,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp walks the issue loop (its control flow warp-uniform);
+        // the MMAs and commits are the elect.sync forms, issued by one lane.
+        // Operand descriptors are built once (per CTA or per ring stage) and
+        // advanced per k-step by a constant.
+        {
             const uint32_t sQ = smem_u32(smem + S::Q), sBand = smem_u32(smem + S::BAND);
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
             constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
             constexpr uint32_t idO = idesc_f16(128, D, BF16, false, true);
-            bool ok = mbar_wait(&bars->q_full, 0, err, abort_flag);
+            const uint64_t dQ = desc_k<G>(sQ, BM, 0), dBand = desc_k<G>(sBand, G::NBAND, 0);
+            const uint64_t dK0 = desc_k<G>(smem_u32(smem + S::K0), BN, 0), dK1 = dadd(dK0, S::KVB);
+            const uint64_t dV0 = desc_mn<G>(smem_u32(smem + S::V0), BN, 0), dV1 = dadd(dV0, S::KVB);
+            bool ok = mbar_wait_warp(&bars->q_full, 0, err, abort_flag);
             int band_used = 0, t_uses = 0;
-            int pv_cnt[2] = {0, 0};   // P.V rounds issued per S buffer
+            int pv_cnt0 = 0, pv_cnt1 = 0;   // P.V rounds issued per S buffer
             // S (and, for band tiles, the two band products) of tile m into buffer m & 1
             auto issue_s = [&](int m, const TileKind& tk) -> bool {
                 const int s = m & 1, use = m >> 1, bf = m & 1;
-                const uint32_t sK = smem_u32(smem + S::K0 + s * S::KVB);
+                const uint64_t dK = s ? dK1 : dK0;
                 if (!tk.uniform) {
                     // the band columns overlap S buffer 1: its last P must have been consumed
-                    if (pv_cnt[1] > 0 && !mbar_wait(&bars->pv_done[1], (pv_cnt[1] - 1) & 1, err, abort_flag))
+                    if (pv_cnt1 > 0 && !mbar_wait_warp(&bars->pv_done[1], (pv_cnt1 - 1) & 1, err, abort_flag))
                         return false;
                     for (int pass = 0; pass < 2; ++pass) {
-                        if (pass == 1 && !mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag)) return false;
-                        if (t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                        if (pass == 1 && !mbar_wait_warp(&bars->kv_full[s], use & 1, err, abort_flag)) return false;
+                        if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
                             return false;
-                        const uint32_t sA = pass == 0 ? sQ : sK;
+                        const uint64_t dA = pass == 0 ? dQ : dK;
                         const int arows = pass == 0 ? BM : BN;
                         for (int c = 0; c < G::NCH; ++c) {
-                            if (!mbar_wait(&bars->band_full, band_used & 1, err, abort_flag)) return false;
+                            if (!mbar_wait_warp(&bars->band_full, band_used & 1, err, abort_flag)) return false;
                             tc_fence_after();
                             for (int k = 0; k < G::CW / 16; ++k)
-                                tc_mma_ss(tmem + TM::T, desc_k<G>(sA, arows, c * (G::CW / 16) + k),
-                                          desc_k<G>(sBand, G::NBAND, k), idT, (c | k) != 0);
-                            tc_commit(&bars->band_empty);
+                                tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, c * (G::CW / 16) + k)),
+                                            dadd(dBand, kofs<G>(G::NBAND, k)), idT, (c | k) != 0);
+                            tc_commit_w(&bars->band_empty);
                             ++band_used;
                         }
-                        tc_commit(&bars->t_full);
+                        tc_commit_w(&bars->t_full);
                         ++t_uses;
                     }
-                } else if (!mbar_wait(&bars->kv_full[s], use & 1, err, abort_flag)) {
+                } else if (!mbar_wait_warp(&bars->kv_full[s], use & 1, err, abort_flag)) {
                     return false;
                 }
                 // buffer bf free: its previous P consumed; buffer 1 also holds band columns
-                if (pv_cnt[bf] > 0 && !mbar_wait(&bars->pv_done[bf], (pv_cnt[bf] - 1) & 1, err, abort_flag))
-                    return false;
-                if (bf == 1 && t_uses > 0 && !mbar_wait(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                const int pvc = bf ? pv_cnt1 : pv_cnt0;
+                if (pvc > 0 && !mbar_wait_warp(&bars->pv_done[bf], (pvc - 1) & 1, err, abort_flag)) return false;
+                if (bf == 1 && t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
                     return false;
                 tc_fence_after();
+#pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    tc_mma_ss(tmem + s_col(m), desc_k<G>(sQ, BM, k), desc_k<G>(sK, BN, k), idS, k != 0);
-                tc_commit(&bars->s_full[bf]);
+                    tc_mma_ss_w(tmem + s_col(m), dadd(dQ, kofs<G>(BM, k)), dadd(dK, kofs<G>(BN, k)), idS, k != 0);
+                tc_commit_w(&bars->s_full[bf]);
                 return true;
             };
-            // the kind of tile it + 1 is fetched while tile it is handled
-            KindRaw kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - BN);
-            if (ok) ok = issue_s(0, classify<BM, BN, 1>(p, dtab, i0));
+            if (ok) ok = issue_s(0, unpack_kind(kinds[0]));
             for (int it = 0; it < ntiles && ok; ++it) {
                 const int s = it & 1;
-                const uint32_t sV = smem_u32(smem + S::V0 + s * S::KVB);
-                const TileKind kn = kind_finish(p, kr);
-                kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - (it + 2) * BN);
+                const uint64_t dV = s ? dV1 : dV0;
+                const TileKind kn = unpack_kind(kinds[it + 1 < ntiles ? it + 1 : it]);
                 // uniform next tile: compute its S while the softmax works on this one
                 const bool next = it + 1 < ntiles;
                 const bool next_band = next && !kn.uniform;
                 if (next && !next_band && !(ok = issue_s(it + 1, kn))) break;
                 // O_h += P_h V_h for the two column halves, each as soon as its P is ready
                 for (int hf = 0; hf < 2 && ok; ++hf) {
-                    if (!(ok = mbar_wait(&bars->p_full[hf], it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->p_full[hf], it & 1, err, abort_flag))) break;
                     tc_fence_after();
+#pragma unroll
                     for (int k = 0; k < BN / 32; ++k)
-                        tc_mma_ts(tmem + (hf ? TM::O1 : TM::O0), tmem + s_col(it) + TM::POFF + hf * (BN / 4) + k * 8,
-                                  desc_mn<G>(sV, BN, hf * (BN / 32) + k), idO, (it | k) != 0);
+                        tc_mma_ts_w(tmem + (hf ? TM::O1 : TM::O0), tmem + s_col(it) + TM::POFF + hf * (BN / 4) + k * 8,
+                                    dadd(dV, mnofs<G>(hf * (BN / 32) + k)), idO, (it | k) != 0);
                 }
                 if (!ok) break;
-                tc_commit(&bars->kv_empty[s]);
-                tc_commit(&bars->pv_done[it & 1]);
-                ++pv_cnt[it & 1];
+                tc_commit_w(&bars->kv_empty[s]);
+                tc_commit_w(&bars->pv_done[it & 1]);
+                if (it & 1) ++pv_cnt1; else ++pv_cnt0;
                 if (next_band && !(ok = issue_s(it + 1, kn))) break;
             }
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
         // Eight warps: warp w owns TMEM lanes 32 (w & 3) .. +31 (query rows)
@@ -304,8 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // per-key column term of a tile (P2C scalar of uniform tiles, with the
         // key mask folded in; key mask of band tiles; -inf past the sequence
         // end).  Its loads are issued two tiles ahead (col_fetch) and used one
-        // tile ahead (col_finish), when it goes to shared memory
-        // (double-buffered); tile kinds are fetched three tiles ahead.
+        // tile ahead, when it goes to shared memory (double-buffered).
         struct ColRaw {
             float cb;
             int ok, mk;
@@ -319,28 +326,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             c.mk = (!k.uniform && p.kmask) ? p.kmask[t0 + js] : 1;
             return c;
         };
-        auto put_colterm = [&](int slot, const ColRaw& c) {
+        auto put_colterm = [&](int slot, ColRaw c) {
+            pin(c.cb);
+            pin(c.ok);
+            pin(c.mk);
             if (tid < BN) colv[slot * BN + tid] = (c.ok && c.mk != 0) ? c.cb : -INFINITY;
         };
-        const TileKind tk0 = classify<BM, BN, 1>(p, dtab, i0);
-        const TileKind tk1 = classify<BM, BN, 1>(p, dtab, i0 - BN);
-        put_colterm(0, col_fetch(0, tk0));
-        ColRaw cr = col_fetch(1, tk1);                                  // tile it + 1
-        KindRaw kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - 2 * BN);       // tile it + 2
-        uint32_t kc = pack_kind(tk0), kn = pack_kind(tk1);              // tiles it, it + 1
+        auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
+        put_colterm(0, col_fetch(0, kind_of(0)));
+        ColRaw cr = col_fetch(1, kind_of(1));                           // tile it + 1
         for (int it = 0; it < ntiles && ok; ++it) {
             const int j0 = it * BN;
-            const TileKind tk = unpack_kind(kc);
+            const TileKind tk = kind_of(it);
             const float* colb = colv + (it & 1) * BN;
             named_bar_sync(1, 256);
             put_colterm((it + 1) & 1, cr);
-            {
-                const TileKind k2 = kind_finish(p, kr);
-                cr = col_fetch(it + 2, k2);
-                kr = kind_fetch<BM, BN, 1>(p, dtab, i0 - j0 - 3 * BN);
-                kc = kn;
-                kn = pack_kind(k2);
-            }
+            cr = col_fetch(it + 2, kind_of(it + 2));
             int own_a = 0;
             if (!tk.uniform) {
                 fill_dwin<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, dwin, tid, 256);

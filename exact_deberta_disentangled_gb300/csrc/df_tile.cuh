@@ -62,6 +62,22 @@ DF_DEV uint64_t desc_mn(uint32_t base, int rows, int kstep) {
     return sdesc(base + (uint32_t)(kstep * 16 * G::CW * 2), (uint32_t)(rows * G::CW * 2), 8 * G::CW * 2, G::SWZ);
 }
 
+// Byte offset of k-step `kstep` within a K-major operand of `rows` rows (the
+// term desc_k adds to the base address), and within an MN-major one
+// (desc_mn).  A descriptor's start-address field holds address >> 4 in 14
+// bits and shared-memory addresses stay below 2^18, so adding offset >> 4 to
+// the descriptor of k-step 0 gives the descriptor of k-step kstep: the MMA
+// issue loops build each operand's descriptor once.
+template <class G>
+__host__ __device__ constexpr uint32_t kofs(int rows, int kstep) {
+    return (uint32_t)((kstep / (G::CW / 16)) * rows * G::CW * 2 + (kstep % (G::CW / 16)) * 32);
+}
+template <class G>
+__host__ __device__ constexpr uint32_t mnofs(int kstep) {
+    return (uint32_t)(kstep * 16 * G::CW * 2);
+}
+DF_DEV uint64_t dadd(uint64_t desc, uint32_t byte_ofs) { return desc + (uint64_t)(byte_ofs >> 4); }
+
 struct TileKind {
     int dlo, dhi;
     int uniform;   // 1: every element has delta == dlo, and dlo is 0 or R-1

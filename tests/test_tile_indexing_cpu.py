@@ -116,3 +116,18 @@ def test_model_catches_a_flipped_relative_index():
     good = tab[np.clip(base + x - (NR - 1), -(L - 1), L - 1) + L - 1]
     bad = tab[np.clip(base - (x - (NR - 1)), -(L - 1), L - 1) + L - 1]
     assert not np.array_equal(good, bad)
+
+
+@pytest.mark.parametrize("GW", [320, 256])
+def test_swizzled_staging_rows_stay_in_their_row(GW):
+    """The backward kernels address element xx of staging row `row` through
+    the TMA 128-byte swizzle (16-byte chunk c of 128-byte segment s stored at
+    c ^ (s & 7)); every row's GW elements must map one-to-one onto that row's
+    own GW slots, so clearing a row clears exactly its sums."""
+    xx = np.arange(GW)
+    for row in range(128):
+        sg = row * (GW // 64) + (xx >> 6)
+        x = xx & 63
+        e = sg * 64 + ((((x >> 3) ^ (sg & 7)) << 3) | (x & 7))
+        assert e.min() >= row * GW and e.max() < (row + 1) * GW
+        assert len(np.unique(e)) == GW

@@ -78,7 +78,7 @@ struct FwdSmem {
 
 struct FwdBars {
     uint64_t q_full;
-    uint64_t kv_full[2], kv_empty[2];
+    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];   // K and V rings: K is released after S, V after P.V
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
     uint64_t s_full[2], p_full[2], pv_done[2];
@@ -119,8 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
             mbar_init(&bars->s_full[s], 1);
             mbar_init(&bars->pv_done[s], 1);
             mbar_init(&bars->p_full[s], 4);
@@ -158,18 +160,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = 0; it < ntiles; ++it) {
                 const int s = it & 1, use = it >> 1;
                 const int j0 = it * BN;
-                if (use > 0 && !mbar_wait(&bars->kv_empty[s], (use - 1) & 1, err, abort_flag)) break;
-                mbar_arrive_expect_tx(&bars->kv_full[s], 2 * S::KVB);
-                for (int c = 0; c < G::NCH; ++c) {
+                // K of tile it as soon as S of tile it - 2 has read its stage
+                if (use > 0 && !mbar_wait(&bars->k_empty[s], (use - 1) & 1, err, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars->k_full[s], S::KVB);
+                for (int c = 0; c < G::NCH; ++c)
                     tma_load_2d(smem + S::K0 + s * S::KVB + c * BN * G::CW * 2, &tmK, h * D + c * G::CW, t0 + j0,
-                                &bars->kv_full[s]);
-                    tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
-                                &bars->kv_full[s]);
-                }
+                                &bars->k_full[s]);
                 const TileKind tk = unpack_kind(kinds[it]);
-                if (tk.uniform) continue;
                 bool ok = true;
-                for (int pass = 0; pass < 2 && ok; ++pass) {
+                for (int pass = 0; pass < 2 && ok && !tk.uniform; ++pass) {
                     for (int c = 0; c < G::NCH; ++c) {
                         if (band_loads > 0 &&
                             !mbar_wait(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
@@ -183,6 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
+                // V of tile it once P.V of tile it - 2 has read its stage
+                if (use > 0 && !mbar_wait(&bars->v_empty[s], (use - 1) & 1, err, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars->v_full[s], S::KVB);
+                for (int c = 0; c < G::NCH; ++c)
+                    tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
+                                &bars->v_full[s]);
             }
         }
     } else if (warp == 1) {
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (pv_cnt1 > 0 && !mbar_wait_warp(&bars->pv_done[1], (pv_cnt1 - 1) & 1, err, abort_flag))
                         return false;
                     for (int pass = 0; pass < 2; ++pass) {
-                        if (pass == 1 && !mbar_wait_warp(&bars->kv_full[s], use & 1, err, abort_flag)) return false;
+                        if (pass == 1 && !mbar_wait_warp(&bars->k_full[s], use & 1, err, abort_flag)) return false;
                         if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
                             return false;
                         const uint64_t dA = pass == 0 ? dQ : dK;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_commit_w(&bars->t_full);
                         ++t_uses;
                     }
-                } else if (!mbar_wait_warp(&bars->kv_full[s], use & 1, err, abort_flag)) {
+                } else if (!mbar_wait_warp(&bars->k_full[s], use & 1, err, abort_flag)) {
                     return false;
                 }
                 // buffer bf free: its previous P consumed; buffer 1 also holds band columns
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < D / 16; ++k)
                     tc_mma_ss_w(tmem + s_col(m), dadd(dQ, kofs<G>(BM, k)), dadd(dK, kofs<G>(BN, k)), idS, k != 0);
                 tc_commit_w(&bars->s_full[bf]);
+                tc_commit_w(&bars->k_empty[s]);
                 return true;
             };
             if (ok) ok = issue_s(0, unpack_kind(kinds[0]));
@@ -253,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool next_band = next && !kn.uniform;
                 if (next && !next_band && !(ok = issue_s(it + 1, kn))) break;
                 // O_h += P_h V_h for the two column halves, each as soon as its P is ready
+                if (!(ok = mbar_wait_warp(&bars->v_full[s], (it >> 1) & 1, err, abort_flag))) break;
                 for (int hf = 0; hf < 2 && ok; ++hf) {
                     if (!(ok = mbar_wait_warp(&bars->p_full[hf], it & 1, err, abort_flag))) break;
                     tc_fence_after();
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     dadd(dV, mnofs<G>(hf * (BN / 32) + k)), idO, (it | k) != 0);
                 }
                 if (!ok) break;
-                tc_commit_w(&bars->kv_empty[s]);
+                tc_commit_w(&bars->v_empty[s]);
                 tc_commit_w(&bars->pv_done[it & 1]);
                 if (it & 1) ++pv_cnt1; else ++pv_cnt0;
                 if (next_band && !(ok = issue_s(it + 1, kn))) break;
@@ -441,12 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mm = attempted ? m_run - rb : INFINITY;
                 float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 float sm[4] = {0.f, 0.f, 0.f, 0.f};
+                // all of this thread's S columns in one tensor-memory round trip
+                uint32_t rr[32 * NCT];
+#pragma unroll
+                for (int cc = 0; cc < NCT; ++cc) tc_ld32p(lane_base + scol + 32 * (cbeg + cc), rr + 32 * cc);
+                tc_wait_ld();
 #pragma unroll
                 for (int cc = 0; cc < NCT; ++cc) {
                     const int c = cbeg + cc;
-                    uint32_t r[32];
-                    tc_ld32(lane_base + scol + 32 * c, r);
-                    tc_wait_ld();
+                    const uint32_t* r = rr + 32 * cc;
                     uint32_t keep = 0xFFFFFFFFu;
                     if constexpr (DROP) keep = keep_bits32_row(p, b, h, i, j0 + 32 * c);
                     const float4* cb4 = reinterpret_cast<const float4*>(colb + 32 * c);

@@ -93,6 +93,9 @@ CASES = [
     (512, 256, 256, 512, 64), (128, 64, 64, 128, 64), (4096, 256, 256, 512, 128), (2048, 256, 256, 512, 32),
     (600, 256, 256, 512, 128), (520, 256, 256, 512, 32), (1536, 256, 256, 512, 64), (333, 17, 12, 100, 64),
     (2048, 256, 0, 0, 64), (1000, 8, 4, 8, 128),
+    # shapes of the edge-case parity tests
+    (1, 256, 256, 512, 64), (7, 256, 256, 512, 64), (130, 256, 256, 512, 64), (700, 256, 0, 0, 64),
+    (600, 8, 4, 8, 64), (1500, 512, 512, 1024, 64), (2048, 512, 512, 1024, 128), (2048, 512, 512, 1024, 32),
 ]
 
 

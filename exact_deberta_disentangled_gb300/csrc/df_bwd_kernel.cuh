@@ -63,10 +63,7 @@ struct BwdSmem {
     using G = Geo<D>;
     static constexpr int kMaxTiles = 8192 / G::BN;          // L <= 8192
     // diagonal-sum staging: one row of GW 16-bit sums per tile row, covering
-    // relative rows [dlo & ~63, (dlo & ~63) + GW), stored as GW / 64 segments of
-    // 128 bytes with the TMA 128-byte swizzle (16-byte chunk c of segment s at
-    // position c ^ (s & 7)), so that the 32 rows of a warp do not all hit the
-    // same bank; a tile reaches at most
+    // relative rows [dlo & ~63, (dlo & ~63) + GW); a tile reaches at most
     // BM + BN - 1 of them, starting at most 63 in
     static constexpr int GW = G::BN == 128 ? 320 : 256;
     static constexpr int R1 = 0;
@@ -414,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
         put_colterms(0, col_fetch(0, kind_of(0)));
         ColRaw cr = col_fetch(1, kind_of(1));                              // tile it + 1
+        BandRaw bn = band_fetch<BM, BN, SIGMA>(p, dtab, tile_base(0), w4, tid, lane);   // band indices, one tile ahead
         for (int it = 0; it < ntiles && ok; ++it) {
             const int c0 = it * BN;
             const int base = tile_base(it);
@@ -424,11 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(1, 256);
             put_colterms((it + 1) & 1, cr);
             cr = col_fetch(it + 2, kind_of(it + 2));
+            BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
+            if (it + 1 < ntiles && !kind_of(it + 1).uniform)
+                bn = band_fetch<BM, BN, SIGMA>(p, dtab, tile_base(it + 1), w4, tid, lane);
             int own_a = 0;
             if (!tk.uniform) {
-                fill_dwin<BM, BN, SIGMA>(p, dtab, base, tk.dlo, dwin, tid, 256);
-                int lo, hi;
-                own_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
+                pin(bc.dw);
+                pin(bc.rng);
+                if (tid < BM + BN - 1) dwin[tid] = (int16_t)(bc.dw - tk.dlo);
+                int lo = __shfl_sync(0xffffffffu, bc.rng, 0) - tk.dlo, hi = __shfl_sync(0xffffffffu, bc.rng, 1) - tk.dlo;
+                const int clo = __shfl_sync(0xffffffffu, bc.rng, 2) - tk.dlo, chi = __shfl_sync(0xffffffffu, bc.rng, 3) - tk.dlo;
                 own_a = lo & ~15;
                 if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
                 tc_fence_after();
@@ -439,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
                 tc_fence_after();
                 if (32 * w4 < BN) {
-                    cross_range<BM, BN, SIGMA>(p, dtab, base, tk.dlo, w4, lo, hi);
+                    lo = clo;
+                    hi = chi;
                     const int ca =
                         copy_band_window(lane_base + TM::T, lo, hi, cross + row * G::CROSS_S, kscale, hf, 2);
                     if (lane == 0 && hf == 0) bars->cross_base[w4] = ca;
@@ -555,75 +559,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, 256);   // own / cross no longer read; every dZ is in tensor memory
                 tc_fence_after();
                 // staging row of this tile row: GW 16-bit sums, relative rows from
-                // (dlo & ~63); half hf clears half of it
-                uint16_t* grow = gstage + (size_t)row * S::GW;
-                // element xx of this row in the swizzled staging
-                auto gat = [&](int xx) -> uint16_t& {
-                    const int sg = row * (S::GW / 64) + (xx >> 6), x = xx & 63;
-                    return gstage[sg * 64 + ((((x >> 3) ^ (sg & 7)) << 3) | (x & 7))];
-                };
-                {
-                    uint4* gz = reinterpret_cast<uint4*>(grow) + hf * (S::GW / 16);
-#pragma unroll
-                    for (int x = 0; x < S::GW / 16; ++x) gz[x] = make_uint4(0u, 0u, 0u, 0u);
-                }
+                // (dlo & ~63); grow[m] holds relative row dlo + m
                 const int off = tk.dlo & 63;
-                bool bad = false;
-                auto gput = [&](int m, float v) {
-                    const int xx = m + off;
-                    const bool in = (unsigned)xx < (unsigned)S::GW;
-                    bad |= !in;
-                    if (in) gat(xx) = f2h16<BF16>(v);
-                };
+                uint16_t* grow = gstage + (size_t)row * S::GW + off;
+                const int mmax = S::GW - 1 - off;   // a clamp: grow[m] stays inside the row
+                {
+                    // the warp clears half hf of its 32 rows one row at a time, its
+                    // lanes on consecutive 16-byte chunks (a thread per row would put
+                    // the 32 stores of a warp on one bank: rows are 640 / 512 bytes apart)
+                    constexpr int NZ = S::GW / 16;   // chunks per half row
+                    uint4* gz = reinterpret_cast<uint4*>(gstage + (size_t)(32 * w4) * S::GW) + hf * NZ + lane;
+#pragma unroll 4
+                    for (int r = 0; r < 32; ++r)
+                        if (lane < NZ) gz[r * (S::GW / 8)] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                const bool bad = tk.dhi - tk.dlo > mmax;   // cannot happen for a valid tile
+                auto gput = [&](int m, float v) { grow[m < mmax ? m : mmax] = f2h16<BF16>(v); };
                 auto dw_at = [&](int col) -> int {
                     return ROWQ ? dwin[row - col + BN - 1] : dwin[col - row + BM - 1];
                 };
-                // this half's dZ columns, 16-bit as the products use them
-                uint32_t zr[HC / 2];
-                if constexpr (HC == 64) {
-                    tc_ld32p(lane_base + TM::Z + hf * (HC / 2), zr);
-                } else {
-                    tc_ld16p(lane_base + TM::Z + hf * (HC / 2), zr);
-                }
-                tc_wait_ld();
                 named_bar_sync(pair_bar, 64);   // the row is cleared
                 // Runs of equal relative index along the row (the index is
-                // monotone in the column).  A run that crosses from the first half
-                // into the second is finished by the first half: the second hands
-                // over its partial sum instead of storing it.
+                // monotone in the column).  With prefix sums along the row, a run
+                // ends where the next column's index differs and its sum is the
+                // difference of the prefix sums at its two ends (so the chain per
+                // element is one add).  Each half stores its runs; a run that
+                // crosses from the first half into the second was stored by the
+                // second half (its first run) and the first half adds its own part
+                // to it afterwards -- the slot is zero otherwise, since the second
+                // half's indices are all on the other side of the first half's.
                 const int cst = hf * HC;
-                const int m_join = hf ? dw_at(cst - 1) : -1;
-                int run_m = dw_at(cst);
-                float acc = 0.f, handoff = 0.f;
+                float pre = 0.f, last = 0.f;
+                int m_cur = dw_at(cst);
+                // this half's dZ columns (16-bit, as the products use them), 32 at a time
+#pragma unroll 1
+                for (int g = 0; g < HC / 32; ++g) {
+                    uint32_t zr[16];
+                    tc_ld16p(lane_base + TM::Z + hf * (HC / 2) + 16 * g, zr);
+                    tc_wait_ld();
 #pragma unroll
-                for (int e = 0; e < HC; ++e) {
-                    const int m = dw_at(cst + e);
-                    const float v = h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
-                    if (m != run_m) {
-                        if (run_m == m_join) handoff = acc; else gput(run_m, acc);
-                        run_m = m;
-                        acc = v;
-                    } else {
-                        acc += v;
+                    for (int e2 = 0; e2 < 32; ++e2) {
+                        const int e = 32 * g + e2;
+                        pre += h16f<BF16>((uint16_t)(zr[e2 >> 1] >> (16 * (e2 & 1))));
+                        if (e + 1 < HC) {
+                            const int m_nxt = dw_at(cst + e + 1);
+                            if (m_nxt != m_cur) {
+                                gput(m_cur, pre - last);
+                                last = pre;
+                                m_cur = m_nxt;
+                            }
+                        }
                     }
                 }
-                if (hf) {
-                    if (run_m == m_join) handoff = acc; else gput(run_m, acc);
-                    xch[row] = handoff;
-                }
+                const float tail = pre - last;   // the run that ends this half
+                if (hf) gput(m_cur, tail);
                 named_bar_sync(pair_bar, 64);
                 if (!hf) {
-                    gput(run_m, acc + xch[row]);
+                    const int ms = m_cur < mmax ? m_cur : mmax;
+                    grow[ms] = f2h16<BF16>(h16f<BF16>(grow[ms]) + tail);
                     // the clamped relative rows (far field) are summed in registers
                     if (tk.dlo == 0) {
-                        g_lo += h16f<BF16>(gat(off));
-                        gat(off) = 0;
+                        g_lo += h16f<BF16>(grow[0]);
+                        grow[0] = 0;
                     }
                     if (tk.dhi == p.R - 1) {
-                        const int xx = p.R - 1 - tk.dlo + off;
-                        if ((unsigned)xx < (unsigned)S::GW) {
-                            g_hi += h16f<BF16>(gat(xx));
-                            gat(xx) = 0;
+                        const int m = p.R - 1 - tk.dlo;
+                        if (m <= mmax) {
+                            g_hi += h16f<BF16>(grow[m]);
+                            grow[m] = 0;
                         }
                     }
                 }
@@ -728,7 +731,7 @@ int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const v
         encode_tmap(&m4, code, 2, tok_dims, tok_str, boxc, G::SWZB, c2) ||
         encode_tmap(&m5, code, 2, rel_dims, rel_str, boxb, G::SWZB, xr) ||
         encode_tmap(&m6, code, 2, rel_dims, rel_str, boxb, G::SWZB, yr) ||
-        encode_tmap(&mg, code, 3, g_dims, g_str, boxg, 128, Gbuf))
+        encode_tmap(&mg, code, 3, g_dims, g_str, boxg, 0, Gbuf))
         return (int)cudaErrorInvalidValue;
     auto kern = bwd_tc_kernel<D, BF16, SIGMA, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);

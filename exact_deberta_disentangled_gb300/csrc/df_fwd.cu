@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
         put_colterm(0, col_fetch(0, kind_of(0)));
         ColRaw cr = col_fetch(1, kind_of(1));                           // tile it + 1
+        BandRaw bn = band_fetch<BM, BN, 1>(p, dtab, i0, w4, tid, lane);      // band indices, one tile ahead
         for (int it = 0; it < ntiles && ok; ++it) {
             const int j0 = it * BN;
             const TileKind tk = kind_of(it);
@@ -349,11 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(1, 256);
             put_colterm((it + 1) & 1, cr);
             cr = col_fetch(it + 2, kind_of(it + 2));
+            BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
+            if (it + 1 < ntiles && !kind_of(it + 1).uniform) bn = band_fetch<BM, BN, 1>(p, dtab, i0 - j0 - BN, w4, tid, lane);
             int own_a = 0;
             if (!tk.uniform) {
-                fill_dwin<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, dwin, tid, 256);
-                int lo, hi;
-                own_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
+                pin(bc.dw);
+                pin(bc.rng);
+                if (tid < BM + BN - 1) dwin[tid] = (int16_t)(bc.dw - tk.dlo);
+                int lo = __shfl_sync(0xffffffffu, bc.rng, 0) - tk.dlo, hi = __shfl_sync(0xffffffffu, bc.rng, 1) - tk.dlo;
+                const int clo = __shfl_sync(0xffffffffu, bc.rng, 2) - tk.dlo, chi = __shfl_sync(0xffffffffu, bc.rng, 3) - tk.dlo;
                 own_a = lo & ~15;
                 // both warps of a lane quarter copy half of each band window
                 if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
@@ -365,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
                 tc_fence_after();
                 if (32 * w4 < BN) {
-                    cross_range<BM, BN, 1>(p, dtab, i0 - j0, tk.dlo, w4, lo, hi);
+                    lo = clo;
+                    hi = chi;
                     const int ca =
                         copy_band_window(lane_base + TM::T, lo, hi, cross + row * G::CROSS_S, kscale, hf, 2);
                     if (lane == 0 && hf == 0) bars->cross_base[w4] = ca;

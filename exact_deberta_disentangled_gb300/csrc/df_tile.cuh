@@ -129,14 +129,37 @@ DF_DEV TileKind classify(const ProblemDev& p, const int32_t* __restrict__ dtab, 
     return kind_finish(p, kind_fetch<NR, NC, SIGMA>(p, dtab, base));
 }
 
-// dwin[x] = delta(r) - dlo for the tile, x = SIGMA*(row - col) + (SIGMA > 0 ? NC - 1 : NR - 1).
+// dwin[x] = delta(r) - dlo for the tile, x = SIGMA*(row - col) + (SIGMA > 0 ? NC - 1 : NR - 1),
+// i.e. r = base + x - (SIGMA > 0 ? NC - 1 : NR - 1); thread x fills entry x (band_fetch).
+
+// The relative indices a band tile needs, as loaded from the table, for one
+// softmax thread: its entry of the tile's index window (thread tid < NR + NC
+// - 1) and, in lanes 0-3, one end each of the own and cross windows of its
+// lane quarter (lane 0 own low, 1 own high, 2 cross low, 3 cross high; the
+// warp reads them with shuffles).  The kernels fetch them one tile ahead and
+// use them when the tile comes, so no band tile waits on the table.
+struct BandRaw {
+    int dw, rng;
+};
+
 template <int NR, int NC, int SIGMA>
-DF_DEV void fill_dwin(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int dlo, int16_t* dwin,
-                      int tid, int nthreads) {
-    for (int x = tid; x < NR + NC - 1; x += nthreads) {
-        const int r = base + x - (SIGMA > 0 ? NC - 1 : NR - 1);
-        dwin[x] = (int16_t)(dclamp(p, dtab, r) - dlo);
-    }
+DF_DEV BandRaw band_fetch(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int w, int tid,
+                          int lane) {
+    BandRaw r;
+    const int x = tid < NR + NC - 1 ? tid : 0;
+    r.dw = dclamp(p, dtab, base + x - (SIGMA > 0 ? NC - 1 : NR - 1));
+    // own window of rows [32w, 32w + 32), cross window of columns [32w, 32w + 32)
+    const int k = lane & 3;
+    const int rel = SIGMA > 0 ? (k == 0   ? base + 32 * w - (NC - 1)
+                                 : k == 1 ? base + 32 * w + 31
+                                 : k == 2 ? base - (32 * w + 31)
+                                          : base + (NR - 1) - 32 * w)
+                              : (k == 0   ? base - (32 * w + 31)
+                                 : k == 1 ? base - 32 * w + (NC - 1)
+                                 : k == 2 ? base + 32 * w - (NR - 1)
+                                          : base + 32 * w + 31);
+    r.rng = dclamp(p, dtab, rel);
+    return r;
 }
 
 // Copy the columns of a band product that a lane quarter needs (`lo` ..
@@ -169,26 +192,6 @@ DF_DEV int copy_band_window(uint32_t t_lane_col0, int lo, int hi, uint16_t* dst,
         }
     }
     return a;
-}
-
-// Band window of the own product for the warp holding rows [32w, 32w + 32).
-template <int NR, int NC, int SIGMA>
-DF_DEV void own_range(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int dlo, int w, int& lo,
-                      int& hi) {
-    const int rmin = SIGMA > 0 ? base + 32 * w - (NC - 1) : base - (32 * w + 31);
-    const int rmax = SIGMA > 0 ? base + 32 * w + 31 : base - 32 * w + (NC - 1);
-    lo = dclamp(p, dtab, rmin) - dlo;
-    hi = dclamp(p, dtab, rmax) - dlo;
-}
-
-// Band window of the cross product for the warp holding columns [32u, 32u + 32).
-template <int NR, int NC, int SIGMA>
-DF_DEV void cross_range(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int dlo, int u, int& lo,
-                        int& hi) {
-    const int rmin = SIGMA > 0 ? base - (32 * u + 31) : base + 32 * u - (NR - 1);
-    const int rmax = SIGMA > 0 ? base + (NR - 1) - 32 * u : base + 32 * u + 31;
-    lo = dclamp(p, dtab, rmin) - dlo;
-    hi = dclamp(p, dtab, rmax) - dlo;
 }
 
 DF_DEV float h2f(uint16_t h) {

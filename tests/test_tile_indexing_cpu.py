@@ -1,6 +1,7 @@
 """CPU model of the tensor-core kernels' band-tile index arithmetic
-(csrc/df_tile.cuh: classify, fill_dwin, own_range, cross_range,
-copy_band_window; csrc/df_bwd.cu: the diagonal-sum staging).  For every tile
+(csrc/df_tile.cuh: classify, band_fetch (the index window and the own /
+cross window ends), copy_band_window; csrc/df_bwd_kernel.cuh: the
+diagonal-sum staging).  For every tile
 of the workloads' shapes it checks that each gathered relative index lies in
 the window the warp copied out of tensor memory, that the copied columns stay
 inside the band product, and that each staged diagonal sum lands inside its
@@ -51,7 +52,7 @@ def check_kernel(L, span, nb, mp, D, sigma, n=None):
             nband_tiles += 1
             assert 0 <= dhi - dlo < NBAND
             x = np.arange(NR + NC - 1)
-            dwin = dcl(base + x - OFF) - dlo                 # fill_dwin
+            dwin = dcl(base + x - OFF) - dlo                 # band_fetch: index window
             assert dwin.min() >= 0 and dwin.max() < NBAND
             m = dwin[xidx]                                   # [NR, NC] gathered band index
             # exact relative index of each element equals the table's value
@@ -120,17 +121,3 @@ def test_model_catches_a_flipped_relative_index():
     bad = tab[np.clip(base - (x - (NR - 1)), -(L - 1), L - 1) + L - 1]
     assert not np.array_equal(good, bad)
 
-
-@pytest.mark.parametrize("GW", [320, 256])
-def test_swizzled_staging_rows_stay_in_their_row(GW):
-    """The backward kernels address element xx of staging row `row` through
-    the TMA 128-byte swizzle (16-byte chunk c of 128-byte segment s stored at
-    c ^ (s & 7)); every row's GW elements must map one-to-one onto that row's
-    own GW slots, so clearing a row clears exactly its sums."""
-    xx = np.arange(GW)
-    for row in range(128):
-        sg = row * (GW // 64) + (xx >> 6)
-        x = xx & 63
-        e = sg * 64 + ((((x >> 3) ^ (sg & 7)) << 3) | (x & 7))
-        assert e.min() >= row * GW and e.max() < (row + 1) * GW
-        assert len(np.unique(e)) == GW

@@ -74,6 +74,9 @@ PROFILE_FILES = {
 
 def kernel_traffic(kernel: str):
     import hashlib
+    if kernel == "bwd_attn":   # the concurrent dQ + dK/dV pair: both kernels' traffic
+        a, b = kernel_traffic("dq"), kernel_traffic("dkv")
+        return None if a is None or b is None else a + b
     if kernel not in PROFILE_FILES:
         return None
     md, srcs = PROFILE_FILES[kernel]
@@ -259,6 +262,7 @@ def run_gpu(args, rank, world, local_rank):
         e.record(stream)
     torch.cuda.synchronize()
     phase_ms = {p: [] for p in PHASES}
+    phase_ms["bwd_attn"] = []   # dQ and dK/dV run concurrently: first start to last end
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
@@ -277,6 +281,10 @@ def run_gpu(args, rank, world, local_rank):
             torch.cuda.synchronize()
             for pi, p in enumerate(PHASES):
                 phase_ms[p].append(ev_ph[2 * pi].elapsed_time(ev_ph[2 * pi + 1]))
+            # the dQ kernel (side stream) and the dK/dV kernel (this stream) overlap
+            s_dq, e_dq, s_dkv, e_dkv = ev_ph[2], ev_ph[3], ev_ph[4], ev_ph[5]
+            t_dkv0, t_dq1, t_dkv1 = (s_dq.elapsed_time(x) for x in (s_dkv, e_dq, e_dkv))
+            phase_ms["bwd_attn"].append(max(t_dq1, t_dkv1) - min(0.0, t_dkv0))
     finally:
         Bd.set_profile_events(None)
     torch.cuda.synchronize()
@@ -314,14 +322,17 @@ def run_gpu(args, rank, world, local_rank):
         return
     peaks, peak_src = load_peaks()
     avg = {p: sum(v) / len(v) for p, v in phase_ms.items()}
-    dominant = max(PHASES, key=lambda p: avg[p])
+    # roofline units: the forward kernel, the concurrent dQ + dK/dV pair, the
+    # relative-gradient kernels
+    dominant = max(("fwd", "bwd_attn", "rel"), key=lambda p: avg[p])
     # algorithmic tensor FLOPs of each kernel by the pages' count:
     #   fwd kernel  4 L^2 D + 4 L R D (all of the forward count)
     #   dK/dV kernel  S^T, dP^T, dV, dK products: 8 L^2 D
     #   dQ kernel     dQ product: 2 L^2 D (its recomputed S, dP are not credited)
     #   rel kernels   the relative-position gradient products: 8 L R D
+    #   bwd_attn      the dQ and dK/dV kernels, which run concurrently: 10 L^2 D
     kflops = {"fwd": fl_f, "dkv": B * H * 8 * L * L * D, "dq": B * H * 2 * L * L * D,
-              "rel": B * H * 8 * L * R * D}
+              "rel": B * H * 8 * L * R * D, "bwd_attn": B * H * 10 * L * L * D}
     peak = peaks.get("bf16_tflops", 1900.0)
     achieved = kflops[dominant] / (avg[dominant] * 1e-3) / 1e12
     traffic = kernel_traffic(dominant)

@@ -5,9 +5,49 @@
 // "DisentangledFlash" (section "Hugging Face usage") splits the fused
 // backward into a dQ kernel and a dK/dV kernel; section "Performance" counts
 // the relative-position gradients.
+//
+// The dQ and dK/dV kernels read the same inputs and write disjoint outputs,
+// so they run concurrently: dQ on a side stream forked from the caller's
+// stream and joined back before the relative-gradient kernels.  Each kernel
+// is 128-row CTAs over (sequence, head) pairs -- at the L = 8192 workload
+// 1,536 CTAs, ten full waves on 152 SMs and a 16-CTA tail -- and running the
+// two together lets one kernel's tail overlap the other's waves.
+#include <mutex>
+
 #include "df_internal.h"
 
 namespace df {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Side stream and fork / join events of each device, created on first use
+// with that device current.  The fork / join pair is shared by every call on
+// the device, so one call's record-and-wait sequence holds `g_mu`.
+std::mutex g_mu;
+bool g_tried[kMaxDevices];
+cudaStream_t g_side[kMaxDevices];
+cudaEvent_t g_fork[kMaxDevices], g_join[kMaxDevices];
+
+bool side_stream(int dev, cudaStream_t& side, cudaEvent_t& fork, cudaEvent_t& join) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    if (!g_tried[dev]) {
+        g_tried[dev] = true;
+        if (cudaStreamCreateWithFlags(&g_side[dev], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&g_fork[dev], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&g_join[dev], cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            g_side[dev] = nullptr;
+        }
+    }
+    if (!g_side[dev]) return false;
+    side = g_side[dev];
+    fork = g_fork[dev];
+    join = g_join[dev];
+    return true;
+}
+
+}  // namespace
 
 int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
                   const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
@@ -18,11 +58,26 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
     cudaError_t ce = cudaMemsetAsync(ws.G, 0, gbytes, st);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(ws.Gp, 0, gbytes, st);
     if (ce != cudaSuccess) return (int)ce;
-    // dQ kernel: rows = queries (Q, dO), columns = keys (K, V); own band Kr, cross Qr
-    int e = launch_bwd_dq(p, ws, dt, q, dout, k, v, kr, qr, ws.G, Rp, ws.acc32a, nullptr, lse, st);
-    if (e) return e;
-    // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO); own band Qr, cross Kr
-    e = launch_bwd_dkv(p, ws, dt, k, v, q, dout, qr, kr, ws.Gp, Rp, ws.acc32b, dv, lse, st);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
+    int e = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        cudaStream_t side = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+        bool conc = side_stream(dev, side, fork, join);
+        if (conc && (cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)) {
+            cudaGetLastError();
+            conc = false;   // both kernels on the caller's stream instead
+        }
+        // dQ kernel: rows = queries (Q, dO), columns = keys (K, V); own band Kr, cross Qr
+        e = launch_bwd_dq(p, ws, dt, q, dout, k, v, kr, qr, ws.G, Rp, ws.acc32a, nullptr, lse, conc ? side : st);
+        if (conc) cudaEventRecord(join, side);
+        // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO); own band Qr, cross Kr
+        if (!e) e = launch_bwd_dkv(p, ws, dt, k, v, q, dout, qr, kr, ws.Gp, Rp, ws.acc32b, dv, lse, st);
+        // the caller's stream continues only after the dQ kernel too
+        if (conc && cudaStreamWaitEvent(st, join, 0) != cudaSuccess && !e) e = (int)cudaErrorUnknown;
+    }
     if (e) return e;
     return launch_rel_tc(p, ws, dt, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st);
 }

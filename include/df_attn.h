@@ -137,6 +137,11 @@ df_status df_attn_fwd(const df_attn_params *p, const void *q, const void *k, con
  * the batch, overwritten).  All gradients are deterministic: the same call
  * gives bitwise the same results (no floating-point atomics; relative-
  * position gradients are reduced in a fixed order).
+ * Ordering: the work is ordered after earlier work on `stream` and later
+ * work on `stream` waits for all of it.  Internally the dQ kernel runs on a
+ * per-device side stream (created on the first backward on that device)
+ * forked from `stream` by an event and joined back before the call's last
+ * kernels, so that it overlaps the dK/dV kernel.
  */
 df_status df_attn_bwd(const df_attn_params *p, const void *q, const void *k, const void *v, const void *qr,
                       const void *kr, const void *out, const float *lse, const void *dout, void *dq, void *dk,

@@ -291,7 +291,14 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+    # a bounded wait that gave up inside a kernel leaves its code in the
+    # workspace's error word: such a step did not do its work
+    ef, eb = Bd.device_error(wsf), Bd.device_error(wsb)
+    if ef or eb:
+        raise SystemExit(f"device error word after the timed steps: forward {ef}, backward {eb}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    print("per-step ms: " + " ".join(f"{t:.3f}" for t in step_ms) + " | fwd: " +
+          " ".join(f"{t:.3f}" for t in phase_ms["fwd"]), file=sys.stderr, flush=True)
     ms = sum(step_ms) / len(step_ms)
     ms = max_over_ranks(ms, world, dev)
     fl_f, fl_b = flops_fwd(B, H, L, D, R), flops_bwd(B, H, L, D, R)

@@ -62,10 +62,14 @@ template <int D>
 struct BwdSmem {
     using G = Geo<D>;
     static constexpr int kMaxTiles = 8192 / G::BN;          // L <= 8192
-    // diagonal-sum staging: one row of GW 16-bit sums per tile row, covering
-    // relative rows [dlo & ~63, (dlo & ~63) + GW); a tile reaches at most
-    // BM + BN - 1 of them, starting at most 63 in
-    static constexpr int GW = G::BN == 128 ? 320 : 256;
+    // diagonal-sum staging, one box per quarter of 32 tile rows: 32 rows of
+    // QW 16-bit sums covering relative rows [qa0, qa0 + QW), qa0 the
+    // quarter's lowest relative row rounded down to a multiple of 8.  The
+    // quarter's rows reach at most BN + 31 relative rows (the relative row
+    // moves by at most one per column), starting at most 7 in: slots up to
+    // BN + 37.
+    static constexpr int QW = (G::BN + 38 + 7) / 8 * 8;
+    static constexpr int QSB = 32 * QW * 2;                  // bytes of one quarter's box
     static constexpr int R1 = 0;
     static constexpr int RB = G::BM * D * 2;
     static constexpr int R2 = R1 + RB;
@@ -78,8 +82,13 @@ struct BwdSmem {
     static constexpr int OWNB = G::BM * G::OWN_S * 2;
     static constexpr int CROSS = STG + (OWNB + 15) / 16 * 16;
     static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
-    static constexpr int GSB = G::BM * GW * 2;
-    static constexpr int STGB = (CROSS - STG) + CROSSB > GSB ? (CROSS - STG) + CROSSB : GSB;
+    // the four boxes go over the cross window when they fit there (the own
+    // window of the next band tile is then written while they drain), else
+    // over both windows
+    static constexpr bool STAGE_IN_CROSS = 4 * QSB <= CROSSB;
+    static constexpr int GST = STAGE_IN_CROSS ? CROSS : STG;
+    static constexpr int STGB = (CROSS - STG) + CROSSB > (GST - STG) + 4 * QSB ? (CROSS - STG) + CROSSB
+                                                                               : (GST - STG) + 4 * QSB;
     static constexpr int DWIN = (STG + STGB + 15) / 16 * 16;
     static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // [2 tiles][colb | cdl][BN]
     static constexpr int XCH = COLV + 4 * G::BN * 4;       // [4][BM] floats: exchanges between the two halves
@@ -88,7 +97,7 @@ struct BwdSmem {
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory");
-    static_assert(STG % 1024 == 0 && GW % 64 == 0 && GW >= 63 + G::BM + G::BN - 1, "staging rows");
+    static_assert(STG % 1024 == 0 && GST % 128 == 0 && QSB % 128 == 0 && QW / 8 <= 256, "staging boxes");
 };
 
 struct BwdBars {
@@ -146,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xch = reinterpret_cast<float*>(smem + S::XCH);
     uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::STG);
     uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
-    uint16_t* gstage = reinterpret_cast<uint16_t*>(smem + S::STG);
+    uint16_t* gstage = reinterpret_cast<uint16_t*>(smem + S::GST);
     uint32_t* kinds = reinterpret_cast<uint32_t*>(smem + S::KINDS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -418,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileKind tk = kind_of(it);
             const float* colb = colv + (it & 1) * 2 * BN;
             const float* cdl = colb + BN;
-            if (tid == 0) bulk_wait_read0();   // the previous G box left shared memory
+            // a band tile overwrites the staging boxes of the previous band tile:
+            // they must have left shared memory (their issuers wait here, or
+            // between the two window copies when the boxes lie over the cross window)
+            if (!S::STAGE_IN_CROSS && !tk.uniform && hf == 0 && lane == 0) bulk_wait_read0();
             named_bar_sync(1, 256);
             put_colterms((it + 1) & 1, cr);
             cr = col_fetch(it + 2, kind_of(it + 2));
@@ -439,6 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->t_empty);
+                if (S::STAGE_IN_CROSS) {
+                    if (hf == 0 && lane == 0) bulk_wait_read0();
+                    named_bar_sync(1, 256);
+                }
                 if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
                 tc_fence_after();
                 if (32 * w4 < BN) {
@@ -558,27 +574,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 named_bar_sync(1, 256);   // own / cross no longer read; every dZ is in tensor memory
                 tc_fence_after();
-                // staging row of this tile row: GW 16-bit sums, relative rows from
-                // (dlo & ~63); grow[m] holds relative row dlo + m
-                const int off = tk.dlo & 63;
-                uint16_t* grow = gstage + (size_t)row * S::GW + off;
-                const int mmax = S::GW - 1 - off;   // a clamp: grow[m] stays inside the row
+                // this quarter's relative rows: the index into dwin grows (or
+                // falls) monotonically from one corner of the quarter to the other
+                const int xa = ROWQ ? 32 * w4 : BM - 32 - 32 * w4;
+                const int xb = xa + BN + 30;
+                const int qa = dwin[xa], qb = dwin[xb];
+                const int qmin = qa < qb ? qa : qb, qmax = qa < qb ? qb : qa;
+                const int qa0 = (tk.dlo + qmin) & ~7;   // first relative row of the box (absolute)
+                const int qoff = tk.dlo - qa0;          // slot of relative row dlo + m is m + qoff
+                uint16_t* qstage = gstage + (size_t)w4 * 32 * S::QW;
+                uint16_t* grow = qstage + lane * S::QW + qoff;
+                const int mmax = S::QW - 1 - qoff;   // a clamp: grow[m] stays inside the row
+                const bool bad = qmax + qoff > S::QW - 1;   // cannot happen for a valid tile
                 {
-                    // the warp clears half hf of its 32 rows one row at a time, its
-                    // lanes on consecutive 16-byte chunks (a thread per row would put
-                    // the 32 stores of a warp on one bank: rows are 640 / 512 bytes apart)
-                    constexpr int NZ = S::GW / 16;   // chunks per half row
-                    uint4* gz = reinterpret_cast<uint4*>(gstage + (size_t)(32 * w4) * S::GW) + hf * NZ + lane;
-#pragma unroll 4
-                    for (int r = 0; r < 32; ++r)
-                        if (lane < NZ) gz[r * (S::GW / 8)] = make_uint4(0u, 0u, 0u, 0u);
+                    // the quarter's two warps clear its box, lanes on consecutive
+                    // 16-byte chunks (the box is one dense block)
+                    constexpr int NCK = S::QSB / 16;
+                    uint4* qz = reinterpret_cast<uint4*>(qstage);
+#pragma unroll
+                    for (int i = hf * 32 + lane; i < NCK; i += 64) qz[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
-                const bool bad = tk.dhi - tk.dlo > mmax;   // cannot happen for a valid tile
                 auto gput = [&](int m, float v) { grow[m < mmax ? m : mmax] = f2h16<BF16>(v); };
-                auto dw_at = [&](int col) -> int {
-                    return ROWQ ? dwin[row - col + BN - 1] : dwin[col - row + BM - 1];
-                };
-                named_bar_sync(pair_bar, 64);   // the row is cleared
+                named_bar_sync(pair_bar, 64);   // the box is cleared
                 // Runs of equal relative index along the row (the index is
                 // monotone in the column).  With prefix sums along the row, a run
                 // ends where the next column's index differs and its sum is the
@@ -589,8 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // to it afterwards -- the slot is zero otherwise, since the second
                 // half's indices are all on the other side of the first half's.
                 const int cst = hf * HC;
+                // relative row of column cst + e of this row: dwp[-e] (query rows) or dwp[e]
+                const int16_t* dwp = ROWQ ? dwin + row - cst + BN - 1 : dwin + cst - row + BM - 1;
                 float pre = 0.f, last = 0.f;
-                int m_cur = dw_at(cst);
+                int m_cur = dwp[0];
                 // this half's dZ columns (16-bit, as the products use them), 32 at a time
 #pragma unroll 1
                 for (int g = 0; g < HC / 32; ++g) {
@@ -598,51 +617,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_ld16p(lane_base + TM::Z + hf * (HC / 2) + 16 * g, zr);
                     tc_wait_ld();
 #pragma unroll
-                    for (int e2 = 0; e2 < 32; ++e2) {
-                        const int e = 32 * g + e2;
-                        pre += h16f<BF16>((uint16_t)(zr[e2 >> 1] >> (16 * (e2 & 1))));
-                        if (e + 1 < HC) {
-                            const int m_nxt = dw_at(cst + e + 1);
-                            if (m_nxt != m_cur) {
-                                gput(m_cur, pre - last);
-                                last = pre;
-                                m_cur = m_nxt;
+                    for (int s16 = 0; s16 < 2; ++s16) {
+                        // the relative rows of the next 16 columns, loaded before any
+                        // staging store so that the loads need not wait for the stores
+                        int mw[16];
+#pragma unroll
+                        for (int e2 = 0; e2 < 16; ++e2) {
+                            const int e = 32 * g + 16 * s16 + e2 + 1;
+                            mw[e2] = e < HC ? (ROWQ ? dwp[-e] : dwp[e]) : m_cur;
+                        }
+#pragma unroll
+                        for (int e2 = 0; e2 < 16; ++e2) {
+                            const int e = 16 * s16 + e2;
+                            pre += h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
+                            if (32 * g + e + 1 < HC) {
+                                const int m_nxt = mw[e2];
+                                if (m_nxt != m_cur) {
+                                    gput(m_cur, pre - last);
+                                    last = pre;
+                                    m_cur = m_nxt;
+                                }
                             }
                         }
                     }
                 }
                 const float tail = pre - last;   // the run that ends this half
-                if (hf) gput(m_cur, tail);
+                if (hf) {
+                    gput(m_cur, tail);
+                    fence_proxy_async_smem();   // the box is read by the tensor-memory-access unit
+                }
+                tc_fence_before();
                 named_bar_sync(pair_bar, 64);
+                if (lane == 0) mbar_arrive(&bars->zread);   // dZ no longer read by this warp
                 if (!hf) {
                     const int ms = m_cur < mmax ? m_cur : mmax;
                     grow[ms] = f2h16<BF16>(h16f<BF16>(grow[ms]) + tail);
                     // the clamped relative rows (far field) are summed in registers
-                    if (tk.dlo == 0) {
+                    if (tk.dlo == 0 && qoff >= 0) {
                         g_lo += h16f<BF16>(grow[0]);
                         grow[0] = 0;
                     }
                     if (tk.dhi == p.R - 1) {
                         const int m = p.R - 1 - tk.dlo;
-                        if (m <= mmax) {
+                        if (m + qoff >= 0 && m <= mmax) {
                             g_hi += h16f<BF16>(grow[m]);
                             grow[m] = 0;
                         }
                     }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_3d(&tmG, qstage, 0, (h * Rp + qa0) >> 3, t0 + r0 + 32 * w4);
+                        bulk_commit();
+                    }
                 }
                 if (bad) raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->zread);
-                named_bar_sync(1, 256);
-                if (tid == 0) {
-                    tma_reduce_add_3d(&tmG, gstage, 0, (h * Rp + tk.dlo) >> 6, t0 + r0);
-                    bulk_commit();
-                }
             }
         }
-        if (tid == 0) bulk_wait0();
+        if (hf == 0 && lane == 0) bulk_wait0();   // this quarter's boxes
         // ------------------------------------------------------------ epilogue
         if (ok) ok = mbar_wait_warp(&bars->mma3_done, (ntiles - 1) & 1, err, abort_flag);
         tc_fence_after();
@@ -716,14 +748,14 @@ int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const v
     const uint64_t tok_str[1] = {(uint64_t)p.H * D * 2};
     const uint64_t rel_dims[2] = {(uint64_t)D, (uint64_t)p.H * p.R};
     const uint64_t rel_str[1] = {(uint64_t)D * 2};
-    // G viewed as [T][H Rp / 64][64]: a box of GW / 64 blocks of 64 sums for
-    // each of BM rows lands in shared memory as dense rows of GW sums
-    const uint64_t g_dims[3] = {64, (uint64_t)p.H * Rp / 64, (uint64_t)p.T};
-    const uint64_t g_str[2] = {128, (uint64_t)p.H * Rp * 2};
+    // G viewed as [T][H Rp / 8][8]: a box of QW / 8 blocks of 8 sums for each
+    // of 32 rows lands in shared memory as dense rows of QW sums
+    const uint64_t g_dims[3] = {8, (uint64_t)p.H * Rp / 8, (uint64_t)p.T};
+    const uint64_t g_str[2] = {16, (uint64_t)p.H * Rp * 2};
     const uint32_t boxr[2] = {(uint32_t)G::CW, (uint32_t)G::BM};
     const uint32_t boxc[2] = {(uint32_t)G::CW, (uint32_t)G::BN};
     const uint32_t boxb[2] = {(uint32_t)G::CW, (uint32_t)G::NBAND};
-    const uint32_t boxg[3] = {64, (uint32_t)(S::GW / 64), (uint32_t)G::BM};
+    const uint32_t boxg[3] = {8, (uint32_t)(S::QW / 8), 32};
     const int code = BF16 ? 0 : 1;
     if (encode_tmap(&m1, code, 2, tok_dims, tok_str, boxr, G::SWZB, r1) ||
         encode_tmap(&m2, code, 2, tok_dims, tok_str, boxr, G::SWZB, r2) ||

@@ -31,6 +31,14 @@ df_status resolve(const df_attn_params* a, ProblemDev& out) {
     const bool bucketing = a->position_buckets > 0 && a->max_relative_positions > 0;
     if (bucketing && (a->position_buckets < 2 || a->max_relative_positions - 1 <= a->position_buckets / 2))
         return DF_ERR_UNSUPPORTED;
+    if (bucketing && a->dtype != DF_FP32) {
+        // the tensor-core kernels size their band windows for a relative index
+        // that moves by at most one per relative position: the log segment's
+        // first step, from |r| = buckets / 2, is its largest
+        const double mid = (double)(a->position_buckets / 2);
+        if ((mid - 1.0) * std::log1p(1.0 / mid) > std::log((a->max_relative_positions - 1) / mid))
+            return DF_ERR_UNSUPPORTED;
+    }
     long long T;
     if (a->cu_seqlens) {
         if (a->query_mask || a->key_mask) return DF_ERR_UNSUPPORTED;  // masks are a padded-layout feature

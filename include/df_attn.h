@@ -110,7 +110,10 @@ typedef struct {
  * Supported contract: D in {32, 64, 128}; 1 <= L <= 8192; 1 <= att_span <=
  * 512; B, H >= 1 and B * L * H < 2^31 (padded) or total_tokens * H < 2^31
  * (packed); when log bucketing is on, position_buckets >= 2 and
- * max_relative_positions - 1 > position_buckets / 2.
+ * max_relative_positions - 1 > position_buckets / 2, and for bf16 / fp16
+ * also (m - 1) ln(1 + 1/m) <= ln((max_relative_positions - 1) / m) with
+ * m = position_buckets / 2 (the bucketed index then moves by at most one per
+ * relative position; e.g. 256 buckets need max_relative_positions >= 345).
  */
 
 /* Bytes of device workspace that df_attn_fwd (backward = 0) or df_attn_bwd

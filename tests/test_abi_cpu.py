@@ -86,6 +86,7 @@ def call_fwd(g, dtype_code=0, ws_bytes=1 << 30, ptr=0x10000, ws_ptr=0x20000):
     (dict(L=8193), B.DF_ERR_UNSUPPORTED),
     (dict(span=600), B.DF_ERR_UNSUPPORTED),
     (dict(nb=256, mp=100), B.DF_ERR_UNSUPPORTED),
+    (dict(nb=256, mp=300), B.DF_ERR_UNSUPPORTED),   # bucket steps of two (16-bit path)
     (dict(B=0), B.DF_ERR_INVALID_ARG),
     (dict(H=0), B.DF_ERR_INVALID_ARG),
     (dict(span=0), B.DF_ERR_INVALID_ARG),
@@ -115,3 +116,21 @@ def test_packed_layout_rules(lib):
     assert call_fwd(g) == B.DF_ERR_INVALID_ARG
     g = geom(cu_seqlens=FakeTensor(), total_tokens=2 * 512 + 1)
     assert call_fwd(g) == B.DF_ERR_INVALID_ARG                  # more tokens than B*L
+
+
+@pytest.mark.parametrize("nb", [4, 12, 64, 256, 512])
+def test_bucket_step_rule_matches_the_relative_index_table(lib, nb):
+    """The 16-bit kernels accept a bucketing configuration exactly when the
+    oracle's relative-index table moves by at most one per relative position
+    (the property their band windows are sized for); fp32 accepts all."""
+    import numpy as np
+    import torch
+
+    from oracle import oracle
+    span = max(nb, 8)
+    for mp in range(nb // 2 + 2, 4 * nb + 2, max(1, nb // 16)):
+        tab = oracle.delta_table(2048, span, nb, mp)
+        unit = int(np.abs(np.diff(tab)).max()) <= 1
+        g = geom(nb=nb, mp=mp, span=span, L=2048)
+        assert (B.workspace_size(g, torch.bfloat16, True) > 0) == unit, (nb, mp)
+        assert B.workspace_size(g, torch.float32, True) > 0

@@ -1,7 +1,7 @@
 """CPU model of the tensor-core kernels' band-tile index arithmetic
 (csrc/df_tile.cuh: classify, band_fetch (the index window and the own /
 cross window ends), copy_band_window; csrc/df_bwd_kernel.cuh: the
-diagonal-sum staging).  For every tile
+per-quarter diagonal-sum staging boxes).  For every tile
 of the workloads' shapes it checks that each gathered relative index lies in
 the window the warp copied out of tensor memory, that the copied columns stay
 inside the band product, and that each staged diagonal sum lands inside its
@@ -19,14 +19,14 @@ def geo(D):
     nband = 192 if BM + BN - 1 <= 192 else 256
     own_s = 114 if BN == 64 else 178
     cross_s = 176
-    gw = 320 if BN == 128 else 256        # staging row width (16-bit sums)
-    return BN, nband, own_s, cross_s, gw
+    qw = (BN + 38 + 7) // 8 * 8           # staging box row width (16-bit sums)
+    return BN, nband, own_s, cross_s, qw
 
 
 def check_kernel(L, span, nb, mp, D, sigma, n=None):
     """All (row tile, column tile) pairs of one sequence of length n <= L."""
     n = L if n is None else n
-    BN, NBAND, OWN_S, CROSS_S, GW = geo(D)
+    BN, NBAND, OWN_S, CROSS_S, QW = geo(D)
     NR, NC = BM, BN
     R = 2 * span
     tab = oracle.delta_table(L, span, nb, mp)
@@ -77,14 +77,24 @@ def check_kernel(L, span, nb, mp, D, sigma, n=None):
                 assert a >= 0 and a + 16 * nch <= NBAND and 16 * nch <= CROSS_S
                 mu = m[:, 32 * u:32 * u + 32]
                 assert mu.min() >= lo and mu.max() <= hi
-            # backward: staged diagonal sums (one row of GW sums per tile row,
-            # relative rows from dlo & ~63) and the far-field entries
-            off = dlo & 63
-            xx = m + off
-            assert xx.min() >= 0 and xx.max() < GW and GW % 64 == 0
-            for far in (0, R - 1):
-                if dlo <= far <= dhi:
-                    assert 0 <= far - dlo + off < GW
+            # backward: staged diagonal sums, one box per quarter of 32 rows
+            # (32 rows of QW sums from the quarter's lowest relative row rounded
+            # down to 8, which the kernel reads at two corners of the index
+            # window), and the far-field entries
+            assert QW % 8 == 0 and QW // 8 <= 256
+            for w in range(4):
+                xa = 32 * w if sigma > 0 else NR - 32 - 32 * w
+                xb = xa + NC + 30
+                mq = m[32 * w:32 * w + 32]
+                qmin, qmax = min(dwin[xa], dwin[xb]), max(dwin[xa], dwin[xb])
+                assert mq.min() == qmin and mq.max() == qmax
+                qa0 = (dlo + qmin) & ~7
+                qoff = dlo - qa0
+                slots = mq + qoff
+                assert slots.min() >= 0 and slots.max() < QW
+                for far in (0, R - 1):
+                    if dlo <= far <= dhi and mq.min() <= far - dlo <= mq.max():
+                        assert 0 <= far - dlo + qoff < QW
     return nband_tiles
 
 

@@ -97,7 +97,7 @@ struct BwdSmem {
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory");
-    static_assert(STG % 1024 == 0 && GST % 128 == 0 && QSB % 128 == 0 && QW / 8 <= 256, "staging boxes");
+    static_assert(STG % 1024 == 0 && GST % 128 == 0 && QSB % 128 == 0 && QW <= 256, "staging boxes");
 };
 
 struct BwdBars {
@@ -106,6 +106,7 @@ struct BwdBars {
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
     uint64_t s_full, sread, z_full, zread, mma3_done;
+    uint64_t colv_full[2];
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -113,12 +114,11 @@ struct BwdBars {
 
 DF_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-DF_DEV void tma_reduce_add_3d(const CUtensorMap* m, const void* smem_src, int x, int y, int z) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            (uint64_t)m),
-        "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
-        : "memory");
+DF_DEV void tma_reduce_add_2d(const CUtensorMap* m, const void* smem_src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     (uint64_t)m),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+                 : "memory");
 }
 DF_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 DF_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -182,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->z_full, 8);
         mbar_init(&bars->zread, 8);
         mbar_init(&bars->mma3_done, 1);
+        mbar_init(&bars->colv_full[0], 32);
+        mbar_init(&bars->colv_full[1], 32);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -201,17 +203,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // The warp walks the tiles: lane 0 issues the tensor copies, and the
+        // warp writes each tile's per-column terms to shared memory
+        // (double-buffered) for the softmax warps:
+        //   cv0 = column bias (P2C of keys / C2P of queries in uniform tiles,
+        //         0 in band tiles, -inf for masked or missing columns), minus the
+        //         column's LSE (base 2) when the columns are queries;
+        //   cv1 = c * Dl of the column (dK/dV kernel only).
+        // Slot m & 1 is free when tile m's columns are loaded: tile m - 2's
+        // column stage was released, so its products -- issued after its
+        // softmax warps finished reading its terms -- have completed.
+        const size_t T = (size_t)p.T;
+        const float* relb_h = relb + (size_t)h * 4 * T;
+        const uint8_t* cmask = ROWQ ? p.kmask : p.qmask;
+        auto put_columns = [&](int m) {
+            const TileKind k = unpack_kind(kinds[m]);
+            float* cv = colv + (m & 1) * 2 * BN;
+            constexpr int NJ = BN / 32;
+            // every load of the tile first (one memory round trip), then the terms
+            float cb[NJ], ls[NJ], rt[NJ];
+            int mk[NJ];
+#pragma unroll
+            for (int q = 0; q < NJ; ++q) {
+                const int ct = m * BN + 32 * q + lane;
+                const int cs = ct < n ? ct : 0;   // an index that is safe to load
+                cb[q] = k.uniform ? ld_early(relb_h + ((ROWQ ? 2 : 0) + k.which) * T + t0 + cs) : 0.f;
+                mk[q] = cmask ? ld_early(cmask + t0 + cs) : 1;
+                ls[q] = ROWQ ? 0.f : ld_early(lse + lse_index(p, b, h, t0, cs));
+                rt[q] = ROWQ ? 0.f : ld_early(rowterm + lse_index(p, b, h, t0, cs));
+            }
+#pragma unroll
+            for (int q = 0; q < NJ; ++q) {
+                const int j = 32 * q + lane;
+                const bool valid = m * BN + j < n && mk[q] != 0;
+                cv[j] = valid ? (ROWQ ? cb[q] : cb[q] - ls[q] * kLog2e) : -INFINITY;
+                cv[BN + j] = valid && !ROWQ ? p.scale * rt[q] : 0.f;
+            }
+            mbar_arrive(&bars->colv_full[m & 1]);
+        };
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars->row_full, 2 * S::RB);
             for (int c = 0; c < G::NCH; ++c) {
                 tma_load_2d(smem + S::R1 + c * BM * G::CW * 2, &tmR1, h * D + c * G::CW, t0 + r0, &bars->row_full);
                 tma_load_2d(smem + S::R2 + c * BM * G::CW * 2, &tmR2, h * D + c * G::CW, t0 + r0, &bars->row_full);
             }
-            int band_loads = 0;
-            for (int it = 0; it < ntiles; ++it) {
-                const int s = it & 1, use = it >> 1;
-                const int c0 = it * BN;
-                if (use > 0 && !mbar_wait(&bars->c_empty[s], (use - 1) & 1, err, abort_flag)) break;
+        }
+        int band_loads = 0;
+        for (int it = 0; it < ntiles; ++it) {
+            const int s = it & 1, use = it >> 1;
+            const int c0 = it * BN;
+            if (use > 0 && !mbar_wait_warp(&bars->c_empty[s], (use - 1) & 1, err, abort_flag)) break;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->c_full[s], 2 * S::CB);
                 for (int c = 0; c < G::NCH; ++c) {
                     tma_load_2d(smem + S::C1 + s * S::CB + c * BN * G::CW * 2, &tmC1, h * D + c * G::CW, t0 + c0,
@@ -219,31 +261,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(smem + S::C2 + s * S::CB + c * BN * G::CW * 2, &tmC2, h * D + c * G::CW, t0 + c0,
                                 &bars->c_full[s]);
                 }
-                const TileKind tk = unpack_kind(kinds[it]);
-                if (tk.uniform) continue;
-                bool ok = true;
-                for (int pass = 0; pass < 2 && ok; ++pass) {
-                    for (int c = 0; c < G::NCH; ++c) {
-                        if (band_loads > 0 &&
-                            !mbar_wait(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
+            }
+            put_columns(it);
+            const TileKind tk = unpack_kind(kinds[it]);
+            if (tk.uniform) continue;
+            bool ok = true;
+            for (int pass = 0; pass < 2 && ok; ++pass) {
+                for (int c = 0; c < G::NCH; ++c) {
+                    if (band_loads > 0 &&
+                        !mbar_wait_warp(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
                         mbar_arrive_expect_tx(&bars->band_full, S::BANDB);
                         tma_load_2d(smem + S::BAND, pass == 0 ? &tmXr : &tmYr, c * G::CW, h * p.R + tk.dlo,
                                     &bars->band_full);
-                        ++band_loads;
                     }
+                    ++band_loads;
                 }
-                if (!ok) break;
             }
+            if (!ok) break;
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Order per tile m:  S / dP of tile m + 1 (once the softmax warps have
         // read tile m's into registers), then the dK / dV (dQ) products of tile
-        // m (once its 16-bit dZ / P~ are written).  When the next tile's band
-        // products would overwrite dZ / P~, they wait for tile m to finish.
+        // m (once its 16-bit dZ / P~ are written).  When tile m + 1 is a band
+        // tile, only its own band product precedes tile m's products.  When the
+        // next tile's band products would overwrite dZ / P~, they wait for
+        // tile m to finish.
         // The whole warp walks the issue loop (its control flow warp-uniform);
         // the MMAs and commits are the elect.sync forms, issued by one lane.
         // Operand descriptors are built once (per CTA or per ring stage) and
@@ -264,27 +311,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dC2m0 = desc_mn<G>(sC20, BN, 0), dC2m1 = dadd(dC2m0, S::CB);
             bool ok = mbar_wait_warp(&bars->row_full, 0, err, abort_flag);
             int band_used = 0, t_uses = 0;
-            auto issue_sdp = [&](int m, const TileKind& tk) -> bool {
+            // band product `pass` of band tile m (0: own, rows x band; 1: cross,
+            // columns x band) into the band columns, once the previous product
+            // was copied out
+            auto issue_band = [&](int m, int pass) -> bool {
+                const int s = m & 1, use = m >> 1;
+                if (pass == 1 && !mbar_wait_warp(&bars->c_full[s], use & 1, err, abort_flag)) return false;
+                if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)) return false;
+                const uint64_t dA = pass == 0 ? dR1 : s ? dC1k1 : dC1k0;
+                const int arows = pass == 0 ? BM : BN;
+                for (int c = 0; c < G::NCH; ++c) {
+                    if (!mbar_wait_warp(&bars->band_full, band_used & 1, err, abort_flag)) return false;
+                    tc_fence_after();
+                    for (int k = 0; k < G::CW / 16; ++k)
+                        tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, c * (G::CW / 16) + k)),
+                                    dadd(dBand, kofs<G>(G::NBAND, k)), idT, (c | k) != 0);
+                    tc_commit_w(&bars->band_empty);
+                    ++band_used;
+                }
+                tc_commit_w(&bars->t_full);
+                ++t_uses;
+                return true;
+            };
+            // S / dP of tile m (after its band products, when it is a band tile)
+            auto issue_s = [&](int m, const TileKind& tk) -> bool {
                 const int s = m & 1, use = m >> 1;
                 if (!tk.uniform) {
-                    for (int pass = 0; pass < 2; ++pass) {
-                        if (pass == 1 && !mbar_wait_warp(&bars->c_full[s], use & 1, err, abort_flag)) return false;
-                        if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
-                            return false;
-                        const uint64_t dA = pass == 0 ? dR1 : s ? dC1k1 : dC1k0;
-                        const int arows = pass == 0 ? BM : BN;
-                        for (int c = 0; c < G::NCH; ++c) {
-                            if (!mbar_wait_warp(&bars->band_full, band_used & 1, err, abort_flag)) return false;
-                            tc_fence_after();
-                            for (int k = 0; k < G::CW / 16; ++k)
-                                tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, c * (G::CW / 16) + k)),
-                                            dadd(dBand, kofs<G>(G::NBAND, k)), idT, (c | k) != 0);
-                            tc_commit_w(&bars->band_empty);
-                            ++band_used;
-                        }
-                        tc_commit_w(&bars->t_full);
-                        ++t_uses;
-                    }
                     // S / dP reuse the band columns: wait until the cross window was copied out
                     if (!mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)) return false;
                 } else if (!mbar_wait_warp(&bars->c_full[s], use & 1, err, abort_flag)) {
@@ -299,6 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit_w(&bars->s_full);
                 return true;
+            };
+            auto issue_sdp = [&](int m, const TileKind& tk) -> bool {
+                if (!tk.uniform && !(issue_band(m, 0) && issue_band(m, 1))) return false;
+                return issue_s(m, tk);
             };
             auto issue_acc = [&](int m) -> bool {
                 const int s = m & 1;
@@ -323,6 +379,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool nxt = it + 1 < ntiles;
                 const TileKind kn = unpack_kind(kinds[nxt ? it + 1 : it]);
                 const bool early = nxt && (!TM::T_OVER_Z || kn.uniform);
+                if (early && !kn.uniform) {
+                    // next tile a band tile: its own product goes first, then this
+                    // tile's products (so that they run while the softmax warps
+                    // finish this tile), then its cross product and S / dP, which
+                    // wait for the softmax warps to copy the windows out
+                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, err, abort_flag))) break;
+                    if (!(ok = issue_band(it + 1, 0))) break;
+                    if (!(ok = issue_acc(it))) break;
+                    if (!(ok = issue_band(it + 1, 1) && issue_s(it + 1, kn))) break;
+                    continue;
+                }
                 if (early) {
                     if (!(ok = mbar_wait_warp(&bars->sread, it & 1, err, abort_flag))) break;
                     if (!(ok = issue_sdp(it + 1, kn))) break;
@@ -377,49 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int t_uses = 0;
         bool ok = true;
         uint16_t* own_row = own + row * G::OWN_S;
-        // per-column terms of a tile:
-        //   cv0 = column bias (P2C of keys / C2P of queries in uniform tiles,
-        //         0 in band tiles, -inf for masked or missing columns), minus the
-        //         column's LSE (base 2) when the columns are queries;
-        //   cv1 = c * Dl of the column (dK/dV kernel only).
-        // Their loads are issued two tiles ahead (col_fetch) and used one tile
-        // ahead, when they go to shared memory (double-buffered).  No loaded
-        // value is used in the tile that loads it.
-        struct ColRaw {
-            float cb, ls, rt;
-            int ok, mk;
-        };
-        auto col_fetch = [&](int jt, const TileKind& k) -> ColRaw {
-            ColRaw c;
-            const int ct = jt * BN + tid;
-            c.ok = tid < BN && ct < n;
-            const int cs = c.ok ? ct : 0;   // an index that is safe to load
-            c.cb = k.uniform ? relb_h[((ROWQ ? 2 : 0) + k.which) * T + t0 + cs] : 0.f;
-            const uint8_t* cmask = ROWQ ? p.kmask : p.qmask;
-            c.mk = cmask ? cmask[t0 + cs] : 1;
-            c.ls = 0.f;
-            c.rt = 0.f;
-            if (!ROWQ) {
-                c.ls = lse[lse_index(p, b, h, t0, cs)];
-                c.rt = rowterm[lse_index(p, b, h, t0, cs)];
-            }
-            return c;
-        };
-        auto put_colterms = [&](int slot, ColRaw c) {
-            pin(c.cb);
-            pin(c.ls);
-            pin(c.rt);
-            pin(c.ok);
-            pin(c.mk);
-            if (tid < BN) {
-                const bool valid = c.ok && c.mk != 0;
-                colv[slot * 2 * BN + tid] = !valid ? -INFINITY : ROWQ ? c.cb : c.cb - c.ls * kLog2e;
-                colv[slot * 2 * BN + BN + tid] = valid && !ROWQ ? p.scale * c.rt : 0.f;
-            }
-        };
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
-        put_colterms(0, col_fetch(0, kind_of(0)));
-        ColRaw cr = col_fetch(1, kind_of(1));                              // tile it + 1
         BandRaw bn = band_fetch<BM, BN, SIGMA>(p, dtab, tile_base(0), w4, tid, lane);   // band indices, one tile ahead
         for (int it = 0; it < ntiles && ok; ++it) {
             const int c0 = it * BN;
@@ -432,8 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // between the two window copies when the boxes lie over the cross window)
             if (!S::STAGE_IN_CROSS && !tk.uniform && hf == 0 && lane == 0) bulk_wait_read0();
             named_bar_sync(1, 256);
-            put_colterms((it + 1) & 1, cr);
-            cr = col_fetch(it + 2, kind_of(it + 2));
             BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
             if (it + 1 < ntiles && !kind_of(it + 1).uniform)
                 bn = band_fetch<BM, BN, SIGMA>(p, dtab, tile_base(it + 1), w4, tid, lane);
@@ -470,6 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 t_uses += 2;
                 named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
+            // this tile's column terms (written by the producer warp)
+            if (!(ok = mbar_wait_warp(&bars->colv_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
             if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
@@ -667,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_reduce_add_3d(&tmG, qstage, 0, (h * Rp + qa0) >> 3, t0 + r0 + 32 * w4);
+                        tma_reduce_add_2d(&tmG, qstage, h * Rp + qa0, t0 + r0 + 32 * w4);
                         bulk_commit();
                     }
                 }
@@ -748,14 +773,14 @@ int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const v
     const uint64_t tok_str[1] = {(uint64_t)p.H * D * 2};
     const uint64_t rel_dims[2] = {(uint64_t)D, (uint64_t)p.H * p.R};
     const uint64_t rel_str[1] = {(uint64_t)D * 2};
-    // G viewed as [T][H Rp / 8][8]: a box of QW / 8 blocks of 8 sums for each
-    // of 32 rows lands in shared memory as dense rows of QW sums
-    const uint64_t g_dims[3] = {8, (uint64_t)p.H * Rp / 8, (uint64_t)p.T};
-    const uint64_t g_str[2] = {16, (uint64_t)p.H * Rp * 2};
+    // G viewed as [T][H Rp]: a box of 32 rows of QW sums (the box starts on a
+    // multiple of 8 sums, 16 bytes)
+    const uint64_t g_dims[2] = {(uint64_t)p.H * Rp, (uint64_t)p.T};
+    const uint64_t g_str[1] = {(uint64_t)p.H * Rp * 2};
     const uint32_t boxr[2] = {(uint32_t)G::CW, (uint32_t)G::BM};
     const uint32_t boxc[2] = {(uint32_t)G::CW, (uint32_t)G::BN};
     const uint32_t boxb[2] = {(uint32_t)G::CW, (uint32_t)G::NBAND};
-    const uint32_t boxg[3] = {8, (uint32_t)(S::QW / 8), 32};
+    const uint32_t boxg[2] = {(uint32_t)S::QW, 32};
     const int code = BF16 ? 0 : 1;
     if (encode_tmap(&m1, code, 2, tok_dims, tok_str, boxr, G::SWZB, r1) ||
         encode_tmap(&m2, code, 2, tok_dims, tok_str, boxr, G::SWZB, r2) ||
@@ -763,7 +788,7 @@ int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const v
         encode_tmap(&m4, code, 2, tok_dims, tok_str, boxc, G::SWZB, c2) ||
         encode_tmap(&m5, code, 2, rel_dims, rel_str, boxb, G::SWZB, xr) ||
         encode_tmap(&m6, code, 2, rel_dims, rel_str, boxb, G::SWZB, yr) ||
-        encode_tmap(&mg, code, 3, g_dims, g_str, boxg, 0, Gbuf))
+        encode_tmap(&mg, code, 2, g_dims, g_str, boxg, 0, Gbuf))
         return (int)cudaErrorInvalidValue;
     auto kern = bwd_tc_kernel<D, BF16, SIGMA, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);

@@ -189,6 +189,26 @@ DF_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err_word, volati
 // Pin a register value at this point of the program: the empty volatile asm
 // "redefines" it, so arithmetic on a value loaded early cannot be hoisted
 // above (and stall right after) the load.  Emits no instruction.
+// Read-only loads whose results are used a tile later (prefetches).  Written
+// as volatile asm they are issued where they stand: the compiler may move an
+// ordinary read-only load down to its first use, and the prefetch would then
+// wait on a fresh load.
+DF_DEV float ld_early(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+DF_DEV int ld_early(const int32_t* p) {
+    int v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+DF_DEV int ld_early(const uint8_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+    return (int)v;
+}
+
 DF_DEV void pin(float& x) { asm volatile("" : "+f"(x)); }
 DF_DEV void pin(int& x) { asm volatile("" : "+r"(x)); }
 

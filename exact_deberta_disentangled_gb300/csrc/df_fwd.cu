@@ -329,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = jt * BN + tid;
             c.ok = tid < BN && j < n;
             const int js = c.ok ? j : 0;   // an index that is safe to load
-            c.cb = k.uniform ? relb_h[(2 + k.which) * T + t0 + js] : 0.f;
-            c.mk = (!k.uniform && p.kmask) ? p.kmask[t0 + js] : 1;
+            c.cb = k.uniform ? ld_early(relb_h + (2 + k.which) * T + t0 + js) : 0.f;
+            c.mk = (!k.uniform && p.kmask) ? ld_early(p.kmask + t0 + js) : 1;
             return c;
         };
         auto put_colterm = [&](int slot, ColRaw c) {

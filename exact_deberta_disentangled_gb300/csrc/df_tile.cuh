@@ -46,6 +46,13 @@ DF_DEV int dclamp(const ProblemDev& p, const int32_t* __restrict__ dtab, int r) 
     return __ldg(dtab + r + p.L - 1);
 }
 
+// dclamp for prefetches (the load is issued where the call stands)
+DF_DEV int dclamp_early(const ProblemDev& p, const int32_t* __restrict__ dtab, int r) {
+    r = r > p.L - 1 ? p.L - 1 : r;
+    r = r < -(p.L - 1) ? -(p.L - 1) : r;
+    return ld_early(dtab + r + p.L - 1);
+}
+
 // K-major operand: `rows` rows of a [rows x D] tile stored as D/CW regions of
 // [rows x CW] (TMA swizzle), k-step of 16 elements.
 template <class G>
@@ -147,7 +154,7 @@ DF_DEV BandRaw band_fetch(const ProblemDev& p, const int32_t* __restrict__ dtab,
                           int lane) {
     BandRaw r;
     const int x = tid < NR + NC - 1 ? tid : 0;
-    r.dw = dclamp(p, dtab, base + x - (SIGMA > 0 ? NC - 1 : NR - 1));
+    r.dw = dclamp_early(p, dtab, base + x - (SIGMA > 0 ? NC - 1 : NR - 1));
     // own window of rows [32w, 32w + 32), cross window of columns [32w, 32w + 32)
     const int k = lane & 3;
     const int rel = SIGMA > 0 ? (k == 0   ? base + 32 * w - (NC - 1)
@@ -158,7 +165,7 @@ DF_DEV BandRaw band_fetch(const ProblemDev& p, const int32_t* __restrict__ dtab,
                                  : k == 1 ? base - 32 * w + (NC - 1)
                                  : k == 2 ? base + 32 * w - (NR - 1)
                                           : base + 32 * w + 31);
-    r.rng = dclamp(p, dtab, rel);
+    r.rng = dclamp_early(p, dtab, rel);
     return r;
 }
 

@@ -66,8 +66,8 @@ struct FwdSmem {
     static constexpr int CROSS = (OWN + OWNB + 15) / 16 * 16;
     static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
     static constexpr int DWIN = CROSS + CROSSB;
-    static constexpr int COLB = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;   // [2 tiles][BN]
-    static constexpr int XCH = COLB + 2 * G::BN * 4;      // [4][BM] floats: the halves' maxima and sums
+    static constexpr int COLB = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;   // [4 tiles][BN]
+    static constexpr int XCH = COLB + 4 * G::BN * 4;      // [4][BM] floats: the halves' maxima and sums
     static constexpr int kMaxTiles = 8192 / G::BN;        // L <= 8192
     static constexpr int KINDS = XCH + 4 * G::BM * 4;     // packed TileKind of every key tile
     static constexpr int MISC = KINDS + kMaxTiles * 4;
@@ -82,6 +82,7 @@ struct FwdBars {
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
     uint64_t s_full[2], p_full[2], pv_done[2];
+    uint64_t colv_full[4];
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->band_empty, 1);
         mbar_init(&bars->t_full, 1);
         mbar_init(&bars->t_empty, 8);
+        for (int s = 0; s < 4; ++s) mbar_init(&bars->colv_full[s], 32);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -149,6 +151,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // The warp walks the key tiles: lane 0 issues the tensor copies, and
+        // the warp writes each tile's per-key column term to shared memory
+        // (P2C scalar of uniform tiles, with the key mask folded in; key mask
+        // of band tiles; -inf past the sequence end), four tiles deep.  Tile
+        // m's term goes to slot m & 3 once V of tile m - 1 is loaded: that
+        // load waited for P.V of tile m - 3, so tile m - 4 is long done.
+        const size_t T = (size_t)p.T;
+        const float* relb_h = relb + (size_t)h * 4 * T;
+        auto put_columns = [&](int m) {
+            const TileKind k = unpack_kind(kinds[m]);
+            float* cv = colv + (m & 3) * BN;
+            constexpr int NJ = BN / 32;
+            float cb[NJ];
+            int mk[NJ];
+#pragma unroll
+            for (int q = 0; q < NJ; ++q) {
+                const int j = m * BN + 32 * q + lane;
+                const int js = j < n ? j : 0;   // an index that is safe to load
+                cb[q] = k.uniform ? ld_early(relb_h + (2 + k.which) * T + t0 + js) : 0.f;
+                mk[q] = (!k.uniform && p.kmask) ? ld_early(p.kmask + t0 + js) : 1;
+            }
+#pragma unroll
+            for (int q = 0; q < NJ; ++q) {
+                const int j = 32 * q + lane;
+                cv[j] = (m * BN + j < n && mk[q] != 0) ? cb[q] : -INFINITY;
+            }
+            mbar_arrive(&bars->colv_full[m & 3]);
+        };
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
@@ -156,39 +186,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&bars->q_full, S::QB);
             for (int c = 0; c < G::NCH; ++c)
                 tma_load_2d(smem + S::Q + c * BM * G::CW * 2, &tmQ, h * D + c * G::CW, t0 + i0, &bars->q_full);
-            int band_loads = 0;
-            for (int it = 0; it < ntiles; ++it) {
-                const int s = it & 1, use = it >> 1;
-                const int j0 = it * BN;
-                // K of tile it as soon as S of tile it - 2 has read its stage
-                if (use > 0 && !mbar_wait(&bars->k_empty[s], (use - 1) & 1, err, abort_flag)) break;
+        }
+        put_columns(0);
+        int band_loads = 0;
+        for (int it = 0; it < ntiles; ++it) {
+            const int s = it & 1, use = it >> 1;
+            const int j0 = it * BN;
+            // K of tile it as soon as S of tile it - 2 has read its stage
+            if (use > 0 && !mbar_wait_warp(&bars->k_empty[s], (use - 1) & 1, err, abort_flag)) break;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->k_full[s], S::KVB);
                 for (int c = 0; c < G::NCH; ++c)
                     tma_load_2d(smem + S::K0 + s * S::KVB + c * BN * G::CW * 2, &tmK, h * D + c * G::CW, t0 + j0,
                                 &bars->k_full[s]);
-                const TileKind tk = unpack_kind(kinds[it]);
-                bool ok = true;
-                for (int pass = 0; pass < 2 && ok && !tk.uniform; ++pass) {
-                    for (int c = 0; c < G::NCH; ++c) {
-                        if (band_loads > 0 &&
-                            !mbar_wait(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
+            }
+            const TileKind tk = unpack_kind(kinds[it]);
+            bool ok = true;
+            for (int pass = 0; pass < 2 && ok && !tk.uniform; ++pass) {
+                for (int c = 0; c < G::NCH; ++c) {
+                    if (band_loads > 0 &&
+                        !mbar_wait_warp(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
                         mbar_arrive_expect_tx(&bars->band_full, S::BANDB);
                         tma_load_2d(smem + S::BAND, pass == 0 ? &tmKr : &tmQr, c * G::CW, h * p.R + tk.dlo,
                                     &bars->band_full);
-                        ++band_loads;
                     }
+                    ++band_loads;
                 }
-                if (!ok) break;
-                // V of tile it once P.V of tile it - 2 has read its stage
-                if (use > 0 && !mbar_wait(&bars->v_empty[s], (use - 1) & 1, err, abort_flag)) break;
+            }
+            if (!ok) break;
+            // V of tile it once P.V of tile it - 2 has read its stage
+            if (use > 0 && !mbar_wait_warp(&bars->v_empty[s], (use - 1) & 1, err, abort_flag)) break;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->v_full[s], S::KVB);
                 for (int c = 0; c < G::NCH; ++c)
                     tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
                                 &bars->v_full[s]);
             }
+            if (it + 1 < ntiles) put_columns(it + 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -316,40 +354,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_st16(lane_base + ocol + 16 * c, r);
             }
         };
-        // per-key column term of a tile (P2C scalar of uniform tiles, with the
-        // key mask folded in; key mask of band tiles; -inf past the sequence
-        // end).  Its loads are issued two tiles ahead (col_fetch) and used one
-        // tile ahead, when it goes to shared memory (double-buffered).
-        struct ColRaw {
-            float cb;
-            int ok, mk;
-        };
-        auto col_fetch = [&](int jt, const TileKind& k) -> ColRaw {
-            ColRaw c;
-            const int j = jt * BN + tid;
-            c.ok = tid < BN && j < n;
-            const int js = c.ok ? j : 0;   // an index that is safe to load
-            c.cb = k.uniform ? ld_early(relb_h + (2 + k.which) * T + t0 + js) : 0.f;
-            c.mk = (!k.uniform && p.kmask) ? ld_early(p.kmask + t0 + js) : 1;
-            return c;
-        };
-        auto put_colterm = [&](int slot, ColRaw c) {
-            pin(c.cb);
-            pin(c.ok);
-            pin(c.mk);
-            if (tid < BN) colv[slot * BN + tid] = (c.ok && c.mk != 0) ? c.cb : -INFINITY;
-        };
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
-        put_colterm(0, col_fetch(0, kind_of(0)));
-        ColRaw cr = col_fetch(1, kind_of(1));                           // tile it + 1
         BandRaw bn = band_fetch<BM, BN, 1>(p, dtab, i0, w4, tid, lane);      // band indices, one tile ahead
         for (int it = 0; it < ntiles && ok; ++it) {
             const int j0 = it * BN;
             const TileKind tk = kind_of(it);
-            const float* colb = colv + (it & 1) * BN;
+            const float* colb = colv + (it & 3) * BN;
             named_bar_sync(1, 256);
-            put_colterm((it + 1) & 1, cr);
-            cr = col_fetch(it + 2, kind_of(it + 2));
             BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
             if (it + 1 < ntiles && !kind_of(it + 1).uniform) bn = band_fetch<BM, BN, 1>(p, dtab, i0 - j0 - BN, w4, tid, lane);
             int own_a = 0;
@@ -382,6 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 t_uses += 2;
                 named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
+            // this tile's column terms (written by the producer warp), then S
+            if (!(ok = mbar_wait_warp(&bars->colv_full[it & 3], (it >> 2) & 1, err, abort_flag))) break;
             if (!(ok = mbar_wait_warp(&bars->s_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
             tc_fence_after();
             const uint32_t scol = s_col(it);

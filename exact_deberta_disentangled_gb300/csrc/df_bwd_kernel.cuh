@@ -50,6 +50,9 @@ template <int D>
 struct BwdTmem {
     using G = Geo<D>;
     static constexpr uint32_t ACC1 = 0, ACC2 = D;                       // fp32 accumulators
+    // dQ kernel (one accumulator): its rows' Q and dO, 16-bit, as the A
+    // operands of S / dP and of the own band product, in ACC2's columns
+    static constexpr uint32_t A1 = D, A2 = D + D / 2;
     static constexpr uint32_t S = 256, P = 256 + G::BN;                 // fp32 S, dP
     static constexpr uint32_t Z = 2 * D + G::BN <= 256 ? 2 * D : 256 + 2 * G::BN;   // 16-bit dZ, then P~
     static constexpr uint32_t T = 256;                                  // band products
@@ -101,7 +104,7 @@ struct BwdSmem {
 };
 
 struct BwdBars {
-    uint64_t row_full;
+    uint64_t row_full, a_full;
     uint64_t c_full[2], c_empty[2];
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
@@ -140,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmXr, const __grid_constant__ CUtensorMap tmYr,
                   const __grid_constant__ CUtensorMap tmG, const ProblemDev p, const int32_t* __restrict__ dtab,
                   const float* __restrict__ relb, const float* __restrict__ lse, const float* __restrict__ rowterm,
-                  float* __restrict__ acc1_out, void* __restrict__ acc2_out, void* __restrict__ Gbuf, int Rp) {
+                  float* __restrict__ acc1_out, void* __restrict__ acc2_out, void* __restrict__ Gbuf, int Rp,
+                  const void* __restrict__ r1_rows, const void* __restrict__ r2_rows) {
     using G = Geo<D>;
     using S = BwdSmem<D>;
     using TM = BwdTmem<D>;
@@ -169,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->row_full, 1);
+        mbar_init(&bars->a_full, 8);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->c_full[s], 1);
             mbar_init(&bars->c_empty[s], 1);
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive(&bars->colv_full[m & 1]);
         };
-        if (lane == 0) {
+        if (lane == 0 && !ROWQ) {   // the dQ kernel's row operands go to tensor memory instead
             mbar_arrive_expect_tx(&bars->row_full, 2 * S::RB);
             for (int c = 0; c < G::NCH; ++c) {
                 tma_load_2d(smem + S::R1 + c * BM * G::CW * 2, &tmR1, h * D + c * G::CW, t0 + r0, &bars->row_full);
@@ -309,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dC2k0 = desc_k<G>(sC20, BN, 0), dC2k1 = dadd(dC2k0, S::CB);
             const uint64_t dC1m0 = desc_mn<G>(sC10, BN, 0), dC1m1 = dadd(dC1m0, S::CB);
             const uint64_t dC2m0 = desc_mn<G>(sC20, BN, 0), dC2m1 = dadd(dC2m0, S::CB);
-            bool ok = mbar_wait_warp(&bars->row_full, 0, err, abort_flag);
+            bool ok = mbar_wait_warp(ROWQ ? &bars->a_full : &bars->row_full, 0, err, abort_flag);
+            if (ROWQ) tc_fence_after();
             int band_used = 0, t_uses = 0;
             // band product `pass` of band tile m (0: own, rows x band; 1: cross,
             // columns x band) into the band columns, once the previous product
@@ -323,9 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < G::NCH; ++c) {
                     if (!mbar_wait_warp(&bars->band_full, band_used & 1, err, abort_flag)) return false;
                     tc_fence_after();
-                    for (int k = 0; k < G::CW / 16; ++k)
-                        tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, c * (G::CW / 16) + k)),
-                                    dadd(dBand, kofs<G>(G::NBAND, k)), idT, (c | k) != 0);
+                    for (int k = 0; k < G::CW / 16; ++k) {
+                        const int ks = c * (G::CW / 16) + k;
+                        if (ROWQ && pass == 0)
+                            tc_mma_ts_w(tmem + TM::T, tmem + TM::A1 + 8 * ks, dadd(dBand, kofs<G>(G::NBAND, k)), idT,
+                                        ks != 0);
+                        else
+                            tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, ks)), dadd(dBand, kofs<G>(G::NBAND, k)),
+                                        idT, ks != 0);
+                    }
                     tc_commit_w(&bars->band_empty);
                     ++band_used;
                 }
@@ -346,8 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dS = s ? dC1k1 : dC1k0, dP = s ? dC2k1 : dC2k0;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    tc_mma_ss_w(tmem + TM::S, dadd(dR1, kofs<G>(BM, k)), dadd(dS, kofs<G>(BN, k)), idS, k != 0);
-                    tc_mma_ss_w(tmem + TM::P, dadd(dR2, kofs<G>(BM, k)), dadd(dP, kofs<G>(BN, k)), idS, k != 0);
+                    if (ROWQ) {
+                        tc_mma_ts_w(tmem + TM::S, tmem + TM::A1 + 8 * k, dadd(dS, kofs<G>(BN, k)), idS, k != 0);
+                        tc_mma_ts_w(tmem + TM::P, tmem + TM::A2 + 8 * k, dadd(dP, kofs<G>(BN, k)), idS, k != 0);
+                    } else {
+                        tc_mma_ss_w(tmem + TM::S, dadd(dR1, kofs<G>(BM, k)), dadd(dS, kofs<G>(BN, k)), idS, k != 0);
+                        tc_mma_ss_w(tmem + TM::P, dadd(dR2, kofs<G>(BM, k)), dadd(dP, kofs<G>(BN, k)), idS, k != 0);
+                    }
                 }
                 tc_commit_w(&bars->s_full);
                 return true;
@@ -440,6 +457,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool rvalid = rb0 != -INFINITY;
         const float dls_row = p.scale * dl;
+        if constexpr (ROWQ) {
+            // the A operands of S / dP: this row's Q (first column half) or dO
+            // (second), 16-bit, two elements per column (zero past the sequence)
+            constexpr int NW = D / 2;
+            uint32_t a[NW];
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(hf ? r2_rows : r1_rows) +
+                                                              ((size_t)(t0 + (row_in ? rt : 0)) * p.H + h) * D);
+#pragma unroll
+            for (int v = 0; v < NW / 4; ++v) {
+                const uint4 w = row_in ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+                a[4 * v] = w.x;
+                a[4 * v + 1] = w.y;
+                a[4 * v + 2] = w.z;
+                a[4 * v + 3] = w.w;
+            }
+            const uint32_t acol = lane_base + (hf ? TM::A2 : TM::A1);
+#pragma unroll
+            for (int q = 0; q < NW / 16; ++q) {
+                uint32_t r16[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r16[e] = a[16 * q + e];
+                tc_st16(acol + 16 * q, r16);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->a_full);
+        }
         float g_lo = 0.f, g_hi = 0.f;     // this thread's share of the diagonal sums at delta 0 and R-1
         int t_uses = 0;
         bool ok = true;
@@ -797,7 +842,7 @@ int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const v
     const int phase = SIGMA > 0 ? kProfDq : kProfDkv;
     prof_record(phase, 0, st);
     kern<<<grid, kThreads, S::ALLOC, st>>>(m1, m2, m3, m4, m5, m6, mg, p, ws.dtab, ws.relb, lse, ws.rowterm, acc1,
-                                           acc2, Gbuf, Rp);
+                                           acc2, Gbuf, Rp, r1, r2);
     prof_record(phase, 1, st);
     return (int)cudaGetLastError();
 }

@@ -501,7 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // they must have left shared memory (their issuers wait here, or
             // between the two window copies when the boxes lie over the cross window)
             if (!S::STAGE_IN_CROSS && !tk.uniform && hf == 0 && lane == 0) bulk_wait_read0();
-            named_bar_sync(1, 256);
+            // band tiles rewrite the index window and the band windows, which
+            // every warp reads: all of them must be done with the previous tile.
+            // A uniform tile writes no shared state (its column terms come from
+            // the producer, announced per slot), so its warps go on unsynchronised.
+            if (!tk.uniform) named_bar_sync(1, 256);
             BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
             if (it + 1 < ntiles && !kind_of(it + 1).uniform)
                 bn = band_fetch<BM, BN, SIGMA>(p, dtab, tile_base(it + 1), w4, tid, lane);

@@ -113,7 +113,9 @@ struct BwdBars {
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
+    uint32_t stepw[9];
 };
+static_assert(sizeof(BwdBars) <= 256, "barrier block (the MISC region)");
 
 DF_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         uint16_t* own_row = own + row * G::OWN_S;
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
-        BandRaw bn = band_fetch<BM, BN, SIGMA>(p, dtab, tile_base(0), w4, tid, lane);   // band indices, one tile ahead
+        BandRaw bn = band_fetch<BM, BN, SIGMA, true>(p, dtab, tile_base(0), w4, tid, lane);   // band indices, one tile ahead
         for (int it = 0; it < ntiles && ok; ++it) {
             const int c0 = it * BN;
             const int base = tile_base(it);
@@ -508,12 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!tk.uniform) named_bar_sync(1, 256);
             BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
             if (it + 1 < ntiles && !kind_of(it + 1).uniform)
-                bn = band_fetch<BM, BN, SIGMA>(p, dtab, tile_base(it + 1), w4, tid, lane);
+                bn = band_fetch<BM, BN, SIGMA, true>(p, dtab, tile_base(it + 1), w4, tid, lane);
             int own_a = 0;
             if (!tk.uniform) {
                 pin(bc.dw);
+                pin(bc.dwp);
                 pin(bc.rng);
                 if (tid < BM + BN - 1) dwin[tid] = (int16_t)(bc.dw - tk.dlo);
+                put_step_bits(bars->stepw, bc, tid, lane, BM + BN - 1);
                 int lo = __shfl_sync(0xffffffffu, bc.rng, 0) - tk.dlo, hi = __shfl_sync(0xffffffffu, bc.rng, 1) - tk.dlo;
                 const int clo = __shfl_sync(0xffffffffu, bc.rng, 2) - tk.dlo, chi = __shfl_sync(0xffffffffu, bc.rng, 3) - tk.dlo;
                 own_a = lo & ~15;
@@ -569,7 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (band) {
                     const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
                     const uint16_t* orow = own_row - own_a;
-                    const int16_t* dw = ROWQ ? dwin + row - 32 * c + BN - 1 : dwin + 32 * c - row + BM - 1;
+                    // relative index of column 32 c + e: the window entry at x0 - e
+                    // (query rows) or x0 + e; it moves by one at each step bit
+                    const int x0 = ROWQ ? row - 32 * c + BN - 1 : 32 * c - row + BM - 1;
+                    int m = dwin[x0];
+                    uint32_t mk = step_bits(bars->stepw, ROWQ ? x0 - 31 : x0 + 1);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 cv = cv0p[q];
@@ -577,9 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
                             const int e = 4 * q + t;
-                            const int m = ROWQ ? dw[-e] : dw[e];
                             sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cvs[t]) + rowc +
                                                     (h2f(orow[m]) + h2f(crow[e * G::CROSS_S + m])));
+                            if (ROWQ) {
+                                m -= (int)(mk >> 31);   // bit 31 - e: step at x0 - e
+                                mk <<= 1;
+                            } else {
+                                m += (int)(mk & 1u);    // bit e: step at x0 + e + 1
+                                mk >>= 1;
+                            }
                         }
                     }
                 } else {
@@ -680,38 +694,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // to it afterwards -- the slot is zero otherwise, since the second
                 // half's indices are all on the other side of the first half's.
                 const int cst = hf * HC;
-                // relative row of column cst + e of this row: dwp[-e] (query rows) or dwp[e]
-                const int16_t* dwp = ROWQ ? dwin + row - cst + BN - 1 : dwin + cst - row + BM - 1;
+                // relative row of column cst + e of this row: the window entry at
+                // x0 - e (query rows) or x0 + e; a run ends where a step bit is set
+                const int x0 = ROWQ ? row - cst + BN - 1 : cst - row + BM - 1;
                 float pre = 0.f, last = 0.f;
-                int m_cur = dwp[0];
+                int m_cur = dwin[x0];
                 // this half's dZ columns (16-bit, as the products use them), 32 at a time
 #pragma unroll 1
                 for (int g = 0; g < HC / 32; ++g) {
                     uint32_t zr[16];
                     tc_ld16p(lane_base + TM::Z + hf * (HC / 2) + 16 * g, zr);
+                    // bit 31 - e2 (query rows) or e2: step between columns 32 g + e2 and + 1
+                    const uint32_t mk = step_bits(bars->stepw, ROWQ ? x0 - 32 * g - 31 : x0 + 32 * g + 1);
                     tc_wait_ld();
 #pragma unroll
-                    for (int s16 = 0; s16 < 2; ++s16) {
-                        // the relative rows of the next 16 columns, loaded before any
-                        // staging store so that the loads need not wait for the stores
-                        int mw[16];
-#pragma unroll
-                        for (int e2 = 0; e2 < 16; ++e2) {
-                            const int e = 32 * g + 16 * s16 + e2 + 1;
-                            mw[e2] = e < HC ? (ROWQ ? dwp[-e] : dwp[e]) : m_cur;
-                        }
-#pragma unroll
-                        for (int e2 = 0; e2 < 16; ++e2) {
-                            const int e = 16 * s16 + e2;
-                            pre += h16f<BF16>((uint16_t)(zr[e >> 1] >> (16 * (e & 1))));
-                            if (32 * g + e + 1 < HC) {
-                                const int m_nxt = mw[e2];
-                                if (m_nxt != m_cur) {
-                                    gput(m_cur, pre - last);
-                                    last = pre;
-                                    m_cur = m_nxt;
-                                }
-                            }
+                    for (int e2 = 0; e2 < 32; ++e2) {
+                        pre += h16f<BF16>((uint16_t)(zr[e2 >> 1] >> (16 * (e2 & 1))));
+                        const bool step = ((ROWQ ? mk >> (31 - e2) : mk >> e2) & 1u) != 0;
+                        if (32 * g + e2 + 1 < HC && step) {
+                            gput(m_cur, pre - last);
+                            last = pre;
+                            m_cur += ROWQ ? -1 : 1;
                         }
                     }
                 }

@@ -146,15 +146,17 @@ DF_DEV TileKind classify(const ProblemDev& p, const int32_t* __restrict__ dtab, 
 // warp reads them with shuffles).  The kernels fetch them one tile ahead and
 // use them when the tile comes, so no band tile waits on the table.
 struct BandRaw {
-    int dw, rng;
+    int dw, dwp, rng;
 };
 
-template <int NR, int NC, int SIGMA>
+// STEPS: also the index one position back (for the step bits)
+template <int NR, int NC, int SIGMA, bool STEPS = false>
 DF_DEV BandRaw band_fetch(const ProblemDev& p, const int32_t* __restrict__ dtab, int base, int w, int tid,
                           int lane) {
     BandRaw r;
     const int x = tid < NR + NC - 1 ? tid : 0;
     r.dw = dclamp_early(p, dtab, base + x - (SIGMA > 0 ? NC - 1 : NR - 1));
+    r.dwp = STEPS ? dclamp_early(p, dtab, base + x - 1 - (SIGMA > 0 ? NC - 1 : NR - 1)) : 0;
     // own window of rows [32w, 32w + 32), cross window of columns [32w, 32w + 32)
     const int k = lane & 3;
     const int rel = SIGMA > 0 ? (k == 0   ? base + 32 * w - (NC - 1)
@@ -167,6 +169,23 @@ DF_DEV BandRaw band_fetch(const ProblemDev& p, const int32_t* __restrict__ dtab,
                                           : base + 32 * w + 31);
     r.rng = dclamp_early(p, dtab, rel);
     return r;
+}
+
+// Step bits of a band tile's index window: bit x of `stepw` (9 words) is set
+// where the window's relative index changes between positions x - 1 and x.
+// The index moves by at most one per position (the host checks the bucketing
+// for 16-bit inputs), so the indices along a row follow from the first one
+// and these bits: one shared-memory load per 32 columns instead of 32.  All
+// 256 softmax threads call this (thread x holds the index at x and x - 1).
+DF_DEV void put_step_bits(uint32_t* stepw, const BandRaw& b, int tid, int lane, int nx) {
+    const unsigned bits = __ballot_sync(0xffffffffu, tid > 0 && tid < nx && b.dw != b.dwp);
+    if (lane == 0) stepw[tid >> 5] = bits;
+    if (tid == 0) stepw[8] = 0u;
+}
+
+// 32 step bits from position xl on (bit k: step at position xl + k), 0 <= xl <= 224
+DF_DEV uint32_t step_bits(const uint32_t* stepw, int xl) {
+    return __funnelshift_r(stepw[xl >> 5], stepw[(xl >> 5) + 1], (uint32_t)(xl & 31));
 }
 
 // Copy the columns of a band product that a lane quarter needs (`lo` ..

@@ -1,6 +1,7 @@
 """CPU model of the tensor-core kernels' band-tile index arithmetic
 (csrc/df_tile.cuh: classify, band_fetch (the index window and the own /
-cross window ends), copy_band_window; csrc/df_bwd_kernel.cuh: the
+cross window ends), copy_band_window, the step bits that give the gathers'
+and the scatter's relative indices; csrc/df_bwd_kernel.cuh: the
 per-quarter diagonal-sum staging boxes).  For every tile
 of the workloads' shapes it checks that each gathered relative index lies in
 the window the warp copied out of tensor memory, that the copied columns stay
@@ -21,6 +22,57 @@ def geo(D):
     cross_s = 176
     qw = (BN + 38 + 7) // 8 * 8           # staging box row width (16-bit sums)
     return BN, nband, own_s, cross_s, qw
+
+
+def step_words(dwin):
+    """The nine 32-bit words put_step_bits writes (256 threads, thread x = position x)."""
+    nx = len(dwin)
+    bits = np.zeros(9 * 32, dtype=np.uint64)
+    for x in range(1, nx):
+        bits[x] = 1 if dwin[x] != dwin[x - 1] else 0
+    return [int(sum(int(bits[32 * w + k]) << k for k in range(32))) for w in range(9)]
+
+
+def step_bits(words, xl):
+    """step_bits: 32 bits from position xl on (funnel shift of two words)."""
+    assert 0 <= xl <= 224
+    v = words[xl >> 5] | (words[(xl >> 5) + 1] << 32)
+    return (v >> (xl & 31)) & 0xFFFFFFFF
+
+
+def check_step_bits(dwin, sigma, NR, NC):
+    steps = np.diff(dwin)
+    assert steps.min() >= 0 and steps.max() <= 1       # the host's bucketing check guarantees it
+    words = step_words(dwin)
+    # gathers: rows x 32-column chunks
+    for row in range(NR):
+        for c in range(NC // 32):
+            x0 = row - 32 * c + NC - 1 if sigma > 0 else 32 * c - row + NR - 1
+            mk = step_bits(words, x0 - 31 if sigma > 0 else x0 + 1)
+            m = int(dwin[x0])
+            for e in range(32):
+                x = x0 - e if sigma > 0 else x0 + e
+                assert m == dwin[x], (row, c, e)
+                if sigma > 0:
+                    m -= (mk >> (31 - e)) & 1
+                else:
+                    m += (mk >> e) & 1
+    # scatter: each column half, 32-column groups; a run ends at a step bit
+    HC = NC // 2
+    for row in range(NR):
+        for hf in range(2):
+            cst = hf * HC
+            x0 = row - cst + NC - 1 if sigma > 0 else cst - row + NR - 1
+            for g in range(HC // 32):
+                mk = step_bits(words, x0 - 32 * g - 31 if sigma > 0 else x0 + 32 * g + 1)
+                for e2 in range(32):
+                    e = 32 * g + e2
+                    if e + 1 >= HC:
+                        continue
+                    xa = x0 - e if sigma > 0 else x0 + e
+                    xb = x0 - e - 1 if sigma > 0 else x0 + e + 1
+                    bit = (mk >> (31 - e2)) & 1 if sigma > 0 else (mk >> e2) & 1
+                    assert bit == (1 if dwin[xa] != dwin[xb] else 0), (row, hf, e)
 
 
 def check_kernel(L, span, nb, mp, D, sigma, n=None):
@@ -77,6 +129,11 @@ def check_kernel(L, span, nb, mp, D, sigma, n=None):
                 assert a >= 0 and a + 16 * nch <= NBAND and 16 * nch <= CROSS_S
                 mu = m[:, 32 * u:32 * u + 32]
                 assert mu.min() >= lo and mu.max() <= hi
+            # step bits (put_step_bits / step_bits): bit x set where the window
+            # index changes between x - 1 and x; the gathers and the scatter
+            # derive every index of a 32-column chunk from its first entry
+            if nband_tiles <= 3:   # (pure-Python loops: a few tiles per case)
+                check_step_bits(dwin, sigma, NR, NC)
             # backward: staged diagonal sums, one box per quarter of 32 rows
             # (32 rows of QW sums from the quarter's lowest relative row rounded
             # down to 8, which the kernel reads at two corners of the index

@@ -109,7 +109,6 @@ struct BwdBars {
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
     uint64_t s_full, sread, z_full, zread, mma3_done;
-    uint64_t colv_full[2];
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -184,13 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->band_empty, 1);
         mbar_init(&bars->t_full, 1);
         mbar_init(&bars->t_empty, 8);
-        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->s_full, 1 + 32);   // S / dP's commit and the producer's 32 lanes (column terms)
         mbar_init(&bars->sread, 8);
         mbar_init(&bars->z_full, 8);
         mbar_init(&bars->zread, 8);
         mbar_init(&bars->mma3_done, 1);
-        mbar_init(&bars->colv_full[0], 32);
-        mbar_init(&bars->colv_full[1], 32);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -219,11 +216,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         //   cv1 = c * Dl of the column (dK/dV kernel only).
         // Slot m & 1 is free when tile m's columns are loaded: tile m - 2's
         // column stage was released, so its products -- issued after its
-        // softmax warps finished reading its terms -- have completed.
+        // softmax warps finished reading its terms -- have completed.  The
+        // terms are announced on tile m's S / dP barrier.
         const size_t T = (size_t)p.T;
         const float* relb_h = relb + (size_t)h * 4 * T;
         const uint8_t* cmask = ROWQ ? p.kmask : p.qmask;
-        auto put_columns = [&](int m) {
+        auto put_columns = [&](int m) -> bool {
             const TileKind k = unpack_kind(kinds[m]);
             float* cv = colv + (m & 1) * 2 * BN;
             constexpr int NJ = BN / 32;
@@ -246,7 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cv[j] = valid ? (ROWQ ? cb[q] : cb[q] - ls[q] * kLog2e) : -INFINITY;
                 cv[BN + j] = valid && !ROWQ ? p.scale * rt[q] : 0.f;
             }
-            mbar_arrive(&bars->colv_full[m & 1]);
+            // the terms are announced with S / dP of tile m (the barrier counts
+            // the producer's lanes too), once the barrier has completed tile
+            // m - 1's phase: an arrival never counts toward an older tile
+            if (m >= 1 && !mbar_wait_warp(&bars->s_full, (m - 1) & 1, err, abort_flag)) return false;
+            mbar_arrive(&bars->s_full);
+            return true;
         };
         if (lane == 0 && !ROWQ) {   // the dQ kernel's row operands go to tensor memory instead
             mbar_arrive_expect_tx(&bars->row_full, 2 * S::RB);
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 &bars->c_full[s]);
                 }
             }
-            put_columns(it);
+            if (!put_columns(it)) break;
             const TileKind tk = unpack_kind(kinds[it]);
             if (tk.uniform) continue;
             bool ok = true;
@@ -546,8 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 t_uses += 2;
                 named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
-            // this tile's column terms (written by the producer warp)
-            if (!(ok = mbar_wait_warp(&bars->colv_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
+            // S / dP of this tile and its column terms (the producer arrives on the same barrier)
             if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);

@@ -82,7 +82,6 @@ struct FwdBars {
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
     uint64_t s_full[2], p_full[2], pv_done[2];
-    uint64_t colv_full[4];
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -124,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->k_empty[s], 1);
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_empty[s], 1);
-            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->s_full[s], 1 + 32);   // S's commit and the producer's 32 lanes (column terms)
             mbar_init(&bars->pv_done[s], 1);
             mbar_init(&bars->p_full[s], 4);
         }
@@ -132,7 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->band_empty, 1);
         mbar_init(&bars->t_full, 1);
         mbar_init(&bars->t_empty, 8);
-        for (int s = 0; s < 4; ++s) mbar_init(&bars->colv_full[s], 32);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -154,12 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The warp walks the key tiles: lane 0 issues the tensor copies, and
         // the warp writes each tile's per-key column term to shared memory
         // (P2C scalar of uniform tiles, with the key mask folded in; key mask
-        // of band tiles; -inf past the sequence end), four tiles deep.  Tile
-        // m's term goes to slot m & 3 once V of tile m - 1 is loaded: that
-        // load waited for P.V of tile m - 3, so tile m - 4 is long done.
+        // of band tiles; -inf past the sequence end), four tiles deep, and
+        // announces it on tile m's S barrier.  Tile m's term goes to slot m & 3
+        // once V of tile m - 1 is loaded: that load waited for P.V of tile
+        // m - 3, so tile m - 4 is long done.
         const size_t T = (size_t)p.T;
         const float* relb_h = relb + (size_t)h * 4 * T;
-        auto put_columns = [&](int m) {
+        auto put_columns = [&](int m) -> bool {
             const TileKind k = unpack_kind(kinds[m]);
             float* cv = colv + (m & 3) * BN;
             constexpr int NJ = BN / 32;
@@ -177,7 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = 32 * q + lane;
                 cv[j] = (m * BN + j < n && mk[q] != 0) ? cb[q] : -INFINITY;
             }
-            mbar_arrive(&bars->colv_full[m & 3]);
+            // the terms are announced with S of tile m (its S buffer's barrier
+            // counts the producer's lanes too), once that barrier has completed
+            // the phase of tile m - 2: an arrival never counts toward an older tile
+            if (m >= 2 && !mbar_wait_warp(&bars->s_full[m & 1], ((m - 2) >> 1) & 1, err, abort_flag)) return false;
+            mbar_arrive(&bars->s_full[m & 1]);
+            return true;
         };
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -187,9 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < G::NCH; ++c)
                 tma_load_2d(smem + S::Q + c * BM * G::CW * 2, &tmQ, h * D + c * G::CW, t0 + i0, &bars->q_full);
         }
-        put_columns(0);
+        bool pc_ok = put_columns(0);
         int band_loads = 0;
-        for (int it = 0; it < ntiles; ++it) {
+        for (int it = 0; it < ntiles && pc_ok; ++it) {
             const int s = it & 1, use = it >> 1;
             const int j0 = it * BN;
             // K of tile it as soon as S of tile it - 2 has read its stage
@@ -226,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
                                 &bars->v_full[s]);
             }
-            if (it + 1 < ntiles) put_columns(it + 1);
+            if (it + 1 < ntiles) pc_ok = put_columns(it + 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -396,8 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 t_uses += 2;
                 named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
-            // this tile's column terms (written by the producer warp), then S
-            if (!(ok = mbar_wait_warp(&bars->colv_full[it & 3], (it >> 2) & 1, err, abort_flag))) break;
+            // S of this tile and its column terms (the producer arrives on the same barrier)
             if (!(ok = mbar_wait_warp(&bars->s_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
             tc_fence_after();
             const uint32_t scol = s_col(it);

@@ -506,11 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // they must have left shared memory (their issuers wait here, or
             // between the two window copies when the boxes lie over the cross window)
             if (!S::STAGE_IN_CROSS && !tk.uniform && hf == 0 && lane == 0) bulk_wait_read0();
-            // band tiles rewrite the index window and the band windows, which
-            // every warp reads: all of them must be done with the previous tile.
-            // A uniform tile writes no shared state (its column terms come from
-            // the producer, announced per slot), so its warps go on unsynchronised.
-            if (!tk.uniform) named_bar_sync(1, 256);
+            // every tile starts with all eight warps: band tiles rewrite the index
+            // window and the band windows, and the per-warp arrivals on the
+            // tile's barriers (counts of 8, or 4 per column half) must never
+            // meet a warp that is a whole tile ahead -- its arrival would
+            // complete the previous tile's phase
+            named_bar_sync(1, 256);
             BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
             if (it + 1 < ntiles && !kind_of(it + 1).uniform)
                 bn = band_fetch<BM, BN, SIGMA, true>(p, dtab, tile_base(it + 1), w4, tid, lane);

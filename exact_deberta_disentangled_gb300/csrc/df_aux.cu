@@ -42,114 +42,182 @@ int launch_check_cu(const ProblemDev& p, cudaStream_t st) {
 
 int launch_clear_error(int* err, cudaStream_t st) { return (int)cudaMemsetAsync(err, 0, sizeof(int), st); }
 
+// 16 bytes of T (8 bf16 / fp16 or 4 fp32 values) from a 16-byte aligned
+// address, as floats.
 template <typename T>
-DF_DEV float to_f(T x);
+DF_DEV void load16(const T* src, float* f);
 template <>
-DF_DEV float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-template <>
-DF_DEV float to_f<__half>(__half x) { return __half2float(x); }
-template <>
-DF_DEV float to_f<float>(float x) { return x; }
-
-DF_DEV float warp_sum(float x) {
+DF_DEV void load16<__nv_bfloat16>(const __nv_bfloat16* src, float* f) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    for (int j = 0; j < 4; ++j) {
+        f[2 * j] = __uint_as_float(w[j] << 16);
+        f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+}
+template <>
+DF_DEV void load16<__half>(const __half* src, float* f) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+        f[2 * j] = v.x;
+        f[2 * j + 1] = v.y;
+    }
+}
+template <>
+DF_DEV void load16<float>(const float* src, float* f) {
+    const float4 v = *reinterpret_cast<const float4*>(src);
+    f[0] = v.x;
+    f[1] = v.y;
+    f[2] = v.z;
+    f[3] = v.w;
+}
+
+// Rows of D values are read 16 bytes per lane: LPR lanes per row, RPW rows
+// per warp; a row's partial dot products meet by shuffles within its lanes.
+template <typename T, int D>
+struct RowSplit {
+    static constexpr int VEC = 16 / (int)sizeof(T);
+    static constexpr int LPR = D / VEC;
+    static constexpr int RPW = 32 / LPR;
+    static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row split");
+};
+
+template <int LPR>
+DF_DEV float group_sum(float x) {
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
+}
+
+template <typename T, int VEC>
+DF_DEV float dot16(const float* a, const T* b) {
+    float f[VEC];
+    load16<T>(b, f);
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) s = fmaf(a[j], f[j], s);
+    return s;
 }
 
 // Per (token t, head h): the four dot products, stored [H, 4, T]: Q_t.Kr[0], Q_t.Kr[R-1],
 // K_t.Qr[0], K_t.Qr[R-1], pre-multiplied by c*log2(e) (the kernels work in
 // base-2 exponent units).  A masked key gets -inf in its two K terms, which
-// is how the key mask enters saturated tiles.  One warp per (t, h).
-template <typename T>
+// is how the key mask enters saturated tiles.
+template <typename T, int D>
 __global__ void relbias_kernel(ProblemDev p, const T* __restrict__ q, const T* __restrict__ k,
                                const T* __restrict__ qr, const T* __restrict__ kr, float* __restrict__ relb) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp >= p.T * p.H) return;
-    const int t = warp / p.H, h = warp % p.H;
-    const int D = p.D, R = p.R;
-    const T* qt = q + ((size_t)t * p.H + h) * D;
-    const T* kt = k + ((size_t)t * p.H + h) * D;
-    const T* kr0 = kr + (size_t)h * R * D;
-    const T* kr1 = kr0 + (size_t)(R - 1) * D;
-    const T* qr0 = qr + (size_t)h * R * D;
-    const T* qr1 = qr0 + (size_t)(R - 1) * D;
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-    for (int d = lane; d < D; d += 32) {
-        const float qd = to_f(qt[d]), kd = to_f(kt[d]);
-        a0 = fmaf(qd, to_f(kr0[d]), a0);
-        a1 = fmaf(qd, to_f(kr1[d]), a1);
-        b0 = fmaf(kd, to_f(qr0[d]), b0);
-        b1 = fmaf(kd, to_f(qr1[d]), b1);
-    }
-    a0 = warp_sum(a0);
-    a1 = warp_sum(a1);
-    b0 = warp_sum(b0);
-    b1 = warp_sum(b1);
-    if (lane == 0) {
+    using RS = RowSplit<T, D>;
+    const long gw = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31, part = lane % RS::LPR;
+    const long row = gw * RS::RPW + lane / RS::LPR;   // t * H + h
+    const bool ok = row < (long)p.T * p.H;
+    const long rs = ok ? row : 0;                     // a row that is safe to load
+    const int t = (int)(rs / p.H), h = (int)(rs % p.H);
+    const int R = p.R, off = part * RS::VEC;
+    float qv[RS::VEC], kv[RS::VEC];
+    load16<T>(q + rs * D + off, qv);
+    load16<T>(k + rs * D + off, kv);
+    const T* kr0 = kr + (size_t)h * R * D + off;
+    const T* qr0 = qr + (size_t)h * R * D + off;
+    float a0 = dot16<T, RS::VEC>(qv, kr0), a1 = dot16<T, RS::VEC>(qv, kr0 + (size_t)(R - 1) * D);
+    float b0 = dot16<T, RS::VEC>(kv, qr0), b1 = dot16<T, RS::VEC>(kv, qr0 + (size_t)(R - 1) * D);
+    a0 = group_sum<RS::LPR>(a0);
+    a1 = group_sum<RS::LPR>(a1);
+    b0 = group_sum<RS::LPR>(b0);
+    b1 = group_sum<RS::LPR>(b1);
+    if (ok && part == 0) {
         const float sc = p.scale * 1.4426950408889634f;
         bool kvalid = true;
         if (p.kmask) kvalid = p.kmask[t] != 0;
-        const size_t T = (size_t)p.T, base = (size_t)h * 4 * T + t;
+        const size_t NT = (size_t)p.T, base = (size_t)h * 4 * NT + t;
         relb[base] = a0 * sc;
-        relb[base + T] = a1 * sc;
-        relb[base + 2 * T] = kvalid ? b0 * sc : -INFINITY;
-        relb[base + 3 * T] = kvalid ? b1 * sc : -INFINITY;
+        relb[base + NT] = a1 * sc;
+        relb[base + 2 * NT] = kvalid ? b0 * sc : -INFINITY;
+        relb[base + 3 * NT] = kvalid ? b1 * sc : -INFINITY;
     }
+}
+
+template <typename T, int D>
+int relbias_one(const ProblemDev& p, const void* q, const void* k, const void* qr, const void* kr, float* relb,
+                cudaStream_t st) {
+    using RS = RowSplit<T, D>;
+    const long warps = ((long)p.T * p.H + RS::RPW - 1) / RS::RPW;
+    const int blocks = (int)((warps * 32 + 255) / 256);
+    relbias_kernel<T, D><<<blocks, 256, 0, st>>>(p, (const T*)q, (const T*)k, (const T*)qr, (const T*)kr, relb);
+    return (int)cudaGetLastError();
+}
+
+template <typename T>
+int relbias_d(const ProblemDev& p, const void* q, const void* k, const void* qr, const void* kr, float* relb,
+              cudaStream_t st) {
+    switch (p.D) {
+        case 32: return relbias_one<T, 32>(p, q, k, qr, kr, relb, st);
+        case 64: return relbias_one<T, 64>(p, q, k, qr, kr, relb, st);
+        case 128: return relbias_one<T, 128>(p, q, k, qr, kr, relb, st);
+    }
+    return (int)cudaErrorInvalidValue;
 }
 
 int launch_relbias(const ProblemDev& p, df_dtype dt, const void* q, const void* k, const void* qr, const void* kr,
                    float* relb, cudaStream_t st) {
-    const long warps = (long)p.T * p.H;
-    const int blocks = (int)((warps * 32 + 255) / 256);
-    if (dt == DF_BF16)
-        relbias_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
-                                                              (const __nv_bfloat16*)qr, (const __nv_bfloat16*)kr,
-                                                              relb);
-    else if (dt == DF_FP16)
-        relbias_kernel<__half><<<blocks, 256, 0, st>>>(p, (const __half*)q, (const __half*)k, (const __half*)qr,
-                                                       (const __half*)kr, relb);
-    else
-        relbias_kernel<float><<<blocks, 256, 0, st>>>(p, (const float*)q, (const float*)k, (const float*)qr,
-                                                      (const float*)kr, relb);
-    return (int)cudaGetLastError();
+    if (dt == DF_BF16) return relbias_d<__nv_bfloat16>(p, q, k, qr, kr, relb, st);
+    if (dt == DF_FP16) return relbias_d<__half>(p, q, k, qr, kr, relb, st);
+    return relbias_d<float>(p, q, k, qr, kr, relb, st);
 }
 
 // Dl_i = sum_d dO[i, d] * O[i, d] in fp32, stored at the LSE index of row i.
-template <typename T>
+// Rows run over the padded index space (b, i, h); packed sequences shorter
+// than L leave the tail of their range unused.
+template <typename T, int D>
 __global__ void rowterm_kernel(ProblemDev p, const T* __restrict__ o, const T* __restrict__ dout,
                                float* __restrict__ rowterm) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp >= p.B * p.L * p.H) return;
-    // (b, i, h) over the padded index space; packed sequences shorter than L
-    // leave the tail of their range unused.
-    const int h = warp % p.H;
-    const int bi = warp / p.H;
-    const int b = bi / p.L, i = bi % p.L;
+    using RS = RowSplit<T, D>;
+    const long gw = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31, part = lane % RS::LPR;
+    const long row = gw * RS::RPW + lane / RS::LPR;
+    bool ok = row < (long)p.B * p.L * p.H;
+    const long rs = ok ? row : 0;
+    const int h = (int)(rs % p.H);
+    const long bi = rs / p.H;
+    const int b = (int)(bi / p.L), i = (int)(bi % p.L);
     int t0, n;
     seq_range(p, b, t0, n);
-    if (n < 0 || n > p.L || t0 < 0 || t0 + n > p.T || i >= n) return;
-    const size_t base = ((size_t)(t0 + i) * p.H + h) * p.D;
-    float acc = 0.f;
-    for (int d = lane; d < p.D; d += 32) acc = fmaf(to_f(dout[base + d]), to_f(o[base + d]), acc);
-    acc = warp_sum(acc);
-    if (lane == 0) rowterm[lse_index(p, b, h, t0, i)] = acc;
+    ok = ok && !(n < 0 || n > p.L || t0 < 0 || t0 + n > p.T || i >= n);
+    const size_t base = ok ? ((size_t)(t0 + i) * p.H + h) * D + part * RS::VEC : (size_t)part * RS::VEC;
+    float ov[RS::VEC];
+    load16<T>(o + base, ov);
+    float acc = group_sum<RS::LPR>(dot16<T, RS::VEC>(ov, dout + base));
+    if (ok && part == 0) rowterm[lse_index(p, b, h, t0, i)] = acc;
+}
+
+template <typename T, int D>
+int rowterm_one(const ProblemDev& p, const void* out, const void* dout, float* rowterm, cudaStream_t st) {
+    using RS = RowSplit<T, D>;
+    const long warps = ((long)p.B * p.L * p.H + RS::RPW - 1) / RS::RPW;
+    const int blocks = (int)((warps * 32 + 255) / 256);
+    rowterm_kernel<T, D><<<blocks, 256, 0, st>>>(p, (const T*)out, (const T*)dout, rowterm);
+    return (int)cudaGetLastError();
+}
+
+template <typename T>
+int rowterm_d(const ProblemDev& p, const void* out, const void* dout, float* rowterm, cudaStream_t st) {
+    switch (p.D) {
+        case 32: return rowterm_one<T, 32>(p, out, dout, rowterm, st);
+        case 64: return rowterm_one<T, 64>(p, out, dout, rowterm, st);
+        case 128: return rowterm_one<T, 128>(p, out, dout, rowterm, st);
+    }
+    return (int)cudaErrorInvalidValue;
 }
 
 int launch_rowterm(const ProblemDev& p, df_dtype dt, const void* out, const void* dout, float* rowterm,
                    cudaStream_t st) {
-    const long warps = (long)p.B * p.L * p.H;
-    const int blocks = (int)((warps * 32 + 255) / 256);
-    if (dt == DF_BF16)
-        rowterm_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(p, (const __nv_bfloat16*)out,
-                                                              (const __nv_bfloat16*)dout, rowterm);
-    else if (dt == DF_FP16)
-        rowterm_kernel<__half><<<blocks, 256, 0, st>>>(p, (const __half*)out, (const __half*)dout, rowterm);
-    else
-        rowterm_kernel<float><<<blocks, 256, 0, st>>>(p, (const float*)out, (const float*)dout, rowterm);
-    return (int)cudaGetLastError();
+    if (dt == DF_BF16) return rowterm_d<__nv_bfloat16>(p, out, dout, rowterm, st);
+    if (dt == DF_FP16) return rowterm_d<__half>(p, out, dout, rowterm, st);
+    return rowterm_d<float>(p, out, dout, rowterm, st);
 }
 
 }  // namespace df

@@ -20,10 +20,10 @@
 //
 // G / G' ([T, H, Rp] in the input dtype) feed the relative-position
 // gradients (df_rel.cu):  dQ += G Kr,  dK += G' Qr,  dKr = sum G^T Q,
-// dQr = sum G'^T K.  A band tile adds its diagonal sums with a TMA
-// reduce-add of a [128 x band] box; every element receives at most two
-// non-zero additions that way (neighbouring tiles share at most one relative
-// row), so the order of the additions cannot change the result.  The two
+// dQr = sum G'^T K.  A band tile adds its diagonal sums with TMA reduce-adds,
+// one [32 rows x QW sums] box per quarter of its rows; every element receives
+// at most two non-zero additions that way (neighbouring tiles share at most
+// one relative row), so the order of the additions cannot change the result.  The two
 // clamped rows (delta 0 and R-1), which collect the far field, are summed in
 // registers and added once at the end.
 #pragma once

@@ -7,16 +7,18 @@
 // forward; section "Status": the [B, H, L, L] matrix is never stored).
 //
 // Warp roles (320 threads):
-//   warp 0      TMA producer: Q once, K/V tiles into a 2-stage ring, and for
-//               band tiles the Kr / Qr band rows.
-//   warp 1      tcgen05 issuer (one thread) and TMEM owner.
+//   warp 0      TMA producer: Q once, K/V tiles into a 2-stage ring, for
+//               band tiles the Kr / Qr band rows; it also writes each key
+//               tile's column term to shared memory.
+//   warp 1      tcgen05 issuer (the whole warp walks the loop, elect.sync
+//               picks the issuing lane) and TMEM owner.
 //   warps 2..9  softmax: a thread owns one query row (= TMEM lane) and one
 //               half of the columns of every key tile.
 // The two column halves of a row run independent online softmaxes, each with
 // its own running max and sum and its own output accumulator in tensor
 // memory (O_h += P_h V_h, K = BN/2 per tile); they are merged once, in the
-// epilogue.  So the warps of a row never wait for each other inside the
-// key loop.
+// epilogue, so no maxima are exchanged inside the key loop (every tile still
+// starts with a barrier of the eight softmax warps).
 // Tensor memory (512 columns): O_0 and O_1 [0, 2D), two S / P buffers, band
 // products aliasing the second S buffer (band tiles wait for it).  Tile n
 // uses S buffer n & 1: the issuer computes S for tile n + 1 while the softmax

@@ -40,6 +40,23 @@ struct Geo {
     static constexpr int CROSS_S = 176;                                // cross window stride (halves)
 };
 
+// Launch order of a sequence's row blocks: the blocks whose key range
+// reaches the band on both sides (the most band tiles, the most work) first,
+// the w blocks at each end of the sequence last, so that a grid's final,
+// partial wave holds the cheapest CTAs.  rank -> row block is a bijection of
+// [0, nrb) for any w; w is the band's reach in row blocks (beyond it the
+// relative index is clamped): max_relative_positions with log bucketing, else
+// att_span.
+DF_DEV int row_block_of(const ProblemDev& p, int rank, int nrb, int bm) {
+    const int reach = p.nb > 0 ? p.mp : p.span;
+    int w = (reach + bm - 1) / bm;
+    const int mid = nrb - 2 * w;
+    if (w <= 0 || mid <= 0) return rank;
+    if (rank < mid) return w + rank;
+    const int e = rank - mid;
+    return e < w ? e : mid + e;
+}
+
 DF_DEV int dclamp(const ProblemDev& p, const int32_t* __restrict__ dtab, int r) {
     r = r > p.L - 1 ? p.L - 1 : r;
     r = r < -(p.L - 1) ? -(p.L - 1) : r;

@@ -164,10 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* kinds = reinterpret_cast<uint32_t*>(smem + S::KINDS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y, b = blockIdx.z;
+    // grid (H, B, row blocks): every (sequence, head) pair's most expensive
+    // row blocks are launched before any pair's cheapest ones
+    const int h = blockIdx.x, b = blockIdx.y;
     int t0, n;
     seq_ok(p, b, t0, n);
-    const int r0 = blockIdx.x * BM;   // first row token (query or key) of this CTA
+    const int r0 = row_block_of(p, blockIdx.z, gridDim.z, BM) * BM;   // first row token (query or key) of this CTA
     if (r0 >= n) return;
     const int ntiles = (n + BN - 1) / BN;
     auto tile_base = [&](int m) { return ROWQ ? r0 - m * BN : m * BN - r0; };
@@ -848,7 +850,7 @@ int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const v
     auto kern = bwd_tc_kernel<D, BF16, SIGMA, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid((p.L + G::BM - 1) / G::BM, p.H, p.B);
+    dim3 grid(p.H, p.B, (p.L + G::BM - 1) / G::BM);
     const int phase = SIGMA > 0 ? kProfDq : kProfDkv;
     prof_record(phase, 0, st);
     kern<<<grid, kThreads, S::ALLOC, st>>>(m1, m2, m3, m4, m5, m6, mg, p, ws.dtab, ws.relb, lse, ws.rowterm, acc1,

@@ -110,12 +110,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* kinds = reinterpret_cast<uint32_t*>(smem + S::KINDS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // grid (H, B, row blocks): every (sequence, head) pair's most expensive
-    // row blocks are launched before any pair's cheapest ones
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int h = blockIdx.y, b = blockIdx.z;
     int t0, n;
     seq_ok(p, b, t0, n);
-    const int i0 = row_block_of(p, blockIdx.z, gridDim.z, BM) * BM;
+    const int i0 = blockIdx.x * BM;
     if (i0 >= n) return;
     const int ntiles = (n + BN - 1) / BN;
     auto s_col = [](int it) -> uint32_t { return (it & 1) ? TM::S1 : TM::S0; };
@@ -648,7 +646,7 @@ int launch_fwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, con
     auto kern = fwd_tc_kernel<D, BF16, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid(p.H, p.B, (p.L + G::BM - 1) / G::BM);
+    dim3 grid((p.L + G::BM - 1) / G::BM, p.H, p.B);
     prof_record(kProfFwd, 0, st);
     kern<<<grid, kThreads, S::ALLOC, st>>>(mq, mk, mv, mkr, mqr, p, ws.dtab, ws.relb, out, lse);
     prof_record(kProfFwd, 1, st);

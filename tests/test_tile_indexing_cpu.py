@@ -188,3 +188,29 @@ def test_model_catches_a_flipped_relative_index():
     bad = tab[np.clip(base - (x - (NR - 1)), -(L - 1), L - 1) + L - 1]
     assert not np.array_equal(good, bad)
 
+
+
+def row_block_of(rank, nrb, bm, nb, mp, span):
+    """Model of row_block_of (csrc/df_tile.cuh): the backward kernels' launch
+    order of a sequence's row blocks."""
+    reach = mp if nb > 0 else span
+    w = (reach + bm - 1) // bm
+    mid = nrb - 2 * w
+    if w <= 0 or mid <= 0:
+        return rank
+    if rank < mid:
+        return w + rank
+    e = rank - mid
+    return e if e < w else mid + e
+
+
+@pytest.mark.parametrize("nb,mp,span", [(256, 512, 256), (0, 0, 256), (4, 8, 8), (512, 1024, 512), (12, 100, 17)])
+def test_row_block_launch_order_is_a_permutation(nb, mp, span):
+    """Every row block of every sequence length is launched exactly once, the
+    blocks within the band's reach of either end last."""
+    for nrb in range(1, 65):
+        order = [row_block_of(r, nrb, BM, nb, mp, span) for r in range(nrb)]
+        assert sorted(order) == list(range(nrb))
+        w = ((mp if nb > 0 else span) + BM - 1) // BM
+        if nrb > 2 * w:
+            assert order[:nrb - 2 * w] == list(range(w, nrb - w))

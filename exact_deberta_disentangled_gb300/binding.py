@@ -24,7 +24,8 @@ DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 
 EXPORTS = ["df_attn_workspace_size", "df_attn_fwd", "df_attn_bwd", "df_attn_step_host_arena_size",
            "df_attn_step_host", "df_rel_index_table", "df_get_device_error", "df_status_string", "df_version",
-           "df_attn_set_profile_events", "df_attn_fwd_noalloc"]
+           "df_attn_set_profile_events", "df_attn_fwd_noalloc", "df_attn_debug_inject_stall",
+           "df_dropout_keep_mask", "df_attn_fwd_inference", "df_attn_fwd_noalloc_device_error"]
 
 
 class DfError(RuntimeError):
@@ -69,6 +70,8 @@ def load():
             lib.df_attn_workspace_size.argtypes = [P, ctypes.c_int]
             lib.df_attn_fwd.restype = ctypes.c_int
             lib.df_attn_fwd.argtypes = [P] + [vp] * 7 + [vp, sz, vp]
+            lib.df_attn_fwd_inference.restype = ctypes.c_int
+            lib.df_attn_fwd_inference.argtypes = [P] + [vp] * 6 + [vp, sz, vp]
             lib.df_attn_bwd.restype = ctypes.c_int
             lib.df_attn_bwd.argtypes = [P] + [vp] * 13 + [vp, sz, vp]
             lib.df_attn_step_host_arena_size.restype = sz
@@ -84,6 +87,12 @@ def load():
             lib.df_version.restype = ctypes.c_char_p
             lib.df_attn_fwd_noalloc.restype = ctypes.c_int
             lib.df_attn_fwd_noalloc.argtypes = [P] + [vp] * 7 + [vp]
+            lib.df_attn_fwd_noalloc_device_error.restype = ctypes.c_int
+            lib.df_attn_fwd_noalloc_device_error.argtypes = [vp]
+            lib.df_dropout_keep_mask.restype = ctypes.c_int
+            lib.df_dropout_keep_mask.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp]
+            lib.df_attn_debug_inject_stall.restype = ctypes.c_int
+            lib.df_attn_debug_inject_stall.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32]
             lib.df_attn_set_profile_events.restype = ctypes.c_int
             lib.df_attn_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
             _lib = lib
@@ -179,6 +188,20 @@ def attn_fwd(g: Geometry, q, k, v, qr, kr, out=None, lse=None, workspace=None, s
     return out, lse, workspace
 
 
+def attn_fwd_inference(g: Geometry, q, k, v, qr, kr, out=None, workspace=None, stream=None, check=True):
+    """Inference forward (no LSE) through df_attn_fwd_inference; returns (out, workspace)."""
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(g, q.dtype, False, q.device)
+    p = g.params(q.dtype)
+    rc = load().df_attn_fwd_inference(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(qr), _ptr(kr), _ptr(out),
+                                      _ptr(workspace), workspace.numel(), _stream(stream))
+    if check and rc != DF_OK:
+        raise DfError(rc, "df_attn_fwd_inference")
+    return out, workspace
+
+
 def attn_bwd(g: Geometry, q, k, v, qr, kr, out, lse, dout, grads=None, workspace=None, stream=None, check=True):
     """Backward through df_attn_bwd; returns ((dq, dk, dv, dqr, dkr), workspace)."""
     dt = q.dtype
@@ -255,3 +278,29 @@ def attn_fwd_noalloc(g: Geometry, q, k, v, qr, kr, out, lse, stream=None, check=
     if check and rc != DF_OK:
         raise DfError(rc, "df_attn_fwd_noalloc")
     return rc
+
+
+def debug_inject_stall(kernel: int, tile: int = 0, wait_limit_ns: int = 0, wait_min_probes: int = 0):
+    """Test hook of the bounded-wait path (df_attn_debug_inject_stall): the
+    MMA-issuing warp of `kernel` (0 forward, 1 dQ, 2 dK/dV) stops at `tile`
+    and device waits give up after the given limits; kernel=-1 switches it off."""
+    rc = load().df_attn_debug_inject_stall(int(kernel), int(tile), int(wait_limit_ns), int(wait_min_probes))
+    if rc != DF_OK:
+        raise DfError(rc, "df_attn_debug_inject_stall")
+
+
+def dropout_keep_mask(g: Geometry, dtype: torch.dtype, b: int, h: int, form: int, n: int, device="cuda",
+                      stream=None) -> torch.Tensor:
+    """The [n, n] keep mask of sequence b, head h as the kernels draw it
+    (form 0: row generator, 1: column generator), via df_dropout_keep_mask."""
+    out = torch.full((n, n), 255, dtype=torch.uint8, device=device)
+    p = g.params(dtype)
+    rc = load().df_dropout_keep_mask(ctypes.byref(p), int(b), int(h), int(form), _ptr(out), _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_dropout_keep_mask")
+    return out
+
+
+def noalloc_device_error(stream=None) -> int:
+    """Error word of df_attn_fwd_noalloc's static scratch on the current device."""
+    return int(load().df_attn_fwd_noalloc_device_error(_stream(stream)))

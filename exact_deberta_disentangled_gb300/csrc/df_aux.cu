@@ -42,6 +42,39 @@ int launch_check_cu(const ProblemDev& p, cudaStream_t st) {
 
 int launch_clear_error(int* err, cudaStream_t st) { return (int)cudaMemsetAsync(err, 0, sizeof(int), st); }
 
+// The dropout keep mask of sequence b, head h, as the attention kernels draw
+// it: form 0 through the row generator (the forward and dQ kernels: one lane
+// per query, 32 keys a call), form 1 through the column generator (the dK/dV
+// kernel: one lane per key, 32 queries a call, lanes of a quad sharing their
+// Philox outputs).  One warp per 32 x 32 block; out[i * n + j] = keep(i, j).
+__global__ void keep_mask_kernel(ProblemDev p, int b, int h, int form, uint8_t* __restrict__ out) {
+    int t0, n;
+    if (!seq_ok(p, b, t0, n)) return;
+    const int lane = threadIdx.x & 31;
+    const long wg = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nb32 = (n + 31) / 32;
+    if (wg >= (long)nb32 * nb32) return;   // the whole warp leaves together
+    const int bi = (int)(wg / nb32), bj = (int)(wg % nb32);
+    if (form == 0) {
+        const int i = 32 * bi + lane;
+        const uint32_t k = keep_bits32_row(p, b, h, i, 32 * bj);
+        if (i < n)
+            for (int e = 0; e < 32 && 32 * bj + e < n; ++e) out[(size_t)i * n + 32 * bj + e] = (uint8_t)((k >> e) & 1u);
+    } else {
+        const int j = 32 * bj + lane;
+        const uint32_t k = keep_bits32_col(p, b, h, 32 * bi, j);
+        if (j < n)
+            for (int q = 0; q < 32 && 32 * bi + q < n; ++q) out[(size_t)(32 * bi + q) * n + j] = (uint8_t)((k >> q) & 1u);
+    }
+}
+
+int launch_keep_mask(const ProblemDev& p, int b, int h, int form, uint8_t* out, cudaStream_t st) {
+    const long nb32 = (p.L + 31) / 32;
+    const long warps = nb32 * nb32;
+    keep_mask_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(p, b, h, form, out);
+    return (int)cudaGetLastError();
+}
+
 // 16 bytes of T (8 bf16 / fp16 or 4 fp32 values) from a 16-byte aligned
 // address, as floats.
 template <typename T>

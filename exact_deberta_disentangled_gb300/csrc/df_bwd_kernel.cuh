@@ -109,6 +109,7 @@ struct BwdBars {
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
     uint64_t s_full, sread, z_full, zread, mma3_done;
+    uint64_t drain;   // the issuer's last MMAs, before the tensor memory is freed
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->z_full, 8);
         mbar_init(&bars->zread, 8);
         mbar_init(&bars->mma3_done, 1);
+        mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -204,8 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    volatile int* abort_flag = &bars->abort_flag;
-    int* err = p.err;
+    const WaitCtx wc = wait_ctx(p, &bars->abort_flag);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the terms are announced with S / dP of tile m (the barrier counts
             // the producer's lanes too), once the barrier has completed tile
             // m - 1's phase: an arrival never counts toward an older tile
-            if (m >= 1 && !mbar_wait_warp(&bars->s_full, (m - 1) & 1, err, abort_flag)) return false;
+            if (m >= 1 && !mbar_wait_warp(&bars->s_full, (m - 1) & 1, wc)) return false;
             mbar_arrive(&bars->s_full);
             return true;
         };
@@ -260,11 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem + S::R2 + c * BM * G::CW * 2, &tmR2, h * D + c * G::CW, t0 + r0, &bars->row_full);
             }
         }
-        int band_loads = 0;
+        int band_loads = 0, c_cnt[2] = {0, 0};   // copies issued per barrier
         for (int it = 0; it < ntiles; ++it) {
             const int s = it & 1, use = it >> 1;
             const int c0 = it * BN;
-            if (use > 0 && !mbar_wait_warp(&bars->c_empty[s], (use - 1) & 1, err, abort_flag)) break;
+            if (use > 0 && !mbar_wait_warp(&bars->c_empty[s], (use - 1) & 1, wc)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->c_full[s], 2 * S::CB);
                 for (int c = 0; c < G::NCH; ++c) {
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 &bars->c_full[s]);
                 }
             }
+            ++c_cnt[s];
             if (!put_columns(it)) break;
             const TileKind tk = unpack_kind(kinds[it]);
             if (tk.uniform) continue;
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int pass = 0; pass < 2 && ok; ++pass) {
                 for (int c = 0; c < G::NCH; ++c) {
                     if (band_loads > 0 &&
-                        !mbar_wait_warp(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
+                        !mbar_wait_warp(&bars->band_empty, (band_loads - 1) & 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -294,6 +296,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
+        }
+        // no copy of this CTA is still landing in shared memory when it exits
+        // (each barrier's last phase is its last copy; the ones before it
+        // completed before that copy was issued)
+        if (lane == 0) {
+            if (!ROWQ) mbar_drain(&bars->row_full, 0, wc.limit_ns);
+            for (int s = 0; s < 2; ++s)
+                if (c_cnt[s] > 0) mbar_drain(&bars->c_full[s], (c_cnt[s] - 1) & 1, wc.limit_ns);
+            if (band_loads > 0) mbar_drain(&bars->band_full, (band_loads - 1) & 1, wc.limit_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dC2k0 = desc_k<G>(sC20, BN, 0), dC2k1 = dadd(dC2k0, S::CB);
             const uint64_t dC1m0 = desc_mn<G>(sC10, BN, 0), dC1m1 = dadd(dC1m0, S::CB);
             const uint64_t dC2m0 = desc_mn<G>(sC20, BN, 0), dC2m1 = dadd(dC2m0, S::CB);
-            bool ok = mbar_wait_warp(ROWQ ? &bars->a_full : &bars->row_full, 0, err, abort_flag);
+            bool ok = mbar_wait_warp(ROWQ ? &bars->a_full : &bars->row_full, 0, wc);
             if (ROWQ) tc_fence_after();
             int band_used = 0, t_uses = 0;
             // band product `pass` of band tile m (0: own, rows x band; 1: cross,
@@ -329,12 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // was copied out
             auto issue_band = [&](int m, int pass) -> bool {
                 const int s = m & 1, use = m >> 1;
-                if (pass == 1 && !mbar_wait_warp(&bars->c_full[s], use & 1, err, abort_flag)) return false;
-                if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)) return false;
+                if (pass == 1 && !mbar_wait_warp(&bars->c_full[s], use & 1, wc)) return false;
+                if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, wc)) return false;
                 const uint64_t dA = pass == 0 ? dR1 : s ? dC1k1 : dC1k0;
                 const int arows = pass == 0 ? BM : BN;
                 for (int c = 0; c < G::NCH; ++c) {
-                    if (!mbar_wait_warp(&bars->band_full, band_used & 1, err, abort_flag)) return false;
+                    if (!mbar_wait_warp(&bars->band_full, band_used & 1, wc)) return false;
                     tc_fence_after();
                     for (int k = 0; k < G::CW / 16; ++k) {
                         const int ks = c * (G::CW / 16) + k;
@@ -357,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = m & 1, use = m >> 1;
                 if (!tk.uniform) {
                     // S / dP reuse the band columns: wait until the cross window was copied out
-                    if (!mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag)) return false;
-                } else if (!mbar_wait_warp(&bars->c_full[s], use & 1, err, abort_flag)) {
+                    if (!mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, wc)) return false;
+                } else if (!mbar_wait_warp(&bars->c_full[s], use & 1, wc)) {
                     return false;
                 }
                 tc_fence_after();
@@ -382,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto issue_acc = [&](int m) -> bool {
                 const int s = m & 1;
-                if (!mbar_wait_warp(&bars->z_full, m & 1, err, abort_flag)) return false;
+                if (!mbar_wait_warp(&bars->z_full, m & 1, wc)) return false;
                 tc_fence_after();
                 const uint64_t d1 = s ? dC1m1 : dC1m0, d2 = s ? dC2m1 : dC2m0;
 #pragma unroll
@@ -398,8 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit_w(&bars->mma3_done);
                 return true;
             };
-            if (ok) ok = issue_sdp(0, unpack_kind(kinds[0]));
+            // test-only stall injection: the issuer stops before this tile, so
+            // that the other roles' bounded waits run out
+            const int stall = p.fault_kernel == (ROWQ ? 1 : 2) ? p.fault_tile : -1;
+            if (ok && stall != 0) ok = issue_sdp(0, unpack_kind(kinds[0]));
             for (int it = 0; it < ntiles && ok; ++it) {
+                if (stall >= 0 && it + 1 >= stall) break;
                 const bool nxt = it + 1 < ntiles;
                 const TileKind kn = unpack_kind(kinds[nxt ? it + 1 : it]);
                 const bool early = nxt && (!TM::T_OVER_Z || kn.uniform);
@@ -408,26 +423,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // tile's products (so that they run while the softmax warps
                     // finish this tile), then its cross product and S / dP, which
                     // wait for the softmax warps to copy the windows out
-                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, wc))) break;
                     if (!(ok = issue_band(it + 1, 0))) break;
                     if (!(ok = issue_acc(it))) break;
                     if (!(ok = issue_band(it + 1, 1) && issue_s(it + 1, kn))) break;
                     continue;
                 }
                 if (early) {
-                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, wc))) break;
                     if (!(ok = issue_sdp(it + 1, kn))) break;
                 }
                 if (!(ok = issue_acc(it))) break;
                 if (nxt && !early) {
                     // the band products overwrite this tile's dZ / P~: wait until the
                     // products and the diagonal sums have read them
-                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, err, abort_flag))) break;
-                    if (!(ok = mbar_wait_warp(&bars->mma3_done, it & 1, err, abort_flag))) break;
-                    if (!(ok = mbar_wait_warp(&bars->zread, it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, wc))) break;
+                    if (!(ok = mbar_wait_warp(&bars->mma3_done, it & 1, wc))) break;
+                    if (!(ok = mbar_wait_warp(&bars->zread, it & 1, wc))) break;
                     if (!(ok = issue_sdp(it + 1, kn))) break;
                 }
             }
+            // every MMA issued above has completed before the tensor memory is freed
+            tc_commit_w(&bars->drain);
+            mbar_drain(&bars->drain, 0, wc.limit_ns);
         }
     } else {
         // ------------------------------------------------------------ softmax / gradient warps
@@ -498,7 +516,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint16_t* own_row = own + row * G::OWN_S;
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
         BandRaw bn = band_fetch<BM, BN, SIGMA, true>(p, dtab, tile_base(0), w4, tid, lane);   // band indices, one tile ahead
-        for (int it = 0; it < ntiles && ok; ++it) {
+        // Every warp walks every tile and meets every named barrier, also after
+        // a bounded wait gave up (ok == false: the work is skipped, no wait is
+        // taken): a warp that left the loop early would leave its siblings
+        // parked in bar.sync for good.
+        for (int it = 0; it < ntiles; ++it) {
             const int c0 = it * BN;
             const int base = tile_base(it);
             const TileKind tk = kind_of(it);
@@ -527,19 +549,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int lo = __shfl_sync(0xffffffffu, bc.rng, 0) - tk.dlo, hi = __shfl_sync(0xffffffffu, bc.rng, 1) - tk.dlo;
                 const int clo = __shfl_sync(0xffffffffu, bc.rng, 2) - tk.dlo, chi = __shfl_sync(0xffffffffu, bc.rng, 3) - tk.dlo;
                 own_a = lo & ~15;
-                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
-                tc_fence_after();
-                copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
+                ok = ok && mbar_wait_warp(&bars->t_full, t_uses & 1, wc);
+                if (ok) {
+                    tc_fence_after();
+                    copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->t_empty);
+                }
                 if (S::STAGE_IN_CROSS) {
                     if (hf == 0 && lane == 0) bulk_wait_read0();
                     named_bar_sync(1, 256);
                 }
-                if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
+                ok = ok && mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, wc);
                 tc_fence_after();
-                if (32 * w4 < BN) {
+                if (ok && 32 * w4 < BN) {
                     lo = clo;
                     hi = chi;
                     const int ca =
@@ -548,12 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
+                if (ok && lane == 0) mbar_arrive(&bars->t_empty);
                 t_uses += 2;
                 named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
             // S / dP of this tile and its column terms (the producer arrives on the same barrier)
-            if (!(ok = mbar_wait_warp(&bars->s_full, it & 1, err, abort_flag))) break;
+            ok = ok && mbar_wait_warp(&bars->s_full, it & 1, wc);
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
             const bool band = !tk.uniform;
@@ -562,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float rs[4] = {0.f, 0.f, 0.f, 0.f};
             // this thread's 32-column chunks: S, dP -> P, dZ (and Pd for the dK/dV kernel)
 #pragma unroll 1
-            for (int cc = 0; cc < NCT; ++cc) {
+            for (int cc = 0; cc < NCT && ok; ++cc) {
                 const int c = cbeg + cc;
                 uint32_t sr[32], pr[32];
                 tc_ld32(lane_base + TM::S + 32 * c, sr);
@@ -648,23 +672,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (cc == 0 && it > 0) {
                     // the previous tile's products must have read their 16-bit operands
-                    if (!(ok = mbar_wait_warp(&bars->mma3_done, (it - 1) & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->mma3_done, (it - 1) & 1, wc))) break;
                     tc_fence_after();
                 }
                 tc_st16(lane_base + TM::Z + 16 * c, zp);
                 if (!ROWQ) tc_st16(lane_base + TM::Z + BN / 2 + 16 * c, pp);
             }
-            if (!ok) break;
             const float rowsum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->z_full);
+            if (ok) {
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->z_full);
+            }
             // ---- diagonal sums of dZ for this tile
             if (!band) {
-                if (tk.which) g_hi += rowsum; else g_lo += rowsum;
-                if (lane == 0) mbar_arrive(&bars->zread);
+                if (ok) {
+                    if (tk.which) g_hi += rowsum; else g_lo += rowsum;
+                    if (lane == 0) mbar_arrive(&bars->zread);
+                }
             } else {
+                // (after a give-up only the named barriers below are met)
                 named_bar_sync(1, 256);   // own / cross no longer read; every dZ is in tensor memory
                 tc_fence_after();
                 // this quarter's relative rows: the index into dwin grows (or
@@ -679,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint16_t* grow = qstage + lane * S::QW + qoff;
                 const int mmax = S::QW - 1 - qoff;   // a clamp: grow[m] stays inside the row
                 const bool bad = qmax + qoff > S::QW - 1;   // cannot happen for a valid tile
-                {
+                if (ok) {
                     // the quarter's two warps clear its box, lanes on consecutive
                     // 16-byte chunks (the box is one dense block)
                     constexpr int NCK = S::QSB / 16;
@@ -706,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int m_cur = dwin[x0];
                 // this half's dZ columns (16-bit, as the products use them), 32 at a time
 #pragma unroll 1
-                for (int g = 0; g < HC / 32; ++g) {
+                for (int g = 0; g < HC / 32 && ok; ++g) {
                     uint32_t zr[16];
                     tc_ld16p(lane_base + TM::Z + hf * (HC / 2) + 16 * g, zr);
                     // bit 31 - e2 (query rows) or e2: step between columns 32 g + e2 and + 1
@@ -724,14 +752,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float tail = pre - last;   // the run that ends this half
-                if (hf) {
+                if (ok && hf) {
                     gput(m_cur, tail);
                     fence_proxy_async_smem();   // the box is read by the tensor-memory-access unit
                 }
                 tc_fence_before();
                 named_bar_sync(pair_bar, 64);
-                if (lane == 0) mbar_arrive(&bars->zread);   // dZ no longer read by this warp
-                if (!hf) {
+                if (ok && lane == 0) mbar_arrive(&bars->zread);   // dZ no longer read by this warp
+                if (ok && !hf) {
                     const int ms = m_cur < mmax ? m_cur : mmax;
                     grow[ms] = f2h16<BF16>(h16f<BF16>(grow[ms]) + tail);
                     // the clamped relative rows (far field) are summed in registers
@@ -753,12 +781,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_commit();
                     }
                 }
-                if (bad) raise_error(err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
+                if (ok && bad) raise_error(p.err, DF_ERR_DEVICE_ARG);   // cannot happen for a valid tile
             }
         }
         if (hf == 0 && lane == 0) bulk_wait0();   // this quarter's boxes
         // ------------------------------------------------------------ epilogue
-        if (ok) ok = mbar_wait_warp(&bars->mma3_done, (ntiles - 1) & 1, err, abort_flag);
+        ok = ok && mbar_wait_warp(&bars->mma3_done, (ntiles - 1) & 1, wc);
         tc_fence_after();
         if (ok) {
             // accumulator columns [hf D/2, (hf+1) D/2), 16 at a time
@@ -797,11 +825,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // the far-field diagonal sums: the two halves' shares, added once;
-            // concurrent box additions to these two entries only ever add zero
-            xch[hf * BM + row] = g_lo;
-            xch[2 * BM + hf * BM + row] = g_hi;
-            named_bar_sync(pair_bar, 64);
+        }
+        // the far-field diagonal sums: the two halves' shares, added once;
+        // concurrent box additions to these two entries only ever add zero
+        xch[hf * BM + row] = g_lo;
+        xch[2 * BM + hf * BM + row] = g_hi;
+        named_bar_sync(pair_bar, 64);   // both warps of the pair, whatever their state
+        if (ok) {
             if (row_in && hf == 0) {
                 const float glo = xch[row] + xch[BM + row];
                 const float ghi = xch[2 * BM + row] + xch[3 * BM + row];

@@ -107,6 +107,7 @@ DF_DEV uint64_t globaltimer_ns() {
 
 DF_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+
 DF_DEV void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
@@ -139,15 +140,29 @@ DF_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up once BOTH kWaitLimitNs
-// have passed on the global timer AND kWaitMinProbes probes have failed (a
-// jump of the global timer alone, as a profiler's clock resynchronisation can
-// cause, does not end a wait that is about to succeed; a real hang still ends,
-// after at most max(2 s, 2^20 probes of <= 20 us)).  On give-up the device
-// error word records DF_ERR_TIMEOUT and the CTA-wide abort flag is set, so
-// that every other role of the CTA stops waiting too.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr uint32_t kWaitMinProbes = 1u << 20;
+// The bounded-wait context of one CTA: the device error word, the CTA-wide
+// abort flag (shared memory) and the limits.  A wait gives up once BOTH
+// limit_ns have passed on the global timer AND min_probes probes have failed
+// (a jump of the global timer alone, as a profiler's clock resynchronisation
+// can cause, does not end a wait that is about to succeed; a real hang still
+// ends, after at most max(limit, min_probes probes of <= 20 us)).  On give-up
+// the error word records DF_ERR_TIMEOUT and the abort flag is set, so that
+// every other role of the CTA stops waiting too.
+struct WaitCtx {
+    int* err;
+    volatile int* abort;
+    unsigned long long limit_ns;
+    uint32_t min_probes;
+};
+
+DF_DEV WaitCtx wait_ctx(const ProblemDev& p, int* abort_flag_smem) {
+    WaitCtx w;
+    w.err = p.err;
+    w.abort = abort_flag_smem;
+    w.limit_ns = p.wait_ns;
+    w.min_probes = p.wait_probes;
+    return w;
+}
 
 // Non-blocking probe of an mbarrier phase (no suspension).
 DF_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
@@ -162,7 +177,7 @@ DF_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err_word, volatile int* abort_flag) {
+DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
     // a phase that has already completed costs one plain probe
     if (mbar_test_wait(bar, parity)) return true;
     if (mbar_try_wait(bar, parity)) return true;
@@ -170,10 +185,10 @@ DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err_word, volatile in
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 7u) == 0) {
-            if (*abort_flag) return false;
-            if (it >= kWaitMinProbes && globaltimer_ns() - t0 > kWaitLimitNs) {
-                raise_error(err_word, DF_ERR_TIMEOUT);
-                *abort_flag = 1;
+            if (*w.abort) return false;
+            if (it >= w.min_probes && globaltimer_ns() - t0 > w.limit_ns) {
+                raise_error(w.err, DF_ERR_TIMEOUT);
+                *w.abort = 1;
                 return false;
             }
         }
@@ -182,8 +197,21 @@ DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err_word, volatile in
 
 // mbar_wait taken by a whole warp with one outcome for every lane, so that
 // warp-collective tcgen05 instructions after it never run divergent.
-DF_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err_word, volatile int* abort_flag) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, err_word, abort_flag));
+DF_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+}
+
+// Wait at exit for this thread's own asynchronous work (a tensor copy in
+// flight, the last MMAs) to land, bounded by time only: it ignores the abort
+// flag, so that a CTA that gave up still never leaves a copy writing into
+// shared memory, or an MMA into tensor memory, after it has released them.
+DF_DEV bool mbar_drain(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
 }
 
 // Pin a register value at this point of the program: the empty volatile asm
@@ -393,12 +421,25 @@ DF_DEV uint32_t keep_bits32_row(const ProblemDev& p, int b, int h, int i, int j0
     return k;
 }
 
-// Keep bits of the 32 queries i0 .. i0+31 for key j, as bits 0..31 (one
-// Philox call per query).
+// Keep bits of the 32 queries i0 .. i0+31 for key j, as bits 0..31.  A
+// warp-collective call: every lane of the warp calls it, and the four lanes
+// of each quad hold the four keys of one Philox output (j & 3 == lane & 3,
+// the same j >> 2).  One Philox call yields one query's bits for all four
+// keys, so each lane of a quad draws 8 of the 32 queries (i0 + a + 4m for
+// lane a = lane & 3, m = 0..7) and the quad exchanges them:
+//   V_a bit (4m + k) = keep(i0 + a + 4m, key k of the quad)
+//   lane a' returns sum_a ((V_a >> a') & 0x11111111) << a.
 DF_DEV uint32_t keep_bits32_col(const ProblemDev& p, int b, int h, int i0, int j) {
-    uint32_t k = 0;
+    const int lane = threadIdx.x & 31, a = lane & 3;
+    uint32_t v = 0;
 #pragma unroll 1
-    for (int q = 0; q < 32; ++q) k |= ((keep_bits4(p, b, h, i0 + q, j >> 2) >> (j & 3)) & 1u) << q;
+    for (int m = 0; m < 8; ++m) v |= keep_bits4(p, b, h, i0 + a + 4 * m, j >> 2) << (4 * m);
+    uint32_t k = 0;
+#pragma unroll
+    for (int src = 0; src < 4; ++src) {
+        const uint32_t vs = __shfl_sync(0xffffffffu, v, (lane & ~3) | src);
+        k |= ((vs >> a) & 0x11111111u) << src;
+    }
     return k;
 }
 

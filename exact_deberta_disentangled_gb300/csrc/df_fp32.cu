@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256) fwd_f32_kernel(ProblemDev p, const int32_
 #pragma unroll
     for (int c = 0; c < kMaxD / 32; ++c)
         if (lane + 32 * c < D) oi[lane + 32 * c] = any ? acc[c] * inv : 0.f;
-    if (lane == 0) lse[lse_index(p, b, h, t0, i)] = any ? m + logf(l) : INFINITY;
+    if (lane == 0 && lse) lse[lse_index(p, b, h, t0, i)] = any ? m + logf(l) : INFINITY;   // lse == NULL: inference
 }
 
 __global__ void __launch_bounds__(256) dq_f32_kernel(ProblemDev p, const int32_t* __restrict__ dtab,

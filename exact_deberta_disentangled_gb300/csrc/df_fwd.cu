@@ -84,6 +84,7 @@ struct FwdBars {
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
     uint64_t s_full[2], p_full[2], pv_done[2];
+    uint64_t drain;   // the issuer's last MMAs, before the tensor memory is freed
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->band_empty, 1);
         mbar_init(&bars->t_full, 1);
         mbar_init(&bars->t_empty, 8);
+        mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -146,8 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    volatile int* abort_flag = &bars->abort_flag;
-    int* err = p.err;
+    const WaitCtx wc = wait_ctx(p, &bars->abort_flag);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the terms are announced with S of tile m (its S buffer's barrier
             // counts the producer's lanes too), once that barrier has completed
             // the phase of tile m - 2: an arrival never counts toward an older tile
-            if (m >= 2 && !mbar_wait_warp(&bars->s_full[m & 1], ((m - 2) >> 1) & 1, err, abort_flag)) return false;
+            if (m >= 2 && !mbar_wait_warp(&bars->s_full[m & 1], ((m - 2) >> 1) & 1, wc)) return false;
             mbar_arrive(&bars->s_full[m & 1]);
             return true;
         };
@@ -194,24 +195,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem + S::Q + c * BM * G::CW * 2, &tmQ, h * D + c * G::CW, t0 + i0, &bars->q_full);
         }
         bool pc_ok = put_columns(0);
-        int band_loads = 0;
+        int band_loads = 0, k_cnt[2] = {0, 0}, v_cnt[2] = {0, 0};   // copies issued per barrier
         for (int it = 0; it < ntiles && pc_ok; ++it) {
             const int s = it & 1, use = it >> 1;
             const int j0 = it * BN;
             // K of tile it as soon as S of tile it - 2 has read its stage
-            if (use > 0 && !mbar_wait_warp(&bars->k_empty[s], (use - 1) & 1, err, abort_flag)) break;
+            if (use > 0 && !mbar_wait_warp(&bars->k_empty[s], (use - 1) & 1, wc)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->k_full[s], S::KVB);
                 for (int c = 0; c < G::NCH; ++c)
                     tma_load_2d(smem + S::K0 + s * S::KVB + c * BN * G::CW * 2, &tmK, h * D + c * G::CW, t0 + j0,
                                 &bars->k_full[s]);
             }
+            ++k_cnt[s];
             const TileKind tk = unpack_kind(kinds[it]);
             bool ok = true;
             for (int pass = 0; pass < 2 && ok && !tk.uniform; ++pass) {
                 for (int c = 0; c < G::NCH; ++c) {
                     if (band_loads > 0 &&
-                        !mbar_wait_warp(&bars->band_empty, (band_loads - 1) & 1, err, abort_flag)) {
+                        !mbar_wait_warp(&bars->band_empty, (band_loads - 1) & 1, wc)) {
                         ok = false;
                         break;
                     }
@@ -225,14 +227,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // V of tile it once P.V of tile it - 2 has read its stage
-            if (use > 0 && !mbar_wait_warp(&bars->v_empty[s], (use - 1) & 1, err, abort_flag)) break;
+            if (use > 0 && !mbar_wait_warp(&bars->v_empty[s], (use - 1) & 1, wc)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->v_full[s], S::KVB);
                 for (int c = 0; c < G::NCH; ++c)
                     tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
                                 &bars->v_full[s]);
             }
+            ++v_cnt[s];
             if (it + 1 < ntiles) pc_ok = put_columns(it + 1);
+        }
+        // no copy of this CTA is still landing in shared memory when it exits
+        // (each barrier's last phase is its last copy; the ones before it
+        // completed before that copy was issued)
+        if (lane == 0) {
+            mbar_drain(&bars->q_full, 0, wc.limit_ns);
+            for (int s = 0; s < 2; ++s) {
+                if (k_cnt[s] > 0) mbar_drain(&bars->k_full[s], (k_cnt[s] - 1) & 1, wc.limit_ns);
+                if (v_cnt[s] > 0) mbar_drain(&bars->v_full[s], (v_cnt[s] - 1) & 1, wc.limit_ns);
+            }
+            if (band_loads > 0) mbar_drain(&bars->band_full, (band_loads - 1) & 1, wc.limit_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -248,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dQ = desc_k<G>(sQ, BM, 0), dBand = desc_k<G>(sBand, G::NBAND, 0);
             const uint64_t dK0 = desc_k<G>(smem_u32(smem + S::K0), BN, 0), dK1 = dadd(dK0, S::KVB);
             const uint64_t dV0 = desc_mn<G>(smem_u32(smem + S::V0), BN, 0), dV1 = dadd(dV0, S::KVB);
-            bool ok = mbar_wait_warp(&bars->q_full, 0, err, abort_flag);
+            bool ok = mbar_wait_warp(&bars->q_full, 0, wc);
             int band_used = 0, t_uses = 0;
             int pv_cnt0 = 0, pv_cnt1 = 0;   // P.V rounds issued per S buffer
             // S (and, for band tiles, the two band products) of tile m into buffer m & 1
@@ -257,16 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dK = s ? dK1 : dK0;
                 if (!tk.uniform) {
                     // the band columns overlap S buffer 1: its last P must have been consumed
-                    if (pv_cnt1 > 0 && !mbar_wait_warp(&bars->pv_done[1], (pv_cnt1 - 1) & 1, err, abort_flag))
+                    if (pv_cnt1 > 0 && !mbar_wait_warp(&bars->pv_done[1], (pv_cnt1 - 1) & 1, wc))
                         return false;
                     for (int pass = 0; pass < 2; ++pass) {
-                        if (pass == 1 && !mbar_wait_warp(&bars->k_full[s], use & 1, err, abort_flag)) return false;
-                        if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                        if (pass == 1 && !mbar_wait_warp(&bars->k_full[s], use & 1, wc)) return false;
+                        if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, wc))
                             return false;
                         const uint64_t dA = pass == 0 ? dQ : dK;
                         const int arows = pass == 0 ? BM : BN;
                         for (int c = 0; c < G::NCH; ++c) {
-                            if (!mbar_wait_warp(&bars->band_full, band_used & 1, err, abort_flag)) return false;
+                            if (!mbar_wait_warp(&bars->band_full, band_used & 1, wc)) return false;
                             tc_fence_after();
                             for (int k = 0; k < G::CW / 16; ++k)
                                 tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, c * (G::CW / 16) + k)),
@@ -277,13 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_commit_w(&bars->t_full);
                         ++t_uses;
                     }
-                } else if (!mbar_wait_warp(&bars->k_full[s], use & 1, err, abort_flag)) {
+                } else if (!mbar_wait_warp(&bars->k_full[s], use & 1, wc)) {
                     return false;
                 }
                 // buffer bf free: its previous P consumed; buffer 1 also holds band columns
                 const int pvc = bf ? pv_cnt1 : pv_cnt0;
-                if (pvc > 0 && !mbar_wait_warp(&bars->pv_done[bf], (pvc - 1) & 1, err, abort_flag)) return false;
-                if (bf == 1 && t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, err, abort_flag))
+                if (pvc > 0 && !mbar_wait_warp(&bars->pv_done[bf], (pvc - 1) & 1, wc)) return false;
+                if (bf == 1 && t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, wc))
                     return false;
                 tc_fence_after();
 #pragma unroll
@@ -293,8 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit_w(&bars->k_empty[s]);
                 return true;
             };
-            if (ok) ok = issue_s(0, unpack_kind(kinds[0]));
+            // test-only stall injection: the issuer stops before this tile, so
+            // that the other roles' bounded waits run out
+            const int stall = p.fault_kernel == 0 ? p.fault_tile : -1;
+            if (ok && stall != 0) ok = issue_s(0, unpack_kind(kinds[0]));
             for (int it = 0; it < ntiles && ok; ++it) {
+                if (stall >= 0 && it + 1 >= stall) break;
                 const int s = it & 1;
                 const uint64_t dV = s ? dV1 : dV0;
                 const TileKind kn = unpack_kind(kinds[it + 1 < ntiles ? it + 1 : it]);
@@ -303,9 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool next_band = next && !kn.uniform;
                 if (next && !next_band && !(ok = issue_s(it + 1, kn))) break;
                 // O_h += P_h V_h for the two column halves, each as soon as its P is ready
-                if (!(ok = mbar_wait_warp(&bars->v_full[s], (it >> 1) & 1, err, abort_flag))) break;
+                if (!(ok = mbar_wait_warp(&bars->v_full[s], (it >> 1) & 1, wc))) break;
                 for (int hf = 0; hf < 2 && ok; ++hf) {
-                    if (!(ok = mbar_wait_warp(&bars->p_full[hf], it & 1, err, abort_flag))) break;
+                    if (!(ok = mbar_wait_warp(&bars->p_full[hf], it & 1, wc))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BN / 32; ++k)
@@ -318,6 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it & 1) ++pv_cnt1; else ++pv_cnt0;
                 if (next_band && !(ok = issue_s(it + 1, kn))) break;
             }
+            // every MMA issued above has completed before the tensor memory is freed
+            tc_commit_w(&bars->drain);
+            mbar_drain(&bars->drain, 0, wc.limit_ns);
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -362,7 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
         BandRaw bn = band_fetch<BM, BN, 1>(p, dtab, i0, w4, tid, lane);      // band indices, one tile ahead
-        for (int it = 0; it < ntiles && ok; ++it) {
+        // Every warp walks every tile and meets every named barrier, also after
+        // a bounded wait gave up (ok == false: the work is skipped, no wait is
+        // taken): a warp that left the loop early would leave its siblings
+        // parked in bar.sync for good.
+        for (int it = 0; it < ntiles; ++it) {
             const int j0 = it * BN;
             const TileKind tk = kind_of(it);
             const float* colb = colv + (it & 3) * BN;
@@ -383,15 +408,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int clo = __shfl_sync(0xffffffffu, bc.rng, 2) - tk.dlo, chi = __shfl_sync(0xffffffffu, bc.rng, 3) - tk.dlo;
                 own_a = lo & ~15;
                 // both warps of a lane quarter copy half of each band window
-                if (!(ok = mbar_wait_warp(&bars->t_full, t_uses & 1, err, abort_flag))) break;
+                ok = ok && mbar_wait_warp(&bars->t_full, t_uses & 1, wc);
+                if (ok) {
+                    tc_fence_after();
+                    copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->t_empty);
+                }
+                ok = ok && mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, wc);
                 tc_fence_after();
-                copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
-                if (!(ok = mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, err, abort_flag))) break;
-                tc_fence_after();
-                if (32 * w4 < BN) {
+                if (ok && 32 * w4 < BN) {
                     lo = clo;
                     hi = chi;
                     const int ca =
@@ -400,12 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->t_empty);
+                if (ok && lane == 0) mbar_arrive(&bars->t_empty);
                 t_uses += 2;
                 named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
             // S of this tile and its column terms (the producer arrives on the same barrier)
-            if (!(ok = mbar_wait_warp(&bars->s_full[it & 1], (it >> 1) & 1, err, abort_flag))) break;
+            ok = ok && mbar_wait_warp(&bars->s_full[it & 1], (it >> 1) & 1, wc);
+            if (!ok) continue;   // no named barrier below this point of the tile
             tc_fence_after();
             const uint32_t scol = s_col(it);
             float rb = tk.uniform ? (tk.which ? a1 : a0) : 0.f;
@@ -561,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             l_part += sum;
             if (__any_sync(0xffffffffu, resc) && it > 0) {
-                if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, err, abort_flag))) break;
+                if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, wc))) continue;
                 tc_fence_after();
                 rescale_o(alpha);
             }
@@ -573,12 +601,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         // merge the two halves: m = max(m_0, m_1), l = sum_h l_h 2^(m_h - m),
         // O = sum_h O_h 2^(m_h - m) / l
-        if (ok) ok = mbar_wait_warp(&bars->pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, err, abort_flag);
+        ok = ok && mbar_wait_warp(&bars->pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, wc);
         tc_fence_after();
+        xch[hf * BM + row] = m_run;
+        xch[2 * BM + hf * BM + row] = l_part;
+        named_bar_sync(pair_bar, 64);   // both warps of the pair, whatever their state
         if (ok) {
-            xch[hf * BM + row] = m_run;
-            xch[2 * BM + hf * BM + row] = l_part;
-            named_bar_sync(pair_bar, 64);
             const float m0 = xch[row], m1 = xch[BM + row];
             const float mx = fmaxf(m0, m1);
             const float s0 = m0 == -INFINITY ? 0.f : ex2(m0 - mx);
@@ -612,7 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (row_in && hf == 0) lse[lse_index(p, b, h, t0, i)] = any ? (mx + log2f(l_run)) * kLn2 : INFINITY;
+            // lse == nullptr: the inference forward, which keeps no LSE
+            if (row_in && hf == 0 && lse) lse[lse_index(p, b, h, t0, i)] = any ? (mx + log2f(l_run)) * kLn2 : INFINITY;
         }
     }
     tc_fence_before();

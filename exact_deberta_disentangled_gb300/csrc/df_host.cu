@@ -17,6 +17,14 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Bounded-wait limits and the test-only stall injection
+// (df_attn_debug_inject_stall), copied into every call's ProblemDev.
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
+constexpr uint32_t kDefaultWaitProbes = 1u << 20;
+unsigned long long g_wait_ns = kDefaultWaitNs;
+uint32_t g_wait_probes = kDefaultWaitProbes;
+int g_fault_kernel = -1, g_fault_tile = -1;
+
 // Validated problem: fills `out` and returns DF_OK, or an error code.
 df_status resolve(const df_attn_params* a, ProblemDev& out) {
     if (!a) return DF_ERR_INVALID_ARG;
@@ -77,6 +85,10 @@ df_status resolve(const df_attn_params* a, ProblemDev& out) {
     out.seed_lo = (uint32_t)a->philox_seed;
     out.seed_hi = (uint32_t)(a->philox_seed >> 32);
     out.philox_offset = (uint32_t)a->philox_offset;
+    out.wait_ns = g_wait_ns;
+    out.wait_probes = g_wait_probes;
+    out.fault_kernel = g_fault_kernel;
+    out.fault_tile = g_fault_tile;
     return DF_OK;
 }
 
@@ -207,6 +219,21 @@ df_status df_attn_set_profile_events(void* const* events, int n) {
     return DF_OK;
 }
 
+df_status df_attn_debug_inject_stall(int kernel, int tile, uint64_t wait_limit_ns, uint32_t wait_min_probes) {
+    if (kernel < 0) {
+        g_fault_kernel = g_fault_tile = -1;
+        g_wait_ns = kDefaultWaitNs;
+        g_wait_probes = kDefaultWaitProbes;
+        return DF_OK;
+    }
+    if (kernel > 2 || tile < 0 || wait_limit_ns == 0 || wait_limit_ns > kDefaultWaitNs) return DF_ERR_INVALID_ARG;
+    g_fault_kernel = kernel;
+    g_fault_tile = tile;
+    g_wait_ns = wait_limit_ns;
+    g_wait_probes = wait_min_probes;
+    return DF_OK;
+}
+
 size_t df_attn_workspace_size(const df_attn_params* a, int backward) {
     ProblemDev p;
     if (resolve(a, p) != DF_OK) return 0;
@@ -228,11 +255,14 @@ static df_status common_prologue(const df_attn_params* a, ProblemDev& p, Workspa
     return DF_OK;
 }
 
-df_status df_attn_fwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
-                      const void* kr, void* out, float* lse, void* workspace, size_t ws_bytes, df_stream_t stream) {
-    const void* ptrs[] = {q, k, v, qr, kr, out, lse};
+// The forward with or without the LSE store (lse == nullptr: inference).
+static df_status fwd_common(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                            const void* kr, void* out, float* lse, void* workspace, size_t ws_bytes,
+                            df_stream_t stream) {
+    const void* ptrs[] = {q, k, v, qr, kr, out};
     for (const void* x : ptrs)
         if (!x || !aligned16(x)) return DF_ERR_INVALID_ARG;
+    if (lse && !aligned16(lse)) return DF_ERR_INVALID_ARG;
     if (a && a->cu_seqlens && ((uintptr_t)a->cu_seqlens & 3u)) return DF_ERR_INVALID_ARG;
     ProblemDev p;
     Workspace w;
@@ -244,6 +274,18 @@ df_status df_attn_fwd(const df_attn_params* a, const void* q, const void* k, con
                                           (const float*)kr, (float*)out, lse, st));
     if (launch_relbias(p, a->dtype, q, k, qr, kr, w.relb, st)) return DF_ERR_CUDA;
     return cuda_status(launch_fwd_tc(p, w, a->dtype, q, k, v, qr, kr, out, lse, st));
+}
+
+df_status df_attn_fwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                      const void* kr, void* out, float* lse, void* workspace, size_t ws_bytes, df_stream_t stream) {
+    if (!lse) return DF_ERR_INVALID_ARG;
+    return fwd_common(a, q, k, v, qr, kr, out, lse, workspace, ws_bytes, stream);
+}
+
+df_status df_attn_fwd_inference(const df_attn_params* a, const void* q, const void* k, const void* v,
+                                const void* qr, const void* kr, void* out, void* workspace, size_t ws_bytes,
+                                df_stream_t stream) {
+    return fwd_common(a, q, k, v, qr, kr, out, nullptr, workspace, ws_bytes, stream);
 }
 
 df_status df_attn_bwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
@@ -376,6 +418,16 @@ df_status df_rel_index_table(int32_t L, int32_t att_span, int32_t nb, int32_t mp
     if (bucketing && (nb < 2 || mp - 1 <= nb / 2)) return DF_ERR_UNSUPPORTED;
     return cuda_status(
         launch_delta_table(L, att_span, bucketing ? nb : 0, bucketing ? mp : 0, out_dev, (cudaStream_t)stream));
+}
+
+df_status df_dropout_keep_mask(const df_attn_params* a, int32_t b, int32_t h, int32_t form, uint8_t* out_dev,
+                               df_stream_t stream) {
+    ProblemDev p;
+    df_status s = resolve(a, p);
+    if (s != DF_OK) return s;
+    if (b < 0 || b >= p.B || h < 0 || h >= p.H || (form != 0 && form != 1) || !out_dev) return DF_ERR_INVALID_ARG;
+    if (a->cu_seqlens && ((uintptr_t)a->cu_seqlens & 3u)) return DF_ERR_INVALID_ARG;
+    return cuda_status(launch_keep_mask(p, b, h, form, out_dev, (cudaStream_t)stream));
 }
 
 df_status df_get_device_error(const void* workspace, df_stream_t stream) {

@@ -25,6 +25,16 @@ struct ProblemDev {
     int dropout;              // p > 0
     uint32_t seed_lo, seed_hi, philox_offset;
     int* err;                 // device error word (workspace)
+    // bounded waits: a wait gives up once wait_ns have passed AND wait_probes
+    // probes have failed (defaults 2 s and 2^20; df_attn_debug_inject_stall
+    // shortens them for its test)
+    unsigned long long wait_ns;
+    uint32_t wait_probes;
+    // test-only stall injection (df_attn_debug_inject_stall): the MMA-issuing
+    // warp of every CTA of kernel `fault_kernel` (0 forward, 1 dQ, 2 dK/dV)
+    // stops before tile `fault_tile`; -1 = off
+    int fault_kernel;
+    int fault_tile;
 };
 
 // Workspace carve-up (device pointers, all 256-byte aligned).
@@ -53,6 +63,7 @@ int launch_relbias(const ProblemDev& p, df_dtype dt, const void* q, const void* 
                    float* relb, cudaStream_t st);
 int launch_rowterm(const ProblemDev& p, df_dtype dt, const void* out, const void* dout, float* rowterm,
                    cudaStream_t st);
+int launch_keep_mask(const ProblemDev& p, int b, int h, int form, uint8_t* out, cudaStream_t st);
 
 // strict fp32 path
 int launch_fwd_f32(const ProblemDev& p, const Workspace& ws, const float* q, const float* k, const float* v,

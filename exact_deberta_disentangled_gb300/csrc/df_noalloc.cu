@@ -55,3 +55,16 @@ extern "C" df_status df_attn_fwd_noalloc(const df_attn_params* p, const void* q,
     // every other scratch byte it reads is written earlier in the same call
     return df_attn_fwd(p, q, k, v, qr, kr, out, lse, scratch, kNoAllocScratchBytes, stream);
 }
+
+extern "C" df_status df_attn_fwd_noalloc_device_error(df_stream_t stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DF_ERR_CUDA;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        scratch = g_scratch_addr[dev];
+    }
+    // no call on this device yet: nothing can have failed
+    if (!scratch) return DF_OK;
+    return df_get_device_error(scratch, stream);
+}

@@ -69,13 +69,15 @@ __global__ void __launch_bounds__(kRelThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    volatile int* abort_flag = &bars->abort_flag;
+    const WaitCtx wc = wait_ctx(p, &bars->abort_flag);
     bool ok = true;
+    int nload[2] = {0, 0};   // copies issued per stage
     if (threadIdx.x == 0) {
         constexpr uint32_t id = idesc_f16(128, D, BF16, false, true);
         auto issue_load = [&](int c) {
             const int s = c & 1;
             uint8_t* st = smem + s * S::STAGE;
+            ++nload[s];
             mbar_arrive_expect_tx(&bars->full[s], S::STAGE);
             tma_load_2d(st, &tmG, h * Rp + 64 * c, tok0, &bars->full[s]);
             for (int q = 0; q < G::NCH; ++q)
@@ -85,22 +87,26 @@ __global__ void __launch_bounds__(kRelThreads, 1)
         if (nk > 1) issue_load(1);
         for (int c = 0; c < nk && ok; ++c) {
             const int s = c & 1;
-            if (!(ok = mbar_wait(&bars->full[s], (c >> 1) & 1, p.err, abort_flag))) break;
+            if (!(ok = mbar_wait(&bars->full[s], (c >> 1) & 1, wc))) break;
             tc_fence_after();
             const uint32_t sA = smem_u32(smem + s * S::STAGE), sB = sA + S::AB;
             for (int k = 0; k < 4; ++k)
                 tc_mma_ss(tmem, sdesc(sA + 32 * k, 16, 1024, 2), desc_mn<G>(sB, 64, k), id, (c | k) != 0);
             tc_commit(&bars->empty[s]);
             if (c + 2 < nk) {
-                if (!(ok = mbar_wait(&bars->empty[s], (c >> 1) & 1, p.err, abort_flag))) break;
+                if (!(ok = mbar_wait(&bars->empty[s], (c >> 1) & 1, wc))) break;
                 issue_load(c + 2);
             }
         }
         tc_commit(&bars->done);
+        // no copy is still landing in shared memory when the CTA exits
+        for (int s = 0; s < 2; ++s)
+            if (nload[s] > 0) mbar_drain(&bars->full[s], (nload[s] - 1) & 1, wc.limit_ns);
     }
     __syncthreads();
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) ok = mbar_wait_warp(&bars->done, 0, p.err, abort_flag);
+    if (ok) ok = mbar_wait_warp(&bars->done, 0, wc);
+    if (!ok) mbar_drain(&bars->done, 0, wc.limit_ns);   // the MMAs, before the tensor memory is freed
     tc_fence_after();
     const int row = 32 * warp + lane, tok = tok0 + row;
     using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
@@ -178,14 +184,16 @@ __global__ void __launch_bounds__(kRelThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    volatile int* abort_flag = &bars->abort_flag;
+    const WaitCtx wc = wait_ctx(p, &bars->abort_flag);
     bool ok = true;
+    int nload[2] = {0, 0};   // copies issued per stage
     if (threadIdx.x == 0 && nk > 0) {
         constexpr uint32_t id = idesc_f16(128, D, BF16, true, true);
         auto issue_load = [&](int c) {
             const int s = c & 1;
             uint8_t* st = smem + s * S::STAGE;
             const int t = tbeg + c * kChunkTok;
+            ++nload[s];
             mbar_arrive_expect_tx(&bars->full[s], S::STAGE);
             tma_load_2d(st, &tmG, h * Rp + 128 * rb, t, &bars->full[s]);
             tma_load_2d(st + kChunkTok * 64 * 2, &tmG, h * Rp + 128 * rb + 64, t, &bars->full[s]);
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(kRelThreads, 1)
         if (nk > 1) issue_load(1);
         for (int c = 0; c < nk && ok; ++c) {
             const int s = c & 1;
-            if (!(ok = mbar_wait(&bars->full[s], (c >> 1) & 1, p.err, abort_flag))) break;
+            if (!(ok = mbar_wait(&bars->full[s], (c >> 1) & 1, wc))) break;
             tc_fence_after();
             const uint32_t sA = smem_u32(smem + s * S::STAGE), sB = sA + S::AB;
             for (int k = 0; k < kChunkTok / 16; ++k) {
@@ -206,15 +214,19 @@ __global__ void __launch_bounds__(kRelThreads, 1)
             }
             tc_commit(&bars->empty[s]);
             if (c + 2 < nk) {
-                if (!(ok = mbar_wait(&bars->empty[s], (c >> 1) & 1, p.err, abort_flag))) break;
+                if (!(ok = mbar_wait(&bars->empty[s], (c >> 1) & 1, wc))) break;
                 issue_load(c + 2);
             }
         }
         tc_commit(&bars->done);
+        // no copy is still landing in shared memory when the CTA exits
+        for (int s = 0; s < 2; ++s)
+            if (nload[s] > 0) mbar_drain(&bars->full[s], (nload[s] - 1) & 1, wc.limit_ns);
     }
     __syncthreads();
     ok = __all_sync(0xffffffffu, ok);
-    if (nk > 0 && ok) ok = mbar_wait_warp(&bars->done, 0, p.err, abort_flag);
+    if (nk > 0 && ok) ok = mbar_wait_warp(&bars->done, 0, wc);
+    if (nk > 0 && !ok) mbar_drain(&bars->done, 0, wc.limit_ns);   // the MMAs, before the tensor memory is freed
     tc_fence_after();
     const int r = 128 * rb + 32 * warp + lane;
     float* dst = part + (((size_t)ch * p.H + h) * p.R + r) * D;

@@ -55,6 +55,11 @@ def _workloads():
                                   B=4, L=4096, dropout_p=0.1)
     w["hd32_dropout"] = Workload("hd32_dropout", H=24, D=32, span=256, nb=256, mp=512, dtype="bf16", seed=4,
                                  B=8, L=2048, dropout_p=0.1)
+    # stand-in for the pages' MNLI evaluation shape (fp16, batch 8, length
+    # bucket 512, a 24-head / 64-dim model): padded batches of 8 sequences
+    # with valid lengths uniform in [16, 512]; synthetic values, no dataset
+    w["mnli_fp16"] = Workload("mnli_fp16", H=24, D=64, span=256, nb=256, mp=512, dtype="fp16", seed=5, B=8,
+                              L=512, len_range=(16, 512))
     return w
 
 
@@ -92,9 +97,15 @@ def packed_lengths(gen: torch.Generator, total: int, lo: int, hi: int) -> list:
 
 def make_inputs(w: Workload, *, B: Optional[int] = None, L: Optional[int] = None, H: Optional[int] = None,
                 total_tokens: Optional[int] = None, dtype: Optional[str] = None, seed: Optional[int] = None,
-                device="cpu") -> Inputs:
+                key_mask: str = "same", device="cpu") -> Inputs:
     """Draw the inputs of workload ``w`` (optionally at reduced sizes for the
-    small parity cases; the recipe stays the same)."""
+    small parity cases; the recipe stays the same).
+
+    ``key_mask`` (padded workloads with a length range only): "same" makes the
+    key mask equal to the query mask (the workloads' recipe); "independent"
+    draws, after everything else, a second set of valid lengths for the keys
+    and then clears about one key in eight at random inside them, so that the
+    two masks differ both at the padding boundary and in scattered positions."""
     B = w.B if B is None else B
     L = w.L if L is None else L
     H = w.H if H is None else H
@@ -129,6 +140,13 @@ def make_inputs(w: Workload, *, B: Optional[int] = None, L: Optional[int] = None
             m = (pos < lens[:, None]).to(torch.uint8).reshape(-1)
             qmask = m.clone()
             kmask = m.clone()
+            if key_mask == "independent":
+                klens = torch.randint(lo, hi + 1, (B,), generator=gen)
+                km = (pos < klens[:, None]).reshape(-1)
+                holes = torch.rand(B * L, generator=gen) < 0.125
+                kmask = (km & ~holes).to(torch.uint8)
+            elif key_mask != "same":
+                raise ValueError(f"key_mask must be 'same' or 'independent', not {key_mask!r}")
     t = [x.to(dt).to(device) for x in (q, k, v, qr, kr, dout)]
     cu = cu.to(device)
     if qmask is not None:

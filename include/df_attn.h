@@ -28,7 +28,9 @@
  * Conventions shared by every entry point
  *   - All tensors are dense and contiguous; the caller owns every buffer.
  *     No entry point allocates device memory; scratch comes from the
- *     caller's workspace (size from df_attn_workspace_size).
+ *     caller's workspace (size from df_attn_workspace_size), except for
+ *     df_attn_fwd_noalloc, whose scratch is an 8 MiB static device array of
+ *     the library (held on every GPU that loads it).
  *   - Device pointers must be 16-byte aligned.
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
  *   - Argument errors return a status before anything is enqueued and
@@ -135,6 +137,18 @@ df_status df_attn_fwd(const df_attn_params *p, const void *q, const void *k, con
                       df_stream_t stream);
 
 /*
+ * Inference forward: the same output as df_attn_fwd without the row
+ * log-sum-exp, which only the backward needs ("DisentangledFlash", section
+ * "Status": an inference path beside the training path; section "Hugging
+ * Face usage": the training forward is the LSE-producing one).  Same
+ * arguments, workspace (df_attn_workspace_size(p, 0)) and errors as
+ * df_attn_fwd, minus lse.
+ */
+df_status df_attn_fwd_inference(const df_attn_params *p, const void *q, const void *k, const void *v,
+                                const void *qr, const void *kr, void *out, void *workspace, size_t workspace_bytes,
+                                df_stream_t stream);
+
+/*
  * Backward.  Takes the forward's inputs, its out and lse, and dout (layout of
  * out); writes dq, dk, dv (layout of q) and dqr, dkr ([H, R, D], summed over
  * the batch, overwritten).  All gradients are deterministic: the same call
@@ -182,11 +196,18 @@ df_status df_attn_step_host(const df_attn_params *p, const void *q, const void *
  *     that device current); make that first call before any stream capture.
  *   - Every call shares the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and give undefined results; serialise them.
- *   - Device-side errors (inconsistent cu_seqlens, a give-up) are not
- *     reported by this entry point; outputs of such a call are unspecified.
+ *   - Device-side errors (inconsistent cu_seqlens, a give-up) land in the
+ *     array's error word: df_attn_fwd_noalloc_device_error reads it.
+ *   - The cached address assumes the device's primary context, which is what
+ *     the CUDA runtime uses; it is not valid after cudaDeviceReset.
  */
 df_status df_attn_fwd_noalloc(const df_attn_params *p, const void *q, const void *k, const void *v,
                               const void *qr, const void *kr, void *out, float *lse, df_stream_t stream);
+
+/* Synchronises `stream` and reads the device error word of the static
+ * scratch used by df_attn_fwd_noalloc on the current device (see
+ * df_get_device_error); DF_OK before the first such call. */
+df_status df_attn_fwd_noalloc_device_error(df_stream_t stream);
 
 /*
  * The relative-position index table delta(r) for r = -(L-1) .. L-1, written
@@ -195,6 +216,20 @@ df_status df_attn_fwd_noalloc(const df_attn_params *p, const void *q, const void
  */
 df_status df_rel_index_table(int32_t L, int32_t att_span, int32_t position_buckets,
                              int32_t max_relative_positions, int32_t *out_dev, df_stream_t stream);
+
+/*
+ * The dropout keep mask of sequence b, head h, drawn on the device by the
+ * same generator code as the attention kernels ("DisentangledFlash",
+ * section "Status": the Philox mask is regenerated in the backward, never
+ * stored -- this entry point exists so that tests can compare it bit for bit
+ * with an independent generator).  form 0: the row generator of the forward
+ * and dQ kernels; form 1: the column generator of the dK/dV kernel.  Writes
+ * out_dev[i * n + j] = keep(i, j) (0 / 1 bytes, device, n * n bytes, n = the
+ * length of sequence b: L padded, cu_seqlens[b+1] - cu_seqlens[b] packed).
+ * Uses p's dropout_p, philox_seed, philox_offset, H and layout.
+ */
+df_status df_dropout_keep_mask(const df_attn_params *p, int32_t b, int32_t h, int32_t form, uint8_t *out_dev,
+                               df_stream_t stream);
 
 /*
  * Synchronises `stream` and reads the device error word of a workspace that
@@ -215,6 +250,20 @@ df_status df_get_device_error(const void *workspace, df_stream_t stream);
  * setting is process-wide and not thread-safe; it exists for measurement only.
  */
 df_status df_attn_set_profile_events(void *const *events, int n);
+
+/*
+ * Test hook for the bounded-wait path (process-wide, not thread-safe).  From
+ * the next call on, the MMA-issuing warp of every CTA of one attention kernel
+ * (kernel 0 = forward, 1 = dQ, 2 = dK/dV) stops issuing when it reaches tile
+ * `tile` of its loop, and every device wait gives up once wait_limit_ns
+ * (at most 2 s) have passed and wait_min_probes probes have failed.  The
+ * kernel's other roles then wait for work that never comes, give up, record
+ * DF_ERR_TIMEOUT (read it with df_get_device_error) and leave the kernel:
+ * the outputs of such a call are unspecified and the CUDA context stays
+ * usable.  kernel = -1 switches the injection off and restores the default
+ * limits (2 s and 2^20 probes).  Nothing else uses it.
+ */
+df_status df_attn_debug_inject_stall(int kernel, int tile, uint64_t wait_limit_ns, uint32_t wait_min_probes);
 
 /* Static, human-readable name of a status code. */
 const char *df_status_string(df_status s);

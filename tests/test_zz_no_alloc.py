@@ -42,6 +42,7 @@ def test_noalloc_forward_matches_workspace_forward_twice(name, kw):
         lse = torch.full(g.lse_shape(), float("nan"), dtype=torch.float32, device=dev)
         B.attn_fwd_noalloc(g, *t, out, lse)
         torch.cuda.synchronize()
+        assert B.noalloc_device_error() == B.DF_OK
         want = ref_out.double().cpu().numpy()
         assert rel_l2(out, want) <= OUT_TOL and max_abs(out, want) <= OUT_MAX
         lw = ref_lse.double().cpu().numpy()

@@ -297,6 +297,7 @@ def run_gpu(args, rank, world, local_rank):
     if ef or eb:
         raise SystemExit(f"device error word after the timed steps: forward {ef}, backward {eb}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    step_q = quantiles(step_ms)
     print("per-step ms: " + " ".join(f"{t:.3f}" for t in step_ms) + " | fwd: " +
           " ".join(f"{t:.3f}" for t in phase_ms["fwd"]), file=sys.stderr, flush=True)
     ms = sum(step_ms) / len(step_ms)
@@ -343,13 +344,17 @@ def run_gpu(args, rank, world, local_rank):
     peak = peaks.get("bf16_tflops", 1900.0)
     achieved = kflops[dominant] / (avg[dominant] * 1e-3) / 1e12
     traffic = kernel_traffic(dominant)
+    extras = None
+    if not args.no_extras:
+        extras = run_extras(dev, args.extra_iters, 3, flush)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         v_cpu, desc, nthr, _ = oracle_sample(args.ref_seconds)
         cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": nthr, "kind": "oracle", "sample": desc}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "step_ms_quantiles": step_q, "higher_is_better": True,
+        "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "length sweep L=8192: B=2, H=12, D=64, att_span=256 (R=512), buckets 256, "
                                "max_rel 512, 16384 tokens per GPU, N(0,1) inputs", "global_batch": B * world,
@@ -368,8 +373,134 @@ def run_gpu(args, rank, world, local_rank):
         # relative-gradient row / column / reduce kernels x2 each
         "gpu_launches": args.steps * 14,
         "clocks": clk,
+        "extras": extras,
     }
     print(json.dumps(line), flush=True)
+
+
+def quantiles(ts):
+    """min / p10 / median / p90 of a list of per-iteration times (ms)."""
+    import numpy as np
+    a = np.asarray(ts, dtype=np.float64)
+    return {"min": float(a.min()), "p10": float(np.percentile(a, 10)), "median": float(np.median(a)),
+            "p90": float(np.percentile(a, 90)), "n": int(a.size)}
+
+
+def workload_flops(x, w, H):
+    """The pages' FLOP count of one call: per (sequence, head) of length l,
+    4 l^2 D + 4 l R D forward and 10 l^2 D + 12 l R D backward; padded
+    workloads are counted on the padded length (every tile is computed)."""
+    lens = (x.cu_seqlens[1:] - x.cu_seqlens[:-1]).tolist()
+    D, R = w.D, w.R
+    f = sum(H * (4 * l * l * D + 4 * l * R * D) for l in lens)
+    b = sum(H * (10 * l * l * D + 12 * l * R * D) for l in lens)
+    return f, b
+
+
+def time_phases(name, dev, iters, warmup, flush, **make_kw):
+    """Forward, backward (alone, from the saved forward outputs) and forward +
+    backward of one workload through the C ABI: per-iteration CUDA-event
+    times on the launching stream, L2 flushed before every iteration."""
+    import torch
+
+    from exact_deberta_disentangled_gb300 import binding as Bd
+    from exact_deberta_disentangled_gb300 import synth
+
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w, **make_kw)
+    H = x.q.shape[1]
+    g = Bd.Geometry(B=x.B, L=x.L, H=H, D=w.D, span=w.span, nb=w.nb, mp=w.mp, dropout_p=w.dropout_p, seed=11,
+                    offset=0)
+    if x.packed:
+        g.cu_seqlens = x.cu_seqlens.to(dev)
+        g.total_tokens = int(x.cu_seqlens[-1])
+    if x.qmask is not None:
+        g.query_mask, g.key_mask = x.qmask.to(dev), x.kmask.to(dev)
+    q, k, v, qr, kr, do = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    out = torch.empty_like(q)
+    lse = torch.empty(g.lse_shape(), dtype=torch.float32, device=dev)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(qr),
+             torch.empty_like(kr))
+    wsf = Bd.alloc_workspace(g, q.dtype, False, dev)
+    wsb = Bd.alloc_workspace(g, q.dtype, True, dev)
+    stream = torch.cuda.current_stream()
+    fwd = lambda: Bd.attn_fwd(g, q, k, v, qr, kr, out=out, lse=lse, workspace=wsf)
+    bwd = lambda: Bd.attn_bwd(g, q, k, v, qr, kr, out, lse, do, grads=grads, workspace=wsb)
+
+    def both():
+        fwd()
+        bwd()
+
+    res = {}
+    for phase, fn in (("fwd", fwd), ("bwd", bwd), ("fwd_bwd", both)):
+        fwd()   # the backward reads the forward's outputs
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res[phase] = quantiles([a.elapsed_time(b) for a, b in ev])
+    if Bd.device_error(wsf) or Bd.device_error(wsb):
+        raise SystemExit(f"device error word set while timing {name}")
+    fl_f, fl_b = workload_flops(x, w, H)
+    for phase, fl in (("fwd", fl_f), ("bwd", fl_b), ("fwd_bwd", fl_f + fl_b)):
+        res[phase]["tflops_at_median"] = fl / (res[phase]["median"] * 1e-3) / 1e12
+    shape = {"B": x.B, "L": x.L, "H": H, "D": w.D, "R": w.R, "dtype": str(q.dtype).replace("torch.", ""),
+             "dropout_p": w.dropout_p, "packed": x.packed, "masked": x.qmask is not None,
+             "tokens": int(x.cu_seqlens[-1]), "fwd_flops": fl_f, "bwd_flops": fl_b}
+    return {"shape": shape, **res}
+
+
+def time_inference(dev, L, iters, warmup, flush, B=8, H=12):
+    """Latency of the inference forward (df_attn_fwd_inference, no LSE) at a
+    short length with the v3-base head layout and padding masks."""
+    import torch
+
+    from exact_deberta_disentangled_gb300 import binding as Bd
+    from exact_deberta_disentangled_gb300 import synth
+
+    w = synth.WORKLOADS["v3_base"]
+    x = synth.make_inputs(w, B=B, L=L, H=H)
+    g = Bd.Geometry(B=B, L=L, H=H, D=w.D, span=w.span, nb=w.nb, mp=w.mp, query_mask=x.qmask.to(dev),
+                    key_mask=x.kmask.to(dev))
+    q, k, v, qr, kr = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr)]
+    out = torch.empty_like(q)
+    ws = Bd.alloc_workspace(g, q.dtype, False, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        Bd.attn_fwd_inference(g, q, k, v, qr, kr, out=out, workspace=ws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        Bd.attn_fwd_inference(g, q, k, v, qr, kr, out=out, workspace=ws)
+        b.record(stream)
+    torch.cuda.synchronize()
+    if Bd.device_error(ws):
+        raise SystemExit(f"device error word set in the inference forward at L={L}")
+    qs = quantiles([a.elapsed_time(b) * 1e3 for a, b in ev])   # microseconds
+    return {"B": B, "L": L, "H": H, "D": w.D, "unit": "us", **qs}
+
+
+def run_extras(dev, iters, warmup, flush):
+    """The length sweep and the other workloads, each timed separately
+    (fwd, bwd alone, fwd + bwd; min / p10 / median / p90), plus the
+    inference latency at short lengths."""
+    sweep = {}
+    for L in (512, 1024, 2048, 4096, 8192):
+        sweep[f"L{L}"] = time_phases(f"sweep_L{L}", dev, iters, warmup, flush)
+    configs = {}
+    for name in ("v3_base", "varlen", "hd128_dropout", "hd32_dropout", "mnli_fp16"):
+        configs[name] = time_phases(name, dev, iters, warmup, flush)
+    infer = {f"L{L}": time_inference(dev, L, iters, warmup, flush) for L in (64, 128, 384)}
+    return {"sweep": sweep, "configs": configs, "inference_latency": infer,
+            "method": "CUDA events on the launching stream per iteration, L2 flushed (512 MB write) before "
+                      "each; bwd timed alone from the saved forward outputs"}
 
 
 def run_profile_case(args, local_rank):
@@ -408,6 +539,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the length sweep, the other workloads and the inference latencies")
+    ap.add_argument("--extra-iters", type=int, default=15)
     ap.add_argument("--profile-run", action="store_true",
                     help="run the small profiling case (L=8192, B=1) without timing")
     args = ap.parse_args()

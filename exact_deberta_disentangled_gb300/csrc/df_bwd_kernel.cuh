@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int BM = G::BM, BN = G::BN;
     constexpr bool ROWQ = SIGMA > 0;   // rows are queries
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem = smem_align1024(smem_raw);
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem + S::MISC);
     int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
     float* colv = reinterpret_cast<float*>(smem + S::COLV);

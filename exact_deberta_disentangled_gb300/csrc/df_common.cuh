@@ -107,6 +107,13 @@ DF_DEV uint64_t globaltimer_ns() {
 
 DF_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// The dynamic shared-memory block rounded up to a 1024-byte boundary (the
+// TMA swizzle atoms and the MMA descriptors need it).  The offset is added to
+// the __shared__ array itself, so that every pointer derived from the result
+// is still known to address shared memory and plain C++ accesses through it
+// compile to shared-memory instructions (a round trip through an integer
+// leaves the compiler only generic addressing).
+DF_DEV uint8_t* smem_align1024(uint8_t* raw) { return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u); }
 
 DF_DEV void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kRelThreads, 1)
     using G = Geo<D>;
     using S = RowSmem<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem = smem_align1024(smem_raw);
     RelBars* bars = reinterpret_cast<RelBars*>(smem + 2 * S::STAGE);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tok0 = blockIdx.x * 128, h = blockIdx.y;
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kRelThreads, 1)
     using G = Geo<D>;
     using S = ColSmem<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem = smem_align1024(smem_raw);
     RelBars* bars = reinterpret_cast<RelBars*>(smem + 2 * S::STAGE);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = blockIdx.x, h = blockIdx.y, ch = blockIdx.z;

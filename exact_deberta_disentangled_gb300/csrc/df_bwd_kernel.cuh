@@ -629,10 +629,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 cv = cv0p[q];
-                        sr[4 * q + 0] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 0]), kscale, cv.x) + rowc);
-                        sr[4 * q + 1] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 1]), kscale, cv.y) + rowc);
-                        sr[4 * q + 2] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 2]), kscale, cv.z) + rowc);
-                        sr[4 * q + 3] = __float_as_uint(fmaf(__uint_as_float(sr[4 * q + 3]), kscale, cv.w) + rowc);
+                        float a0, a1, a2, a3;
+                        ffma2(a0, a1, __uint_as_float(sr[4 * q + 0]), __uint_as_float(sr[4 * q + 1]), kscale, kscale,
+                              cv.x, cv.y);
+                        ffma2(a2, a3, __uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3]), kscale, kscale,
+                              cv.z, cv.w);
+                        fadd2(a0, a1, a0, a1, rowc, rowc);
+                        fadd2(a2, a3, a2, a3, rowc, rowc);
+                        sr[4 * q + 0] = __float_as_uint(a0);
+                        sr[4 * q + 1] = __float_as_uint(a1);
+                        sr[4 * q + 2] = __float_as_uint(a2);
+                        sr[4 * q + 3] = __float_as_uint(a3);
                     }
                 }
                 uint32_t keep = 0xFFFFFFFFu;
@@ -651,19 +658,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dlq[3] = d4.w;
                     }
                     float z[4], pd[4];
+                    if constexpr (DROP) {
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int e = 4 * q + t;
-                        const float pr_ = ex2(__uint_as_float(sr[e]));
-                        if constexpr (DROP) {
+                        for (int t = 0; t < 4; ++t) {
+                            const int e = 4 * q + t;
+                            const float pr_ = ex2(__uint_as_float(sr[e]));
                             const float kp = ((keep >> e) & 1u) ? p.drop_scale : 0.f;
                             z[t] = pr_ * fmaf(__uint_as_float(pr[e]), p.scale * kp, -dlq[t]);
                             pd[t] = pr_ * kp;
-                        } else {
-                            z[t] = pr_ * fmaf(__uint_as_float(pr[e]), p.scale, -dlq[t]);
-                            pd[t] = pr_;
+                            rs[t] += z[t];
                         }
-                        rs[t] += z[t];
+                    } else {
+                        // the same arithmetic as above with keep = 1, two lanes per instruction
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) pd[t] = ex2(__uint_as_float(sr[4 * q + t]));
+                        float u0, u1, u2, u3;
+                        ffma2(u0, u1, __uint_as_float(pr[4 * q + 0]), __uint_as_float(pr[4 * q + 1]), p.scale,
+                              p.scale, -dlq[0], -dlq[1]);
+                        ffma2(u2, u3, __uint_as_float(pr[4 * q + 2]), __uint_as_float(pr[4 * q + 3]), p.scale,
+                              p.scale, -dlq[2], -dlq[3]);
+                        fmul2(z[0], z[1], pd[0], pd[1], u0, u1);
+                        fmul2(z[2], z[3], pd[2], pd[3], u2, u3);
+                        fadd2(rs[0], rs[1], rs[0], rs[1], z[0], z[1]);
+                        fadd2(rs[2], rs[3], rs[2], rs[3], z[2], z[3]);
                     }
                     zp[2 * q] = pack2<BF16>(z[0], z[1]);
                     zp[2 * q + 1] = pack2<BF16>(z[2], z[3]);

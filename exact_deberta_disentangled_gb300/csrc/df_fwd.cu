@@ -461,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto p_pass = [&](auto raw_tag) -> float {
                 constexpr bool RAW = decltype(raw_tag)::value;
                 const float mm = (m_run == -INFINITY || rb == -INFINITY) ? INFINITY : m_run - rb;
-                float sm = 0.f;
+                const float nmm = -mm;
+                float sm0 = 0.f, sm1 = 0.f;
 #pragma unroll 1
                 for (int cc = 0; cc < NCT; ++cc) {
                     const int c = chunk(cc);
@@ -470,18 +471,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_wait_ld();
                     uint32_t keep = 0xFFFFFFFFu;
                     if constexpr (DROP) keep = keep_bits32_row(p, b, h, i, j0 + 32 * c);
-                    const float* cbp = colb + 32 * c;
+                    const float2* cbp = reinterpret_cast<const float2*>(colb + 32 * c);
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float x0 = __uint_as_float(r[2 * e]), x1 = __uint_as_float(r[2 * e + 1]);
                         if constexpr (RAW) {
-                            x0 = fmaf(x0, kscale, cbp[2 * e]);
-                            x1 = fmaf(x1, kscale, cbp[2 * e + 1]);
+                            const float2 cv = cbp[e];
+                            ffma2(x0, x1, x0, x1, kscale, kscale, cv.x, cv.y);
                         }
-                        const float p0 = ex2(x0 - mm);
-                        const float p1 = ex2(x1 - mm);
-                        sm += p0 + p1;
+                        fadd2(x0, x1, x0, x1, nmm, nmm);
+                        const float p0 = ex2(x0);
+                        const float p1 = ex2(x1);
+                        fadd2(sm0, sm1, sm0, sm1, p0, p1);
                         float d0 = p0, d1 = p1;
                         if constexpr (DROP) {
                             d0 = ((keep >> (2 * e)) & 1u) ? p0 * p.drop_scale : 0.f;
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_st16(lane_base + scol + TM::POFF + 16 * c, pk);
                 }
-                return sm;
+                return sm0 + sm1;
             };
             float sum = 0.f;
             if (!band) {
@@ -503,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[16 * NCT];
                 const bool attempted = m_run != -INFINITY && rb != -INFINITY;
                 const float mm = attempted ? m_run - rb : INFINITY;
-                float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                const float nmm = -mm;
+                float tm01 = -INFINITY, tm23 = -INFINITY;
                 float sm[4] = {0.f, 0.f, 0.f, 0.f};
                 // all of this thread's S columns in one tensor-memory round trip
                 uint32_t rr[32 * NCT];
@@ -520,20 +523,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 cv = cb4[q];
-                        const float x0 = fmaf(__uint_as_float(r[4 * q + 0]), kscale, cv.x);
-                        const float x1 = fmaf(__uint_as_float(r[4 * q + 1]), kscale, cv.y);
-                        const float x2 = fmaf(__uint_as_float(r[4 * q + 2]), kscale, cv.z);
-                        const float x3 = fmaf(__uint_as_float(r[4 * q + 3]), kscale, cv.w);
-                        tm[0] = fmaxf(tm[0], x0);
-                        tm[1] = fmaxf(tm[1], x1);
-                        tm[2] = fmaxf(tm[2], x2);
-                        tm[3] = fmaxf(tm[3], x3);
-                        float p0 = ex2(x0 - mm), p1 = ex2(x1 - mm);
-                        float p2 = ex2(x2 - mm), p3 = ex2(x3 - mm);
-                        sm[0] += p0;
-                        sm[1] += p1;
-                        sm[2] += p2;
-                        sm[3] += p3;
+                        float x0, x1, x2, x3;
+                        ffma2(x0, x1, __uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]), kscale, kscale,
+                              cv.x, cv.y);
+                        ffma2(x2, x3, __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]), kscale, kscale,
+                              cv.z, cv.w);
+                        tm01 = fmax3(tm01, x0, x1);
+                        tm23 = fmax3(tm23, x2, x3);
+                        float d0, d1, d2, d3;
+                        fadd2(d0, d1, x0, x1, nmm, nmm);
+                        fadd2(d2, d3, x2, x3, nmm, nmm);
+                        float p0 = ex2(d0), p1 = ex2(d1);
+                        float p2 = ex2(d2), p3 = ex2(d3);
+                        fadd2(sm[0], sm[1], sm[0], sm[1], p0, p1);
+                        fadd2(sm[2], sm[3], sm[2], sm[3], p2, p3);
                         if constexpr (DROP) {
                             const uint32_t kq = keep >> (4 * q);
                             p0 = (kq & 1u) ? p0 * p.drop_scale : 0.f;
@@ -546,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 sum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-                raise_max(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) + rb);
+                raise_max(fmaxf(tm01, tm23) + rb);
                 const bool redo = resc || (!attempted && m_run != -INFINITY && rb != -INFINITY);
                 if (__any_sync(0xffffffffu, redo)) {
                     sum = p_pass(std::true_type{});

@@ -487,6 +487,63 @@ def time_inference(dev, L, iters, warmup, flush, B=8, H=12):
     return {"B": B, "L": L, "H": H, "D": w.D, "unit": "us", **qs}
 
 
+def time_side_steps(dev, iters, warmup, flush):
+    """The steps on either side of the attention at a DeBERTa-v3-base layer
+    over the 16,384-token workload (hidden 768 = 12 x 64, R = 512): fused QKV
+    projection forward / backward (GEMM TFLOP/s: 2 T C 3HD forward, twice that
+    backward), relative projections forward / backward, and packing the
+    varlen workload's padded batch (rows of 12 x 64 bf16)."""
+    import torch
+
+    from exact_deberta_disentangled_gb300 import binding as Bd
+    from exact_deberta_disentangled_gb300 import synth
+
+    g = torch.Generator().manual_seed(21)
+    T, C, H, D, R = 16384, 768, 12, 64, 512
+    mk = lambda shape, sc=1.0: (torch.randn(shape, generator=g) * sc).to(torch.bfloat16).to(dev)
+    x, w, b, dqkv = mk((T, C)), mk((3, H * D, C), C ** -0.5), mk((3, H * D), 0.1), mk((3, T, H * D))
+    rel, gamma, beta = mk((R, C)), mk((C,), 0.1), mk((C,), 0.1)
+    dqr, dkr = mk((H, R, D)), mk((H, R, D))
+    stream = torch.cuda.current_stream()
+    qr, kr, rel_ln, stats = Bd.rel_proj_fwd(rel, gamma, beta, 1e-7, w, b, H, D)
+    dw = torch.empty_like(w)
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, e in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return quantiles([a.elapsed_time(e) for a, e in ev])
+
+    res = {"qkv_fwd": timed(lambda: Bd.qkv_proj_fwd(x, w, b)),
+           "qkv_bwd": timed(lambda: Bd.qkv_proj_bwd(x, w, dqkv, dw=dw)),
+           "rel_fwd": timed(lambda: Bd.rel_proj_fwd(rel, gamma, beta, 1e-7, w, b, H, D)),
+           "rel_bwd": timed(lambda: Bd.rel_proj_bwd(rel, gamma, rel_ln, stats, w, dqr, dkr, dw))}
+    fl = 2.0 * T * C * 3 * H * D
+    res["qkv_fwd"]["tflops_at_median"] = fl / (res["qkv_fwd"]["median"] * 1e-3) / 1e12
+    res["qkv_bwd"]["tflops_at_median"] = 2 * fl / (res["qkv_bwd"]["median"] * 1e-3) / 1e12
+    # packing: the varlen workload's sequences as a padded batch of their longest length
+    v = synth.make_inputs(synth.WORKLOADS["varlen"])
+    lens = (v.cu_seqlens[1:] - v.cu_seqlens[:-1])
+    nb, Lmax = len(lens), int(lens.max())
+    mask = (torch.arange(Lmax)[None, :] < lens[:, None]).to(torch.uint8).to(dev)
+    padded = torch.randn((nb, Lmax, H, D), generator=g).to(torch.bfloat16).to(dev)
+    pi = Bd.pack_info(mask)
+    packed = Bd.pack_rows(padded, pi)
+    res["pack_info"] = timed(lambda: Bd.pack_info(mask))
+    res["pack_rows"] = timed(lambda: Bd.pack_rows(padded, pi))
+    res["unpack_rows"] = timed(lambda: Bd.unpack_rows(packed, pi))
+    res["pack_bytes"] = 2 * pi.total * H * D * 2
+    res["shapes"] = {"T": T, "C": C, "H": H, "D": D, "R": R, "pack_batch": [nb, Lmax], "pack_tokens": pi.total}
+    return res
+
+
 def run_extras(dev, iters, warmup, flush):
     """The length sweep and the other workloads, each timed separately
     (fwd, bwd alone, fwd + bwd; min / p10 / median / p90), plus the
@@ -498,7 +555,8 @@ def run_extras(dev, iters, warmup, flush):
     for name in ("v3_base", "varlen", "hd128_dropout", "hd32_dropout", "mnli_fp16"):
         configs[name] = time_phases(name, dev, iters, warmup, flush)
     infer = {f"L{L}": time_inference(dev, L, iters, warmup, flush) for L in (64, 128, 384)}
-    return {"sweep": sweep, "configs": configs, "inference_latency": infer,
+    side = time_side_steps(dev, iters, warmup, flush)
+    return {"sweep": sweep, "configs": configs, "inference_latency": infer, "steps_either_side": side,
             "method": "CUDA events on the launching stream per iteration, L2 flushed (512 MB write) before "
                       "each; bwd timed alone from the saved forward outputs"}
 

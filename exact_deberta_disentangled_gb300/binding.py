@@ -25,7 +25,10 @@ DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 EXPORTS = ["df_attn_workspace_size", "df_attn_fwd", "df_attn_bwd", "df_attn_step_host_arena_size",
            "df_attn_step_host", "df_rel_index_table", "df_get_device_error", "df_status_string", "df_version",
            "df_attn_set_profile_events", "df_attn_fwd_noalloc", "df_attn_debug_inject_stall",
-           "df_dropout_keep_mask", "df_attn_fwd_inference", "df_attn_fwd_noalloc_device_error"]
+           "df_dropout_keep_mask", "df_attn_fwd_inference", "df_attn_fwd_noalloc_device_error",
+           "df_pack_workspace_size", "df_pack_info", "df_pack_rows", "df_unpack_rows",
+           "df_qkv_proj_fwd", "df_qkv_proj_bwd", "df_rel_proj_workspace_size", "df_rel_proj_fwd",
+           "df_rel_proj_bwd"]
 
 
 class DfError(RuntimeError):
@@ -93,6 +96,26 @@ def load():
             lib.df_dropout_keep_mask.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp]
             lib.df_attn_debug_inject_stall.restype = ctypes.c_int
             lib.df_attn_debug_inject_stall.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32]
+            lib.df_pack_workspace_size.restype = sz
+            lib.df_pack_workspace_size.argtypes = [ctypes.c_int32]
+            lib.df_pack_info.restype = ctypes.c_int
+            lib.df_pack_info.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp, sz, vp]
+            lib.df_pack_rows.restype = ctypes.c_int
+            lib.df_pack_rows.argtypes = [vp, ctypes.c_int32, vp, vp, ctypes.c_int32, sz, vp, vp]
+            lib.df_unpack_rows.restype = ctypes.c_int
+            lib.df_unpack_rows.argtypes = [vp, vp, vp, ctypes.c_int32, sz, ctypes.c_int32, vp, vp]
+            i32 = ctypes.c_int32
+            lib.df_qkv_proj_fwd.restype = ctypes.c_int
+            lib.df_qkv_proj_fwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp]
+            lib.df_qkv_proj_bwd.restype = ctypes.c_int
+            lib.df_qkv_proj_bwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp, vp, i32, vp]
+            lib.df_rel_proj_workspace_size.restype = sz
+            lib.df_rel_proj_workspace_size.argtypes = [i32] * 4
+            lib.df_rel_proj_fwd.restype = ctypes.c_int
+            lib.df_rel_proj_fwd.argtypes = [i32] * 4 + [ctypes.c_int, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
+                                                        vp, vp, vp]
+            lib.df_rel_proj_bwd.restype = ctypes.c_int
+            lib.df_rel_proj_bwd.argtypes = [i32] * 4 + [ctypes.c_int] + [vp] * 12 + [i32, vp, sz, vp]
             lib.df_attn_set_profile_events.restype = ctypes.c_int
             lib.df_attn_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
             _lib = lib
@@ -304,3 +327,142 @@ def dropout_keep_mask(g: Geometry, dtype: torch.dtype, b: int, h: int, form: int
 def noalloc_device_error(stream=None) -> int:
     """Error word of df_attn_fwd_noalloc's static scratch on the current device."""
     return int(load().df_attn_fwd_noalloc_device_error(_stream(stream)))
+
+
+@dataclass
+class PackInfo:
+    """What df_pack_info found for a padded batch (device tensors plus the
+    three counts read back to the host)."""
+    cu_seqlens: torch.Tensor   # device int32 [nseq + 1]
+    index: torch.Tensor        # device int32 [total]: padded row b * L + l of each packed row
+    total: int
+    max_seqlen: int
+    nseq: int
+    B: int
+    L: int
+
+
+def pack_info(mask: torch.Tensor, stream=None) -> PackInfo:
+    """Sequence offsets and row index of the packed layout of a padded batch
+    (mask [B, L], device, nonzero = valid), via df_pack_info.  Reads the three
+    counts back to the host (one synchronisation)."""
+    B, L = mask.shape
+    m = mask.to(torch.uint8).contiguous()
+    dev = m.device
+    cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    index = torch.empty(B * L, dtype=torch.int32, device=dev)
+    info = torch.empty(4, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(int(load().df_pack_workspace_size(B)), 16), dtype=torch.uint8, device=dev)
+    rc = load().df_pack_info(_ptr(m), B, L, _ptr(cu), _ptr(index), _ptr(info), _ptr(ws), ws.numel(),
+                             _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_pack_info")
+    total, longest, nseq = (int(v) for v in info[:3].cpu())
+    return PackInfo(cu[:nseq + 1], index[:total], total, longest, nseq, B, L)
+
+
+def _rows(x: torch.Tensor, lead: int):
+    return x.numel() // lead * x.element_size()
+
+
+def pack_rows(x: torch.Tensor, pi: PackInfo, stream=None) -> torch.Tensor:
+    """[B, L, ...] -> [total, ...]: the valid rows, sequence after sequence."""
+    x = x.contiguous()
+    out = torch.empty((pi.total,) + tuple(x.shape[2:]), dtype=x.dtype, device=x.device)
+    if pi.total == 0:
+        return out
+    info = torch.tensor([pi.total, pi.max_seqlen, pi.nseq, 0], dtype=torch.int32, device=x.device)
+    rc = load().df_pack_rows(_ptr(x), pi.B * pi.L, _ptr(pi.index), _ptr(info), pi.total, _rows(x, pi.B * pi.L),
+                             _ptr(out), _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_pack_rows")
+    return out
+
+
+def unpack_rows(packed: torch.Tensor, pi: PackInfo, stream=None) -> torch.Tensor:
+    """[total, ...] -> [B, L, ...] with zero rows at the padding."""
+    packed = packed.contiguous()
+    out = torch.empty((pi.B, pi.L) + tuple(packed.shape[1:]), dtype=packed.dtype, device=packed.device)
+    row_bytes = _rows(out, pi.B * pi.L)
+    if pi.total == 0:
+        return out.zero_()
+    info = torch.tensor([pi.total, pi.max_seqlen, pi.nseq, 0], dtype=torch.int32, device=packed.device)
+    rc = load().df_unpack_rows(_ptr(packed), _ptr(pi.index), _ptr(info), pi.total, row_bytes, pi.B * pi.L,
+                               _ptr(out), _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_unpack_rows")
+    return out
+
+
+def pack_padded_with_info(x: torch.Tensor, mask: torch.Tensor, stream=None):
+    """Pack a padded batch x [B, L, ...] by its mask [B, L]: (packed, PackInfo)."""
+    pi = pack_info(mask, stream)
+    return pack_rows(x, pi, stream), pi
+
+
+def unpack_packed(packed: torch.Tensor, pi: PackInfo, stream=None) -> torch.Tensor:
+    """Inverse of pack_padded_with_info: [total, ...] -> [B, L, ...], zero at the padding."""
+    return unpack_rows(packed, pi, stream)
+
+
+def qkv_proj_fwd(x, w, bias=None, stream=None):
+    """Fused QKV projection (df_qkv_proj_fwd): x [T, C], w [3, H*D, C], bias
+    [3, H*D] -> qkv [3, T, H*D] (Q, K, V back to back)."""
+    T, C = x.shape
+    HD = w.shape[1]
+    qkv = torch.empty((3, T, HD), dtype=x.dtype, device=x.device)
+    rc = load().df_qkv_proj_fwd(T, C, HD, DTYPE_CODE[x.dtype], _ptr(x), _ptr(w), _ptr(bias), _ptr(qkv),
+                                _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_qkv_proj_fwd")
+    return qkv
+
+
+def qkv_proj_bwd(x, w, dqkv, with_bias=True, dw=None, dbias=None, accumulate=False, stream=None):
+    """Backward of qkv_proj_fwd (df_qkv_proj_bwd): returns (dx, dw, dbias)."""
+    T, C = x.shape
+    HD = w.shape[1]
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(w) if dw is None else dw
+    if with_bias and dbias is None:
+        dbias = torch.empty((3, HD), dtype=x.dtype, device=x.device)
+    rc = load().df_qkv_proj_bwd(T, C, HD, DTYPE_CODE[x.dtype], _ptr(x), _ptr(w), _ptr(dqkv), _ptr(dx), _ptr(dw),
+                                _ptr(dbias if with_bias else None), 1 if accumulate else 0, _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_qkv_proj_bwd")
+    return dx, dw, dbias
+
+
+def rel_proj_fwd(rel, gamma, beta, eps, w, bias, H, D, stream=None):
+    """Relative projections (df_rel_proj_fwd): returns (qr [H, R, D], kr, rel_ln, ln_stats)."""
+    R, C = rel.shape
+    dev = rel.device
+    rel_ln = torch.empty_like(rel)
+    stats = torch.empty((R, 2), dtype=torch.float32, device=dev)
+    qr = torch.empty((H, R, D), dtype=rel.dtype, device=dev)
+    kr = torch.empty_like(qr)
+    rc = load().df_rel_proj_fwd(R, C, H, D, DTYPE_CODE[rel.dtype], _ptr(rel), _ptr(gamma), _ptr(beta), float(eps),
+                                _ptr(w), _ptr(bias), _ptr(rel_ln), _ptr(stats), _ptr(qr), _ptr(kr), _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_rel_proj_fwd")
+    return qr, kr, rel_ln, stats
+
+
+def rel_proj_bwd(rel, gamma, rel_ln, stats, w, dqr, dkr, dw, dbias=None, dgamma=None, dbeta=None,
+                 accumulate=False, stream=None):
+    """Backward of rel_proj_fwd (df_rel_proj_bwd): returns (drel, dgamma, dbeta);
+    dw / dbias rows q and k are written (or, accumulate, added to)."""
+    R, C = rel.shape
+    H, _, D = dqr.shape
+    drel = torch.empty_like(rel)
+    # with accumulate the library adds to dgamma / dbeta too: fresh buffers start at zero
+    dgamma = torch.zeros_like(gamma) if dgamma is None else dgamma
+    dbeta = torch.zeros_like(gamma) if dbeta is None else dbeta
+    ws = torch.empty(int(load().df_rel_proj_workspace_size(R, C, H, D)), dtype=torch.uint8, device=rel.device)
+    rc = load().df_rel_proj_bwd(R, C, H, D, DTYPE_CODE[rel.dtype], _ptr(rel), _ptr(gamma), _ptr(rel_ln),
+                                _ptr(stats), _ptr(w), _ptr(dqr), _ptr(dkr), _ptr(drel), _ptr(dgamma), _ptr(dbeta),
+                                _ptr(dw), _ptr(dbias), 1 if accumulate else 0, _ptr(ws), ws.numel(),
+                                _stream(stream))
+    if rc != DF_OK:
+        raise DfError(rc, "df_rel_proj_bwd")
+    return drel, dgamma, dbeta

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libdfattn.so")
-SOURCES = ["df_host.cu", "df_aux.cu", "df_fp32.cu", "df_fwd.cu", "df_bwd.cu", "df_bwd_dq.cu", "df_bwd_dkv.cu", "df_rel.cu", "df_noalloc.cu"]
+SOURCES = ["df_host.cu", "df_aux.cu", "df_fp32.cu", "df_fwd.cu", "df_bwd.cu", "df_bwd_dq.cu", "df_bwd_dkv.cu", "df_rel.cu", "df_noalloc.cu", "df_pack.cu", "df_proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
@@ -55,7 +55,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublasLt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -210,6 +210,83 @@ df_status df_attn_fwd_noalloc(const df_attn_params *p, const void *q, const void
 df_status df_attn_fwd_noalloc_device_error(df_stream_t stream);
 
 /*
+ * Packing ("DisentangledFlash", section "Packed unpadded inference and
+ * training": pack_padded_with_info / unpack_packed).  A padded batch of B
+ * sequences of L positions with a padding mask [B, L] (device bytes, 0 =
+ * padding) becomes the packed layout: the valid positions of each sequence in
+ * order, sequence after sequence; a sequence without any valid position is
+ * dropped.  With right padding (every sequence's valid positions first),
+ * attention over the packed layout equals the masked padded attention on the
+ * valid rows; other masks move positions, and with them relative positions.
+ *
+ * df_pack_info writes, on the device and asynchronously on `stream`:
+ *   cu_seqlens [B + 1] int32: offsets of the non-empty sequences (the first
+ *     info[2] + 1 entries are used);
+ *   index [B * L] int32: index[t] = b * L + l, the padded row of packed row t
+ *     (the first info[0] entries are used);
+ *   info [3] int32: total packed tokens, longest sequence, non-empty sequences
+ *     (read it back for the attention's total_tokens, L and B).
+ * workspace: df_pack_workspace_size(B) bytes, 4-byte aligned.
+ *
+ * df_pack_rows: packed[t] = padded[index[t]] for t < min(info[0], max_rows),
+ *   rows of row_bytes bytes (a multiple of 16, both buffers 16-byte aligned);
+ *   padded has padded_rows rows (an index outside them gives a zero row).
+ * df_unpack_rows: padded[index[t]] = packed[t] for t < min(info[0],
+ *   max_rows); every other of the padded_rows rows is zero.
+ * All three are deterministic (no atomics on the data).
+ */
+size_t df_pack_workspace_size(int32_t B);
+df_status df_pack_info(const uint8_t *mask, int32_t B, int32_t L, int32_t *cu_seqlens, int32_t *index,
+                       int32_t *info, void *workspace, size_t workspace_bytes, df_stream_t stream);
+df_status df_pack_rows(const void *padded, int32_t padded_rows, const int32_t *index, const int32_t *info,
+                       int32_t max_rows, size_t row_bytes, void *packed, df_stream_t stream);
+df_status df_unpack_rows(const void *packed, const int32_t *index, const int32_t *info, int32_t max_rows,
+                         size_t row_bytes, int32_t padded_rows, void *padded, df_stream_t stream);
+
+/*
+ * The steps on either side of the attention ("DisentangledFlash", section
+ * "Status": the fused QKV projection is always on; section "Hugging Face
+ * usage": the query / key / value and relative-position projections stay in
+ * the autograd graph).  DeBERTa-v2/v3 with shared attention keys: one weight
+ * w = [W_q; W_k; W_v] ([3, H*D, C], row-major, rows of head h at h*D) and
+ * bias b = [b_q; b_k; b_v] ([3, H*D], or NULL) project the hidden states, and
+ * W_q, W_k with b_q, b_k also project the layer-normalised relative
+ * embeddings.  bf16 / fp16 storage, fp32 accumulation (cuBLASLt products
+ * without workspace, small kernels for the layer norm and the sums, which
+ * run in a fixed order).  Device pointers 16-byte aligned; C, H*D and D
+ * multiples of 8.  Nothing is allocated.
+ *
+ * df_qkv_proj_fwd: qkv [3, T, H*D] = x [T, C] W_j^T + b_j for j = q, k, v (Q,
+ *   K, V back to back, each in the [T, H, D] layout of df_attn_fwd).
+ * df_qkv_proj_bwd: from dqkv [3, T, H*D]: dx [T, C] = sum_j dY_j W_j (j in
+ *   order); dw [3, H*D, C] (+)= dY_j^T x; dbias [3, H*D] (+)= sum_t dY_j[t]
+ *   (skipped when NULL); `accumulate` != 0 adds to dw / dbias.
+ * df_rel_proj_fwd: rel_ln [R, C] = LayerNorm(rel [R, C]; gamma, beta, eps)
+ *   (kept for the backward, with ln_stats [R, 2] fp32 = mean, 1/std);
+ *   qr[h] = rel_ln W_q[h]^T + b_q[h], kr[h] = rel_ln W_k[h]^T + b_k[h] ([H, R,
+ *   D], the layout of df_attn_fwd).  rel holds the R = 2 * att_span rows of
+ *   the relative-embedding table the attention uses.
+ * df_rel_proj_bwd: from dqr, dkr [H, R, D]: drel [R, C]; dgamma, dbeta [C];
+ *   rows q and k of dw [3, H*D, C] and of dbias [3, H*D] (NULL: skipped);
+ *   `accumulate` != 0 adds to dgamma, dbeta, dw and dbias (after
+ *   df_qkv_proj_bwd, for the shared weights).  workspace:
+ *   df_rel_proj_workspace_size bytes.
+ */
+df_status df_qkv_proj_fwd(int32_t T, int32_t C, int32_t HD, df_dtype dtype, const void *x, const void *w,
+                          const void *bias, void *qkv, df_stream_t stream);
+df_status df_qkv_proj_bwd(int32_t T, int32_t C, int32_t HD, df_dtype dtype, const void *x, const void *w,
+                          const void *dqkv, void *dx, void *dw, void *dbias, int32_t accumulate, df_stream_t stream);
+size_t df_rel_proj_workspace_size(int32_t R, int32_t C, int32_t H, int32_t D);
+df_status df_rel_proj_fwd(int32_t R, int32_t C, int32_t H, int32_t D, df_dtype dtype, const void *rel,
+                          const void *gamma, const void *beta, float eps, const void *w, const void *bias,
+                          void *rel_ln, float *ln_stats, void *qr, void *kr, df_stream_t stream);
+df_status df_rel_proj_bwd(int32_t R, int32_t C, int32_t H, int32_t D, df_dtype dtype, const void *rel,
+                          const void *gamma, const void *rel_ln, const float *ln_stats, const void *w,
+                          const void *dqr, const void *dkr, void *drel, void *dgamma, void *dbeta, void *dw,
+                          void *dbias, int32_t accumulate, void *workspace, size_t workspace_bytes,
+                          df_stream_t stream);
+
+/*
  * The relative-position index table delta(r) for r = -(L-1) .. L-1, written
  * as int32 to out_dev[r + L - 1] (device, 2L - 1 entries), computed on the
  * device exactly as the attention kernels use it.  For bit-exact checks.

@@ -261,3 +261,74 @@ def step_rows_sample(prob: Problem, pairs, r0: int, r1: int, q, k, v, qr, kr, do
     return float(_load().orc_step_rows_sample(ctypes.byref(c), len(pr) // 2, pr.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
                                               int(r0), int(r1), _dp(q), _dp(k), _dp(v), _dp(qr), _dp(kr), _dp(dout),
                                               int(nthreads)))
+
+
+# --------------------------------------------------------------------------
+# The steps on either side of the attention: the fused QKV projection and
+# the relative-position projections (DeBERTa-v2/v3 with shared attention
+# keys), written from their definitions in float64 numpy.  "DisentangledFlash",
+# section "Status" (the fused QKV projection) and section "Hugging Face usage"
+# (the query / key / value and relative-position projections in the autograd
+# graph).  The backward functions are the plain calculus of the forward ones.
+
+def qkv_projection(x, w, b=None):
+    """[Q; K; V] = x W_j^T + b_j: x [T, C], w [3, HD, C], b [3, HD] -> [3, T, HD]."""
+    x, w = _f64(x), _f64(w)
+    y = np.einsum("tc,jnc->jtn", x, w)
+    if b is not None:
+        y = y + _f64(b)[:, None, :]
+    return y
+
+
+def qkv_projection_backward(x, w, dy):
+    """Gradients of qkv_projection for dy [3, T, HD]: dx [T, C] = sum_j dy_j W_j,
+    dw [3, HD, C] = dy_j^T x, db [3, HD] = sum_t dy_j[t]."""
+    x, w, dy = _f64(x), _f64(w), _f64(dy)
+    dx = np.einsum("jtn,jnc->tc", dy, w)
+    dw = np.einsum("jtn,tc->jnc", dy, x)
+    db = dy.sum(axis=1)
+    return dx, dw, db
+
+
+def layer_norm(x, gamma, beta, eps):
+    """Row-wise layer norm of x [R, C]: (x - mean) / sqrt(var + eps) gamma + beta
+    (biased variance); also returns mean and 1/std."""
+    x = _f64(x)
+    mean = x.mean(axis=1, keepdims=True)
+    var = ((x - mean) ** 2).mean(axis=1, keepdims=True)
+    rstd = 1.0 / np.sqrt(var + eps)
+    return (x - mean) * rstd * _f64(gamma) + _f64(beta), mean[:, 0], rstd[:, 0]
+
+
+def rel_projection(rel, gamma, beta, eps, w, b, H, D):
+    """E = LayerNorm(rel); Qr[h] = E W_q[h]^T + b_q[h], Kr[h] = E W_k[h]^T + b_k[h]
+    with W_q = w[0], W_k = w[1] ([HD, C], head h = rows h D .. h D + D).
+    Returns (E [R, C], Qr [H, R, D], Kr [H, R, D])."""
+    e, _, _ = layer_norm(rel, gamma, beta, eps)
+    w = _f64(w)
+    out = []
+    for j in (0, 1):
+        y = e @ w[j].T                                   # [R, HD]
+        if b is not None:
+            y = y + _f64(b)[j][None, :]
+        out.append(y.reshape(e.shape[0], H, D).transpose(1, 0, 2))
+    return e, out[0], out[1]
+
+
+def rel_projection_backward(rel, gamma, beta, eps, w, dqr, dkr, H, D):
+    """Gradients of rel_projection for dqr, dkr [H, R, D]: drel [R, C],
+    dgamma [C], dbeta [C], dw_qk [2, HD, C], db_qk [2, HD]."""
+    x = _f64(rel)
+    e, mean, rstd = layer_norm(x, gamma, beta, eps)
+    w = _f64(w)
+    R, C = x.shape
+    g_rows = [_f64(d).transpose(1, 0, 2).reshape(R, H * D) for d in (dqr, dkr)]   # [R, HD]
+    dw = np.stack([g.T @ e for g in g_rows])
+    db = np.stack([g.sum(axis=0) for g in g_rows])
+    de = g_rows[0] @ w[0] + g_rows[1] @ w[1]              # dL/dE  [R, C]
+    xh = (x - mean[:, None]) * rstd[:, None]
+    dbeta = de.sum(axis=0)
+    dgamma = (de * xh).sum(axis=0)
+    g = de * _f64(gamma)
+    drel = rstd[:, None] * (g - g.mean(axis=1, keepdims=True) - xh * (g * xh).mean(axis=1, keepdims=True))
+    return drel, dgamma, dbeta, dw, db

@@ -134,3 +134,22 @@ def test_bucket_step_rule_matches_the_relative_index_table(lib, nb):
         g = geom(nb=nb, mp=mp, span=span, L=2048)
         assert (B.workspace_size(g, torch.bfloat16, True) > 0) == unit, (nb, mp)
         assert B.workspace_size(g, torch.float32, True) > 0
+
+
+def test_packing_validation_codes(lib):
+    """df_pack_info / df_pack_rows / df_unpack_rows check their arguments on
+    the host and return a status before any device work."""
+    vp = ctypes.c_void_p
+    a, w = vp(0x10000), vp(0x20000)
+    assert lib.df_pack_workspace_size(0) == 0 and lib.df_pack_workspace_size(5) >= 40
+    assert lib.df_pack_info(a, 0, 8, a, a, a, w, 1 << 20, None) == B.DF_ERR_INVALID_ARG
+    assert lib.df_pack_info(a, 2, 0, a, a, a, w, 1 << 20, None) == B.DF_ERR_INVALID_ARG
+    assert lib.df_pack_info(None, 2, 8, a, a, a, w, 1 << 20, None) == B.DF_ERR_INVALID_ARG
+    assert lib.df_pack_info(a, 2, 8, a, a, a, None, 0, None) == B.DF_ERR_WORKSPACE
+    assert lib.df_pack_info(a, 2, 8, a, a, a, w, 4, None) == B.DF_ERR_WORKSPACE
+    assert lib.df_pack_info(a, 1 << 16, 1 << 16, a, a, a, w, 1 << 30, None) == B.DF_ERR_UNSUPPORTED
+    assert lib.df_pack_rows(a, 16, a, a, 16, 24, a, None) == B.DF_ERR_INVALID_ARG        # 24-byte rows
+    assert lib.df_pack_rows(vp(0x10008), 16, a, a, 16, 32, a, None) == B.DF_ERR_INVALID_ARG   # unaligned
+    assert lib.df_pack_rows(a, 16, a, a, 0, 32, a, None) == B.DF_ERR_INVALID_ARG
+    assert lib.df_unpack_rows(a, a, a, 16, 32, 0, a, None) == B.DF_ERR_INVALID_ARG
+    assert lib.df_unpack_rows(a, None, a, 16, 32, 16, a, None) == B.DF_ERR_INVALID_ARG

@@ -27,7 +27,7 @@ EXPORTS = ["df_attn_workspace_size", "df_attn_fwd", "df_attn_bwd", "df_attn_step
            "df_attn_set_profile_events", "df_attn_fwd_noalloc", "df_attn_debug_inject_stall",
            "df_dropout_keep_mask", "df_attn_fwd_inference", "df_attn_fwd_noalloc_device_error",
            "df_pack_workspace_size", "df_pack_info", "df_pack_rows", "df_unpack_rows",
-           "df_qkv_proj_fwd", "df_qkv_proj_bwd", "df_rel_proj_workspace_size", "df_rel_proj_fwd",
+           "df_qkv_proj_fwd", "df_qkv_proj_bwd", "df_qkv_proj_workspace_size", "df_rel_proj_workspace_size", "df_rel_proj_fwd",
            "df_rel_proj_bwd"]
 
 
@@ -108,7 +108,9 @@ def load():
             lib.df_qkv_proj_fwd.restype = ctypes.c_int
             lib.df_qkv_proj_fwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp]
             lib.df_qkv_proj_bwd.restype = ctypes.c_int
-            lib.df_qkv_proj_bwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp, vp, i32, vp]
+            lib.df_qkv_proj_bwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+            lib.df_qkv_proj_workspace_size.restype = sz
+            lib.df_qkv_proj_workspace_size.argtypes = [i32]
             lib.df_rel_proj_workspace_size.restype = sz
             lib.df_rel_proj_workspace_size.argtypes = [i32] * 4
             lib.df_rel_proj_fwd.restype = ctypes.c_int
@@ -426,8 +428,10 @@ def qkv_proj_bwd(x, w, dqkv, with_bias=True, dw=None, dbias=None, accumulate=Fal
     dw = torch.empty_like(w) if dw is None else dw
     if with_bias and dbias is None:
         dbias = torch.empty((3, HD), dtype=x.dtype, device=x.device)
+    ws = torch.empty(int(load().df_qkv_proj_workspace_size(HD)), dtype=torch.uint8, device=x.device)
     rc = load().df_qkv_proj_bwd(T, C, HD, DTYPE_CODE[x.dtype], _ptr(x), _ptr(w), _ptr(dqkv), _ptr(dx), _ptr(dw),
-                                _ptr(dbias if with_bias else None), 1 if accumulate else 0, _stream(stream))
+                                _ptr(dbias if with_bias else None), 1 if accumulate else 0, _ptr(ws), ws.numel(),
+                                _stream(stream))
     if rc != DF_OK:
         raise DfError(rc, "df_qkv_proj_bwd")
     return dx, dw, dbias

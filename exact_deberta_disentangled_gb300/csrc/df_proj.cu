@@ -171,29 +171,65 @@ __global__ void layernorm_bwd_kernel(const T* __restrict__ x, const T* __restric
     }
 }
 
-// Column sums of `nmat` matrices a[j] ([R, C] each, j-th at a + j * sa), rows in
-// order, fp32: out[j * C + c] (+)= sum_r a[j][r, c].  With xs (the layer
-// norm's input) also out2[c] (+)= sum_r a[r, c] xh[r, c] (the gamma gradient).
+// Column sums in two passes, both in a fixed order (so the result is
+// deterministic) and with enough threads to stream the matrix:
+//   pass 1: part[k][0][col] = sum of rows in chunk k of column col, where
+//           col = j * C + c addresses column c of matrix a[j] ([R, C] at
+//           a + j * sa); with xs (the layer norm's input) also
+//           part[k][1][col] = sum over the chunk of a[r, c] xh[r, c]
+//   pass 2: out[col] (+)= sum over k of part[k][0][col] (k ascending), and
+//           out2[c] (+)= sum over k of part[k][1][c]
+constexpr int kColChunks = 64;
+
 template <typename TA, typename T>
-__global__ void colsum_kernel(const TA* __restrict__ a, long sa, int nmat, int R, int C, int accumulate,
-                              T* __restrict__ out, const T* __restrict__ xs, const float* __restrict__ stats,
-                              T* __restrict__ out2) {
-    const int col = blockIdx.x * blockDim.x + threadIdx.x;
-    if (col >= nmat * C) return;
+__global__ void colsum_part_kernel(const TA* __restrict__ a, long sa, int nmat, int R, int C, int rows_per,
+                                   const T* __restrict__ xs, const float* __restrict__ stats,
+                                   float* __restrict__ part) {
+    const int col = blockIdx.x * blockDim.x + threadIdx.x, k = blockIdx.y;
+    const int ncol = nmat * C;
+    if (col >= ncol) return;
     const int j = col / C, c = col % C;
     const TA* aj = a + (size_t)j * sa;
+    const int r0 = k * rows_per, r1 = min(R, r0 + rows_per);
     float s = 0.f, s2 = 0.f;
-    for (int r = 0; r < R; ++r) {
+    for (int r = r0; r < r1; ++r) {
         const float v = tof(aj[(size_t)r * C + c]);
         s += v;
         if (xs) s2 += v * (tof(xs[(size_t)r * C + c]) - stats[2 * r]) * stats[2 * r + 1];
     }
+    part[((size_t)k * 2) * ncol + col] = s;
+    part[((size_t)k * 2 + 1) * ncol + col] = s2;
+}
+
+template <typename T>
+__global__ void colsum_final_kernel(const float* __restrict__ part, int nchunk, int ncol, int accumulate,
+                                    T* __restrict__ out, T* __restrict__ out2) {
+    const int col = blockIdx.x * blockDim.x + threadIdx.x;
+    if (col >= ncol) return;
+    float s = 0.f, s2 = 0.f;
+    for (int k = 0; k < nchunk; ++k) {
+        s += part[((size_t)k * 2) * ncol + col];
+        s2 += part[((size_t)k * 2 + 1) * ncol + col];
+    }
     if (accumulate) s += tof(out[col]);
     out[col] = fromf<T>(s);
-    if (xs) {
-        if (accumulate) s2 += tof(out2[c]);
-        out2[c] = fromf<T>(s2);
+    if (out2) {
+        if (accumulate) s2 += tof(out2[col]);
+        out2[col] = fromf<T>(s2);
     }
+}
+
+size_t colsum_ws_bytes(int ncol) { return (size_t)kColChunks * 2 * (size_t)ncol * sizeof(float); }
+
+template <typename TA, typename T>
+void colsum(const TA* a, long sa, int nmat, int R, int C, int accumulate, T* out, const T* xs, const float* stats,
+            T* out2, float* part, cudaStream_t st) {
+    const int ncol = nmat * C;
+    const int nchunk = R < kColChunks ? R : kColChunks;
+    const int rows_per = (R + nchunk - 1) / nchunk;
+    colsum_part_kernel<TA, T><<<dim3((ncol + 127) / 128, nchunk), 128, 0, st>>>(a, sa, nmat, R, C, rows_per, xs, stats,
+                                                                               part);
+    colsum_final_kernel<T><<<(ncol + 127) / 128, 128, 0, st>>>(part, nchunk, ncol, accumulate, out, out2);
 }
 
 // [H, R, D] -> [R, H D]
@@ -227,6 +263,7 @@ df_status rel_bwd_impl(int R, int C, int H, int D, df_dtype dt, const void* rel,
     T* dq_t = reinterpret_cast<T*>(ws);
     T* dk_t = dq_t + (size_t)R * HD;
     float* de = reinterpret_cast<float*>(ws + 2 * sizeof(T) * (size_t)R * HD);
+    float* part = de + (size_t)R * C;
     const long n = (long)H * R * D;
     heads_to_rows_kernel<T><<<nblocks(n, 256), 256, 0, st>>>((const T*)dqr, H, R, D, dq_t);
     heads_to_rows_kernel<T><<<nblocks(n, 256), 256, 0, st>>>((const T*)dkr, H, R, D, dk_t);
@@ -238,11 +275,8 @@ df_status rel_bwd_impl(int R, int C, int H, int D, df_dtype dt, const void* rel,
         gemm(ab, ab, true, false, HD, C, R, dk_t, HD, 0, rel_ln, C, 0, b0, dW + (size_t)HD * C, C, 0, nullptr, 0, 1,
              st))
         return DF_ERR_CUDA;
-    if (dbias) {
-        colsum_kernel<T, T><<<nblocks(HD, 128), 128, 0, st>>>(dq_t, 0, 1, R, HD, acc, (T*)dbias, nullptr, nullptr,
-                                                              nullptr);
-        colsum_kernel<T, T><<<nblocks(HD, 128), 128, 0, st>>>(dk_t, 0, 1, R, HD, acc, (T*)dbias + HD, nullptr,
-                                                              nullptr, nullptr);
+    if (dbias) {   // rows q and k of dbias: the two transposed gradients are adjacent ([2, R, HD])
+        colsum<T, T>(dq_t, (long)R * HD, 2, R, HD, acc, (T*)dbias, (const T*)nullptr, nullptr, (T*)nullptr, part, st);
     }
     // dE = dQr_t W_q + dKr_t W_k    ([R, HD] x [HD, C], fp32)
     if (gemm(ab, CUDA_R_32F, false, false, R, C, HD, dq_t, HD, 0, W, C, 0, 0.f, de, C, 0, nullptr, 0, 1, st) ||
@@ -250,8 +284,7 @@ df_status rel_bwd_impl(int R, int C, int H, int D, df_dtype dt, const void* rel,
              0, 1, st))
         return DF_ERR_CUDA;
     layernorm_bwd_kernel<T><<<nblocks(R, 8), 256, 0, st>>>((const T*)rel, (const T*)gamma, stats, de, R, C, (T*)drel);
-    colsum_kernel<float, T><<<nblocks(C, 128), 128, 0, st>>>(de, 0, 1, R, C, acc, (T*)dbeta, (const T*)rel, stats,
-                                                             (T*)dgamma);
+    colsum<float, T>(de, 0, 1, R, C, acc, (T*)dbeta, (const T*)rel, stats, (T*)dgamma, part, st);
     return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
@@ -275,12 +308,17 @@ df_status df_qkv_proj_fwd(int32_t T, int32_t C, int32_t HD, df_dtype dt, const v
     return DF_OK;
 }
 
+size_t df_qkv_proj_workspace_size(int32_t HD) { return HD < 1 ? 0 : colsum_ws_bytes(3 * HD); }
+
 df_status df_qkv_proj_bwd(int32_t T, int32_t C, int32_t HD, df_dtype dt, const void* x, const void* w,
-                          const void* dqkv, void* dx, void* dw, void* dbias, int32_t accumulate, df_stream_t stream) {
+                          const void* dqkv, void* dx, void* dw, void* dbias, int32_t accumulate, void* workspace,
+                          size_t workspace_bytes, df_stream_t stream) {
     if (T < 1 || C < 1 || HD < 1 || !x || !w || !dqkv || !dx || !dw) return DF_ERR_INVALID_ARG;
     if (dt != DF_BF16 && dt != DF_FP16) return DF_ERR_UNSUPPORTED;
     if (!al16(x) || !al16(w) || !al16(dqkv) || !al16(dx) || !al16(dw) || (dbias && !al16(dbias)) || C % 8 || HD % 8)
         return DF_ERR_INVALID_ARG;
+    if (dbias && (!workspace || !al16(workspace) || workspace_bytes < df_qkv_proj_workspace_size(HD)))
+        return DF_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     const cudaDataType_t ab = cuda_type(dt);
     const size_t es = 2;
@@ -296,20 +334,22 @@ df_status df_qkv_proj_bwd(int32_t T, int32_t C, int32_t HD, df_dtype dt, const v
              (long)HD * C, nullptr, 0, 3, st))
         return DF_ERR_CUDA;
     if (dbias) {
+        float* part = (float*)workspace;
         if (dt == DF_BF16)
-            colsum_kernel<__nv_bfloat16, __nv_bfloat16><<<nblocks(3L * HD, 128), 128, 0, st>>>(
-                (const __nv_bfloat16*)dqkv, (long)T * HD, 3, T, HD, accumulate, (__nv_bfloat16*)dbias, nullptr,
-                nullptr, nullptr);
+            colsum<__nv_bfloat16, __nv_bfloat16>((const __nv_bfloat16*)dqkv, (long)T * HD, 3, T, HD, accumulate,
+                                                 (__nv_bfloat16*)dbias, (const __nv_bfloat16*)nullptr, nullptr,
+                                                 (__nv_bfloat16*)nullptr, part, st);
         else
-            colsum_kernel<__half, __half><<<nblocks(3L * HD, 128), 128, 0, st>>>(
-                (const __half*)dqkv, (long)T * HD, 3, T, HD, accumulate, (__half*)dbias, nullptr, nullptr, nullptr);
+            colsum<__half, __half>((const __half*)dqkv, (long)T * HD, 3, T, HD, accumulate, (__half*)dbias,
+                                   (const __half*)nullptr, nullptr, (__half*)nullptr, part, st);
     }
     return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
 size_t df_rel_proj_workspace_size(int32_t R, int32_t C, int32_t H, int32_t D) {
     if (R < 1 || C < 1 || H < 1 || D < 1) return 0;
-    return 2 * 2 * (size_t)R * H * D + 4 * (size_t)R * C;
+    const int ncol = 2 * H * D > C ? 2 * H * D : C;
+    return 2 * 2 * (size_t)R * H * D + 4 * (size_t)R * C + colsum_ws_bytes(ncol);
 }
 
 df_status df_rel_proj_fwd(int32_t R, int32_t C, int32_t H, int32_t D, df_dtype dt, const void* rel, const void* gamma,

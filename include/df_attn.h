@@ -260,7 +260,9 @@ df_status df_unpack_rows(const void *packed, const int32_t *index, const int32_t
  *   K, V back to back, each in the [T, H, D] layout of df_attn_fwd).
  * df_qkv_proj_bwd: from dqkv [3, T, H*D]: dx [T, C] = sum_j dY_j W_j (j in
  *   order); dw [3, H*D, C] (+)= dY_j^T x; dbias [3, H*D] (+)= sum_t dY_j[t]
- *   (skipped when NULL); `accumulate` != 0 adds to dw / dbias.
+ *   (skipped when NULL; then the workspace may be NULL); `accumulate` != 0
+ *   adds to dw / dbias.  workspace: df_qkv_proj_workspace_size(H*D) bytes
+ *   (fp32 partial column sums).
  * df_rel_proj_fwd: rel_ln [R, C] = LayerNorm(rel [R, C]; gamma, beta, eps)
  *   (kept for the backward, with ln_stats [R, 2] fp32 = mean, 1/std);
  *   qr[h] = rel_ln W_q[h]^T + b_q[h], kr[h] = rel_ln W_k[h]^T + b_k[h] ([H, R,
@@ -274,8 +276,10 @@ df_status df_unpack_rows(const void *packed, const int32_t *index, const int32_t
  */
 df_status df_qkv_proj_fwd(int32_t T, int32_t C, int32_t HD, df_dtype dtype, const void *x, const void *w,
                           const void *bias, void *qkv, df_stream_t stream);
+size_t df_qkv_proj_workspace_size(int32_t HD);
 df_status df_qkv_proj_bwd(int32_t T, int32_t C, int32_t HD, df_dtype dtype, const void *x, const void *w,
-                          const void *dqkv, void *dx, void *dw, void *dbias, int32_t accumulate, df_stream_t stream);
+                          const void *dqkv, void *dx, void *dw, void *dbias, int32_t accumulate, void *workspace,
+                          size_t workspace_bytes, df_stream_t stream);
 size_t df_rel_proj_workspace_size(int32_t R, int32_t C, int32_t H, int32_t D);
 df_status df_rel_proj_fwd(int32_t R, int32_t C, int32_t H, int32_t D, df_dtype dtype, const void *rel,
                           const void *gamma, const void *beta, float eps, const void *w, const void *bias,

@@ -350,6 +350,36 @@ Arena arena_layout(const df_attn_params* a, const ProblemDev& p) {
 }
 }  // namespace
 
+namespace {
+// A copy stream and its events per device for df_attn_step_host, created on
+// first use with that device current: dO goes up while the forward runs, and
+// O and the LSE come down while the backward runs.  The events are shared by
+// every call on the device, so one call's enqueue sequence holds g_copy_mu.
+constexpr int kMaxCopyDevices = 64;
+std::mutex g_copy_mu;
+bool g_copy_tried[kMaxCopyDevices];
+cudaStream_t g_copy_st[kMaxCopyDevices];
+cudaEvent_t g_copy_ev[kMaxCopyDevices][4];   // start, dout up, forward done, out / lse down
+
+bool copy_stream(int dev, cudaStream_t& cs, cudaEvent_t*& ev) {
+    if (dev < 0 || dev >= kMaxCopyDevices) return false;
+    if (!g_copy_tried[dev]) {
+        g_copy_tried[dev] = true;
+        bool ok = cudaStreamCreateWithFlags(&g_copy_st[dev], cudaStreamNonBlocking) == cudaSuccess;
+        for (int i = 0; i < 4 && ok; ++i)
+            ok = cudaEventCreateWithFlags(&g_copy_ev[dev][i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            g_copy_st[dev] = nullptr;
+        }
+    }
+    if (!g_copy_st[dev]) return false;
+    cs = g_copy_st[dev];
+    ev = g_copy_ev[dev];
+    return true;
+}
+}  // namespace
+
 size_t df_attn_step_host_arena_size(const df_attn_params* a) {
     ProblemDev p;
     if (resolve(a, p) != DF_OK) return 0;
@@ -377,12 +407,25 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     auto h2d = [&](size_t off, const void* src, size_t n) {
         return cudaMemcpyAsync(base + off, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
     };
-    auto d2h = [&](void* dst, size_t off, size_t n) {
-        return cudaMemcpyAsync(dst, base + off, n, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    auto d2h = [&](void* dst, size_t off, size_t n, cudaStream_t s2) {
+        return cudaMemcpyAsync(dst, base + off, n, cudaMemcpyDeviceToHost, s2) == cudaSuccess;
     };
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DF_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_copy_mu);
+    cudaStream_t cs = nullptr;
+    cudaEvent_t* ev = nullptr;
+    const bool side = copy_stream(dev, cs, ev);
     df_attn_params dp = *a;
     bool ok = h2d(L.q, q, tok) && h2d(L.k, k, tok) && h2d(L.v, v, tok) && h2d(L.qr, qr, rel) &&
-              h2d(L.kr, kr, rel) && h2d(L.dout, dout, tok);
+              h2d(L.kr, kr, rel);
+    // dO is needed by the backward only: on the copy stream, during the forward
+    if (side)
+        ok = ok && cudaEventRecord(ev[0], st) == cudaSuccess && cudaStreamWaitEvent(cs, ev[0], 0) == cudaSuccess &&
+             cudaMemcpyAsync(base + L.dout, dout, tok, cudaMemcpyHostToDevice, cs) == cudaSuccess &&
+             cudaEventRecord(ev[1], cs) == cudaSuccess;
+    else
+        ok = ok && h2d(L.dout, dout, tok);
     if (ok && a->cu_seqlens) {
         ok = h2d(L.cu, a->cu_seqlens, sizeof(int32_t) * (size_t)(p.B + 1));
         dp.cu_seqlens = (const int32_t*)(base + L.cu);
@@ -400,12 +443,21 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     s = df_attn_fwd(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
                     (float*)(base + L.lse), base + L.ws, wsb, stream);
     if (s != DF_OK) return s;
+    // O and the LSE are final after the forward: down on the copy stream during the backward
+    if (side) {
+        ok = cudaEventRecord(ev[2], st) == cudaSuccess && cudaStreamWaitEvent(cs, ev[2], 0) == cudaSuccess &&
+             d2h(out, L.out, tok, cs) && d2h(lse, L.lse, lseb, cs) && cudaEventRecord(ev[3], cs) == cudaSuccess &&
+             cudaStreamWaitEvent(st, ev[1], 0) == cudaSuccess;
+        if (!ok) return DF_ERR_CUDA;
+    }
     s = df_attn_bwd(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
                     (const float*)(base + L.lse), base + L.dout, base + L.dq, base + L.dk, base + L.dv,
                     base + L.dqr, base + L.dkr, base + L.ws, wsb, stream);
     if (s != DF_OK) return s;
-    ok = d2h(out, L.out, tok) && d2h(lse, L.lse, lseb) && d2h(dq, L.dq, tok) && d2h(dk, L.dk, tok) &&
-         d2h(dv, L.dv, tok) && d2h(dqr, L.dqr, rel) && d2h(dkr, L.dkr, rel);
+    ok = d2h(dq, L.dq, tok, st) && d2h(dk, L.dk, tok, st) && d2h(dv, L.dv, tok, st) && d2h(dqr, L.dqr, rel, st) &&
+         d2h(dkr, L.dkr, rel, st);
+    if (!side) ok = ok && d2h(out, L.out, tok, st) && d2h(lse, L.lse, lseb, st);
+    else ok = ok && cudaStreamWaitEvent(st, ev[3], 0) == cudaSuccess;
     if (!ok) return DF_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return DF_ERR_CUDA;
     return df_get_device_error(base + L.ws, stream);

@@ -4,7 +4,8 @@ One step = df_attn_fwd + df_attn_bwd over one batch of the L=8192 length-sweep
 workload (B=2, H=12, D=64, bf16, att_span 256 -> R=512, buckets 256 / max
 relative positions 512, 16,384 tokens, N(0,1) synthetic inputs).  Throughput
 is counted with the pages' FLOP formula: BH(4L^2 D + 4LRD) forward plus
-BH(10L^2 D + 12LRD) backward.
+BH(10L^2 D + 12LRD) backward.  The forward saves the band bias for the
+backward (df_attn_params.band_bias), as a training step would.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -237,6 +238,7 @@ def run_gpu(args, rank, world, local_rank):
     B, L, H, D, R = x.B, x.L, w.H, w.D, w.R
     g = Bd.Geometry(B=B, L=L, H=H, D=D, span=w.span, nb=w.nb, mp=w.mp)
     q, k, v, qr, kr, do = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    g.band_bias = Bd.alloc_band_bias(g, q.dtype, dev)   # saved by the forward, read by the backward
     out = torch.empty_like(q)
     lse = torch.empty(g.lse_shape(), dtype=torch.float32, device=dev)
     grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(qr),
@@ -417,6 +419,7 @@ def time_phases(name, dev, iters, warmup, flush, **make_kw):
     if x.qmask is not None:
         g.query_mask, g.key_mask = x.qmask.to(dev), x.kmask.to(dev)
     q, k, v, qr, kr, do = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    g.band_bias = Bd.alloc_band_bias(g, q.dtype, dev)
     out = torch.empty_like(q)
     lse = torch.empty(g.lse_shape(), dtype=torch.float32, device=dev)
     grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(qr),
@@ -577,6 +580,7 @@ def run_profile_case(args, local_rank):
     x = synth.make_inputs(w, B=1)
     g = Bd.Geometry(B=x.B, L=x.L, H=w.H, D=w.D, span=w.span, nb=w.nb, mp=w.mp)
     q, k, v, qr, kr, do = [t.to(dev) for t in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    g.band_bias = Bd.alloc_band_bias(g, q.dtype, dev)
     out, lse, wsf = Bd.attn_fwd(g, q, k, v, qr, kr)
     grads, wsb = Bd.attn_bwd(g, q, k, v, qr, kr, out, lse, do)
     for _ in range(args.warmup + args.steps - 1):

@@ -28,7 +28,7 @@ EXPORTS = ["df_attn_workspace_size", "df_attn_fwd", "df_attn_bwd", "df_attn_step
            "df_dropout_keep_mask", "df_attn_fwd_inference", "df_attn_fwd_noalloc_device_error",
            "df_pack_workspace_size", "df_pack_info", "df_pack_rows", "df_unpack_rows",
            "df_qkv_proj_fwd", "df_qkv_proj_bwd", "df_qkv_proj_workspace_size", "df_rel_proj_workspace_size", "df_rel_proj_fwd",
-           "df_rel_proj_bwd"]
+           "df_rel_proj_bwd", "df_attn_band_bias_size"]
 
 
 class DfError(RuntimeError):
@@ -52,6 +52,7 @@ class Params(ctypes.Structure):
         ("philox_offset", ctypes.c_uint64),
         ("softmax_scale", ctypes.c_float),
         ("dtype", ctypes.c_int),
+        ("band_bias", ctypes.c_void_p),
     ]
 
 
@@ -71,6 +72,8 @@ def load():
             P = ctypes.POINTER(Params)
             lib.df_attn_workspace_size.restype = sz
             lib.df_attn_workspace_size.argtypes = [P, ctypes.c_int]
+            lib.df_attn_band_bias_size.restype = sz
+            lib.df_attn_band_bias_size.argtypes = [P]
             lib.df_attn_fwd.restype = ctypes.c_int
             lib.df_attn_fwd.argtypes = [P] + [vp] * 7 + [vp, sz, vp]
             lib.df_attn_fwd_inference.restype = ctypes.c_int
@@ -156,6 +159,7 @@ class Geometry:
     seed: int = 0
     offset: int = 0
     scale: float = 0.0
+    band_bias: Optional[torch.Tensor] = None    # saved band bias (device uint8, band_bias_size bytes)
 
     @property
     def R(self):
@@ -178,6 +182,7 @@ class Geometry:
         p.philox_offset = self.offset
         p.softmax_scale = self.scale
         p.dtype = DTYPE_CODE[dtype]
+        p.band_bias = None if self.band_bias is None else self.band_bias.data_ptr()
         return p
 
     def lse_shape(self):
@@ -187,6 +192,16 @@ class Geometry:
 def workspace_size(g: Geometry, dtype: torch.dtype, backward: bool) -> int:
     p = g.params(dtype)
     return int(load().df_attn_workspace_size(ctypes.byref(p), 1 if backward else 0))
+
+
+def band_bias_size(g: Geometry, dtype: torch.dtype) -> int:
+    p = g.params(dtype)
+    return int(load().df_attn_band_bias_size(ctypes.byref(p)))
+
+
+def alloc_band_bias(g: Geometry, dtype: torch.dtype, device="cuda") -> torch.Tensor:
+    """A saved-band-bias buffer for g (set g.band_bias to it before the forward)."""
+    return torch.empty(max(band_bias_size(g, dtype), 16), dtype=torch.uint8, device=device)
 
 
 def alloc_workspace(g: Geometry, dtype: torch.dtype, backward: bool, device="cuda") -> torch.Tensor:

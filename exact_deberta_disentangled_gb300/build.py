@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libdfattn.so")
-SOURCES = ["df_host.cu", "df_aux.cu", "df_fp32.cu", "df_fwd.cu", "df_bwd.cu", "df_bwd_dq.cu", "df_bwd_dkv.cu", "df_rel.cu", "df_noalloc.cu", "df_pack.cu", "df_proj.cu"]
+SOURCES = ["df_host.cu", "df_aux.cu", "df_fp32.cu", "df_fwd.cu", "df_bwd.cu", "df_bwd_dq.cu", "df_bwd_dkv.cu", "df_bias.cu", "df_rel.cu", "df_noalloc.cu", "df_pack.cu", "df_proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

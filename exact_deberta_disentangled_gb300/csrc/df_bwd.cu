@@ -1,6 +1,6 @@
 // df_bwd.cu -- the backward pass: clears the diagonal-sum buffers G / G',
-// runs the dQ kernel and the dK/dV kernel (df_bwd_kernel.cuh) and then the
-// relative-position gradients (df_rel.cu).
+// stores the band bias (df_bias.cu), runs the dQ kernel and the dK/dV kernel
+// (df_bwd_kernel.cuh) and then the relative-position gradients (df_rel.cu).
 //
 // "DisentangledFlash" (section "Hugging Face usage") splits the fused
 // backward into a dQ kernel and a dK/dV kernel; section "Performance" counts
@@ -58,9 +58,12 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
     cudaError_t ce = cudaMemsetAsync(ws.G, 0, gbytes, st);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(ws.Gp, 0, gbytes, st);
     if (ce != cudaSuccess) return (int)ce;
+    // the relative-position bias of every band block, read by both kernels
+    // (unless the forward saved it)
+    int e = p.saved_bias ? 0 : launch_band_bias(p, ws, dt, q, k, qr, kr, st);
+    if (e) return e;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
-    int e = 0;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         cudaStream_t side = nullptr;
@@ -70,11 +73,11 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
             cudaGetLastError();
             conc = false;   // both kernels on the caller's stream instead
         }
-        // dQ kernel: rows = queries (Q, dO), columns = keys (K, V); own band Kr, cross Qr
-        e = launch_bwd_dq(p, ws, dt, q, dout, k, v, kr, qr, ws.G, Rp, ws.acc32a, nullptr, lse, conc ? side : st);
+        // dQ kernel: rows = queries (Q, dO), columns = keys (K, V)
+        e = launch_bwd_dq(p, ws, dt, q, dout, k, v, ws.G, Rp, ws.acc32a, nullptr, lse, conc ? side : st);
         if (conc) cudaEventRecord(join, side);
-        // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO); own band Qr, cross Kr
-        if (!e) e = launch_bwd_dkv(p, ws, dt, k, v, q, dout, qr, kr, ws.Gp, Rp, ws.acc32b, dv, lse, st);
+        // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO)
+        if (!e) e = launch_bwd_dkv(p, ws, dt, k, v, q, dout, ws.Gp, Rp, ws.acc32b, dv, lse, st);
         // the caller's stream continues only after the dQ kernel too
         if (conc && cudaStreamWaitEvent(st, join, 0) != cudaSuccess && !e) e = (int)cudaErrorUnknown;
     }

@@ -6,9 +6,9 @@
 namespace df {
 
 int launch_bwd_dkv(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* r1, const void* r2, const void* c1,
-         const void* c2, const void* xr, const void* yr, void* Gbuf, int Rp, float* acc1, void* acc2,
+         const void* c2, void* Gbuf, int Rp, float* acc1, void* acc2,
          const float* lse, cudaStream_t st) {
-#define DF_ONE(D_, BF_, DR_) launch_one<D_, BF_, -1, DR_>(p, ws, r1, r2, c1, c2, xr, yr, Gbuf, Rp, acc1, acc2, lse, st)
+#define DF_ONE(D_, BF_, DR_) launch_one<D_, BF_, -1, DR_>(p, ws, r1, r2, c1, c2, Gbuf, Rp, acc1, acc2, lse, st)
 #define DF_DT(D_, DR_) (dt == DF_BF16 ? DF_ONE(D_, true, DR_) : DF_ONE(D_, false, DR_))
 #define DF_DROP(D_) (p.dropout ? DF_DT(D_, true) : DF_DT(D_, false))
     switch (p.D) {

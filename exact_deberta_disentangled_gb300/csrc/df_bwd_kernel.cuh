@@ -18,6 +18,12 @@
 // one owner CTA and every sum runs in a fixed order, so the result is
 // bitwise reproducible with no floating-point atomics.
 //
+// The relative-position part of a score is a per-row and a per-column
+// scalar in uniform tiles (the per-token table of df_aux.cu) and, in band
+// tiles, a value per pair read from the stored band bias (df_bias.cu writes
+// it before these kernels run): one tensor copy of the tile's bias box into a
+// double-buffered stage.
+//
 // G / G' ([T, H, Rp] in the input dtype) feed the relative-position
 // gradients (df_rel.cu):  dQ += G Kr,  dK += G' Qr,  dKr = sum G^T Q,
 // dQr = sum G'^T K.  A band tile adds its diagonal sums with TMA reduce-adds,
@@ -42,10 +48,10 @@ constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Tensor-memory columns (512 per CTA).  The fp32 S and dP of the tile being
-// processed sit in [256, 256 + 2 BN); the band products alias them.  The
-// 16-bit dZ and P~ that feed the dK / dQ / dV products have their own
-// columns, so the issuer can compute the next tile's S / dP as soon as the
-// softmax warps have read this tile's into registers.
+// processed sit in [256, 256 + 2 BN).  The 16-bit dZ and P~ that feed the
+// dK / dQ / dV products have their own columns, so the issuer can compute the
+// next tile's S / dP as soon as the softmax warps have read this tile's into
+// registers.
 template <int D>
 struct BwdTmem {
     using G = Geo<D>;
@@ -55,9 +61,7 @@ struct BwdTmem {
     static constexpr uint32_t A1 = D, A2 = D + D / 2;
     static constexpr uint32_t S = 256, P = 256 + G::BN;                 // fp32 S, dP
     static constexpr uint32_t Z = 2 * D + G::BN <= 256 ? 2 * D : 256 + 2 * G::BN;   // 16-bit dZ, then P~
-    static constexpr uint32_t T = 256;                                  // band products
-    static constexpr bool T_OVER_Z = Z >= 256 && T + G::NBAND > Z;      // band products overwrite dZ / P~
-    static_assert(P + G::BN <= 512 && Z + G::BN <= 512 && T + G::NBAND <= 512, "tensor memory");
+    static_assert(P + G::BN <= 512 && Z + G::BN <= 512, "tensor memory");
     static_assert(Z >= 2 * D && (Z + G::BN <= 256 || Z >= P + G::BN), "overlap");
 };
 
@@ -79,20 +83,11 @@ struct BwdSmem {
     static constexpr int CB = G::BN * D * 2;
     static constexpr int C1 = R2 + RB;                       // [2] stages
     static constexpr int C2 = C1 + 2 * CB;                   // [2] stages
-    static constexpr int BAND = C2 + 2 * CB;
-    static constexpr int BANDB = G::NBAND * G::CW * 2;
-    static constexpr int STG = BAND + BANDB;                 // own | cross, aliased by the G boxes
-    static constexpr int OWNB = G::BM * G::OWN_S * 2;
-    static constexpr int CROSS = STG + (OWNB + 15) / 16 * 16;
-    static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
-    // the four boxes go over the cross window when they fit there (the own
-    // window of the next band tile is then written while they drain), else
-    // over both windows
-    static constexpr bool STAGE_IN_CROSS = 4 * QSB <= CROSSB;
-    static constexpr int GST = STAGE_IN_CROSS ? CROSS : STG;
-    static constexpr int STGB = (CROSS - STG) + CROSSB > (GST - STG) + 4 * QSB ? (CROSS - STG) + CROSSB
-                                                                               : (GST - STG) + 4 * QSB;
-    static constexpr int DWIN = (STG + STGB + 15) / 16 * 16;
+    // a band tile's stored bias: rows x columns halves, [2] stages
+    static constexpr int BIAS = C2 + 2 * CB;
+    static constexpr int BIASB = G::BM * G::BN * 2;
+    static constexpr int GST = BIAS + 2 * BIASB;             // the four diagonal-sum boxes
+    static constexpr int DWIN = (GST + 4 * QSB + 15) / 16 * 16;
     static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // [2 tiles][colb | cdl][BN]
     static constexpr int XCH = COLV + 4 * G::BN * 4;       // [4][BM] floats: exchanges between the two halves
     static constexpr int KINDS = XCH + 4 * G::BM * 4;        // packed TileKind of every column tile
@@ -100,19 +95,17 @@ struct BwdSmem {
     static constexpr int BYTES = MISC + 256;
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory");
-    static_assert(STG % 1024 == 0 && GST % 128 == 0 && QSB % 128 == 0 && QW <= 256, "staging boxes");
+    static_assert(BIAS % 1024 == 0 && GST % 128 == 0 && QSB % 128 == 0 && QW <= 256, "staging boxes");
 };
 
 struct BwdBars {
     uint64_t row_full, a_full;
     uint64_t c_full[2], c_empty[2];
-    uint64_t band_full, band_empty;
-    uint64_t t_full, t_empty;
+    uint64_t bias_full[2], bias_empty[2];   // stored-bias stages of band tiles
     uint64_t s_full, sread, z_full, zread, mma3_done;
     uint64_t drain;   // the issuer's last MMAs, before the tensor memory is freed
     uint32_t tmem_base;
     int abort_flag;
-    int cross_base[4];
     uint32_t stepw[9];
 };
 static_assert(sizeof(BwdBars) <= 256, "barrier block (the MISC region)");
@@ -142,8 +135,7 @@ template <int D, bool BF16, int SIGMA, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmR1, const __grid_constant__ CUtensorMap tmR2,
                   const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmC2,
-                  const __grid_constant__ CUtensorMap tmXr, const __grid_constant__ CUtensorMap tmYr,
-                  const __grid_constant__ CUtensorMap tmG, const ProblemDev p, const int32_t* __restrict__ dtab,
+                  const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmG, const ProblemDev p, const int32_t* __restrict__ dtab,
                   const float* __restrict__ relb, const float* __restrict__ lse, const float* __restrict__ rowterm,
                   float* __restrict__ acc1_out, void* __restrict__ acc2_out, void* __restrict__ Gbuf, int Rp,
                   const void* __restrict__ r1_rows, const void* __restrict__ r2_rows) {
@@ -159,8 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
     float* colv = reinterpret_cast<float*>(smem + S::COLV);
     float* xch = reinterpret_cast<float*>(smem + S::XCH);
-    uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::STG);
-    uint16_t* cross = reinterpret_cast<uint16_t*>(smem + S::CROSS);
     uint16_t* gstage = reinterpret_cast<uint16_t*>(smem + S::GST);
     uint32_t* kinds = reinterpret_cast<uint32_t*>(smem + S::KINDS);
 
@@ -182,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->c_full[s], 1);
             mbar_init(&bars->c_empty[s], 1);
         }
-        mbar_init(&bars->band_full, 1);
-        mbar_init(&bars->band_empty, 1);
-        mbar_init(&bars->t_full, 1);
-        mbar_init(&bars->t_empty, 8);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->bias_full[s], 1);
+            mbar_init(&bars->bias_empty[s], 8);
+        }
         mbar_init(&bars->s_full, 1 + 32);   // S / dP's commit and the producer's 32 lanes (column terms)
         mbar_init(&bars->sread, 8);
         mbar_init(&bars->z_full, 8);
@@ -261,7 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem + S::R2 + c * BM * G::CW * 2, &tmR2, h * D + c * G::CW, t0 + r0, &bars->row_full);
             }
         }
-        int band_loads = 0, c_cnt[2] = {0, 0};   // copies issued per barrier
+        int c_cnt[2] = {0, 0}, b_cnt[2] = {0, 0};   // copies issued per barrier
+        int bias_loads = 0;                          // band tiles so far
+        // the stored-bias box of a column tile: the 128 x 128 block of the
+        // (query block, key block) pair, and the tile's part of it
+        const int rblk = r0 / kBiasBB;
         for (int it = 0; it < ntiles; ++it) {
             const int s = it & 1, use = it >> 1;
             const int c0 = it * BN;
@@ -279,23 +273,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!put_columns(it)) break;
             const TileKind tk = unpack_kind(kinds[it]);
             if (tk.uniform) continue;
-            bool ok = true;
-            for (int pass = 0; pass < 2 && ok; ++pass) {
-                for (int c = 0; c < G::NCH; ++c) {
-                    if (band_loads > 0 &&
-                        !mbar_wait_warp(&bars->band_empty, (band_loads - 1) & 1, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&bars->band_full, S::BANDB);
-                        tma_load_2d(smem + S::BAND, pass == 0 ? &tmXr : &tmYr, c * G::CW, h * p.R + tk.dlo,
-                                    &bars->band_full);
-                    }
-                    ++band_loads;
+            // a band tile: its bias box into stage bias_loads & 1, once the
+            // softmax warps are done with the band tile that used the stage before
+            const int bs = bias_loads & 1, buse = bias_loads >> 1;
+            if (buse > 0 && !mbar_wait_warp(&bars->bias_empty[bs], (buse - 1) & 1, wc)) break;
+            if (lane == 0) {
+                const int cblk = c0 / kBiasBB, cin = c0 % kBiasBB;
+                int brow = ROWQ ? bias_block_row(p, b, h, t0, rblk, cblk) : bias_block_row(p, b, h, t0, cblk, rblk);
+                if (brow < 0) {   // cannot happen: the table keeps every band block
+                    raise_error(p.err, DF_ERR_DEVICE_ARG);
+                    brow = 0;
                 }
+                mbar_arrive_expect_tx(&bars->bias_full[bs], S::BIASB);
+                // query rows x key columns: the dQ kernel's rows are the box rows,
+                // the dK/dV kernel's columns are
+                tma_load_2d(smem + S::BIAS + bs * S::BIASB, &tmB, ROWQ ? cin : 0, brow + (ROWQ ? 0 : cin),
+                            &bars->bias_full[bs]);
             }
-            if (!ok) break;
+            ++b_cnt[bs];
+            ++bias_loads;
         }
         // no copy of this CTA is still landing in shared memory when it exits
         // (each barrier's last phase is its last copy; the ones before it
@@ -304,28 +300,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ROWQ) mbar_drain(&bars->row_full, 0, wc.limit_ns);
             for (int s = 0; s < 2; ++s)
                 if (c_cnt[s] > 0) mbar_drain(&bars->c_full[s], (c_cnt[s] - 1) & 1, wc.limit_ns);
-            if (band_loads > 0) mbar_drain(&bars->band_full, (band_loads - 1) & 1, wc.limit_ns);
+            for (int s = 0; s < 2; ++s)
+                if (b_cnt[s] > 0) mbar_drain(&bars->bias_full[s], (b_cnt[s] - 1) & 1, wc.limit_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Order per tile m:  S / dP of tile m + 1 (once the softmax warps have
         // read tile m's into registers), then the dK / dV (dQ) products of tile
-        // m (once its 16-bit dZ / P~ are written).  When tile m + 1 is a band
-        // tile, only its own band product precedes tile m's products.  When the
-        // next tile's band products would overwrite dZ / P~, they wait for
-        // tile m to finish.
+        // m (once its 16-bit dZ / P~ are written).  Band tiles take the same
+        // order: their relative-position part comes from the stored bias.
         // The whole warp walks the issue loop (its control flow warp-uniform);
         // the MMAs and commits are the elect.sync forms, issued by one lane.
         // Operand descriptors are built once (per CTA or per ring stage) and
         // advanced per k-step by a constant.
         {
             const uint32_t sR1 = smem_u32(smem + S::R1), sR2 = smem_u32(smem + S::R2);
-            const uint32_t sBand = smem_u32(smem + S::BAND);
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
-            constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
             constexpr uint32_t idA = idesc_f16(128, D, BF16, false, true);
             const uint64_t dR1 = desc_k<G>(sR1, BM, 0), dR2 = desc_k<G>(sR2, BM, 0);
-            const uint64_t dBand = desc_k<G>(sBand, G::NBAND, 0);
             // column operands, K-major and MN-major, of ring stages 0 and 1
             const uint32_t sC10 = smem_u32(smem + S::C1), sC20 = smem_u32(smem + S::C2);
             const uint64_t dC1k0 = desc_k<G>(sC10, BN, 0), dC1k1 = dadd(dC1k0, S::CB);
@@ -334,44 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dC2m0 = desc_mn<G>(sC20, BN, 0), dC2m1 = dadd(dC2m0, S::CB);
             bool ok = mbar_wait_warp(ROWQ ? &bars->a_full : &bars->row_full, 0, wc);
             if (ROWQ) tc_fence_after();
-            int band_used = 0, t_uses = 0;
-            // band product `pass` of band tile m (0: own, rows x band; 1: cross,
-            // columns x band) into the band columns, once the previous product
-            // was copied out
-            auto issue_band = [&](int m, int pass) -> bool {
+            // S / dP of tile m
+            auto issue_s = [&](int m) -> bool {
                 const int s = m & 1, use = m >> 1;
-                if (pass == 1 && !mbar_wait_warp(&bars->c_full[s], use & 1, wc)) return false;
-                if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, wc)) return false;
-                const uint64_t dA = pass == 0 ? dR1 : s ? dC1k1 : dC1k0;
-                const int arows = pass == 0 ? BM : BN;
-                for (int c = 0; c < G::NCH; ++c) {
-                    if (!mbar_wait_warp(&bars->band_full, band_used & 1, wc)) return false;
-                    tc_fence_after();
-                    for (int k = 0; k < G::CW / 16; ++k) {
-                        const int ks = c * (G::CW / 16) + k;
-                        if (ROWQ && pass == 0)
-                            tc_mma_ts_w(tmem + TM::T, tmem + TM::A1 + 8 * ks, dadd(dBand, kofs<G>(G::NBAND, k)), idT,
-                                        ks != 0);
-                        else
-                            tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, ks)), dadd(dBand, kofs<G>(G::NBAND, k)),
-                                        idT, ks != 0);
-                    }
-                    tc_commit_w(&bars->band_empty);
-                    ++band_used;
-                }
-                tc_commit_w(&bars->t_full);
-                ++t_uses;
-                return true;
-            };
-            // S / dP of tile m (after its band products, when it is a band tile)
-            auto issue_s = [&](int m, const TileKind& tk) -> bool {
-                const int s = m & 1, use = m >> 1;
-                if (!tk.uniform) {
-                    // S / dP reuse the band columns: wait until the cross window was copied out
-                    if (!mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, wc)) return false;
-                } else if (!mbar_wait_warp(&bars->c_full[s], use & 1, wc)) {
-                    return false;
-                }
+                if (!mbar_wait_warp(&bars->c_full[s], use & 1, wc)) return false;
                 tc_fence_after();
                 const uint64_t dS = s ? dC1k1 : dC1k0, dP = s ? dC2k1 : dC2k0;
 #pragma unroll
@@ -386,10 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit_w(&bars->s_full);
                 return true;
-            };
-            auto issue_sdp = [&](int m, const TileKind& tk) -> bool {
-                if (!tk.uniform && !(issue_band(m, 0) && issue_band(m, 1))) return false;
-                return issue_s(m, tk);
             };
             auto issue_acc = [&](int m) -> bool {
                 const int s = m & 1;
@@ -412,36 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // test-only stall injection: the issuer stops before this tile, so
             // that the other roles' bounded waits run out
             const int stall = p.fault_kernel == (ROWQ ? 1 : 2) ? p.fault_tile : -1;
-            if (ok && stall != 0) ok = issue_sdp(0, unpack_kind(kinds[0]));
+            if (ok && stall != 0) ok = issue_s(0);
             for (int it = 0; it < ntiles && ok; ++it) {
                 if (stall >= 0 && it + 1 >= stall) break;
-                const bool nxt = it + 1 < ntiles;
-                const TileKind kn = unpack_kind(kinds[nxt ? it + 1 : it]);
-                const bool early = nxt && (!TM::T_OVER_Z || kn.uniform);
-                if (early && !kn.uniform) {
-                    // next tile a band tile: its own product goes first, then this
-                    // tile's products (so that they run while the softmax warps
-                    // finish this tile), then its cross product and S / dP, which
-                    // wait for the softmax warps to copy the windows out
+                if (it + 1 < ntiles) {
                     if (!(ok = mbar_wait_warp(&bars->sread, it & 1, wc))) break;
-                    if (!(ok = issue_band(it + 1, 0))) break;
-                    if (!(ok = issue_acc(it))) break;
-                    if (!(ok = issue_band(it + 1, 1) && issue_s(it + 1, kn))) break;
-                    continue;
-                }
-                if (early) {
-                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, wc))) break;
-                    if (!(ok = issue_sdp(it + 1, kn))) break;
+                    if (!(ok = issue_s(it + 1))) break;
                 }
                 if (!(ok = issue_acc(it))) break;
-                if (nxt && !early) {
-                    // the band products overwrite this tile's dZ / P~: wait until the
-                    // products and the diagonal sums have read them
-                    if (!(ok = mbar_wait_warp(&bars->sread, it & 1, wc))) break;
-                    if (!(ok = mbar_wait_warp(&bars->mma3_done, it & 1, wc))) break;
-                    if (!(ok = mbar_wait_warp(&bars->zread, it & 1, wc))) break;
-                    if (!(ok = issue_sdp(it + 1, kn))) break;
-                }
             }
             // every MMA issued above has completed before the tensor memory is freed
             tc_commit_w(&bars->drain);
@@ -511,9 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bars->a_full);
         }
         float g_lo = 0.f, g_hi = 0.f;     // this thread's share of the diagonal sums at delta 0 and R-1
-        int t_uses = 0;
+        int bias_uses = 0;                // band tiles so far (stored-bias stage bias_uses & 1)
         bool ok = true;
-        uint16_t* own_row = own + row * G::OWN_S;
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
         BandRaw bn = band_fetch<BM, BN, SIGMA, true>(p, dtab, tile_base(0), w4, tid, lane);   // band indices, one tile ahead
         // Every warp walks every tile and meets every named barrier, also after
@@ -527,60 +458,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* colb = colv + (it & 1) * 2 * BN;
             const float* cdl = colb + BN;
             // a band tile overwrites the staging boxes of the previous band tile:
-            // they must have left shared memory (their issuers wait here, or
-            // between the two window copies when the boxes lie over the cross window)
-            if (!S::STAGE_IN_CROSS && !tk.uniform && hf == 0 && lane == 0) bulk_wait_read0();
+            // they must have left shared memory (their issuers wait here)
+            if (!tk.uniform && hf == 0 && lane == 0) bulk_wait_read0();
             // every tile starts with all eight warps: band tiles rewrite the index
-            // window and the band windows, and the per-warp arrivals on the
-            // tile's barriers (counts of 8, or 4 per column half) must never
-            // meet a warp that is a whole tile ahead -- its arrival would
-            // complete the previous tile's phase
+            // window, and the per-warp arrivals on the tile's barriers (counts
+            // of 8, or 4 per column half) must never meet a warp that is a whole
+            // tile ahead -- its arrival would complete the previous tile's phase
             named_bar_sync(1, 256);
             BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
             if (it + 1 < ntiles && !kind_of(it + 1).uniform)
                 bn = band_fetch<BM, BN, SIGMA, true>(p, dtab, tile_base(it + 1), w4, tid, lane);
-            int own_a = 0;
             if (!tk.uniform) {
+                // the index window and its step bits, read by the diagonal sums
+                // after the tile's middle barrier
                 pin(bc.dw);
                 pin(bc.dwp);
-                pin(bc.rng);
                 if (tid < BM + BN - 1) dwin[tid] = (int16_t)(bc.dw - tk.dlo);
                 put_step_bits(bars->stepw, bc, tid, lane, BM + BN - 1);
-                int lo = __shfl_sync(0xffffffffu, bc.rng, 0) - tk.dlo, hi = __shfl_sync(0xffffffffu, bc.rng, 1) - tk.dlo;
-                const int clo = __shfl_sync(0xffffffffu, bc.rng, 2) - tk.dlo, chi = __shfl_sync(0xffffffffu, bc.rng, 3) - tk.dlo;
-                own_a = lo & ~15;
-                ok = ok && mbar_wait_warp(&bars->t_full, t_uses & 1, wc);
-                if (ok) {
-                    tc_fence_after();
-                    copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->t_empty);
-                }
-                if (S::STAGE_IN_CROSS) {
-                    if (hf == 0 && lane == 0) bulk_wait_read0();
-                    named_bar_sync(1, 256);
-                }
-                ok = ok && mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, wc);
-                tc_fence_after();
-                if (ok && 32 * w4 < BN) {
-                    lo = clo;
-                    hi = chi;
-                    const int ca =
-                        copy_band_window(lane_base + TM::T, lo, hi, cross + row * G::CROSS_S, kscale, hf, 2);
-                    if (lane == 0 && hf == 0) bars->cross_base[w4] = ca;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (ok && lane == 0) mbar_arrive(&bars->t_empty);
-                t_uses += 2;
-                named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
             // S / dP of this tile and its column terms (the producer arrives on the same barrier)
             ok = ok && mbar_wait_warp(&bars->s_full, it & 1, wc);
+            const bool band = !tk.uniform;
+            const int bstage = bias_uses & 1;
+            // and, for a band tile, its stored bias
+            if (band) ok = ok && mbar_wait_warp(&bars->bias_full[bstage], (bias_uses >> 1) & 1, wc);
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
-            const bool band = !tk.uniform;
+            const uint16_t* bbox = reinterpret_cast<const uint16_t*>(smem + S::BIAS + bstage * S::BIASB);
             // per-row constant of the exponent (base 2): row bias, minus the row LSE for query rows
             const float rowc = ROWQ ? rb - lse2 : rb;
             float rs[4] = {0.f, 0.f, 0.f, 0.f};
@@ -600,28 +504,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float4* cv0p = reinterpret_cast<const float4*>(colb + 32 * c);
                 if (band) {
-                    const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
-                    const uint16_t* orow = own_row - own_a;
-                    // relative index of column 32 c + e: the window entry at x0 - e
-                    // (query rows) or x0 + e; it moves by one at each step bit
-                    const int x0 = ROWQ ? row - 32 * c + BN - 1 : 32 * c - row + BM - 1;
-                    int m = dwin[x0];
-                    uint32_t mk = step_bits(bars->stepw, ROWQ ? x0 - 31 : x0 + 1);
+                    // the stored bias of these 32 columns (base-2 units, fp16)
+                    if constexpr (ROWQ) {
+                        // box row `row`: this tile's columns of the block row, as
+                        // 16-byte chunks starting at block chunk xo
+                        const int xo = (c0 % kBiasBB) / 8;
+                        const uint4* brow4 = reinterpret_cast<const uint4*>(bbox + row * BN);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 cv = cv0p[q];
-                        const float cvs[4] = {cv.x, cv.y, cv.z, cv.w};
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 w = brow4[bias_chunk(row, xo + 4 * c + q) - xo];
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                            const float4 ca = cv0p[2 * q], cb = cv0p[2 * q + 1];
+                            const float cvs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const int e = 4 * q + t;
-                            sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cvs[t]) + rowc +
-                                                    (h2f(orow[m]) + h2f(crow[e * G::CROSS_S + m])));
-                            if (ROWQ) {
-                                m -= (int)(mk >> 31);   // bit 31 - e: step at x0 - e
-                                mk <<= 1;
-                            } else {
-                                m += (int)(mk & 1u);    // bit e: step at x0 + e + 1
-                                mk >>= 1;
+                            for (int t = 0; t < 8; ++t) {
+                                const int e = 8 * q + t;
+                                const uint16_t hv = (uint16_t)(ww[t >> 1] >> (16 * (t & 1)));
+                                sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cvs[t]) + rowc + h2f(hv));
+                            }
+                        }
+                    } else {
+                        // box column `row` (this thread's key), one half per query row
+                        const uint16_t* bcol = bbox + ((row >> 3) & 8) * 8 + (row & 7);
+                        const int r3 = (row >> 3) & 7;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 cv = cv0p[q];
+                            const float cvs[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int e = 4 * q + t;
+                                const float bv = h2f(bcol[(32 * c + e) * kBiasBB + ((r3 ^ e) & 7) * 8]);
+                                sr[e] = __float_as_uint(fmaf(__uint_as_float(sr[e]), kscale, cvs[t]) + rowc + bv);
                             }
                         }
                     }
@@ -695,6 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_st16(lane_base + TM::Z + 16 * c, zp);
                 if (!ROWQ) tc_st16(lane_base + TM::Z + BN / 2 + 16 * c, pp);
             }
+            if (band) {
+                // the stored bias of this tile is no longer read
+                if (ok) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->bias_empty[bstage]);
+                }
+                ++bias_uses;
+            }
             const float rowsum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
             if (ok) {
                 tc_wait_st();
@@ -710,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // (after a give-up only the named barriers below are met)
-                named_bar_sync(1, 256);   // own / cross no longer read; every dZ is in tensor memory
+                named_bar_sync(1, 256);   // every dZ is in tensor memory; the index window is complete
                 tc_fence_after();
                 // this quarter's relative rows: the index into dwin grows (or
                 // falls) monotonically from one corner of the quarter to the other
@@ -868,30 +790,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool BF16, int SIGMA, bool DROP>
 int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const void* r2, const void* c1,
-               const void* c2, const void* xr, const void* yr, void* Gbuf, int Rp, float* acc1, void* acc2,
-               const float* lse, cudaStream_t st) {
+               const void* c2, void* Gbuf, int Rp, float* acc1, void* acc2, const float* lse, cudaStream_t st) {
     using G = Geo<D>;
     using S = BwdSmem<D>;
-    CUtensorMap m1, m2, m3, m4, m5, m6, mg;
+    CUtensorMap m1, m2, m3, m4, mb, mg;
     const uint64_t tok_dims[2] = {(uint64_t)p.H * D, (uint64_t)p.T};
     const uint64_t tok_str[1] = {(uint64_t)p.H * D * 2};
-    const uint64_t rel_dims[2] = {(uint64_t)D, (uint64_t)p.H * p.R};
-    const uint64_t rel_str[1] = {(uint64_t)D * 2};
+    // the stored band bias as [rows][128] halves; the box is the tile's part
+    // of a block: 128 query rows x BN key columns (dQ kernel) or BN query
+    // rows x 128 key columns (dK/dV kernel)
+    const uint64_t b_dims[2] = {(uint64_t)kBiasBB, (uint64_t)ws.bias_rows};
+    const uint64_t b_str[1] = {(uint64_t)kBiasBB * 2};
     // G viewed as [T][H Rp]: a box of 32 rows of QW sums (the box starts on a
     // multiple of 8 sums, 16 bytes)
     const uint64_t g_dims[2] = {(uint64_t)p.H * Rp, (uint64_t)p.T};
     const uint64_t g_str[1] = {(uint64_t)p.H * Rp * 2};
     const uint32_t boxr[2] = {(uint32_t)G::CW, (uint32_t)G::BM};
     const uint32_t boxc[2] = {(uint32_t)G::CW, (uint32_t)G::BN};
-    const uint32_t boxb[2] = {(uint32_t)G::CW, (uint32_t)G::NBAND};
+    const uint32_t boxb[2] = {(uint32_t)(SIGMA > 0 ? G::BN : kBiasBB), (uint32_t)(SIGMA > 0 ? kBiasBB : G::BN)};
     const uint32_t boxg[2] = {(uint32_t)S::QW, 32};
     const int code = BF16 ? 0 : 1;
     if (encode_tmap(&m1, code, 2, tok_dims, tok_str, boxr, G::SWZB, r1) ||
         encode_tmap(&m2, code, 2, tok_dims, tok_str, boxr, G::SWZB, r2) ||
         encode_tmap(&m3, code, 2, tok_dims, tok_str, boxc, G::SWZB, c1) ||
         encode_tmap(&m4, code, 2, tok_dims, tok_str, boxc, G::SWZB, c2) ||
-        encode_tmap(&m5, code, 2, rel_dims, rel_str, boxb, G::SWZB, xr) ||
-        encode_tmap(&m6, code, 2, rel_dims, rel_str, boxb, G::SWZB, yr) ||
+        encode_tmap(&mb, 1, 2, b_dims, b_str, boxb, 0, ws.bias) ||
         encode_tmap(&mg, code, 2, g_dims, g_str, boxg, 0, Gbuf))
         return (int)cudaErrorInvalidValue;
     auto kern = bwd_tc_kernel<D, BF16, SIGMA, DROP>;
@@ -900,7 +823,7 @@ int launch_one(const ProblemDev& p, const Workspace& ws, const void* r1, const v
     dim3 grid(p.H, p.B, (p.L + G::BM - 1) / G::BM);
     const int phase = SIGMA > 0 ? kProfDq : kProfDkv;
     prof_record(phase, 0, st);
-    kern<<<grid, kThreads, S::ALLOC, st>>>(m1, m2, m3, m4, m5, m6, mg, p, ws.dtab, ws.relb, lse, ws.rowterm, acc1,
+    kern<<<grid, kThreads, S::ALLOC, st>>>(m1, m2, m3, m4, mb, mg, p, ws.dtab, ws.relb, lse, ws.rowterm, acc1,
                                            acc2, Gbuf, Rp, r1, r2);
     prof_record(phase, 1, st);
     return (int)cudaGetLastError();

@@ -138,8 +138,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         bars->abort_flag = 0;
         fence_barrier_init();
     }
-    // the kind of every key tile (two relative-index loads each), once
-    for (int t = threadIdx.x; t < ntiles; t += kThreads) kinds[t] = pack_kind(classify<BM, BN, 1>(p, dtab, i0 - t * BN));
+    // the kind of every key tile (two relative-index loads each), once.  When
+    // the band bias is saved, every tile of a 128 x 128 band block is a band
+    // tile (the saved blocks are then complete; with BN = 128 tile = block).
+    for (int t = threadIdx.x; t < ntiles; t += kThreads) {
+        TileKind k = classify<BM, BN, 1>(p, dtab, i0 - t * BN);
+        if (BN < kBiasBB && p.saved_bias && k.uniform) {
+            const int j0b = t * BN / kBiasBB * kBiasBB;
+            if (!classify<BM, kBiasBB, 1>(p, dtab, i0 - j0b).uniform) k.uniform = 0;
+        }
+        kinds[t] = pack_kind(k);
+    }
     if (warp == 1) {
         tc_alloc(&bars->tmem_base, 512);
         tc_relinquish();
@@ -564,8 +573,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // ---- band tile, pass 1: biased logits (written back over S) and
-                // the tile max; pass 2 (p_pass): probabilities
+                // the tile max; pass 2 (p_pass): probabilities.  With a saved
+                // band bias, pass 1 also stores this row's bias values.
                 float tm = -INFINITY;
+                uint4* bias_dst = nullptr;
+                if (p.saved_bias) {
+                    const int brow = bias_block_row(p, b, h, t0, i0 / kBiasBB, j0 / kBiasBB);
+                    if (brow >= 0)
+                        bias_dst = reinterpret_cast<uint4*>(p.saved_bias + ((size_t)brow + row) * kBiasBB);
+                    else if (lane == 0)
+                        raise_error(p.err, DF_ERR_DEVICE_ARG);   // cannot happen: the table keeps every band block
+                }
 #pragma unroll 1
                 for (int cc = 0; cc < NCT; ++cc) {
                     const int c = cbeg + cc;
@@ -576,25 +594,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
                     const int16_t* dw = dwin + row - 32 * c + BN - 1;
                     const uint16_t* orow = own_row - own_a;
+                    uint32_t bpk[16];
+                    float bprev = 0.f;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int m = dw[-e];
-                        const float x = fmaf(__uint_as_float(r[e]), kscale, cbp[e]) + h2f(orow[m]) +
-                                        h2f(crow[e * G::CROSS_S + m]);
+                        const float bb = band_bias(orow[m], crow[e * G::CROSS_S + m]);
+                        const float x = fmaf(__uint_as_float(r[e]), kscale, cbp[e]) + bb;
                         tm = fmaxf(tm, x);
                         r[e] = __float_as_uint(x);
+                        if (e & 1) bpk[e >> 1] = pack2<false>(bprev, bb); else bprev = bb;
                     }
                     tc_st32(lane_base + scol + 32 * c, r);
+                    if (bias_dst) {
+                        const int lc0 = (j0 % kBiasBB + 32 * c) / 8;   // block chunk of column 32 c
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            bias_dst[bias_chunk(row, lc0 + q)] =
+                                make_uint4(bpk[4 * q], bpk[4 * q + 1], bpk[4 * q + 2], bpk[4 * q + 3]);
+                    }
                 }
                 tc_wait_st();
                 raise_max(tm + rb);
                 sum = p_pass(std::false_type{});
             }
             l_part += sum;
-            if (__any_sync(0xffffffffu, resc) && it > 0) {
+            // P.V of the previous tile has completed before this tile's P is
+            // announced.  The issuer computes S of the next tile before it waits
+            // for this tile's P (and V), so without this wait a slow V copy could
+            // let the softmax warps announce two tiles' P before the issuer takes
+            // the first: p_full would then have moved two phases, its parity
+            // wait could not tell them apart, and the issuer would wait for good.
+            // P.V of the previous tile was issued once that tile's P was in, so
+            // the wait costs nothing in the steady state.  A rescale of O_h also
+            // needs that P.V to have landed.
+            if (it > 0) {
                 if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, wc))) continue;
                 tc_fence_after();
-                rescale_o(alpha);
+                if (__any_sync(0xffffffffu, resc)) rescale_o(alpha);
             }
             tc_wait_st();
             tc_fence_before();

@@ -25,6 +25,47 @@ unsigned long long g_wait_ns = kDefaultWaitNs;
 uint32_t g_wait_probes = kDefaultWaitProbes;
 int g_fault_kernel = -1, g_fault_tile = -1;
 
+// The relative index of the kernels (delta_of in df_common.cuh), in double
+// precision on the host, for sizing the stored-bias table.
+int host_delta(int r, int span, int nb, int mp) {
+    int bkt = r;
+    if (nb > 0 && mp > 0) {
+        const int mid = nb / 2, a = r < 0 ? -r : r;
+        if (a > mid) {
+            const double x = std::log((double)a / mid) / std::log((double)(mp - 1) / mid) * (double)(mid - 1);
+            const int m = mid + (int)std::ceil(x);
+            bkt = r < 0 ? -m : m;
+        }
+    }
+    const int d = bkt + span;
+    return d < 0 ? 0 : (d > 2 * span - 1 ? 2 * span - 1 : d);
+}
+
+// Key blocks kept on each side of a query block in the stored-bias table:
+// the largest |qt - kt| of a 128 x 128 band block (relative positions
+// [128 k - 127, 128 k + 127] for k = qt - kt not all clamped to R-1, or to 0
+// for k < 0), plus one block of margin, so that a last-bit difference
+// between the host's and the device's logarithm cannot move a band block
+// out of the table.  The relative index is monotone in r, so the first
+// clamped position on each side is found by bisection.
+int bias_reach(const ProblemDev& p) {
+    const int nrb = (p.L + 127) / 128, last = p.L - 1;
+    auto first_clamped = [&](int sign, int target) {
+        if (host_delta(sign * last, p.span, p.nb, p.mp) != target) return last + 1;
+        int lo = 0, hi = last;   // delta(sign * hi) == target
+        while (lo < hi) {
+            const int mid = (lo + hi) / 2;
+            if (host_delta(sign * mid, p.span, p.nb, p.mp) == target) hi = mid; else lo = mid + 1;
+        }
+        return lo;
+    };
+    const int rpos = first_clamped(1, p.R - 1), rneg = first_clamped(-1, 0);
+    int kb = 0;
+    for (int k = 1; k < nrb; ++k)
+        if (128 * k - 127 < rpos || 128 * k - 127 < rneg) kb = k;
+    return kb + 1 < nrb ? kb + 1 : nrb - 1;
+}
+
 // Validated problem: fills `out` and returns DF_OK, or an error code.
 df_status resolve(const df_attn_params* a, ProblemDev& out) {
     if (!a) return DF_ERR_INVALID_ARG;
@@ -89,6 +130,13 @@ df_status resolve(const df_attn_params* a, ProblemDev& out) {
     out.wait_probes = g_wait_probes;
     out.fault_kernel = g_fault_kernel;
     out.fault_tile = g_fault_tile;
+    out.bias_kb = bias_reach(out);
+    out.bias_nslot = 2 * out.bias_kb + 1;
+    out.saved_bias = nullptr;
+    if (a->band_bias && a->dtype != DF_FP32) {
+        if ((uintptr_t)a->band_bias & 15u) return DF_ERR_INVALID_ARG;
+        out.saved_bias = (uint16_t*)a->band_bias;
+    }
     return DF_OK;
 }
 
@@ -102,6 +150,14 @@ int rel_chunks(const ProblemDev& p) {
     const int maxc = (p.T + 511) / 512;
     if (c > maxc) c = maxc;
     return c < 1 ? 1 : c;
+}
+
+// Rows of the stored band bias ([rows][128] fp16): 128 x 128 blocks,
+// bias_nslot per query block of each (sequence, head) pair (row index in
+// df_tile.cuh, bias_block_row).
+size_t bias_table_rows(const ProblemDev& p) {
+    const size_t nrbg = (size_t)(p.T - 1) / 128 + (size_t)p.B + 1;
+    return nrbg * (size_t)p.H * (size_t)p.bias_nslot * 128;
 }
 
 // Carve the workspace; with base == nullptr only the size is computed.
@@ -131,6 +187,9 @@ Workspace carve(const ProblemDev& p, df_dtype dt, bool backward, void* base) {
             const size_t a = sizeof(float) * (size_t)p.T * p.H * p.D;
             w.acc32a = (float*)take(a);
             w.acc32b = (float*)take(a);
+            // stored band bias: the caller's saved buffer, else part of the workspace
+            w.bias_rows = bias_table_rows(p);
+            w.bias = p.saved_bias ? p.saved_bias : (uint16_t*)take(sizeof(uint16_t) * w.bias_rows * 128);
         }
     }
     w.bytes = off;
@@ -234,6 +293,12 @@ df_status df_attn_debug_inject_stall(int kernel, int tile, uint64_t wait_limit_n
     return DF_OK;
 }
 
+size_t df_attn_band_bias_size(const df_attn_params* a) {
+    ProblemDev p;
+    if (resolve(a, p) != DF_OK || a->dtype == DF_FP32) return 0;
+    return sizeof(uint16_t) * bias_table_rows(p) * 128;
+}
+
 size_t df_attn_workspace_size(const df_attn_params* a, int backward) {
     ProblemDev p;
     if (resolve(a, p) != DF_OK) return 0;
@@ -313,7 +378,7 @@ df_status df_attn_bwd(const df_attn_params* a, const void* q, const void* k, con
 
 namespace {
 struct Arena {
-    size_t q, k, v, qr, kr, dout, out, lse, dq, dk, dv, dqr, dkr, cu, qm, km, ws, bytes;
+    size_t q, k, v, qr, kr, dout, out, lse, dq, dk, dv, dqr, dkr, cu, qm, km, bias, ws, bytes;
 };
 Arena arena_layout(const df_attn_params* a, const ProblemDev& p) {
     Arena r;
@@ -343,7 +408,13 @@ Arena arena_layout(const df_attn_params* a, const ProblemDev& p) {
     r.cu = take(sizeof(int32_t) * (size_t)(p.B + 1));
     r.qm = take((size_t)p.B * p.L);
     r.km = take((size_t)p.B * p.L);
-    const size_t wf = carve(p, a->dtype, false, nullptr).bytes, wb = carve(p, a->dtype, true, nullptr).bytes;
+    // the band bias, saved by the forward for the backward (bf16 / fp16): the
+    // workspace then leaves it out
+    const size_t bb = a->dtype == DF_FP32 ? 0 : sizeof(uint16_t) * bias_table_rows(p) * 128;
+    r.bias = take(bb);
+    ProblemDev ps = p;
+    if (bb) ps.saved_bias = reinterpret_cast<uint16_t*>(kAlign);   // any non-null value: sizes only
+    const size_t wf = carve(ps, a->dtype, false, nullptr).bytes, wb = carve(ps, a->dtype, true, nullptr).bytes;
     r.ws = take(wf > wb ? wf : wb);
     r.bytes = off;
     return r;
@@ -417,6 +488,7 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     cudaEvent_t* ev = nullptr;
     const bool side = copy_stream(dev, cs, ev);
     df_attn_params dp = *a;
+    if (a->dtype != DF_FP32) dp.band_bias = base + L.bias;
     bool ok = h2d(L.q, q, tok) && h2d(L.k, k, tok) && h2d(L.v, v, tok) && h2d(L.qr, qr, rel) &&
               h2d(L.kr, kr, rel);
     // dO is needed by the backward only: on the copy stream, during the forward

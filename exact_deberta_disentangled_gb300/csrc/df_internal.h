@@ -35,6 +35,12 @@ struct ProblemDev {
     // stops before tile `fault_tile`; -1 = off
     int fault_kernel;
     int fault_tile;
+    // stored band bias: key blocks kept on each side of a query block, slots
+    // per query block (2 bias_kb + 1), and the caller's saved-bias buffer
+    // (df_attn_params.band_bias; the forward writes it, the backward reads
+    // it) or nullptr
+    int bias_kb, bias_nslot;
+    uint16_t* saved_bias;
 };
 
 // Workspace carve-up (device pointers, all 256-byte aligned).
@@ -49,6 +55,8 @@ struct Workspace {
     float* part_qr;           // [nchunk, H, R, D] partial dQr (backward)
     float* acc32a;            // [T, H, D] fp32 dQ before the relative term (backward)
     float* acc32b;            // [T, H, D] fp32 dK before the relative term (backward)
+    uint16_t* bias;           // stored band bias, [bias_rows, 128] fp16 (backward, tensor-core path)
+    size_t bias_rows;
     int nchunk;
     int Rp;                   // row length of G / G' (R, or R rounded up to 64 on the tensor-core path)
     size_t bytes;
@@ -80,13 +88,16 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
                   void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st);
 
 // the two attention-backward kernels (df_bwd_dq.cu, df_bwd_dkv.cu): rows r1 / r2,
-// columns c1 / c2, own band rows xr, cross band rows yr
+// columns c1 / c2; band tiles read the stored band bias (ws.bias)
 int launch_bwd_dq(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* r1, const void* r2,
-                  const void* c1, const void* c2, const void* xr, const void* yr, void* Gbuf, int Rp, float* acc1,
-                  void* acc2, const float* lse, cudaStream_t st);
+                  const void* c1, const void* c2, void* Gbuf, int Rp, float* acc1, void* acc2, const float* lse,
+                  cudaStream_t st);
 int launch_bwd_dkv(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* r1, const void* r2,
-                   const void* c1, const void* c2, const void* xr, const void* yr, void* Gbuf, int Rp, float* acc1,
-                   void* acc2, const float* lse, cudaStream_t st);
+                   const void* c1, const void* c2, void* Gbuf, int Rp, float* acc1, void* acc2, const float* lse,
+                   cudaStream_t st);
+// the stored band bias of every band block (df_bias.cu)
+int launch_band_bias(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
+                     const void* qr, const void* kr, cudaStream_t st);
 int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, const void* q, const void* k,
                   const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st);
 

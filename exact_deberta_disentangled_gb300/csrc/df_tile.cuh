@@ -237,10 +237,46 @@ DF_DEV int copy_band_window(uint32_t t_lane_col0, int lo, int hi, uint16_t* dst,
     return a;
 }
 
+// ---- stored band bias (written by df_bias.cu, read by the backward kernels)
+//
+// The bias of a band tile, c log2(e) (Q_i . Kr[delta] + K_j . Qr[delta]),
+// kept per 128 x 128 block of (query, key) pairs of one sequence: query block
+// qt, key block kt.  Only blocks near the diagonal can be band blocks; the
+// table keeps 2 bias_kb + 1 key blocks per query block (slot = kt - qt +
+// bias_kb), fp16, [block][128 query rows][128 key columns].
+constexpr int kBiasBB = 128;
+
+// floor(t0 / 128) + qt + b differs for every (sequence, query block) pair
+// and stays below (T - 1) / 128 + B + 1: the table's query-block rows.
+DF_DEV int bias_rbg(int t0, int qt, int b) { return t0 / kBiasBB + qt + b; }
+
+// First row of block (qt, kt) of (b, h) in the table viewed as [rows x 128]
+// halves, or -1 when kt is outside the kept band of key blocks.
+DF_DEV int bias_block_row(const ProblemDev& p, int b, int h, int t0, int qt, int kt) {
+    const int slot = kt - qt + p.bias_kb;
+    if (slot < 0 || slot >= p.bias_nslot) return -1;
+    return ((bias_rbg(t0, qt, b) * p.H + h) * p.bias_nslot + slot) * kBiasBB;
+}
+
+// 16-byte chunk c (eight halves) of block row r sits at chunk
+// (c & 8) | ((c ^ r) & 7): a warp reading one logical chunk of 32
+// consecutive rows touches every bank, and each 64-column half of a row stays
+// in its own half.
+DF_DEV int bias_chunk(int r, int c) { return (c & 8) | ((c ^ r) & 7); }
+
 DF_DEV float h2f(uint16_t h) {
     float f;
     asm("{ .reg .f16 t; mov.b16 t, %1; cvt.f32.f16 %0, t; }" : "=f"(f) : "h"(h));
     return f;
+}
+
+// The band bias of a pair as every kernel uses it: the own and cross window
+// values (fp16) summed and rounded to fp16 once more, so that the forward
+// and the stored bias of the backward give the same logits.
+DF_DEV float band_bias(uint16_t own_v, uint16_t cross_v) {
+    uint16_t h;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(h2f(own_v) + h2f(cross_v)));
+    return h2f(h);
 }
 
 }  // namespace df

@@ -106,6 +106,7 @@ typedef struct {
     uint64_t philox_offset;
     float softmax_scale;
     df_dtype dtype;
+    void *band_bias;               /* saved band bias (device) or NULL; below */
 } df_attn_params;
 
 /*
@@ -118,13 +119,30 @@ typedef struct {
  * relative position; e.g. 256 buckets need max_relative_positions >= 345).
  */
 
+/*
+ * Saved band bias (bf16 / fp16 only; ignored for DF_FP32).  Near the
+ * diagonal every (query, key) pair has its own relative-position term
+ * c log2(e) (Q_i . Kr[delta] + K_j . Qr[delta]) ("DisentangledFlash",
+ * section "Status": C2P and P2C).  The backward needs it again for every
+ * band tile.  With p->band_bias == NULL the backward recomputes it into its
+ * workspace; with a device buffer of df_attn_band_bias_size(p) bytes
+ * (16-byte aligned, caller-owned) df_attn_fwd writes it there as a by-product
+ * and df_attn_bwd reads it from there, like the LSE: the backward must then
+ * get the same buffer, unchanged since the forward with the same inputs and
+ * parameters.  Layout: fp16 128 x 128 blocks of 128-query x 128-key pairs,
+ * base-2 units, kept for the key blocks within a fixed reach of each query
+ * block (private to the library).  0 for invalid parameters or DF_FP32.
+ */
+size_t df_attn_band_bias_size(const df_attn_params *p);
+
 /* Bytes of device workspace that df_attn_fwd (backward = 0) or df_attn_bwd
  * (backward != 0) needs for these parameters; 0 if the parameters are
  * invalid.  The workspace holds the relative-index table, per-token
  * relative-position dot products, the device error word and, for the
  * backward, the row terms Dl_i, the diagonal sums of dZ used for the
  * relative-position gradients ([T, H, R] twice, in the input dtype for bf16 /
- * fp16 and fp32 for strict fp32) and fp32 partial sums of dQr / dKr. */
+ * fp16 and fp32 for strict fp32), fp32 partial sums of dQr / dKr and, for
+ * bf16 / fp16 when p->band_bias is NULL, the band bias. */
 size_t df_attn_workspace_size(const df_attn_params *p, int backward);
 
 /*

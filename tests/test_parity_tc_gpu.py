@@ -38,9 +38,11 @@ def geometry(x, w, H, p_drop=0.0, seed=0, offset=0):
     return g
 
 
-def run_gpu(x, w, H, **kw):
+def run_gpu(x, w, H, saved_bias=False, **kw):
     g = geometry(x, w, H, **kw)
     t = [a.to(DEV) for a in (x.q, x.k, x.v, x.qr, x.kr, x.dout)]
+    if saved_bias:   # the forward saves the band bias, the backward reads it
+        g.band_bias = B.alloc_band_bias(g, t[0].dtype)
     out, lse, ws = B.attn_fwd(g, *t[:5])
     grads, wsb = B.attn_bwd(g, *t[:5], out, lse, t[5])
     torch.cuda.synchronize()
@@ -48,8 +50,8 @@ def run_gpu(x, w, H, **kw):
     return g, t, out, lse, grads
 
 
-def check_against_oracle(x, w, H, p_drop=0.0, seed=0, offset=0, backward=True):
-    g, t, out, lse, grads = run_gpu(x, w, H, p_drop=p_drop, seed=seed, offset=offset)
+def check_against_oracle(x, w, H, p_drop=0.0, seed=0, offset=0, backward=True, saved_bias=False):
+    g, t, out, lse, grads = run_gpu(x, w, H, saved_bias=saved_bias, p_drop=p_drop, seed=seed, offset=offset)
     prob = problem_of(x, w, H, p_drop, seed, offset)
     args = [f64(a) for a in (x.q, x.k, x.v, x.qr, x.kr)]
     o_ref, lse_ref = oracle.forward(prob, *args)

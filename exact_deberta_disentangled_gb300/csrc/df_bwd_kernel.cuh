@@ -457,9 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileKind tk = kind_of(it);
             const float* colb = colv + (it & 1) * 2 * BN;
             const float* cdl = colb + BN;
-            // a band tile overwrites the staging boxes of the previous band tile:
-            // they must have left shared memory (their issuers wait here)
-            if (!tk.uniform && hf == 0 && lane == 0) bulk_wait_read0();
             // every tile starts with all eight warps: band tiles rewrite the index
             // window, and the per-warp arrivals on the tile's barriers (counts
             // of 8, or 4 per column half) must never meet a warp that is a whole
@@ -646,6 +643,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint16_t* grow = qstage + lane * S::QW + qoff;
                 const int mmax = S::QW - 1 - qoff;   // a clamp: grow[m] stays inside the row
                 const bool bad = qmax + qoff > S::QW - 1;   // cannot happen for a valid tile
+                // this box still holds the previous band tile's sums until their
+                // reduce-add has read it: its issuer waits here, a whole chunk
+                // loop after issuing it, and the pair barrier passes that on
+                if (hf == 0 && lane == 0) bulk_wait_read0();
+                named_bar_sync(pair_bar, 64);
                 if (ok) {
                     // the quarter's two warps clear its box, lanes on consecutive
                     // 16-byte chunks (the box is one dense block)

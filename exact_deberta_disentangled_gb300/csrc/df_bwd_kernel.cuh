@@ -81,15 +81,22 @@ struct BwdSmem {
     static constexpr int RB = G::BM * D * 2;
     static constexpr int R2 = R1 + RB;
     static constexpr int CB = G::BN * D * 2;
-    static constexpr int C1 = R2 + RB;                       // [2] stages
-    static constexpr int C2 = C1 + 2 * CB;                   // [2] stages
-    // a band tile's stored bias: rows x columns halves, [2] stages
-    static constexpr int BIAS = C2 + 2 * CB;
+    // Column tiles go through a three-stage ring: a stage is released when
+    // the tile's dK / dV (dQ) products complete, at the end of its softmax
+    // pass, and the copy of the tile three ahead then has a tile and a half to
+    // land before its S / dP are due.
+    static constexpr int CST = 3;
+    static constexpr int C1 = R2 + RB;                       // [CST] stages
+    static constexpr int C2 = C1 + CST * CB;                 // [CST] stages
+    // a band tile's stored bias: rows x columns halves, one stage (a band
+    // tile's copy lands while the previous band tile sums its diagonals)
+    static constexpr int BST = 1;
+    static constexpr int BIAS = C2 + CST * CB;
     static constexpr int BIASB = G::BM * G::BN * 2;
-    static constexpr int GST = BIAS + 2 * BIASB;             // the four diagonal-sum boxes
+    static constexpr int GST = BIAS + BST * BIASB;           // the four diagonal-sum boxes
     static constexpr int DWIN = (GST + 4 * QSB + 15) / 16 * 16;
-    static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // [2 tiles][colb | cdl][BN]
-    static constexpr int XCH = COLV + 4 * G::BN * 4;       // [4][BM] floats: exchanges between the two halves
+    static constexpr int COLV = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;  // [4 tiles][colb | cdl][BN]
+    static constexpr int XCH = COLV + 8 * G::BN * 4;       // [4][BM] floats: exchanges between the two halves
     static constexpr int KINDS = XCH + 4 * G::BM * 4;        // packed TileKind of every column tile
     static constexpr int MISC = KINDS + kMaxTiles * 4;
     static constexpr int BYTES = MISC + 256;
@@ -100,8 +107,8 @@ struct BwdSmem {
 
 struct BwdBars {
     uint64_t row_full, a_full;
-    uint64_t c_full[2], c_empty[2];
-    uint64_t bias_full[2], bias_empty[2];   // stored-bias stages of band tiles
+    uint64_t c_full[3], c_empty[3];        // column-tile ring
+    uint64_t bias_full[1], bias_empty[1];  // stored-bias stage of band tiles
     uint64_t s_full, sread, z_full, zread, mma3_done;
     uint64_t drain;   // the issuer's last MMAs, before the tensor memory is freed
     uint32_t tmem_base;
@@ -168,11 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bars->row_full, 1);
         mbar_init(&bars->a_full, 8);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < S::CST; ++s) {
             mbar_init(&bars->c_full[s], 1);
             mbar_init(&bars->c_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < S::BST; ++s) {
             mbar_init(&bars->bias_full[s], 1);
             mbar_init(&bars->bias_empty[s], 8);
         }
@@ -207,16 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         //         0 in band tiles, -inf for masked or missing columns), minus the
         //         column's LSE (base 2) when the columns are queries;
         //   cv1 = c * Dl of the column (dK/dV kernel only).
-        // Slot m & 1 is free when tile m's columns are loaded: tile m - 2's
-        // column stage was released, so its products -- issued after its
-        // softmax warps finished reading its terms -- have completed.  The
-        // terms are announced on tile m's S / dP barrier.
+        // Slot m & 3 is free when tile m's columns are loaded: tile m - 3's
+        // column stage was released, so its products -- issued after the
+        // softmax warps finished reading tile m - 3's terms, and those of tile
+        // m - 4 before them -- have completed.  The terms are announced on tile
+        // m's S / dP barrier.
         const size_t T = (size_t)p.T;
         const float* relb_h = relb + (size_t)h * 4 * T;
         const uint8_t* cmask = ROWQ ? p.kmask : p.qmask;
         auto put_columns = [&](int m) -> bool {
             const TileKind k = unpack_kind(kinds[m]);
-            float* cv = colv + (m & 1) * 2 * BN;
+            float* cv = colv + (m & 3) * 2 * BN;
             constexpr int NJ = BN / 32;
             // every load of the tile first (one memory round trip), then the terms
             float cb[NJ], ls[NJ], rt[NJ];
@@ -251,13 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem + S::R2 + c * BM * G::CW * 2, &tmR2, h * D + c * G::CW, t0 + r0, &bars->row_full);
             }
         }
-        int c_cnt[2] = {0, 0}, b_cnt[2] = {0, 0};   // copies issued per barrier
+        int c_cnt[S::CST] = {}, b_cnt[S::BST] = {};   // copies issued per barrier
         int bias_loads = 0;                          // band tiles so far
         // the stored-bias box of a column tile: the 128 x 128 block of the
         // (query block, key block) pair, and the tile's part of it
         const int rblk = r0 / kBiasBB;
         for (int it = 0; it < ntiles; ++it) {
-            const int s = it & 1, use = it >> 1;
+            const int s = it % S::CST, use = it / S::CST;
             const int c0 = it * BN;
             if (use > 0 && !mbar_wait_warp(&bars->c_empty[s], (use - 1) & 1, wc)) break;
             if (lane == 0) {
@@ -273,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!put_columns(it)) break;
             const TileKind tk = unpack_kind(kinds[it]);
             if (tk.uniform) continue;
-            // a band tile: its bias box into stage bias_loads & 1, once the
+            // a band tile: its bias box into stage bias_loads % BST, once the
             // softmax warps are done with the band tile that used the stage before
-            const int bs = bias_loads & 1, buse = bias_loads >> 1;
+            const int bs = bias_loads % S::BST, buse = bias_loads / S::BST;
             if (buse > 0 && !mbar_wait_warp(&bars->bias_empty[bs], (buse - 1) & 1, wc)) break;
             if (lane == 0) {
                 const int cblk = c0 / kBiasBB, cin = c0 % kBiasBB;
@@ -298,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // completed before that copy was issued)
         if (lane == 0) {
             if (!ROWQ) mbar_drain(&bars->row_full, 0, wc.limit_ns);
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < S::CST; ++s)
                 if (c_cnt[s] > 0) mbar_drain(&bars->c_full[s], (c_cnt[s] - 1) & 1, wc.limit_ns);
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < S::BST; ++s)
                 if (b_cnt[s] > 0) mbar_drain(&bars->bias_full[s], (b_cnt[s] - 1) & 1, wc.limit_ns);
         }
     } else if (warp == 1) {
@@ -320,18 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dR1 = desc_k<G>(sR1, BM, 0), dR2 = desc_k<G>(sR2, BM, 0);
             // column operands, K-major and MN-major, of ring stages 0 and 1
             const uint32_t sC10 = smem_u32(smem + S::C1), sC20 = smem_u32(smem + S::C2);
-            const uint64_t dC1k0 = desc_k<G>(sC10, BN, 0), dC1k1 = dadd(dC1k0, S::CB);
-            const uint64_t dC2k0 = desc_k<G>(sC20, BN, 0), dC2k1 = dadd(dC2k0, S::CB);
-            const uint64_t dC1m0 = desc_mn<G>(sC10, BN, 0), dC1m1 = dadd(dC1m0, S::CB);
-            const uint64_t dC2m0 = desc_mn<G>(sC20, BN, 0), dC2m1 = dadd(dC2m0, S::CB);
+            const uint64_t dC1k0 = desc_k<G>(sC10, BN, 0), dC2k0 = desc_k<G>(sC20, BN, 0);
+            const uint64_t dC1m0 = desc_mn<G>(sC10, BN, 0), dC2m0 = desc_mn<G>(sC20, BN, 0);
+            auto stage_ofs = [](int s) { return (uint32_t)(s * S::CB); };
             bool ok = mbar_wait_warp(ROWQ ? &bars->a_full : &bars->row_full, 0, wc);
             if (ROWQ) tc_fence_after();
             // S / dP of tile m
             auto issue_s = [&](int m) -> bool {
-                const int s = m & 1, use = m >> 1;
+                const int s = m % S::CST, use = m / S::CST;
                 if (!mbar_wait_warp(&bars->c_full[s], use & 1, wc)) return false;
                 tc_fence_after();
-                const uint64_t dS = s ? dC1k1 : dC1k0, dP = s ? dC2k1 : dC2k0;
+                const uint64_t dS = dadd(dC1k0, stage_ofs(s)), dP = dadd(dC2k0, stage_ofs(s));
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     if (ROWQ) {
@@ -346,10 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto issue_acc = [&](int m) -> bool {
-                const int s = m & 1;
+                const int s = m % S::CST;
                 if (!mbar_wait_warp(&bars->z_full, m & 1, wc)) return false;
                 tc_fence_after();
-                const uint64_t d1 = s ? dC1m1 : dC1m0, d2 = s ? dC2m1 : dC2m0;
+                const uint64_t d1 = dadd(dC1m0, stage_ofs(s)), d2 = dadd(dC2m0, stage_ofs(s));
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     // acc1 += dZ . C1   (dQ += dZ K  |  dK += dZ^T Q)
@@ -443,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bars->a_full);
         }
         float g_lo = 0.f, g_hi = 0.f;     // this thread's share of the diagonal sums at delta 0 and R-1
-        int bias_uses = 0;                // band tiles so far (stored-bias stage bias_uses & 1)
+        int bias_uses = 0;                // band tiles so far (stored-bias stage bias_uses % BST)
         bool ok = true;
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
         BandRaw bn = band_fetch<BM, BN, SIGMA, true>(p, dtab, tile_base(0), w4, tid, lane);   // band indices, one tile ahead
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c0 = it * BN;
             const int base = tile_base(it);
             const TileKind tk = kind_of(it);
-            const float* colb = colv + (it & 1) * 2 * BN;
+            const float* colb = colv + (it & 3) * 2 * BN;
             const float* cdl = colb + BN;
             // every tile starts with all eight warps: band tiles rewrite the index
             // window, and the per-warp arrivals on the tile's barriers (counts
@@ -476,9 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S / dP of this tile and its column terms (the producer arrives on the same barrier)
             ok = ok && mbar_wait_warp(&bars->s_full, it & 1, wc);
             const bool band = !tk.uniform;
-            const int bstage = bias_uses & 1;
+            const int bstage = bias_uses % S::BST;
             // and, for a band tile, its stored bias
-            if (band) ok = ok && mbar_wait_warp(&bars->bias_full[bstage], (bias_uses >> 1) & 1, wc);
+            if (band) ok = ok && mbar_wait_warp(&bars->bias_full[bstage], (bias_uses / S::BST) & 1, wc);
             tc_fence_after();
             const float rb = tk.uniform ? (tk.which ? rb1 : rb0) : (rvalid ? 0.f : -INFINITY);
             const uint16_t* bbox = reinterpret_cast<const uint16_t*>(smem + S::BIAS + bstage * S::BIASB);

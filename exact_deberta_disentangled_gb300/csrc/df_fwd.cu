@@ -83,7 +83,8 @@ struct FwdBars {
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];   // K and V rings: K is released after S, V after P.V
     uint64_t band_full, band_empty;
     uint64_t t_full, t_empty;
-    uint64_t s_full[2], p_full[2], pv_done[2];
+    uint64_t s_full[2], pv_done[2];
+    uint64_t p_full[4];   // [column half][tile parity]: P of a half of a tile is in tensor memory
     uint64_t drain;   // the issuer's last MMAs, before the tensor memory is freed
     uint32_t tmem_base;
     int abort_flag;
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->s_full[s], 1 + 32);   // S's commit and the producer's 32 lanes (column terms)
             mbar_init(&bars->pv_done[s], 1);
             mbar_init(&bars->p_full[s], 4);
+            mbar_init(&bars->p_full[2 + s], 4);
         }
         mbar_init(&bars->band_full, 1);
         mbar_init(&bars->band_empty, 1);
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O_h += P_h V_h for the two column halves, each as soon as its P is ready
                 if (!(ok = mbar_wait_warp(&bars->v_full[s], (it >> 1) & 1, wc))) break;
                 for (int hf = 0; hf < 2 && ok; ++hf) {
-                    if (!(ok = mbar_wait_warp(&bars->p_full[hf], it & 1, wc))) break;
+                    if (!(ok = mbar_wait_warp(&bars->p_full[2 * hf + (it & 1)], (it >> 1) & 1, wc))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < BN / 32; ++k)
@@ -619,24 +621,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sum = p_pass(std::false_type{});
             }
             l_part += sum;
-            // P.V of the previous tile has completed before this tile's P is
-            // announced.  The issuer computes S of the next tile before it waits
-            // for this tile's P (and V), so without this wait a slow V copy could
-            // let the softmax warps announce two tiles' P before the issuer takes
-            // the first: p_full would then have moved two phases, its parity
-            // wait could not tell them apart, and the issuer would wait for good.
-            // P.V of the previous tile was issued once that tile's P was in, so
-            // the wait costs nothing in the steady state.  A rescale of O_h also
-            // needs that P.V to have landed.
-            if (it > 0) {
+            // a new running max: O_h is rescaled once P.V of the previous tile
+            // has landed in it
+            if (__any_sync(0xffffffffu, resc) && it > 0) {
                 if (!(ok = mbar_wait_warp(&bars->pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, wc))) continue;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, resc)) rescale_o(alpha);
+                rescale_o(alpha);
             }
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[hf]);
+            // P of this half is announced on the barrier of the tile's parity.
+            // The issuer computes S of the next tile before it waits for this
+            // tile's P (and V), so the softmax warps can announce the next tile's
+            // P before the issuer takes this one; on a single barrier the two
+            // phases would be indistinguishable to the issuer's parity wait (a
+            // slow V copy made it wait for good).  The next phase of this tile's
+            // barrier is two tiles on, whose S the issuer computes only after it
+            // has taken this one.
+            if (lane == 0) mbar_arrive(&bars->p_full[2 * hf + (it & 1)]);
         }
         // ------------------------------------------------------------ epilogue
         // merge the two halves: m = max(m_0, m_1), l = sum_h l_h 2^(m_h - m),

@@ -131,18 +131,18 @@ DF_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
                  : "memory");
 }
 
-// One bounded probe of an mbarrier phase.  The suspend-time hint lets the
-// waiting thread sleep (instead of re-issuing the probe) until the phase
-// completes or about 20 us have passed, leaving issue slots to the warps that
-// share its SM sub-partition.
+// One bounded probe of an mbarrier phase: the waiting thread may be
+// suspended for a system-dependent time while the phase is incomplete.  (A
+// suspend-time hint of 20 us was measured slower: the backward pair took
+// ~1 % longer, its waiters resuming later after the phase completed.)
 DF_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -152,7 +152,7 @@ DF_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // limit_ns have passed on the global timer AND min_probes probes have failed
 // (a jump of the global timer alone, as a profiler's clock resynchronisation
 // can cause, does not end a wait that is about to succeed; a real hang still
-// ends, after at most max(limit, min_probes probes of <= 20 us)).  On give-up
+// ends, after at most max(limit, min_probes probes)).  On give-up
 // the error word records DF_ERR_TIMEOUT and the abort flag is set, so that
 // every other role of the CTA stops waiting too.
 struct WaitCtx {

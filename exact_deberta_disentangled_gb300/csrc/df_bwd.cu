@@ -51,7 +51,7 @@ bool side_stream(int dev, cudaStream_t& side, cudaEvent_t& fork, cudaEvent_t& jo
 
 int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
                   const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
-                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st) {
+                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st, const BwdHook* hook) {
     if (p.D != 32 && p.D != 64 && p.D != 128) return (int)cudaErrorInvalidValue;
     const int Rp = ws.Rp;
     const size_t gbytes = (size_t)p.T * p.H * Rp * 2;
@@ -78,11 +78,12 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
         if (conc) cudaEventRecord(join, side);
         // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO)
         if (!e) e = launch_bwd_dkv(p, ws, dt, k, v, q, dout, ws.Gp, Rp, ws.acc32b, dv, lse, st);
+        if (!e && hook) hook->fn(hook->ctx, 0, st);   // dV is final
         // the caller's stream continues only after the dQ kernel too
         if (conc && cudaStreamWaitEvent(st, join, 0) != cudaSuccess && !e) e = (int)cudaErrorUnknown;
     }
     if (e) return e;
-    return launch_rel_tc(p, ws, dt, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st);
+    return launch_rel_tc(p, ws, dt, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook);
 }
 
 }  // namespace df

@@ -353,9 +353,12 @@ df_status df_attn_fwd_inference(const df_attn_params* a, const void* q, const vo
     return fwd_common(a, q, k, v, qr, kr, out, nullptr, workspace, ws_bytes, stream);
 }
 
-df_status df_attn_bwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
-                      const void* kr, const void* out, const float* lse, const void* dout, void* dq, void* dk,
-                      void* dv, void* dqr, void* dkr, void* workspace, size_t ws_bytes, df_stream_t stream) {
+// The backward, with the optional hook of the tensor-core path (the
+// host-buffer step copies finished gradients down while later kernels run).
+static df_status bwd_common(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                            const void* kr, const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                            void* dv, void* dqr, void* dkr, void* workspace, size_t ws_bytes, df_stream_t stream,
+                            const BwdHook* hook) {
     const void* ptrs[] = {q, k, v, qr, kr, out, lse, dout, dq, dk, dv, dqr, dkr};
     for (const void* x : ptrs)
         if (!x || !aligned16(x)) return DF_ERR_INVALID_ARG;
@@ -371,7 +374,13 @@ df_status df_attn_bwd(const df_attn_params* a, const void* q, const void* k, con
                                           (const float*)qr, (const float*)kr, lse, (const float*)dout, (float*)dq,
                                           (float*)dk, (float*)dv, (float*)dqr, (float*)dkr, st));
     if (launch_relbias(p, a->dtype, q, k, qr, kr, w.relb, st)) return DF_ERR_CUDA;
-    return cuda_status(launch_bwd_tc(p, w, a->dtype, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st));
+    return cuda_status(launch_bwd_tc(p, w, a->dtype, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st, hook));
+}
+
+df_status df_attn_bwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                      const void* kr, const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                      void* dv, void* dqr, void* dkr, void* workspace, size_t ws_bytes, df_stream_t stream) {
+    return bwd_common(a, q, k, v, qr, kr, out, lse, dout, dq, dk, dv, dqr, dkr, workspace, ws_bytes, stream, nullptr);
 }
 
 // ------------------------------------------------------- host-buffer step
@@ -430,14 +439,14 @@ constexpr int kMaxCopyDevices = 64;
 std::mutex g_copy_mu;
 bool g_copy_tried[kMaxCopyDevices];
 cudaStream_t g_copy_st[kMaxCopyDevices];
-cudaEvent_t g_copy_ev[kMaxCopyDevices][4];   // start, dout up, forward done, out / lse down
+cudaEvent_t g_copy_ev[kMaxCopyDevices][6];   // start, dout up, forward done, copies down done, dV / dQ+dK final
 
 bool copy_stream(int dev, cudaStream_t& cs, cudaEvent_t*& ev) {
     if (dev < 0 || dev >= kMaxCopyDevices) return false;
     if (!g_copy_tried[dev]) {
         g_copy_tried[dev] = true;
         bool ok = cudaStreamCreateWithFlags(&g_copy_st[dev], cudaStreamNonBlocking) == cudaSuccess;
-        for (int i = 0; i < 4 && ok; ++i)
+        for (int i = 0; i < 6 && ok; ++i)
             ok = cudaEventCreateWithFlags(&g_copy_ev[dev][i], cudaEventDisableTiming) == cudaSuccess;
         if (!ok) {
             cudaGetLastError();
@@ -518,18 +527,48 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     // O and the LSE are final after the forward: down on the copy stream during the backward
     if (side) {
         ok = cudaEventRecord(ev[2], st) == cudaSuccess && cudaStreamWaitEvent(cs, ev[2], 0) == cudaSuccess &&
-             d2h(out, L.out, tok, cs) && d2h(lse, L.lse, lseb, cs) && cudaEventRecord(ev[3], cs) == cudaSuccess &&
-             cudaStreamWaitEvent(st, ev[1], 0) == cudaSuccess;
+             d2h(out, L.out, tok, cs) && d2h(lse, L.lse, lseb, cs) && cudaStreamWaitEvent(st, ev[1], 0) == cudaSuccess;
         if (!ok) return DF_ERR_CUDA;
     }
-    s = df_attn_bwd(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
-                    (const float*)(base + L.lse), base + L.dout, base + L.dq, base + L.dk, base + L.dv,
-                    base + L.dqr, base + L.dkr, base + L.ws, wsb, stream);
+    // dV, then dQ and dK, are final before the backward's last kernels: the
+    // backward's hook sends them down on the copy stream while those run
+    struct Down {
+        cudaStream_t cs;
+        cudaEvent_t* ev;
+        const char* base;
+        size_t off_dv, off_dq, off_dk, tok;
+        void *dv, *dq, *dk;
+        bool dv_sent, dqdk_sent, ok;
+    } down{cs, ev, base, L.dv, L.dq, L.dk, tok, dv, dq, dk, false, false, true};
+    const BwdHook hook{[](void* ctx, int point, cudaStream_t s2) {
+                           Down& d = *static_cast<Down*>(ctx);
+                           cudaEvent_t e = d.ev[4 + point];
+                           d.ok = d.ok && cudaEventRecord(e, s2) == cudaSuccess &&
+                                  cudaStreamWaitEvent(d.cs, e, 0) == cudaSuccess;
+                           auto down1 = [&](void* dst, size_t off) {
+                               d.ok = d.ok && cudaMemcpyAsync(dst, d.base + off, d.tok, cudaMemcpyDeviceToHost,
+                                                              d.cs) == cudaSuccess;
+                           };
+                           if (point == 0) {
+                               down1(d.dv, d.off_dv);
+                               d.dv_sent = true;
+                           } else {
+                               down1(d.dq, d.off_dq);
+                               down1(d.dk, d.off_dk);
+                               d.dqdk_sent = true;
+                           }
+                       },
+                       &down};
+    s = bwd_common(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
+                   (const float*)(base + L.lse), base + L.dout, base + L.dq, base + L.dk, base + L.dv, base + L.dqr,
+                   base + L.dkr, base + L.ws, wsb, stream, side ? &hook : nullptr);
     if (s != DF_OK) return s;
-    ok = d2h(dq, L.dq, tok, st) && d2h(dk, L.dk, tok, st) && d2h(dv, L.dv, tok, st) && d2h(dqr, L.dqr, rel, st) &&
-         d2h(dkr, L.dkr, rel, st);
+    if (!down.ok) return DF_ERR_CUDA;
+    ok = d2h(dqr, L.dqr, rel, st) && d2h(dkr, L.dkr, rel, st);
+    if (!down.dv_sent) ok = ok && d2h(dv, L.dv, tok, st);
+    if (!down.dqdk_sent) ok = ok && d2h(dq, L.dq, tok, st) && d2h(dk, L.dk, tok, st);
     if (!side) ok = ok && d2h(out, L.out, tok, st) && d2h(lse, L.lse, lseb, st);
-    else ok = ok && cudaStreamWaitEvent(st, ev[3], 0) == cudaSuccess;
+    else ok = ok && cudaEventRecord(ev[3], cs) == cudaSuccess && cudaStreamWaitEvent(st, ev[3], 0) == cudaSuccess;
     if (!ok) return DF_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return DF_ERR_CUDA;
     return df_get_device_error(base + L.ws, stream);

@@ -83,9 +83,16 @@ int launch_bwd_f32(const ProblemDev& p, const Workspace& ws, const float* q, con
 // tensor-core path (bf16 / fp16)
 int launch_fwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
                   const void* v, const void* qr, const void* kr, void* out, float* lse, cudaStream_t st);
+// Optional hook of the tensor-core backward: called with the launching stream
+// right after the launches that finish dV (point 0) and dQ / dK (point 1), so
+// that a caller can start copying those gradients while the rest runs.
+struct BwdHook {
+    void (*fn)(void* ctx, int point, cudaStream_t st);
+    void* ctx;
+};
 int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
                   const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
-                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st);
+                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st, const BwdHook* hook = nullptr);
 
 // the two attention-backward kernels (df_bwd_dq.cu, df_bwd_dkv.cu): rows r1 / r2,
 // columns c1 / c2; band tiles read the stored band bias (ws.bias)
@@ -99,7 +106,8 @@ int launch_bwd_dkv(const ProblemDev& p, const Workspace& ws, df_dtype dt, const 
 int launch_band_bias(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
                      const void* qr, const void* kr, cudaStream_t st);
 int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, const void* q, const void* k,
-                  const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st);
+                  const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st,
+                  const BwdHook* hook = nullptr);
 
 // Optional benchmark timing hooks (df_attn_set_profile_events): record the
 // begin / end event of a kernel phase on the launching stream.

@@ -274,7 +274,7 @@ __global__ void rel_reduce_kernel(const float* __restrict__ part, int nchunk, si
 
 template <int D, bool BF16>
 int rel_impl(const ProblemDev& p, const Workspace& ws, int Rp, const void* q, const void* k, const void* qr,
-             const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st) {
+             const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st, const BwdHook* hook) {
     using G = Geo<D>;
     const int code = BF16 ? 0 : 1;
     CUtensorMap mG, mGp, mKr, mQr, mQ, mK, mGc, mGpc;
@@ -305,6 +305,7 @@ int rel_impl(const ProblemDev& p, const Workspace& ws, int Rp, const void* q, co
         kern<<<grid, kRelThreads, RowSmem<D>::ALLOC, st>>>(mG, mKr, p, Rp, ws.acc32a, dq);
         kern<<<grid, kRelThreads, RowSmem<D>::ALLOC, st>>>(mGp, mQr, p, Rp, ws.acc32b, dk);
         if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
+        if (hook) hook->fn(hook->ctx, 1, st);   // dQ and dK are final
     }
     {
         auto kern = rel_col_kernel<D, BF16>;
@@ -327,15 +328,16 @@ int rel_impl(const ProblemDev& p, const Workspace& ws, int Rp, const void* q, co
 }  // namespace
 
 int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, const void* q, const void* k,
-                  const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st) {
+                  const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st,
+                  const BwdHook* hook) {
     const bool bf = dt == DF_BF16;
     switch (p.D) {
-        case 32: return bf ? rel_impl<32, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st)
-                           : rel_impl<32, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st);
-        case 64: return bf ? rel_impl<64, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st)
-                           : rel_impl<64, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st);
-        case 128: return bf ? rel_impl<128, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st)
-                            : rel_impl<128, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st);
+        case 32: return bf ? rel_impl<32, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook)
+                           : rel_impl<32, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook);
+        case 64: return bf ? rel_impl<64, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook)
+                           : rel_impl<64, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook);
+        case 128: return bf ? rel_impl<128, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook)
+                            : rel_impl<128, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook);
     }
     return (int)cudaErrorInvalidValue;
 }

@@ -191,9 +191,10 @@ df_status df_attn_bwd(const df_attn_params *p, const void *q, const void *k, con
  * p->cu_seqlens, p->query_mask and p->key_mask are HOST pointers (copied
  * too).  Host buffers should be pinned for full copy bandwidth.  The device
  * arena (caller-owned, df_attn_step_host_arena_size bytes) holds the device
- * copies and the workspace.  dout is copied up on a per-device copy stream
- * (created on the first call on that device) while the forward runs, and out
- * and lse are copied down on it while the backward runs.
+ * copies, the band bias the forward saves for the backward and the workspace.  dout is copied up on a per-device copy stream
+ * (created on the first call on that device) while the forward runs; out and
+ * lse are copied down on it while the backward runs, dv once its kernel has
+ * finished and dq, dk once theirs have, while the remaining kernels run.
  */
 size_t df_attn_step_host_arena_size(const df_attn_params *p);
 df_status df_attn_step_host(const df_attn_params *p, const void *q, const void *k, const void *v, const void *qr,

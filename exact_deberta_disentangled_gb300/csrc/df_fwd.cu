@@ -19,10 +19,15 @@
 // memory (O_h += P_h V_h, K = BN/2 per tile); they are merged once, in the
 // epilogue, so no maxima are exchanged inside the key loop (every tile still
 // starts with a barrier of the eight softmax warps).
-// Tensor memory (512 columns): O_0 and O_1 [0, 2D), two S / P buffers, band
-// products aliasing the second S buffer (band tiles wait for it).  Tile n
-// uses S buffer n & 1: the issuer computes S for tile n + 1 while the softmax
-// works on tile n.  P (16-bit) is written over the middle half of S, columns
+// Tensor memory (512 columns): O_0 and O_1 [0, 2D), two S / P buffers and,
+// in [384, 512), two buffers of band-product chunks.  Tile n uses S buffer
+// n & 1: the issuer computes S for tile n + 1 while the softmax works on
+// tile n, band tile or not.  A band tile's two products (own, then cross)
+// are computed 64 band positions at a time (only the chunks the tile's
+// relative-index range reaches) into the chunk buffers alternately, so that
+// the softmax warps copy one chunk to shared memory while the next one is
+// computed; the first two chunks of a band tile are computed while the
+// softmax still works on the tile before it.  P (16-bit) is written over the middle half of S, columns
 // [BN/4, 3 BN/4), half h's part inside the S columns half h has already read
 // (the first half walks its chunks backwards), and feeds the P.V products
 // straight from tensor memory.
@@ -40,6 +45,10 @@ constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;   // keep a stale max while the new one exceeds it by <= 8 (2^8 headroom)
+constexpr int kBandChunk = 64;         // band positions per band-product chunk
+
+// chunks of one band product a tile needs: its relative rows dlo .. dhi
+DF_DEV int band_chunks(const TileKind& k) { return (k.dhi - k.dlo) / kBandChunk + 1; }
 
 template <int D>
 struct FwdTmem {
@@ -47,9 +56,9 @@ struct FwdTmem {
     static constexpr uint32_t O0 = 0, O1 = D;                  // output accumulators of the column halves
     static constexpr uint32_t S0 = 2 * D > 128 ? 2 * D : 128;  // S / P of even tiles
     static constexpr uint32_t S1 = S0 + G::BN;                 // S / P of odd tiles
-    static constexpr uint32_t T = S1;                          // band products
+    static constexpr uint32_t TB = 384;                        // two band-product chunk buffers
     static constexpr uint32_t POFF = G::BN / 4;                // P starts a quarter into its S buffer
-    static_assert(T + G::NBAND <= 512 && S1 + G::BN <= 512, "tensor memory");
+    static_assert(S1 + G::BN <= TB && TB + 2 * kBandChunk <= 512, "tensor memory");
 };
 
 template <int D>
@@ -62,18 +71,20 @@ struct FwdSmem {
     static constexpr int K0 = Q + QB;
     static constexpr int V0 = K0 + kStages * KVB;
     static constexpr int BAND = V0 + kStages * KVB;
-    static constexpr int BANDB = G::NBAND * G::CW * 2;
+    static constexpr int BSLOT = kBandChunk * D * 2;      // one chunk's band rows ([D / CW][64][CW])
+    static constexpr int NBS = D == 128 ? 2 : 4;          // band-row ring slots
+    static constexpr int BANDB = NBS * BSLOT;
     static constexpr int OWN = BAND + BANDB;
     static constexpr int OWNB = G::BM * G::OWN_S * 2;
     static constexpr int CROSS = (OWN + OWNB + 15) / 16 * 16;
     static constexpr int CROSSB = G::BN * G::CROSS_S * 2;
     static constexpr int DWIN = CROSS + CROSSB;
-    static constexpr int COLB = (DWIN + (G::BM + G::BN) * 2 + 15) / 16 * 16;   // [4 tiles][BN]
+    static constexpr int COLB = (DWIN + (G::BM + G::BN) * 4 + 15) / 16 * 16;   // [4 tiles][BN]
     static constexpr int XCH = COLB + 4 * G::BN * 4;      // [4][BM] floats: the halves' maxima and sums
     static constexpr int kMaxTiles = 8192 / G::BN;        // L <= 8192
     static constexpr int KINDS = XCH + 4 * G::BM * 4;     // packed TileKind of every key tile
     static constexpr int MISC = KINDS + kMaxTiles * 4;
-    static constexpr int BYTES = MISC + 256;
+    static constexpr int BYTES = MISC + 512;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
     static_assert(ALLOC <= 232448, "shared memory");
 };
@@ -81,8 +92,8 @@ struct FwdSmem {
 struct FwdBars {
     uint64_t q_full;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];   // K and V rings: K is released after S, V after P.V
-    uint64_t band_full, band_empty;
-    uint64_t t_full, t_empty;
+    uint64_t band_full[4], band_empty[4];   // band-row ring (NBS slots)
+    uint64_t tb_full[2], tb_empty[2];       // band-product chunk buffers in tensor memory
     uint64_t s_full[2], pv_done[2];
     uint64_t p_full[4];   // [column half][tile parity]: P of a half of a tile is in tensor memory
     uint64_t drain;   // the issuer's last MMAs, before the tensor memory is freed
@@ -90,6 +101,7 @@ struct FwdBars {
     int abort_flag;
     int cross_base[4];
 };
+static_assert(sizeof(FwdBars) <= 512, "barrier block");
 
 template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -104,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align1024(smem_raw);
     FwdBars* bars = reinterpret_cast<FwdBars*>(smem + S::MISC);
-    int16_t* dwin = reinterpret_cast<int16_t*>(smem + S::DWIN);
+    uint32_t* dwin2 = reinterpret_cast<uint32_t*>(smem + S::DWIN);
     float* colv = reinterpret_cast<float*>(smem + S::COLB);
     float* xch = reinterpret_cast<float*>(smem + S::XCH);
     uint16_t* own = reinterpret_cast<uint16_t*>(smem + S::OWN);
@@ -132,10 +144,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->p_full[s], 4);
             mbar_init(&bars->p_full[2 + s], 4);
         }
-        mbar_init(&bars->band_full, 1);
-        mbar_init(&bars->band_empty, 1);
-        mbar_init(&bars->t_full, 1);
-        mbar_init(&bars->t_empty, 8);
+        for (int r = 0; r < S::NBS; ++r) {
+            mbar_init(&bars->band_full[r], 1);
+            mbar_init(&bars->band_empty[r], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->tb_full[s], 1);
+            mbar_init(&bars->tb_empty[s], 8);
+        }
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_barrier_init();
@@ -210,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < ntiles && pc_ok; ++it) {
             const int s = it & 1, use = it >> 1;
             const int j0 = it * BN;
-            // K of tile it as soon as S of tile it - 2 has read its stage
+            // K of tile it as soon as S (band tile: and the cross product) of
+            // tile it - 2 has read its stage
             if (use > 0 && !mbar_wait_warp(&bars->k_empty[s], (use - 1) & 1, wc)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->k_full[s], S::KVB);
@@ -221,20 +238,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++k_cnt[s];
             const TileKind tk = unpack_kind(kinds[it]);
             bool ok = true;
-            for (int pass = 0; pass < 2 && ok && !tk.uniform; ++pass) {
-                for (int c = 0; c < G::NCH; ++c) {
-                    if (band_loads > 0 &&
-                        !mbar_wait_warp(&bars->band_empty, (band_loads - 1) & 1, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&bars->band_full, S::BANDB);
-                        tma_load_2d(smem + S::BAND, pass == 0 ? &tmKr : &tmQr, c * G::CW, h * p.R + tk.dlo,
-                                    &bars->band_full);
-                    }
-                    ++band_loads;
+            // band rows of the tile's product chunks: Kr rows for the own
+            // product, then Qr rows for the cross product, 64 per ring slot
+            const int nch = tk.uniform ? 0 : band_chunks(tk);
+            for (int g = 0; g < 2 * nch; ++g) {
+                const int r = band_loads % S::NBS, u = band_loads / S::NBS;
+                if (u > 0 && !mbar_wait_warp(&bars->band_empty[r], (u - 1) & 1, wc)) {
+                    ok = false;
+                    break;
                 }
+                if (lane == 0) {
+                    const int row0 = h * p.R + tk.dlo + kBandChunk * (g < nch ? g : g - nch);
+                    mbar_arrive_expect_tx(&bars->band_full[r], S::BSLOT);
+                    for (int c = 0; c < G::NCH; ++c)
+                        tma_load_2d(smem + S::BAND + r * S::BSLOT + c * kBandChunk * G::CW * 2,
+                                    g < nch ? &tmKr : &tmQr, c * G::CW, row0, &bars->band_full[r]);
+                }
+                ++band_loads;
             }
             if (!ok) break;
             // V of tile it once P.V of tile it - 2 has read its stage
@@ -257,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k_cnt[s] > 0) mbar_drain(&bars->k_full[s], (k_cnt[s] - 1) & 1, wc.limit_ns);
                 if (v_cnt[s] > 0) mbar_drain(&bars->v_full[s], (v_cnt[s] - 1) & 1, wc.limit_ns);
             }
-            if (band_loads > 0) mbar_drain(&bars->band_full, (band_loads - 1) & 1, wc.limit_ns);
+            for (int r = 0; r < S::NBS && r < band_loads; ++r)
+                mbar_drain(&bars->band_full[r], ((band_loads - 1 - r) / S::NBS) & 1, wc.limit_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -268,69 +289,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             const uint32_t sQ = smem_u32(smem + S::Q), sBand = smem_u32(smem + S::BAND);
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
-            constexpr uint32_t idT = idesc_f16(128, G::NBAND, BF16, false, false);
+            constexpr uint32_t idT = idesc_f16(128, kBandChunk, BF16, false, false);
             constexpr uint32_t idO = idesc_f16(128, D, BF16, false, true);
-            const uint64_t dQ = desc_k<G>(sQ, BM, 0), dBand = desc_k<G>(sBand, G::NBAND, 0);
+            const uint64_t dQ = desc_k<G>(sQ, BM, 0), dBand = desc_k<G>(sBand, kBandChunk, 0);
             const uint64_t dK0 = desc_k<G>(smem_u32(smem + S::K0), BN, 0), dK1 = dadd(dK0, S::KVB);
             const uint64_t dV0 = desc_mn<G>(smem_u32(smem + S::V0), BN, 0), dV1 = dadd(dV0, S::KVB);
             bool ok = mbar_wait_warp(&bars->q_full, 0, wc);
-            int band_used = 0, t_uses = 0;
             int pv_cnt0 = 0, pv_cnt1 = 0;   // P.V rounds issued per S buffer
-            // S (and, for band tiles, the two band products) of tile m into buffer m & 1
+            int bc = 0;                     // band chunks issued: ring slot bc % NBS, chunk buffer bc & 1
+            // S of tile m into buffer m & 1.  K's stage is released here for a
+            // uniform tile, after the cross product for a band tile.
             auto issue_s = [&](int m, const TileKind& tk) -> bool {
-                const int s = m & 1, use = m >> 1, bf = m & 1;
+                const int s = m & 1, use = m >> 1;
                 const uint64_t dK = s ? dK1 : dK0;
-                if (!tk.uniform) {
-                    // the band columns overlap S buffer 1: its last P must have been consumed
-                    if (pv_cnt1 > 0 && !mbar_wait_warp(&bars->pv_done[1], (pv_cnt1 - 1) & 1, wc))
-                        return false;
-                    for (int pass = 0; pass < 2; ++pass) {
-                        if (pass == 1 && !mbar_wait_warp(&bars->k_full[s], use & 1, wc)) return false;
-                        if (t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, wc))
-                            return false;
-                        const uint64_t dA = pass == 0 ? dQ : dK;
-                        const int arows = pass == 0 ? BM : BN;
-                        for (int c = 0; c < G::NCH; ++c) {
-                            if (!mbar_wait_warp(&bars->band_full, band_used & 1, wc)) return false;
-                            tc_fence_after();
-                            for (int k = 0; k < G::CW / 16; ++k)
-                                tc_mma_ss_w(tmem + TM::T, dadd(dA, kofs<G>(arows, c * (G::CW / 16) + k)),
-                                            dadd(dBand, kofs<G>(G::NBAND, k)), idT, (c | k) != 0);
-                            tc_commit_w(&bars->band_empty);
-                            ++band_used;
-                        }
-                        tc_commit_w(&bars->t_full);
-                        ++t_uses;
-                    }
-                } else if (!mbar_wait_warp(&bars->k_full[s], use & 1, wc)) {
-                    return false;
-                }
-                // buffer bf free: its previous P consumed; buffer 1 also holds band columns
-                const int pvc = bf ? pv_cnt1 : pv_cnt0;
-                if (pvc > 0 && !mbar_wait_warp(&bars->pv_done[bf], (pvc - 1) & 1, wc)) return false;
-                if (bf == 1 && t_uses > 0 && !mbar_wait_warp(&bars->t_empty, (t_uses - 1) & 1, wc))
-                    return false;
+                if (!mbar_wait_warp(&bars->k_full[s], use & 1, wc)) return false;
+                // buffer s free: its previous P consumed
+                const int pvc = s ? pv_cnt1 : pv_cnt0;
+                if (pvc > 0 && !mbar_wait_warp(&bars->pv_done[s], (pvc - 1) & 1, wc)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
                     tc_mma_ss_w(tmem + s_col(m), dadd(dQ, kofs<G>(BM, k)), dadd(dK, kofs<G>(BN, k)), idS, k != 0);
-                tc_commit_w(&bars->s_full[bf]);
-                tc_commit_w(&bars->k_empty[s]);
+                tc_commit_w(&bars->s_full[s]);
+                if (tk.uniform) tc_commit_w(&bars->k_empty[s]);
+                return true;
+            };
+            // chunks g0 .. g1 - 1 of band tile m's products: chunk g < nch is
+            // Q . Kr[dlo + 64 g ..]^T (lanes = query rows), chunk nch + g is
+            // K . Qr[dlo + 64 g ..]^T (lanes = key columns).  Each waits for its
+            // chunk buffer's previous chunk to be copied out and its band rows.
+            auto issue_band = [&](int m, const TileKind& tk, int g0, int g1) -> bool {
+                const int nch = band_chunks(tk);
+                const int s = m & 1, use = m >> 1;
+                const uint64_t dK = s ? dK1 : dK0;
+                for (int g = g0; g < g1 && g < 2 * nch; ++g) {
+                    const int tb = bc & 1, r = bc % S::NBS;
+                    if (bc >= 2 && !mbar_wait_warp(&bars->tb_empty[tb], ((bc >> 1) - 1) & 1, wc)) return false;
+                    if (!mbar_wait_warp(&bars->band_full[r], (bc / S::NBS) & 1, wc)) return false;
+                    // K of tile m stays in its stage until the last cross chunk (S(m) has waited for it)
+                    if (g == nch && !mbar_wait_warp(&bars->k_full[s], use & 1, wc)) return false;
+                    tc_fence_after();
+                    const bool cross_pass = g >= nch;
+                    const uint64_t dA = cross_pass ? dK : dQ;
+                    const int arows = cross_pass ? BN : BM;
+                    const uint64_t dB = dadd(dBand, (uint32_t)(r * S::BSLOT));
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)
+                        tc_mma_ss_w(tmem + TM::TB + tb * kBandChunk, dadd(dA, kofs<G>(arows, k)),
+                                    dadd(dB, kofs<G>(kBandChunk, k)), idT, k != 0);
+                    tc_commit_w(&bars->band_empty[r]);
+                    tc_commit_w(&bars->tb_full[tb]);
+                    if (g == 2 * nch - 1) tc_commit_w(&bars->k_empty[s]);
+                    ++bc;
+                }
                 return true;
             };
             // test-only stall injection: the issuer stops before this tile, so
             // that the other roles' bounded waits run out
             const int stall = p.fault_kernel == 0 ? p.fault_tile : -1;
-            if (ok && stall != 0) ok = issue_s(0, unpack_kind(kinds[0]));
+            if (ok && stall != 0) {
+                const TileKind k0 = unpack_kind(kinds[0]);
+                ok = issue_s(0, k0) && (k0.uniform || issue_band(0, k0, 0, 8));
+            }
             for (int it = 0; it < ntiles && ok; ++it) {
                 if (stall >= 0 && it + 1 >= stall) break;
                 const int s = it & 1;
                 const uint64_t dV = s ? dV1 : dV0;
                 const TileKind kn = unpack_kind(kinds[it + 1 < ntiles ? it + 1 : it]);
-                // uniform next tile: compute its S while the softmax works on this one
+                // the next tile's S (and the first two chunks of its band
+                // products) while the softmax works on this one; the two
+                // chunks' buffers were copied out at the start of this tile
                 const bool next = it + 1 < ntiles;
                 const bool next_band = next && !kn.uniform;
-                if (next && !next_band && !(ok = issue_s(it + 1, kn))) break;
+                if (next && !(ok = issue_s(it + 1, kn))) break;
+                if (next_band && !(ok = issue_band(it + 1, kn, 0, 2))) break;
                 // O_h += P_h V_h for the two column halves, each as soon as its P is ready
                 if (!(ok = mbar_wait_warp(&bars->v_full[s], (it >> 1) & 1, wc))) break;
                 for (int hf = 0; hf < 2 && ok; ++hf) {
@@ -345,7 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit_w(&bars->v_empty[s]);
                 tc_commit_w(&bars->pv_done[it & 1]);
                 if (it & 1) ++pv_cnt1; else ++pv_cnt0;
-                if (next_band && !(ok = issue_s(it + 1, kn))) break;
+                // the rest of the next tile's chunks, each as the softmax warps
+                // copy out the chunk before it in the same buffer
+                if (next_band && !(ok = issue_band(it + 1, kn, 2, 8))) break;
             }
             // every MMA issued above has completed before the tensor memory is freed
             tc_commit_w(&bars->drain);
@@ -377,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float a1 = row_in ? relb_h[T + t0 + i] : 0.f;
         const float kscale = p.scale * kLog2e;
         float m_run = -INFINITY, l_part = 0.f;   // this half's running max (log2 units) and sum
-        int t_uses = 0;
+        int gc = 0;   // band-product chunks copied out (chunk buffer gc & 1)
         bool ok = true;
         uint16_t* own_row = own + row * G::OWN_S;
         // this half's output accumulator, all D columns, 16 at a time
@@ -393,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         auto kind_of = [&](int t) { return unpack_kind(kinds[t < ntiles ? t : ntiles - 1]); };
-        BandRaw bn = band_fetch<BM, BN, 1>(p, dtab, i0, w4, tid, lane);      // band indices, one tile ahead
+        BandRaw bn = band_fetch<BM, BN, 1, true>(p, dtab, i0, w4, tid, lane);   // band indices, one tile ahead
         // Every warp walks every tile and meets every named barrier, also after
         // a bounded wait gave up (ok == false: the work is skipped, no wait is
         // taken): a warp that left the loop early would leave its siblings
@@ -409,37 +443,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             // complete the previous tile's phase
             named_bar_sync(1, 256);
             BandRaw bc = bn;   // this tile's band indices (fetched during the previous tile)
-            if (it + 1 < ntiles && !kind_of(it + 1).uniform) bn = band_fetch<BM, BN, 1>(p, dtab, i0 - j0 - BN, w4, tid, lane);
+            if (it + 1 < ntiles && !kind_of(it + 1).uniform)
+                bn = band_fetch<BM, BN, 1, true>(p, dtab, i0 - j0 - BN, w4, tid, lane);
             int own_a = 0;
             if (!tk.uniform) {
                 pin(bc.dw);
+                pin(bc.dwp);
                 pin(bc.rng);
-                if (tid < BM + BN - 1) dwin[tid] = (int16_t)(bc.dw - tk.dlo);
+                // index window entry x with entry x - 1 beside it: the band
+                // coordinates of two neighbouring columns of a row in one load
+                if (tid < BM + BN - 1)
+                    dwin2[tid] = ((uint32_t)(bc.dw - tk.dlo) & 0xFFFFu) | ((uint32_t)(bc.dwp - tk.dlo) << 16);
                 int lo = __shfl_sync(0xffffffffu, bc.rng, 0) - tk.dlo, hi = __shfl_sync(0xffffffffu, bc.rng, 1) - tk.dlo;
                 const int clo = __shfl_sync(0xffffffffu, bc.rng, 2) - tk.dlo, chi = __shfl_sync(0xffffffffu, bc.rng, 3) - tk.dlo;
                 own_a = lo & ~15;
-                // both warps of a lane quarter copy half of each band window
-                ok = ok && mbar_wait_warp(&bars->t_full, t_uses & 1, wc);
-                if (ok) {
+                const int ca = clo & ~15;
+                // the chunks of the own product, then of the cross product; the
+                // two warps of a lane quarter copy half of each chunk's part of
+                // the quarter's window
+                const int nch = band_chunks(tk);
+                for (int g = 0; g < 2 * nch; ++g, ++gc) {
+                    const int tb = gc & 1;
+                    ok = ok && mbar_wait_warp(&bars->tb_full[tb], (gc >> 1) & 1, wc);
+                    if (!ok) continue;
                     tc_fence_after();
-                    copy_band_window(lane_base + TM::T, lo, hi, own_row, kscale, hf, 2);
+                    const uint32_t tcol = lane_base + TM::TB + tb * kBandChunk;
+                    if (g < nch)
+                        copy_band_chunk(tcol, kBandChunk * g, lo, hi, own_a, own_row, kscale, hf);
+                    else if (32 * w4 < BN)
+                        copy_band_chunk(tcol, kBandChunk * (g - nch), clo, chi, ca, cross + row * G::CROSS_S,
+                                        kscale, hf);
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->t_empty);
+                    if (lane == 0) mbar_arrive(&bars->tb_empty[tb]);
                 }
-                ok = ok && mbar_wait_warp(&bars->t_full, (t_uses + 1) & 1, wc);
-                tc_fence_after();
-                if (ok && 32 * w4 < BN) {
-                    lo = clo;
-                    hi = chi;
-                    const int ca =
-                        copy_band_window(lane_base + TM::T, lo, hi, cross + row * G::CROSS_S, kscale, hf, 2);
-                    if (lane == 0 && hf == 0) bars->cross_base[w4] = ca;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (ok && lane == 0) mbar_arrive(&bars->t_empty);
-                t_uses += 2;
+                if (lane == 0 && hf == 0) bars->cross_base[w4] = ca;
                 named_bar_sync(1, 256);   // dwin, own / cross windows complete
             }
             // S of this tile and its column terms (the producer arrives on the same barrier)
@@ -592,20 +630,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     tc_ld32(lane_base + scol + 32 * c, r);
                     tc_wait_ld();
-                    const float* cbp = colb + 32 * c;
+                    const float2* cb2 = reinterpret_cast<const float2*>(colb + 32 * c);
                     const uint16_t* crow = cross + 32 * c * G::CROSS_S - bars->cross_base[c];
-                    const int16_t* dw = dwin + row - 32 * c + BN - 1;
+                    const uint32_t* dw2 = dwin2 + row - 32 * c + BN - 1;
                     const uint16_t* orow = own_row - own_a;
                     uint32_t bpk[16];
-                    float bprev = 0.f;
+                    // columns 2q, 2q + 1: band coordinates m0, m1 (entries x, x - 1)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int m = dw[-e];
-                        const float bb = band_bias(orow[m], crow[e * G::CROSS_S + m]);
-                        const float x = fmaf(__uint_as_float(r[e]), kscale, cbp[e]) + bb;
-                        tm = fmaxf(tm, x);
-                        r[e] = __float_as_uint(x);
-                        if (e & 1) bpk[e >> 1] = pack2<false>(bprev, bb); else bprev = bb;
+                    for (int q = 0; q < 16; ++q) {
+                        const uint32_t mm = dw2[-2 * q];
+                        const int m0 = (int)(mm & 0xFFFFu), m1 = (int)(mm >> 16);
+                        const uint32_t ov = __byte_perm(orow[m0], orow[m1], 0x5410);
+                        const uint32_t cv =
+                            __byte_perm(crow[2 * q * G::CROSS_S + m0], crow[(2 * q + 1) * G::CROSS_S + m1], 0x5410);
+                        const uint32_t bb = band_bias2(ov, cv);
+                        bpk[q] = bb;
+                        float b0, b1;
+                        h2x2f(bb, b0, b1);
+                        const float2 cb = cb2[q];
+                        float x0, x1;
+                        ffma2(x0, x1, __uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]), kscale, kscale, cb.x,
+                              cb.y);
+                        fadd2(x0, x1, x0, x1, b0, b1);
+                        tm = fmax3(tm, x0, x1);
+                        r[2 * q] = __float_as_uint(x0);
+                        r[2 * q + 1] = __float_as_uint(x1);
                     }
                     tc_st32(lane_base + scol + 32 * c, r);
                     if (bias_dst) {
@@ -707,7 +756,7 @@ int launch_fwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, con
     const uint64_t rel_str[1] = {(uint64_t)D * 2};
     const uint32_t boxq[2] = {(uint32_t)G::CW, (uint32_t)G::BM};
     const uint32_t boxk[2] = {(uint32_t)G::CW, (uint32_t)G::BN};
-    const uint32_t boxr[2] = {(uint32_t)G::CW, (uint32_t)G::NBAND};
+    const uint32_t boxr[2] = {(uint32_t)G::CW, (uint32_t)kBandChunk};
     const int code = BF16 ? 0 : 1;
     if (encode_tmap(&mq, code, 2, tok_dims, tok_str, boxq, G::SWZB, q) ||
         encode_tmap(&mk, code, 2, tok_dims, tok_str, boxk, G::SWZB, k) ||

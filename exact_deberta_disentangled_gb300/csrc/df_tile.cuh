@@ -237,6 +237,36 @@ DF_DEV int copy_band_window(uint32_t t_lane_col0, int lo, int hi, uint16_t* dst,
     return a;
 }
 
+// Band products computed in chunks of 64 band positions: copy the part of
+// the chunk at band coordinates [kb, kb + 64) (tensor-memory columns t_chunk
+// .. + 63 of the warp's lanes) that the lane quarter's window [lo, hi]
+// covers, scaled and rounded as in copy_band_window, to dst[x - a] for band
+// coordinate x (a = lo & ~15, so the 16-column parts land where
+// copy_band_window puts them).  The chunk's four 16-column parts go to the
+// quarter's two warps alternately (part 0 / 1): one tensor-memory round trip
+// per warp.
+DF_DEV void copy_band_chunk(uint32_t t_chunk, int kb, int lo, int hi, int a, uint16_t* dst, float scale, int part) {
+    if (hi < kb || lo >= kb + 64) return;
+    const int s = (lo > kb ? (lo - kb) >> 4 : 0) + part;
+    const int s_hi = hi < kb + 63 ? (hi - kb) >> 4 : 3;
+    if (s > s_hi) return;
+    const bool two = s + 2 <= s_hi;
+    uint32_t r[32];
+    tc_ld16p(t_chunk + (uint32_t)(16 * s), r);
+    if (two) tc_ld16p(t_chunk + (uint32_t)(16 * (s + 2)), r + 16);
+    tc_wait_ld();
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + (kb + 16 * s - a));
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+        d32[x] = pack2<false>(__uint_as_float(r[2 * x]) * scale, __uint_as_float(r[2 * x + 1]) * scale);
+    if (two) {
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+            d32[16 + x] = pack2<false>(__uint_as_float(r[16 + 2 * x]) * scale,
+                                       __uint_as_float(r[16 + 2 * x + 1]) * scale);
+    }
+}
+
 // ---- stored band bias (written by df_bias.cu, read by the backward kernels)
 //
 // The bias of a band tile, c log2(e) (Q_i . Kr[delta] + K_j . Qr[delta]),
@@ -272,11 +302,23 @@ DF_DEV float h2f(uint16_t h) {
 
 // The band bias of a pair as every kernel uses it: the own and cross window
 // values (fp16) summed and rounded to fp16 once more, so that the forward
-// and the stored bias of the backward give the same logits.
-DF_DEV float band_bias(uint16_t own_v, uint16_t cross_v) {
-    uint16_t h;
-    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(h2f(own_v) + h2f(cross_v)));
-    return h2f(h);
+// and the stored bias of the backward give the same logits.  band_bias2 does
+// two pairs with one f16x2 addition: the sum of two fp16 values is exact in
+// fp32 unless their exponents differ by more than 13, and then the smaller
+// one is below a quarter of the larger one's fp16 spacing, so rounding the
+// fp32 sum to fp16 and rounding the exact sum to fp16 (add.rn.f16x2) both
+// give the larger value: the two forms agree bit for bit.
+DF_DEV uint32_t band_bias2(uint32_t own_v2, uint32_t cross_v2) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(own_v2), "r"(cross_v2));
+    return d;
+}
+
+// both halves of an f16x2 word as fp32 (low half first)
+DF_DEV void h2x2f(uint32_t h, float& lo, float& hi) {
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
 }
 
 }  // namespace df

@@ -12,7 +12,10 @@ for no bucketing, a small span and the largest span.  The library keeps one
 block of margin beyond the exact reach.
 
 Also: the size is 0 for strict fp32, a backward given a saved buffer needs
-exactly that much less workspace, and a misaligned buffer is rejected.
+exactly that much less workspace, and a misaligned buffer is rejected.  And
+the rounding rule the forward relies on when it adds the own and cross
+values of two pairs with one f16x2 addition: rounding the fp32 sum of two
+fp16 values to fp16 equals rounding their exact sum to fp16.
 """
 import numpy as np
 import pytest
@@ -99,3 +102,33 @@ def test_misaligned_buffer_is_invalid():
     g.band_bias = Fake(0x10008)
     assert B.workspace_size(g, torch.bfloat16, True) == 0
     assert B.band_bias_size(g, torch.bfloat16) == 0
+
+
+def test_fp16_sum_rounding_through_fp32_is_exact_rounding():
+    """rn16(rn32(a + b)) == rn16(a + b) for fp16 a, b: every finite pair whose
+    exponents are within 13 of each other (the sum is exact in fp32), every
+    pair 14 or more apart (the small one is below a quarter spacing), ties,
+    subnormals and a dense random sample.  The exact sum is taken in fp64,
+    where every sum of two fp16 values is exact."""
+    # the fp64 -> fp16 conversion used as the reference rounds directly (a
+    # value just above a tie rounds up; through fp32 it would round to even)
+    assert np.float16(np.float64(1 + 2.0 ** -11 + 2.0 ** -40)) == np.float16(1 + 2.0 ** -10)
+    rng = np.random.default_rng(7)
+    allh = np.arange(0, 1 << 16, dtype=np.uint16).view(np.float16)
+    finite = allh[np.isfinite(allh)]
+    # every finite fp16 against a spread of partners: powers of two, values just
+    # off them, subnormals, the largest values, and random ones
+    partners = np.concatenate([
+        np.float16(2.0) ** np.arange(-24, 16, dtype=np.float64),
+        np.nextafter(np.float16(2.0) ** np.arange(-14, 16, dtype=np.float64), np.float16(0)).astype(np.float16),
+        allh[1:64], -allh[1:64], np.array([65504.0, -65504.0, 0.5, -0.5, 1.0, -1.0]),
+        rng.choice(finite, 400)]).astype(np.float16)
+    a = np.repeat(finite, partners.size)
+    b = np.tile(partners, finite.size)
+    extra = rng.choice(finite, (2, 4_000_000))
+    a = np.concatenate([a, extra[0]])
+    b = np.concatenate([b, extra[1]])
+    exact = (a.astype(np.float64) + b.astype(np.float64)).astype(np.float16)
+    via32 = (a.astype(np.float32) + b.astype(np.float32)).astype(np.float16)
+    same = (exact.view(np.uint16) == via32.view(np.uint16)) | (np.isnan(exact) & np.isnan(via32))
+    assert same.all(), (a[~same][:5], b[~same][:5])

@@ -6,14 +6,20 @@
 // ("DisentangledFlash", section "Hugging Face usage": an LSE-producing
 // forward; section "Status": the [B, H, L, L] matrix is never stored).
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warp 0      TMA producer: Q once, K/V tiles into a 2-stage ring, for
 //               band tiles the Kr / Qr band rows; it also writes each key
 //               tile's column term to shared memory.
-//   warp 1      tcgen05 issuer (the whole warp walks the loop, elect.sync
-//               picks the issuing lane) and TMEM owner.
+//   warp 1      tcgen05 issuer of S and the band products (the whole warp
+//               walks the loop, elect.sync picks the issuing lane) and TMEM
+//               owner.
 //   warps 2..9  softmax: a thread owns one query row (= TMEM lane) and one
 //               half of the columns of every key tile.
+//   warp 10     tcgen05 issuer of the P.V products.  S of tile n + 2 waits
+//               for P.V of tile n (same S buffer); with one issuer for both,
+//               P.V of tile n + 1 queued behind that wait.  A commit tracks
+//               the MMAs of its own thread, so each issuer's barriers see
+//               only its own products.
 // The two column halves of a row run independent online softmaxes, each with
 // its own running max and sum and its own output accumulator in tensor
 // memory (O_h += P_h V_h, K = BN/2 per tile); they are merged once, in the
@@ -41,7 +47,7 @@
 namespace df {
 namespace {
 
-constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
+constexpr int kThreads = 352;   // producer, S issuer, eight softmax warps, P.V issuer
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;   // keep a stale max while the new one exceeds it by <= 8 (2^8 headroom)
@@ -96,7 +102,7 @@ struct FwdBars {
     uint64_t tb_full[2], tb_empty[2];       // band-product chunk buffers in tensor memory
     uint64_t s_full[2], pv_done[2];
     uint64_t p_full[4];   // [column half][tile parity]: P of a half of a tile is in tensor memory
-    uint64_t drain;   // the issuer's last MMAs, before the tensor memory is freed
+    uint64_t drain;   // both issuers' last MMAs, before the tensor memory is freed
     uint32_t tmem_base;
     int abort_flag;
     int cross_base[4];
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->tb_full[s], 1);
             mbar_init(&bars->tb_empty[s], 8);
         }
-        mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain, 2);
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_drain(&bars->band_full[r], ((band_loads - 1 - r) / S::NBS) & 1, wc.limit_ns);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ S / band-product issuer
         // The whole warp walks the issue loop (its control flow warp-uniform);
         // the MMAs and commits are the elect.sync forms, issued by one lane.
         // Operand descriptors are built once (per CTA or per ring stage) and
@@ -290,22 +296,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sQ = smem_u32(smem + S::Q), sBand = smem_u32(smem + S::BAND);
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
             constexpr uint32_t idT = idesc_f16(128, kBandChunk, BF16, false, false);
-            constexpr uint32_t idO = idesc_f16(128, D, BF16, false, true);
             const uint64_t dQ = desc_k<G>(sQ, BM, 0), dBand = desc_k<G>(sBand, kBandChunk, 0);
             const uint64_t dK0 = desc_k<G>(smem_u32(smem + S::K0), BN, 0), dK1 = dadd(dK0, S::KVB);
-            const uint64_t dV0 = desc_mn<G>(smem_u32(smem + S::V0), BN, 0), dV1 = dadd(dV0, S::KVB);
             bool ok = mbar_wait_warp(&bars->q_full, 0, wc);
-            int pv_cnt0 = 0, pv_cnt1 = 0;   // P.V rounds issued per S buffer
-            int bc = 0;                     // band chunks issued: ring slot bc % NBS, chunk buffer bc & 1
+            int bc = 0;   // band chunks issued: ring slot bc % NBS, chunk buffer bc & 1
             // S of tile m into buffer m & 1.  K's stage is released here for a
             // uniform tile, after the cross product for a band tile.
             auto issue_s = [&](int m, const TileKind& tk) -> bool {
                 const int s = m & 1, use = m >> 1;
                 const uint64_t dK = s ? dK1 : dK0;
                 if (!mbar_wait_warp(&bars->k_full[s], use & 1, wc)) return false;
-                // buffer s free: its previous P consumed
-                const int pvc = s ? pv_cnt1 : pv_cnt0;
-                if (pvc > 0 && !mbar_wait_warp(&bars->pv_done[s], (pvc - 1) & 1, wc)) return false;
+                // buffer s free: P.V of tile m - 2 has consumed its P
+                if (m >= 2 && !mbar_wait_warp(&bars->pv_done[s], ((m - 2) >> 1) & 1, wc)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
@@ -314,15 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (tk.uniform) tc_commit_w(&bars->k_empty[s]);
                 return true;
             };
-            // chunks g0 .. g1 - 1 of band tile m's products: chunk g < nch is
+            // the chunks of band tile m's products: chunk g < nch is
             // Q . Kr[dlo + 64 g ..]^T (lanes = query rows), chunk nch + g is
             // K . Qr[dlo + 64 g ..]^T (lanes = key columns).  Each waits for its
             // chunk buffer's previous chunk to be copied out and its band rows.
-            auto issue_band = [&](int m, const TileKind& tk, int g0, int g1) -> bool {
+            auto issue_band = [&](int m, const TileKind& tk) -> bool {
                 const int nch = band_chunks(tk);
                 const int s = m & 1, use = m >> 1;
                 const uint64_t dK = s ? dK1 : dK0;
-                for (int g = g0; g < g1 && g < 2 * nch; ++g) {
+                for (int g = 0; g < 2 * nch; ++g) {
                     const int tb = bc & 1, r = bc % S::NBS;
                     if (bc >= 2 && !mbar_wait_warp(&bars->tb_empty[tb], ((bc >> 1) - 1) & 1, wc)) return false;
                     if (!mbar_wait_warp(&bars->band_full[r], (bc / S::NBS) & 1, wc)) return false;
@@ -347,23 +349,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             // test-only stall injection: the issuer stops before this tile, so
             // that the other roles' bounded waits run out
             const int stall = p.fault_kernel == 0 ? p.fault_tile : -1;
-            if (ok && stall != 0) {
-                const TileKind k0 = unpack_kind(kinds[0]);
-                ok = issue_s(0, k0) && (k0.uniform || issue_band(0, k0, 0, 8));
+            // S of every tile, then its band chunks: the first two as soon as
+            // the previous band tile's chunks are copied out (early in that
+            // tile), the rest as the softmax warps copy this tile's own, so S
+            // of the next tile follows this tile's copies, well before the
+            // softmax warps need it
+            for (int m = 0; m < ntiles && ok; ++m) {
+                if (stall >= 0 && m >= stall) break;
+                const TileKind tk = unpack_kind(kinds[m]);
+                ok = issue_s(m, tk) && (tk.uniform || issue_band(m, tk));
             }
+            // every MMA issued above has completed before the tensor memory is freed
+            tc_commit_w(&bars->drain);
+            mbar_drain(&bars->drain, 0, wc.limit_ns);
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ P.V issuer
+        // O_h += P_h V_h for the two column halves of every tile, each as soon
+        // as its P is ready; V's stage and the S buffer are released after.
+        {
+            constexpr uint32_t idO = idesc_f16(128, D, BF16, false, true);
+            const uint64_t dV0 = desc_mn<G>(smem_u32(smem + S::V0), BN, 0), dV1 = dadd(dV0, S::KVB);
+            bool ok = true;
             for (int it = 0; it < ntiles && ok; ++it) {
-                if (stall >= 0 && it + 1 >= stall) break;
                 const int s = it & 1;
                 const uint64_t dV = s ? dV1 : dV0;
-                const TileKind kn = unpack_kind(kinds[it + 1 < ntiles ? it + 1 : it]);
-                // the next tile's S (and the first two chunks of its band
-                // products) while the softmax works on this one; the two
-                // chunks' buffers were copied out at the start of this tile
-                const bool next = it + 1 < ntiles;
-                const bool next_band = next && !kn.uniform;
-                if (next && !(ok = issue_s(it + 1, kn))) break;
-                if (next_band && !(ok = issue_band(it + 1, kn, 0, 2))) break;
-                // O_h += P_h V_h for the two column halves, each as soon as its P is ready
                 if (!(ok = mbar_wait_warp(&bars->v_full[s], (it >> 1) & 1, wc))) break;
                 for (int hf = 0; hf < 2 && ok; ++hf) {
                     if (!(ok = mbar_wait_warp(&bars->p_full[2 * hf + (it & 1)], (it >> 1) & 1, wc))) break;
@@ -376,12 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_commit_w(&bars->v_empty[s]);
                 tc_commit_w(&bars->pv_done[it & 1]);
-                if (it & 1) ++pv_cnt1; else ++pv_cnt0;
-                // the rest of the next tile's chunks, each as the softmax warps
-                // copy out the chunk before it in the same buffer
-                if (next_band && !(ok = issue_band(it + 1, kn, 2, 8))) break;
             }
-            // every MMA issued above has completed before the tensor memory is freed
             tc_commit_w(&bars->drain);
             mbar_drain(&bars->drain, 0, wc.limit_ns);
         }

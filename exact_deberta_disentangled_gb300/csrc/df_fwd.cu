@@ -191,15 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of band tiles; -inf past the sequence end), four tiles deep, and
         // announces it on tile m's S barrier.  Tile m's term goes to slot m & 3
         // once V of tile m - 1 is loaded: that load waited for P.V of tile
-        // m - 3, so tile m - 4 is long done.
+        // m - 3, so tile m - 4 is long done.  Per tile n: V(n), then K(n + 1),
+        // the column terms of n + 1 (their global loads issued a tile ahead)
+        // and the band rows of n + 1, so that K, which S waits for, is never
+        // queued behind the column terms' loads.
         const size_t T = (size_t)p.T;
         const float* relb_h = relb + (size_t)h * 4 * T;
-        auto put_columns = [&](int m) -> bool {
+        constexpr int NJ = BN / 32;
+        float cb[NJ];
+        int mk[NJ];
+        auto fetch_columns = [&](int m) {
             const TileKind k = unpack_kind(kinds[m]);
-            float* cv = colv + (m & 3) * BN;
-            constexpr int NJ = BN / 32;
-            float cb[NJ];
-            int mk[NJ];
 #pragma unroll
             for (int q = 0; q < NJ; ++q) {
                 const int j = m * BN + 32 * q + lane;
@@ -207,6 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cb[q] = k.uniform ? ld_early(relb_h + (2 + k.which) * T + t0 + js) : 0.f;
                 mk[q] = (!k.uniform && p.kmask) ? ld_early(p.kmask + t0 + js) : 1;
             }
+        };
+        auto put_columns = [&](int m) -> bool {
+            float* cv = colv + (m & 3) * BN;
 #pragma unroll
             for (int q = 0; q < NJ; ++q) {
                 const int j = 32 * q + lane;
@@ -219,40 +224,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bars->s_full[m & 1]);
             return true;
         };
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(&bars->q_full, S::QB);
-            for (int c = 0; c < G::NCH; ++c)
-                tma_load_2d(smem + S::Q + c * BM * G::CW * 2, &tmQ, h * D + c * G::CW, t0 + i0, &bars->q_full);
-        }
-        bool pc_ok = put_columns(0);
         int band_loads = 0, k_cnt[2] = {0, 0}, v_cnt[2] = {0, 0};   // copies issued per barrier
-        for (int it = 0; it < ntiles && pc_ok; ++it) {
-            const int s = it & 1, use = it >> 1;
-            const int j0 = it * BN;
-            // K of tile it as soon as S (band tile: and the cross product) of
-            // tile it - 2 has read its stage
-            if (use > 0 && !mbar_wait_warp(&bars->k_empty[s], (use - 1) & 1, wc)) break;
+        // K of tile m as soon as S (band tile: and the cross product) of tile
+        // m - 2 has read its stage
+        auto load_k = [&](int m) -> bool {
+            const int s = m & 1, use = m >> 1;
+            if (use > 0 && !mbar_wait_warp(&bars->k_empty[s], (use - 1) & 1, wc)) return false;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->k_full[s], S::KVB);
                 for (int c = 0; c < G::NCH; ++c)
-                    tma_load_2d(smem + S::K0 + s * S::KVB + c * BN * G::CW * 2, &tmK, h * D + c * G::CW, t0 + j0,
-                                &bars->k_full[s]);
+                    tma_load_2d(smem + S::K0 + s * S::KVB + c * BN * G::CW * 2, &tmK, h * D + c * G::CW,
+                                t0 + m * BN, &bars->k_full[s]);
             }
             ++k_cnt[s];
-            const TileKind tk = unpack_kind(kinds[it]);
-            bool ok = true;
-            // band rows of the tile's product chunks: Kr rows for the own
-            // product, then Qr rows for the cross product, 64 per ring slot
+            return true;
+        };
+        // V of tile m once P.V of tile m - 2 has read its stage
+        auto load_v = [&](int m) -> bool {
+            const int s = m & 1, use = m >> 1;
+            if (use > 0 && !mbar_wait_warp(&bars->v_empty[s], (use - 1) & 1, wc)) return false;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->v_full[s], S::KVB);
+                for (int c = 0; c < G::NCH; ++c)
+                    tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW,
+                                t0 + m * BN, &bars->v_full[s]);
+            }
+            ++v_cnt[s];
+            return true;
+        };
+        // band rows of tile m's product chunks: Kr rows for the own product,
+        // then Qr rows for the cross product, 64 per ring slot
+        auto load_band = [&](int m) -> bool {
+            const TileKind tk = unpack_kind(kinds[m]);
             const int nch = tk.uniform ? 0 : band_chunks(tk);
             for (int g = 0; g < 2 * nch; ++g) {
                 const int r = band_loads % S::NBS, u = band_loads / S::NBS;
-                if (u > 0 && !mbar_wait_warp(&bars->band_empty[r], (u - 1) & 1, wc)) {
-                    ok = false;
-                    break;
-                }
+                if (u > 0 && !mbar_wait_warp(&bars->band_empty[r], (u - 1) & 1, wc)) return false;
                 if (lane == 0) {
                     const int row0 = h * p.R + tk.dlo + kBandChunk * (g < nch ? g : g - nch);
                     mbar_arrive_expect_tx(&bars->band_full[r], S::BSLOT);
@@ -262,17 +269,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++band_loads;
             }
-            if (!ok) break;
-            // V of tile it once P.V of tile it - 2 has read its stage
-            if (use > 0 && !mbar_wait_warp(&bars->v_empty[s], (use - 1) & 1, wc)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars->v_full[s], S::KVB);
-                for (int c = 0; c < G::NCH; ++c)
-                    tma_load_2d(smem + S::V0 + s * S::KVB + c * BN * G::CW * 2, &tmV, h * D + c * G::CW, t0 + j0,
-                                &bars->v_full[s]);
-            }
-            ++v_cnt[s];
-            if (it + 1 < ntiles) pc_ok = put_columns(it + 1);
+            return true;
+        };
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(&bars->q_full, S::QB);
+            for (int c = 0; c < G::NCH; ++c)
+                tma_load_2d(smem + S::Q + c * BM * G::CW * 2, &tmQ, h * D + c * G::CW, t0 + i0, &bars->q_full);
+        }
+        fetch_columns(0);
+        bool ok = load_k(0) && put_columns(0);
+        if (ntiles > 1) fetch_columns(1);
+        ok = ok && load_band(0);
+        for (int it = 0; it < ntiles && ok; ++it) {
+            if (!(ok = load_v(it)) || it + 1 == ntiles) break;
+            ok = load_k(it + 1) && put_columns(it + 1);
+            if (it + 2 < ntiles) fetch_columns(it + 2);
+            ok = ok && load_band(it + 1);
         }
         // no copy of this CTA is still landing in shared memory when it exits
         // (each barrier's last phase is its last copy; the ones before it

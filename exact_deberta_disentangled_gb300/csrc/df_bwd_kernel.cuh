@@ -649,6 +649,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint16_t* qstage = gstage + (size_t)w4 * 32 * S::QW;
                 uint16_t* grow = qstage + lane * S::QW + qoff;
                 const int mmax = S::QW - 1 - qoff;   // a clamp: grow[m] stays inside the row
+                // every relative row of the quarter has its slot in the box
+                // (qmin + qoff >= 0 by the choice of qa0); a tile breaking the
+                // other end is flagged and its runs are not stored
                 const bool bad = qmax + qoff > S::QW - 1;   // cannot happen for a valid tile
                 // this box still holds the previous band tile's sums until their
                 // reduce-add has read it: its issuer waits here, a whole chunk
@@ -663,7 +666,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = hf * 32 + lane; i < NCK; i += 64) qz[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
-                auto gput = [&](int m, float v) { grow[m < mmax ? m : mmax] = f2h16<BF16>(v); };
                 named_bar_sync(pair_bar, 64);   // the box is cleared
                 // Runs of equal relative index along the row (the index is
                 // monotone in the column).  With prefix sums along the row, a run
@@ -680,28 +682,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int x0 = ROWQ ? row - cst + BN - 1 : cst - row + BM - 1;
                 float pre = 0.f, last = 0.f;
                 int m_cur = dwin[x0];
-                // this half's dZ columns (16-bit, as the products use them), 32 at a time
-#pragma unroll 1
-                for (int g = 0; g < HC / 32 && ok; ++g) {
-                    uint32_t zr[16];
-                    tc_ld16p(lane_base + TM::Z + hf * (HC / 2) + 16 * g, zr);
-                    // bit 31 - e2 (query rows) or e2: step between columns 32 g + e2 and + 1
-                    const uint32_t mk = step_bits(bars->stepw, ROWQ ? x0 - 32 * g - 31 : x0 + 32 * g + 1);
-                    tc_wait_ld();
+                uint16_t* gp = grow + m_cur;   // the slot of the current run
+                if (ok && !bad) {
+                    // this half's dZ columns (16-bit, as the products use them), 32 at a time
 #pragma unroll
-                    for (int e2 = 0; e2 < 32; ++e2) {
-                        pre += h16f<BF16>((uint16_t)(zr[e2 >> 1] >> (16 * (e2 & 1))));
-                        const bool step = ((ROWQ ? mk >> (31 - e2) : mk >> e2) & 1u) != 0;
-                        if (32 * g + e2 + 1 < HC && step) {
-                            gput(m_cur, pre - last);
-                            last = pre;
-                            m_cur += ROWQ ? -1 : 1;
+                    for (int g = 0; g < HC / 32; ++g) {
+                        uint32_t zr[16];
+                        tc_ld16p(lane_base + TM::Z + hf * (HC / 2) + 16 * g, zr);
+                        // bit 31 - e2 (query rows) or e2: step between columns 32 g + e2 and + 1
+                        const uint32_t mk = step_bits(bars->stepw, ROWQ ? x0 - 32 * g - 31 : x0 + 32 * g + 1);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e2 = 0; e2 < 32; ++e2) {
+                            pre += h16f<BF16>((uint16_t)(zr[e2 >> 1] >> (16 * (e2 & 1))));
+                            const bool step = ((ROWQ ? mk >> (31 - e2) : mk >> e2) & 1u) != 0;
+                            if (32 * g + e2 + 1 < HC && step) {
+                                *gp = f2h16<BF16>(pre - last);
+                                last = pre;
+                                gp += ROWQ ? -1 : 1;
+                            }
                         }
                     }
+                    m_cur = (int)(gp - grow);
                 }
                 const float tail = pre - last;   // the run that ends this half
                 if (ok && hf) {
-                    gput(m_cur, tail);
+                    if (!bad) *gp = f2h16<BF16>(tail);
                     fence_proxy_async_smem();   // the box is read by the tensor-memory-access unit
                 }
                 tc_fence_before();

@@ -1,14 +1,15 @@
 // df_bwd.cu -- the backward pass: clears the diagonal-sum buffers G / G',
 // stores the band bias (df_bias.cu), runs the dQ kernel and the dK/dV kernel
-// (df_bwd_kernel.cuh) and then the relative-position gradients (df_rel.cu).
+// (df_bwd_kernel.cuh), each followed by the half of the relative-position
+// gradients (df_rel.cu) that needs only its own diagonal sums.
 //
 // "DisentangledFlash" (section "Hugging Face usage") splits the fused
 // backward into a dQ kernel and a dK/dV kernel; section "Performance" counts
 // the relative-position gradients.
 //
 // The dQ and dK/dV kernels read the same inputs and write disjoint outputs,
-// so they run concurrently: dQ on a side stream forked from the caller's
-// stream and joined back before the relative-gradient kernels.  Each kernel
+// so they run concurrently: dQ and its relative-gradient half on a side
+// stream forked from the caller's stream and joined back at the end.  Each kernel
 // is 128-row CTAs over (sequence, head) pairs -- at the L = 8192 workload
 // 1,536 CTAs, ten full waves on 152 SMs and a 16-CTA tail -- and running the
 // two together lets one kernel's tail overlap the other's waves.
@@ -55,8 +56,9 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
     if (p.D != 32 && p.D != 64 && p.D != 128) return (int)cudaErrorInvalidValue;
     const int Rp = ws.Rp;
     const size_t gbytes = (size_t)p.T * p.H * Rp * 2;
+    // G (the dQ kernel's) is cleared before the fork, G' (the dK/dV kernel's)
+    // after it, while the dQ kernel starts
     cudaError_t ce = cudaMemsetAsync(ws.G, 0, gbytes, st);
-    if (ce == cudaSuccess) ce = cudaMemsetAsync(ws.Gp, 0, gbytes, st);
     if (ce != cudaSuccess) return (int)ce;
     // the relative-position bias of every band block, read by both kernels
     // (unless the forward saved it)
@@ -73,17 +75,25 @@ int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const v
             cudaGetLastError();
             conc = false;   // both kernels on the caller's stream instead
         }
-        // dQ kernel: rows = queries (Q, dO), columns = keys (K, V)
-        e = launch_bwd_dq(p, ws, dt, q, dout, k, v, ws.G, Rp, ws.acc32a, nullptr, lse, conc ? side : st);
+        // dQ kernel: rows = queries (Q, dO), columns = keys (K, V); then the
+        // relative-position gradients that need only its G (dQ, dKr), while
+        // the dK/dV kernel still runs
+        const cudaStream_t sq = conc ? side : st;
+        e = launch_bwd_dq(p, ws, dt, q, dout, k, v, ws.G, Rp, ws.acc32a, nullptr, lse, sq);
+        if (!e) e = launch_rel_tc(p, ws, dt, Rp, 0, q, kr, dq, dkr, sq, hook);
         if (conc) cudaEventRecord(join, side);
-        // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO)
+        // dK/dV kernel: rows = keys (K, V), columns = queries (Q, dO); then dK,
+        // dQr.  Launched after the dQ kernel has been handed to the side
+        // stream, so that the dQ kernel, the shorter of the two, takes the SMs
+        // first and the dK/dV kernel's waves fill in behind it.
+        if (!e && (ce = cudaMemsetAsync(ws.Gp, 0, gbytes, st)) != cudaSuccess) e = (int)ce;
         if (!e) e = launch_bwd_dkv(p, ws, dt, k, v, q, dout, ws.Gp, Rp, ws.acc32b, dv, lse, st);
         if (!e && hook) hook->fn(hook->ctx, 0, st);   // dV is final
-        // the caller's stream continues only after the dQ kernel too
+        if (!e) e = launch_rel_tc(p, ws, dt, Rp, 1, k, qr, dk, dqr, st, hook);
+        // the caller's stream continues only after the side stream's work too
         if (conc && cudaStreamWaitEvent(st, join, 0) != cudaSuccess && !e) e = (int)cudaErrorUnknown;
     }
-    if (e) return e;
-    return launch_rel_tc(p, ws, dt, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook);
+    return e;
 }
 
 }  // namespace df

@@ -439,14 +439,14 @@ constexpr int kMaxCopyDevices = 64;
 std::mutex g_copy_mu;
 bool g_copy_tried[kMaxCopyDevices];
 cudaStream_t g_copy_st[kMaxCopyDevices];
-cudaEvent_t g_copy_ev[kMaxCopyDevices][6];   // start, dout up, forward done, copies down done, dV / dQ+dK final
+cudaEvent_t g_copy_ev[kMaxCopyDevices][7];   // start, dout up, forward done, copies down done, dV / dQ / dK final
 
 bool copy_stream(int dev, cudaStream_t& cs, cudaEvent_t*& ev) {
     if (dev < 0 || dev >= kMaxCopyDevices) return false;
     if (!g_copy_tried[dev]) {
         g_copy_tried[dev] = true;
         bool ok = cudaStreamCreateWithFlags(&g_copy_st[dev], cudaStreamNonBlocking) == cudaSuccess;
-        for (int i = 0; i < 6 && ok; ++i)
+        for (int i = 0; i < 7 && ok; ++i)
             ok = cudaEventCreateWithFlags(&g_copy_ev[dev][i], cudaEventDisableTiming) == cudaSuccess;
         if (!ok) {
             cudaGetLastError();
@@ -530,16 +530,17 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
              d2h(out, L.out, tok, cs) && d2h(lse, L.lse, lseb, cs) && cudaStreamWaitEvent(st, ev[1], 0) == cudaSuccess;
         if (!ok) return DF_ERR_CUDA;
     }
-    // dV, then dQ and dK, are final before the backward's last kernels: the
-    // backward's hook sends them down on the copy stream while those run
+    // dQ (after the dQ kernel and its relative-gradient half), dV and dK are
+    // final before the backward's last kernels: the backward's hook sends each
+    // down on the copy stream while the rest runs
     struct Down {
         cudaStream_t cs;
         cudaEvent_t* ev;
         const char* base;
         size_t off_dv, off_dq, off_dk, tok;
         void *dv, *dq, *dk;
-        bool dv_sent, dqdk_sent, ok;
-    } down{cs, ev, base, L.dv, L.dq, L.dk, tok, dv, dq, dk, false, false, true};
+        bool sent[3], ok;
+    } down{cs, ev, base, L.dv, L.dq, L.dk, tok, dv, dq, dk, {false, false, false}, true};
     const BwdHook hook{[](void* ctx, int point, cudaStream_t s2) {
                            Down& d = *static_cast<Down*>(ctx);
                            cudaEvent_t e = d.ev[4 + point];
@@ -549,14 +550,10 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
                                d.ok = d.ok && cudaMemcpyAsync(dst, d.base + off, d.tok, cudaMemcpyDeviceToHost,
                                                               d.cs) == cudaSuccess;
                            };
-                           if (point == 0) {
-                               down1(d.dv, d.off_dv);
-                               d.dv_sent = true;
-                           } else {
-                               down1(d.dq, d.off_dq);
-                               down1(d.dk, d.off_dk);
-                               d.dqdk_sent = true;
-                           }
+                           if (point == 0) down1(d.dv, d.off_dv);
+                           else if (point == 1) down1(d.dq, d.off_dq);
+                           else down1(d.dk, d.off_dk);
+                           d.sent[point] = true;
                        },
                        &down};
     s = bwd_common(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
@@ -565,8 +562,9 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     if (s != DF_OK) return s;
     if (!down.ok) return DF_ERR_CUDA;
     ok = d2h(dqr, L.dqr, rel, st) && d2h(dkr, L.dkr, rel, st);
-    if (!down.dv_sent) ok = ok && d2h(dv, L.dv, tok, st);
-    if (!down.dqdk_sent) ok = ok && d2h(dq, L.dq, tok, st) && d2h(dk, L.dk, tok, st);
+    if (!down.sent[0]) ok = ok && d2h(dv, L.dv, tok, st);
+    if (!down.sent[1]) ok = ok && d2h(dq, L.dq, tok, st);
+    if (!down.sent[2]) ok = ok && d2h(dk, L.dk, tok, st);
     if (!side) ok = ok && d2h(out, L.out, tok, st) && d2h(lse, L.lse, lseb, st);
     else ok = ok && cudaEventRecord(ev[3], cs) == cudaSuccess && cudaStreamWaitEvent(st, ev[3], 0) == cudaSuccess;
     if (!ok) return DF_ERR_CUDA;

@@ -84,8 +84,9 @@ int launch_bwd_f32(const ProblemDev& p, const Workspace& ws, const float* q, con
 int launch_fwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
                   const void* v, const void* qr, const void* kr, void* out, float* lse, cudaStream_t st);
 // Optional hook of the tensor-core backward: called with the launching stream
-// right after the launches that finish dV (point 0) and dQ / dK (point 1), so
-// that a caller can start copying those gradients while the rest runs.
+// right after the launches that finish dV (point 0), dQ (point 1, on the
+// stream of the dQ kernel) and dK (point 2), so that a caller can start
+// copying those gradients while the rest runs.
 struct BwdHook {
     void (*fn)(void* ctx, int point, cudaStream_t st);
     void* ctx;
@@ -105,9 +106,13 @@ int launch_bwd_dkv(const ProblemDev& p, const Workspace& ws, df_dtype dt, const 
 // the stored band bias of every band block (df_bias.cu)
 int launch_band_bias(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
                      const void* qr, const void* kr, cudaStream_t st);
-int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, const void* q, const void* k,
-                  const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st,
-                  const BwdHook* hook = nullptr);
+// One half of the relative-position gradients (df_rel.cu).  Half 0, from G
+// (the dQ kernel's diagonal sums):  dQ = acc(dQ) + G Kr,  dKr = sum G^T Q.
+// Half 1, from G' (the dK/dV kernel's):  dK = acc(dK) + G' Qr,  dQr = sum G'^T K.
+// x / xr are Q / Kr (half 0) or K / Qr (half 1); out_tok is dQ / dK and
+// out_rel dKr / dQr.  The hook is called at point 1 + half once out_tok is final.
+int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, int half, const void* x,
+                  const void* xr, void* out_tok, void* out_rel, cudaStream_t st, const BwdHook* hook = nullptr);
 
 // Optional benchmark timing hooks (df_attn_set_profile_events): record the
 // begin / end event of a kernel phase on the launching stream.

@@ -273,11 +273,14 @@ __global__ void rel_reduce_kernel(const float* __restrict__ part, int nchunk, si
 }
 
 template <int D, bool BF16>
-int rel_impl(const ProblemDev& p, const Workspace& ws, int Rp, const void* q, const void* k, const void* qr,
-             const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st, const BwdHook* hook) {
+int rel_impl(const ProblemDev& p, const Workspace& ws, int Rp, int half, const void* x, const void* xr,
+             void* out_tok, void* out_rel, cudaStream_t st, const BwdHook* hook) {
     using G = Geo<D>;
     const int code = BF16 ? 0 : 1;
-    CUtensorMap mG, mGp, mKr, mQr, mQ, mK, mGc, mGpc;
+    void* gbuf = half ? ws.Gp : ws.G;
+    const float* acc = half ? ws.acc32b : ws.acc32a;
+    float* part = half ? ws.part_qr : ws.part_kr;
+    CUtensorMap mG, mXr, mX, mGc;
     const uint64_t g_dims[2] = {(uint64_t)p.H * Rp, (uint64_t)p.T};
     const uint64_t g_str[1] = {(uint64_t)p.H * Rp * 2};
     const uint64_t rel_dims[2] = {(uint64_t)D, (uint64_t)p.H * p.R};
@@ -287,25 +290,21 @@ int rel_impl(const ProblemDev& p, const Workspace& ws, int Rp, const void* q, co
     const uint32_t box_ga[2] = {64, 128};
     const uint32_t box_gc[2] = {64, (uint32_t)kChunkTok};
     const uint32_t box_x[2] = {(uint32_t)G::CW, 64};
-    if (encode_tmap(&mG, code, 2, g_dims, g_str, box_ga, 128, ws.G) ||
-        encode_tmap(&mGp, code, 2, g_dims, g_str, box_ga, 128, ws.Gp) ||
-        encode_tmap(&mKr, code, 2, rel_dims, rel_str, box_x, G::SWZB, kr) ||
-        encode_tmap(&mQr, code, 2, rel_dims, rel_str, box_x, G::SWZB, qr) ||
-        encode_tmap(&mQ, code, 2, tok_dims, tok_str, box_x, G::SWZB, q) ||
-        encode_tmap(&mK, code, 2, tok_dims, tok_str, box_x, G::SWZB, k) ||
-        encode_tmap(&mGc, code, 2, g_dims, g_str, box_gc, 128, ws.G) ||
-        encode_tmap(&mGpc, code, 2, g_dims, g_str, box_gc, 128, ws.Gp))
+    if (encode_tmap(&mG, code, 2, g_dims, g_str, box_ga, 128, gbuf) ||
+        encode_tmap(&mXr, code, 2, rel_dims, rel_str, box_x, G::SWZB, xr) ||
+        encode_tmap(&mX, code, 2, tok_dims, tok_str, box_x, G::SWZB, x) ||
+        encode_tmap(&mGc, code, 2, g_dims, g_str, box_gc, 128, gbuf))
         return (int)cudaErrorInvalidValue;
-    prof_record(kProfRel, 0, st);
+    // the benchmark's relative-gradient phase is the half on the caller's stream
+    if (half) prof_record(kProfRel, 0, st);
     {
         auto kern = rel_row_kernel<D, BF16>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RowSmem<D>::ALLOC);
         if (e != cudaSuccess) return (int)e;
         dim3 grid((p.T + 127) / 128, p.H);
-        kern<<<grid, kRelThreads, RowSmem<D>::ALLOC, st>>>(mG, mKr, p, Rp, ws.acc32a, dq);
-        kern<<<grid, kRelThreads, RowSmem<D>::ALLOC, st>>>(mGp, mQr, p, Rp, ws.acc32b, dk);
+        kern<<<grid, kRelThreads, RowSmem<D>::ALLOC, st>>>(mG, mXr, p, Rp, acc, out_tok);
         if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
-        if (hook) hook->fn(hook->ctx, 1, st);   // dQ and dK are final
+        if (hook) hook->fn(hook->ctx, 1 + half, st);   // dQ (dK) is final
     }
     {
         auto kern = rel_col_kernel<D, BF16>;
@@ -313,32 +312,29 @@ int rel_impl(const ProblemDev& p, const Workspace& ws, int Rp, const void* q, co
         if (e != cudaSuccess) return (int)e;
         const int chunk_tokens = ((p.T + ws.nchunk - 1) / ws.nchunk + kChunkTok - 1) / kChunkTok * kChunkTok;
         dim3 grid((p.R + 127) / 128, p.H, ws.nchunk);
-        kern<<<grid, kRelThreads, ColSmem<D>::ALLOC, st>>>(mGc, mQ, p, Rp, chunk_tokens, ws.part_kr);
-        kern<<<grid, kRelThreads, ColSmem<D>::ALLOC, st>>>(mGpc, mK, p, Rp, chunk_tokens, ws.part_qr);
+        kern<<<grid, kRelThreads, ColSmem<D>::ALLOC, st>>>(mGc, mX, p, Rp, chunk_tokens, part);
         if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
     }
     const size_t per = (size_t)p.H * p.R * D;
     const int blocks = (int)((per + 255) / 256 < 1024 ? (per + 255) / 256 : 1024);
-    rel_reduce_kernel<BF16><<<blocks, 256, 0, st>>>(ws.part_kr, ws.nchunk, per, dkr);
-    rel_reduce_kernel<BF16><<<blocks, 256, 0, st>>>(ws.part_qr, ws.nchunk, per, dqr);
-    prof_record(kProfRel, 1, st);
+    rel_reduce_kernel<BF16><<<blocks, 256, 0, st>>>(part, ws.nchunk, per, out_rel);
+    if (half) prof_record(kProfRel, 1, st);
     return (int)cudaGetLastError();
 }
 
 }  // namespace
 
-int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, const void* q, const void* k,
-                  const void* qr, const void* kr, void* dq, void* dk, void* dqr, void* dkr, cudaStream_t st,
-                  const BwdHook* hook) {
+int launch_rel_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, int Rp, int half, const void* x,
+                  const void* xr, void* out_tok, void* out_rel, cudaStream_t st, const BwdHook* hook) {
     const bool bf = dt == DF_BF16;
+#define DF_REL(D_) (bf ? rel_impl<D_, true>(p, ws, Rp, half, x, xr, out_tok, out_rel, st, hook) \
+                       : rel_impl<D_, false>(p, ws, Rp, half, x, xr, out_tok, out_rel, st, hook))
     switch (p.D) {
-        case 32: return bf ? rel_impl<32, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook)
-                           : rel_impl<32, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook);
-        case 64: return bf ? rel_impl<64, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook)
-                           : rel_impl<64, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook);
-        case 128: return bf ? rel_impl<128, true>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook)
-                            : rel_impl<128, false>(p, ws, Rp, q, k, qr, kr, dq, dk, dqr, dkr, st, hook);
+        case 32: return DF_REL(32);
+        case 64: return DF_REL(64);
+        case 128: return DF_REL(128);
     }
+#undef DF_REL
     return (int)cudaErrorInvalidValue;
 }
 

@@ -339,10 +339,13 @@ def run_gpu(args, rank, world, local_rank):
     #   fwd kernel  4 L^2 D + 4 L R D (all of the forward count)
     #   dK/dV kernel  S^T, dP^T, dV, dK products: 8 L^2 D
     #   dQ kernel     dQ product: 2 L^2 D (its recomputed S, dP are not credited)
-    #   rel kernels   the relative-position gradient products: 8 L R D
-    #   bwd_attn      the dQ and dK/dV kernels, which run concurrently: 10 L^2 D
+    #   rel           the relative-position gradient half on the caller's
+    #                 stream after the dK/dV kernel (dK += G' Qr, dQr): 4 L R D
+    #   bwd_attn      the dQ and dK/dV kernels, which run concurrently, and the
+    #                 other relative half (dQ += G Kr, dKr), which runs on the
+    #                 dQ kernel's stream inside the same window: 10 L^2 D + 4 L R D
     kflops = {"fwd": fl_f, "dkv": B * H * 8 * L * L * D, "dq": B * H * 2 * L * L * D,
-              "rel": B * H * 8 * L * R * D, "bwd_attn": B * H * 10 * L * L * D}
+              "rel": B * H * 4 * L * R * D, "bwd_attn": B * H * (10 * L * L * D + 4 * L * R * D)}
     peak = peaks.get("bf16_tflops", 1900.0)
     achieved = kflops[dominant] / (avg[dominant] * 1e-3) / 1e12
     traffic = kernel_traffic(dominant)

@@ -8,6 +8,7 @@ it raises -- there is no other implementation to fall back on.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -67,64 +68,83 @@ def load():
         if _lib is None:
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(f"{LIB_PATH} is missing: build it with exact_deberta_disentangled_gb300.build.build()")
-            lib = ctypes.CDLL(LIB_PATH)
-            vp, sz = ctypes.c_void_p, ctypes.c_size_t
-            P = ctypes.POINTER(Params)
-            lib.df_attn_workspace_size.restype = sz
-            lib.df_attn_workspace_size.argtypes = [P, ctypes.c_int]
-            lib.df_attn_band_bias_size.restype = sz
-            lib.df_attn_band_bias_size.argtypes = [P]
-            lib.df_attn_fwd.restype = ctypes.c_int
-            lib.df_attn_fwd.argtypes = [P] + [vp] * 7 + [vp, sz, vp]
-            lib.df_attn_fwd_inference.restype = ctypes.c_int
-            lib.df_attn_fwd_inference.argtypes = [P] + [vp] * 6 + [vp, sz, vp]
-            lib.df_attn_bwd.restype = ctypes.c_int
-            lib.df_attn_bwd.argtypes = [P] + [vp] * 13 + [vp, sz, vp]
-            lib.df_attn_step_host_arena_size.restype = sz
-            lib.df_attn_step_host_arena_size.argtypes = [P]
-            lib.df_attn_step_host.restype = ctypes.c_int
-            lib.df_attn_step_host.argtypes = [P] + [vp] * 13 + [vp, sz, vp]
-            lib.df_rel_index_table.restype = ctypes.c_int
-            lib.df_rel_index_table.argtypes = [ctypes.c_int32] * 4 + [vp, vp]
-            lib.df_get_device_error.restype = ctypes.c_int
-            lib.df_get_device_error.argtypes = [vp, vp]
-            lib.df_status_string.restype = ctypes.c_char_p
-            lib.df_status_string.argtypes = [ctypes.c_int]
-            lib.df_version.restype = ctypes.c_char_p
-            lib.df_attn_fwd_noalloc.restype = ctypes.c_int
-            lib.df_attn_fwd_noalloc.argtypes = [P] + [vp] * 7 + [vp]
-            lib.df_attn_fwd_noalloc_device_error.restype = ctypes.c_int
-            lib.df_attn_fwd_noalloc_device_error.argtypes = [vp]
-            lib.df_dropout_keep_mask.restype = ctypes.c_int
-            lib.df_dropout_keep_mask.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp]
-            lib.df_attn_debug_inject_stall.restype = ctypes.c_int
-            lib.df_attn_debug_inject_stall.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32]
-            lib.df_pack_workspace_size.restype = sz
-            lib.df_pack_workspace_size.argtypes = [ctypes.c_int32]
-            lib.df_pack_info.restype = ctypes.c_int
-            lib.df_pack_info.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp, sz, vp]
-            lib.df_pack_rows.restype = ctypes.c_int
-            lib.df_pack_rows.argtypes = [vp, ctypes.c_int32, vp, vp, ctypes.c_int32, sz, vp, vp]
-            lib.df_unpack_rows.restype = ctypes.c_int
-            lib.df_unpack_rows.argtypes = [vp, vp, vp, ctypes.c_int32, sz, ctypes.c_int32, vp, vp]
-            i32 = ctypes.c_int32
-            lib.df_qkv_proj_fwd.restype = ctypes.c_int
-            lib.df_qkv_proj_fwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp]
-            lib.df_qkv_proj_bwd.restype = ctypes.c_int
-            lib.df_qkv_proj_bwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
-            lib.df_qkv_proj_workspace_size.restype = sz
-            lib.df_qkv_proj_workspace_size.argtypes = [i32]
-            lib.df_rel_proj_workspace_size.restype = sz
-            lib.df_rel_proj_workspace_size.argtypes = [i32] * 4
-            lib.df_rel_proj_fwd.restype = ctypes.c_int
-            lib.df_rel_proj_fwd.argtypes = [i32] * 4 + [ctypes.c_int, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
-                                                        vp, vp, vp]
-            lib.df_rel_proj_bwd.restype = ctypes.c_int
-            lib.df_rel_proj_bwd.argtypes = [i32] * 4 + [ctypes.c_int] + [vp] * 12 + [i32, vp, sz, vp]
-            lib.df_attn_set_profile_events.restype = ctypes.c_int
-            lib.df_attn_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
-            _lib = lib
+            _lib = _configure(ctypes.CDLL(LIB_PATH))
     return _lib
+
+
+@contextlib.contextmanager
+def checked_library(path: str):
+    """Route every call of this module to the library at `path` (a build
+    with DF_CHECKED, see build.build(checked=True)) inside the block."""
+    global _lib
+    lib = _configure(ctypes.CDLL(path))
+    with _lock:
+        prev, _lib = _lib, lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def _configure(lib):
+    """Declare the argument and result types of the library's entry points."""
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    P = ctypes.POINTER(Params)
+    lib.df_attn_workspace_size.restype = sz
+    lib.df_attn_workspace_size.argtypes = [P, ctypes.c_int]
+    lib.df_attn_band_bias_size.restype = sz
+    lib.df_attn_band_bias_size.argtypes = [P]
+    lib.df_attn_fwd.restype = ctypes.c_int
+    lib.df_attn_fwd.argtypes = [P] + [vp] * 7 + [vp, sz, vp]
+    lib.df_attn_fwd_inference.restype = ctypes.c_int
+    lib.df_attn_fwd_inference.argtypes = [P] + [vp] * 6 + [vp, sz, vp]
+    lib.df_attn_bwd.restype = ctypes.c_int
+    lib.df_attn_bwd.argtypes = [P] + [vp] * 13 + [vp, sz, vp]
+    lib.df_attn_step_host_arena_size.restype = sz
+    lib.df_attn_step_host_arena_size.argtypes = [P]
+    lib.df_attn_step_host.restype = ctypes.c_int
+    lib.df_attn_step_host.argtypes = [P] + [vp] * 13 + [vp, sz, vp]
+    lib.df_rel_index_table.restype = ctypes.c_int
+    lib.df_rel_index_table.argtypes = [ctypes.c_int32] * 4 + [vp, vp]
+    lib.df_get_device_error.restype = ctypes.c_int
+    lib.df_get_device_error.argtypes = [vp, vp]
+    lib.df_status_string.restype = ctypes.c_char_p
+    lib.df_status_string.argtypes = [ctypes.c_int]
+    lib.df_version.restype = ctypes.c_char_p
+    lib.df_attn_fwd_noalloc.restype = ctypes.c_int
+    lib.df_attn_fwd_noalloc.argtypes = [P] + [vp] * 7 + [vp]
+    lib.df_attn_fwd_noalloc_device_error.restype = ctypes.c_int
+    lib.df_attn_fwd_noalloc_device_error.argtypes = [vp]
+    lib.df_dropout_keep_mask.restype = ctypes.c_int
+    lib.df_dropout_keep_mask.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp]
+    lib.df_attn_debug_inject_stall.restype = ctypes.c_int
+    lib.df_attn_debug_inject_stall.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32]
+    lib.df_pack_workspace_size.restype = sz
+    lib.df_pack_workspace_size.argtypes = [ctypes.c_int32]
+    lib.df_pack_info.restype = ctypes.c_int
+    lib.df_pack_info.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp, sz, vp]
+    lib.df_pack_rows.restype = ctypes.c_int
+    lib.df_pack_rows.argtypes = [vp, ctypes.c_int32, vp, vp, ctypes.c_int32, sz, vp, vp]
+    lib.df_unpack_rows.restype = ctypes.c_int
+    lib.df_unpack_rows.argtypes = [vp, vp, vp, ctypes.c_int32, sz, ctypes.c_int32, vp, vp]
+    i32 = ctypes.c_int32
+    lib.df_qkv_proj_fwd.restype = ctypes.c_int
+    lib.df_qkv_proj_fwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp]
+    lib.df_qkv_proj_bwd.restype = ctypes.c_int
+    lib.df_qkv_proj_bwd.argtypes = [i32, i32, i32, ctypes.c_int, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+    lib.df_qkv_proj_workspace_size.restype = sz
+    lib.df_qkv_proj_workspace_size.argtypes = [i32]
+    lib.df_rel_proj_workspace_size.restype = sz
+    lib.df_rel_proj_workspace_size.argtypes = [i32] * 4
+    lib.df_rel_proj_fwd.restype = ctypes.c_int
+    lib.df_rel_proj_fwd.argtypes = [i32] * 4 + [ctypes.c_int, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
+                                                vp, vp, vp]
+    lib.df_rel_proj_bwd.restype = ctypes.c_int
+    lib.df_rel_proj_bwd.argtypes = [i32] * 4 + [ctypes.c_int] + [vp] * 12 + [i32, vp, sz, vp]
+    lib.df_attn_set_profile_events.restype = ctypes.c_int
+    lib.df_attn_set_profile_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+    return lib
 
 
 def status_string(code: int) -> str:

@@ -298,7 +298,10 @@ __global__ void __launch_bounds__(kBiasThreads, 1)
             float vprev = 0.f;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const float v = h2f(orow[mi]) + h2f(crow[e * S::CROSS_S + mi]);
+                int mo = mi, mc = mi;
+                DF_CLAMP_CHECK(mo, own_a, own_a + S::OWN_S, p.err);
+                DF_CLAMP_CHECK(mc, bars->cross_base[cq], bars->cross_base[cq] + S::CROSS_S, p.err);
+                const float v = h2f(orow[mo]) + h2f(crow[e * S::CROSS_S + mc]);
                 mi -= (int)(mk >> 31);
                 mk <<= 1;
                 if (e & 1) pk[e >> 1] = pack2<false>(vprev, v); else vprev = v;

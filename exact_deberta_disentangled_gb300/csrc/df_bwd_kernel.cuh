@@ -516,7 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint4* brow4 = reinterpret_cast<const uint4*>(bbox + row * BN);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const uint4 w = brow4[bias_chunk(row, xo + 4 * c + q) - xo];
+                            int ci = bias_chunk(row, xo + 4 * c + q) - xo;   // 16-byte chunk of the box row
+                            DF_CLAMP_CHECK(ci, 0, BN / 8, p.err);
+                            const uint4 w = brow4[ci];
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
                             const float4 ca = cv0p[2 * q], cb = cv0p[2 * q + 1];
                             const float cvs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};

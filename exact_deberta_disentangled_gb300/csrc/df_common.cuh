@@ -97,6 +97,25 @@ DF_DEV void raise_error(int* word, int code) {
     if (word) atomicCAS(word, 0, code);
 }
 
+// Index checks of a checked build (compiled with DF_CHECKED): an index x
+// outside [lo, hi) records DF_ERR_DEVICE_CHECK in the error word and is
+// clamped into the range, so the access stays inside its buffer (no trap,
+// no fault).  Without DF_CHECKED the check is empty and the code is that of
+// the plain build.
+#ifdef DF_CHECKED
+#define DF_CLAMP_CHECK(x, lo, hi, err)                     \
+    do {                                                   \
+        if ((x) < (lo) || (x) >= (hi)) {                   \
+            raise_error((err), DF_ERR_DEVICE_CHECK);       \
+            (x) = (x) < (lo) ? (lo) : (hi) - 1;            \
+        }                                                  \
+    } while (0)
+#else
+#define DF_CLAMP_CHECK(x, lo, hi, err) \
+    do {                               \
+    } while (0)
+#endif
+
 DF_DEV uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -489,10 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t tcol = lane_base + TM::TB + tb * kBandChunk;
                     if (g < nch)
-                        copy_band_chunk(tcol, kBandChunk * g, lo, hi, own_a, own_row, kscale, hf);
+                        copy_band_chunk(tcol, kBandChunk * g, lo, hi, own_a, own_row, kscale, hf, G::OWN_S, p.err);
                     else if (32 * w4 < BN)
                         copy_band_chunk(tcol, kBandChunk * (g - nch), clo, chi, ca, cross + row * G::CROSS_S,
-                                        kscale, hf);
+                                        kscale, hf, G::CROSS_S, p.err);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars->tb_empty[tb]);
@@ -659,10 +659,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         const uint32_t mm = dw2[-2 * q];
-                        const int m0 = (int)(mm & 0xFFFFu), m1 = (int)(mm >> 16);
+                        int m0 = (int)(mm & 0xFFFFu), m1 = (int)(mm >> 16);
+                        int c0 = m0, c1 = m1;   // the cross window's own range check
+                        DF_CLAMP_CHECK(m0, own_a, own_a + G::OWN_S, p.err);
+                        DF_CLAMP_CHECK(m1, own_a, own_a + G::OWN_S, p.err);
+                        DF_CLAMP_CHECK(c0, bars->cross_base[c], bars->cross_base[c] + G::CROSS_S, p.err);
+                        DF_CLAMP_CHECK(c1, bars->cross_base[c], bars->cross_base[c] + G::CROSS_S, p.err);
                         const uint32_t ov = __byte_perm(orow[m0], orow[m1], 0x5410);
                         const uint32_t cv =
-                            __byte_perm(crow[2 * q * G::CROSS_S + m0], crow[(2 * q + 1) * G::CROSS_S + m1], 0x5410);
+                            __byte_perm(crow[2 * q * G::CROSS_S + c0], crow[(2 * q + 1) * G::CROSS_S + c1], 0x5410);
                         const uint32_t bb = band_bias2(ov, cv);
                         bpk[q] = bb;
                         float b0, b1;

@@ -258,6 +258,7 @@ const char* df_status_string(df_status s) {
         case DF_ERR_CUDA: return "DF_ERR_CUDA: CUDA runtime or launch error";
         case DF_ERR_TIMEOUT: return "DF_ERR_TIMEOUT: a bounded device wait gave up";
         case DF_ERR_DEVICE_ARG: return "DF_ERR_DEVICE_ARG: cu_seqlens inconsistent with B, L, total_tokens";
+        case DF_ERR_DEVICE_CHECK: return "DF_ERR_DEVICE_CHECK: a checked build found an index outside its buffer";
     }
     return "unknown df_status";
 }

@@ -245,7 +245,10 @@ DF_DEV int copy_band_window(uint32_t t_lane_col0, int lo, int hi, uint16_t* dst,
 // copy_band_window puts them).  The chunk's four 16-column parts go to the
 // quarter's two warps alternately (part 0 / 1): one tensor-memory round trip
 // per warp.
-DF_DEV void copy_band_chunk(uint32_t t_chunk, int kb, int lo, int hi, int a, uint16_t* dst, float scale, int part) {
+// (stride: the destination row's length in halves, for a checked build's
+// range check; err: the error word)
+DF_DEV void copy_band_chunk(uint32_t t_chunk, int kb, int lo, int hi, int a, uint16_t* dst, float scale, int part,
+                            int stride, int* err) {
     if (hi < kb || lo >= kb + 64) return;
     const int s = (lo > kb ? (lo - kb) >> 4 : 0) + part;
     const int s_hi = hi < kb + 63 ? (hi - kb) >> 4 : 3;
@@ -255,7 +258,9 @@ DF_DEV void copy_band_chunk(uint32_t t_chunk, int kb, int lo, int hi, int a, uin
     tc_ld16p(t_chunk + (uint32_t)(16 * s), r);
     if (two) tc_ld16p(t_chunk + (uint32_t)(16 * (s + 2)), r + 16);
     tc_wait_ld();
-    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + (kb + 16 * s - a));
+    int off = kb + 16 * s - a;   // the parts written: [off, off + 16) and, if two, [off + 32, off + 48)
+    DF_CLAMP_CHECK(off, 0, stride - (two ? 47 : 15), err);
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + off);
 #pragma unroll
     for (int x = 0; x < 8; ++x)
         d32[x] = pack2<false>(__uint_as_float(r[2 * x]) * scale, __uint_as_float(r[2 * x + 1]) * scale);

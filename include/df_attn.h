@@ -61,7 +61,8 @@ typedef enum {
     DF_ERR_WORKSPACE = 3,     /* workspace missing or too small             */
     DF_ERR_CUDA = 4,          /* a CUDA runtime / launch error              */
     DF_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up         */
-    DF_ERR_DEVICE_ARG = 6     /* the device found inconsistent cu_seqlens   */
+    DF_ERR_DEVICE_ARG = 6,    /* the device found inconsistent cu_seqlens   */
+    DF_ERR_DEVICE_CHECK = 7   /* checked build: an index outside its buffer */
 } df_status;
 
 typedef enum {
@@ -336,8 +337,12 @@ df_status df_dropout_keep_mask(const df_attn_params *p, int32_t b, int32_t h, in
 /*
  * Synchronises `stream` and reads the device error word of a workspace that
  * was passed to df_attn_fwd / df_attn_bwd: DF_OK, DF_ERR_DEVICE_ARG
- * (cu_seqlens inconsistent with B, L, total_tokens) or DF_ERR_TIMEOUT (a
- * bounded device wait gave up; the affected outputs are unspecified).  The
+ * (cu_seqlens inconsistent with B, L, total_tokens), DF_ERR_TIMEOUT (a
+ * bounded device wait gave up; the affected outputs are unspecified) or, in
+ * a library built with DF_CHECKED (exact_deberta_disentangled_gb300.build,
+ * checked=True), DF_ERR_DEVICE_CHECK: a shared-memory gather or window copy
+ * of a tensor-core kernel computed an index outside its buffer (the access
+ * was clamped into range; the outputs are unspecified).  The
  * word is cleared at the start of every df_attn_fwd / df_attn_bwd call.
  */
 df_status df_get_device_error(const void *workspace, df_stream_t stream);

@@ -142,12 +142,13 @@ DF_DEV float dot16(const float* a, const T* b) {
 // is how the key mask enters saturated tiles.
 template <typename T, int D>
 __global__ void relbias_kernel(ProblemDev p, const T* __restrict__ q, const T* __restrict__ k,
-                               const T* __restrict__ qr, const T* __restrict__ kr, float* __restrict__ relb) {
+                               const T* __restrict__ qr, const T* __restrict__ kr, float* __restrict__ relb,
+                               long row0, long row1) {
     using RS = RowSplit<T, D>;
     const long gw = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31, part = lane % RS::LPR;
-    const long row = gw * RS::RPW + lane / RS::LPR;   // t * H + h
-    const bool ok = row < (long)p.T * p.H;
+    const long row = row0 + gw * RS::RPW + lane / RS::LPR;   // t * H + h
+    const bool ok = row < row1;
     const long rs = ok ? row : 0;                     // a row that is safe to load
     const int t = (int)(rs / p.H), h = (int)(rs % p.H);
     const int R = p.R, off = part * RS::VEC;
@@ -176,30 +177,34 @@ __global__ void relbias_kernel(ProblemDev p, const T* __restrict__ q, const T* _
 
 template <typename T, int D>
 int relbias_one(const ProblemDev& p, const void* q, const void* k, const void* qr, const void* kr, float* relb,
-                cudaStream_t st) {
+                cudaStream_t st, int tok0, int tok1) {
     using RS = RowSplit<T, D>;
-    const long warps = ((long)p.T * p.H + RS::RPW - 1) / RS::RPW;
+    const long row0 = (long)tok0 * p.H, row1 = (long)tok1 * p.H;
+    if (row1 <= row0) return 0;
+    const long warps = (row1 - row0 + RS::RPW - 1) / RS::RPW;
     const int blocks = (int)((warps * 32 + 255) / 256);
-    relbias_kernel<T, D><<<blocks, 256, 0, st>>>(p, (const T*)q, (const T*)k, (const T*)qr, (const T*)kr, relb);
+    relbias_kernel<T, D><<<blocks, 256, 0, st>>>(p, (const T*)q, (const T*)k, (const T*)qr, (const T*)kr, relb, row0,
+                                                row1);
     return (int)cudaGetLastError();
 }
 
 template <typename T>
 int relbias_d(const ProblemDev& p, const void* q, const void* k, const void* qr, const void* kr, float* relb,
-              cudaStream_t st) {
+              cudaStream_t st, int tok0, int tok1) {
     switch (p.D) {
-        case 32: return relbias_one<T, 32>(p, q, k, qr, kr, relb, st);
-        case 64: return relbias_one<T, 64>(p, q, k, qr, kr, relb, st);
-        case 128: return relbias_one<T, 128>(p, q, k, qr, kr, relb, st);
+        case 32: return relbias_one<T, 32>(p, q, k, qr, kr, relb, st, tok0, tok1);
+        case 64: return relbias_one<T, 64>(p, q, k, qr, kr, relb, st, tok0, tok1);
+        case 128: return relbias_one<T, 128>(p, q, k, qr, kr, relb, st, tok0, tok1);
     }
     return (int)cudaErrorInvalidValue;
 }
 
 int launch_relbias(const ProblemDev& p, df_dtype dt, const void* q, const void* k, const void* qr, const void* kr,
-                   float* relb, cudaStream_t st) {
-    if (dt == DF_BF16) return relbias_d<__nv_bfloat16>(p, q, k, qr, kr, relb, st);
-    if (dt == DF_FP16) return relbias_d<__half>(p, q, k, qr, kr, relb, st);
-    return relbias_d<float>(p, q, k, qr, kr, relb, st);
+                   float* relb, cudaStream_t st, int tok0, int tok1) {
+    if (tok1 < 0) tok1 = p.T;
+    if (dt == DF_BF16) return relbias_d<__nv_bfloat16>(p, q, k, qr, kr, relb, st, tok0, tok1);
+    if (dt == DF_FP16) return relbias_d<__half>(p, q, k, qr, kr, relb, st, tok0, tok1);
+    return relbias_d<float>(p, q, k, qr, kr, relb, st, tok0, tok1);
 }
 
 // Dl_i = sum_d dO[i, d] * O[i, d] in fp32, stored at the LSE index of row i.

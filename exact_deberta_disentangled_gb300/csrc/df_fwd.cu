@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int t0, n;
     seq_ok(p, b, t0, n);
     const int i0 = blockIdx.x * BM;
-    if (i0 >= n) return;
+    if (i0 >= n || b < p.b_base) return;   // (sequences before b_base: an earlier part's)
     const int ntiles = (n + BN - 1) / BN;
     auto s_col = [](int it) -> uint32_t { return (it & 1) ? TM::S1 : TM::S0; };
 
@@ -792,7 +792,7 @@ int launch_fwd_impl(const ProblemDev& p, const Workspace& ws, const void* q, con
     auto kern = fwd_tc_kernel<D, BF16, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid((p.L + G::BM - 1) / G::BM, p.H, p.B);
+    dim3 grid((p.L + G::BM - 1) / G::BM, p.H, p.b_count > 0 ? p.b_base + p.b_count : p.B);
     prof_record(kProfFwd, 0, st);
     kern<<<grid, kThreads, S::ALLOC, st>>>(mq, mk, mv, mkr, mqr, p, ws.dtab, ws.relb, out, lse);
     prof_record(kProfFwd, 1, st);

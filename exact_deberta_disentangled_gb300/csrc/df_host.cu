@@ -321,10 +321,18 @@ static df_status common_prologue(const df_attn_params* a, ProblemDev& p, Workspa
     return DF_OK;
 }
 
+// A forward in two parts (the host-buffer step): sequences [0, b_split),
+// then, once `second_ready` has been recorded, sequences [b_split, B), whose
+// tokens start at tok_split.
+struct FwdParts {
+    int b_split, tok_split;
+    cudaEvent_t second_ready;
+};
+
 // The forward with or without the LSE store (lse == nullptr: inference).
 static df_status fwd_common(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
                             const void* kr, void* out, float* lse, void* workspace, size_t ws_bytes,
-                            df_stream_t stream) {
+                            df_stream_t stream, const FwdParts* parts = nullptr) {
     const void* ptrs[] = {q, k, v, qr, kr, out};
     for (const void* x : ptrs)
         if (!x || !aligned16(x)) return DF_ERR_INVALID_ARG;
@@ -338,6 +346,18 @@ static df_status fwd_common(const df_attn_params* a, const void* q, const void* 
     if (a->dtype == DF_FP32)
         return cuda_status(launch_fwd_f32(p, w, (const float*)q, (const float*)k, (const float*)v, (const float*)qr,
                                           (const float*)kr, (float*)out, lse, st));
+    if (parts && parts->b_split > 0 && parts->b_split < p.B) {
+        ProblemDev p1 = p, p2 = p;
+        p1.b_count = parts->b_split;
+        p2.b_base = parts->b_split;
+        p2.b_count = p.B - parts->b_split;
+        if (launch_relbias(p, a->dtype, q, k, qr, kr, w.relb, st, 0, parts->tok_split) ||
+            launch_fwd_tc(p1, w, a->dtype, q, k, v, qr, kr, out, lse, st) ||
+            cudaStreamWaitEvent(st, parts->second_ready, 0) != cudaSuccess ||
+            launch_relbias(p, a->dtype, q, k, qr, kr, w.relb, st, parts->tok_split, -1))
+            return DF_ERR_CUDA;
+        return cuda_status(launch_fwd_tc(p2, w, a->dtype, q, k, v, qr, kr, out, lse, st));
+    }
     if (launch_relbias(p, a->dtype, q, k, qr, kr, w.relb, st)) return DF_ERR_CUDA;
     return cuda_status(launch_fwd_tc(p, w, a->dtype, q, k, v, qr, kr, out, lse, st));
 }
@@ -433,21 +453,23 @@ Arena arena_layout(const df_attn_params* a, const ProblemDev& p) {
 
 namespace {
 // A copy stream and its events per device for df_attn_step_host, created on
-// first use with that device current: dO goes up while the forward runs, and
-// O and the LSE come down while the backward runs.  The events are shared by
+// first use with that device current: the second half of the sequences' Q /
+// K / V and then dO go up while the forward runs, and the results come down
+// while the backward runs.  The events are shared by
 // every call on the device, so one call's enqueue sequence holds g_copy_mu.
 constexpr int kMaxCopyDevices = 64;
 std::mutex g_copy_mu;
 bool g_copy_tried[kMaxCopyDevices];
 cudaStream_t g_copy_st[kMaxCopyDevices];
-cudaEvent_t g_copy_ev[kMaxCopyDevices][7];   // start, dout up, forward done, copies down done, dV / dQ / dK final
+cudaEvent_t g_copy_ev[kMaxCopyDevices][8];   // start, dout up, forward done, copies down done, dV / dQ / dK final,
+                                              // second forward part's inputs up
 
 bool copy_stream(int dev, cudaStream_t& cs, cudaEvent_t*& ev) {
     if (dev < 0 || dev >= kMaxCopyDevices) return false;
     if (!g_copy_tried[dev]) {
         g_copy_tried[dev] = true;
         bool ok = cudaStreamCreateWithFlags(&g_copy_st[dev], cudaStreamNonBlocking) == cudaSuccess;
-        for (int i = 0; i < 7 && ok; ++i)
+        for (int i = 0; i < 8 && ok; ++i)
             ok = cudaEventCreateWithFlags(&g_copy_ev[dev][i], cudaEventDisableTiming) == cudaSuccess;
         if (!ok) {
             cudaGetLastError();
@@ -499,15 +521,32 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     const bool side = copy_stream(dev, cs, ev);
     df_attn_params dp = *a;
     if (a->dtype != DF_FP32) dp.band_bias = base + L.bias;
-    bool ok = h2d(L.q, q, tok) && h2d(L.k, k, tok) && h2d(L.v, v, tok) && h2d(L.qr, qr, rel) &&
-              h2d(L.kr, kr, rel);
+    // With two or more sequences the tensor-core forward runs in two parts:
+    // the first half of the sequences' Q / K / V go up on the caller's
+    // stream, the rest on the copy stream while the first part runs
+    FwdParts parts{0, 0, side ? ev[7] : nullptr};
+    if (side && a->dtype != DF_FP32 && p.B >= 2) {
+        parts.b_split = p.B / 2;
+        parts.tok_split = a->cu_seqlens ? a->cu_seqlens[parts.b_split] : parts.b_split * p.L;
+    }
+    const size_t tok1 = e * (size_t)parts.tok_split * p.H * p.D;   // bytes of the first part's rows
+    bool ok = h2d(L.qr, qr, rel) && h2d(L.kr, kr, rel) && h2d(L.q, q, tok1 ? tok1 : tok) &&
+              h2d(L.k, k, tok1 ? tok1 : tok) && h2d(L.v, v, tok1 ? tok1 : tok);
     // dO is needed by the backward only: on the copy stream, during the forward
-    if (side)
-        ok = ok && cudaEventRecord(ev[0], st) == cudaSuccess && cudaStreamWaitEvent(cs, ev[0], 0) == cudaSuccess &&
-             cudaMemcpyAsync(base + L.dout, dout, tok, cudaMemcpyHostToDevice, cs) == cudaSuccess &&
+    if (side) {
+        ok = ok && cudaEventRecord(ev[0], st) == cudaSuccess && cudaStreamWaitEvent(cs, ev[0], 0) == cudaSuccess;
+        if (tok1) {
+            auto up2 = [&](size_t off, const void* src) {
+                return cudaMemcpyAsync(base + off + tok1, (const char*)src + tok1, tok - tok1, cudaMemcpyHostToDevice,
+                                       cs) == cudaSuccess;
+            };
+            ok = ok && up2(L.q, q) && up2(L.k, k) && up2(L.v, v) && cudaEventRecord(ev[7], cs) == cudaSuccess;
+        }
+        ok = ok && cudaMemcpyAsync(base + L.dout, dout, tok, cudaMemcpyHostToDevice, cs) == cudaSuccess &&
              cudaEventRecord(ev[1], cs) == cudaSuccess;
-    else
+    } else {
         ok = ok && h2d(L.dout, dout, tok);
+    }
     if (ok && a->cu_seqlens) {
         ok = h2d(L.cu, a->cu_seqlens, sizeof(int32_t) * (size_t)(p.B + 1));
         dp.cu_seqlens = (const int32_t*)(base + L.cu);
@@ -522,8 +561,8 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     }
     if (!ok) return DF_ERR_CUDA;
     const size_t wsb = arena_bytes - L.ws;
-    s = df_attn_fwd(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
-                    (float*)(base + L.lse), base + L.ws, wsb, stream);
+    s = fwd_common(&dp, base + L.q, base + L.k, base + L.v, base + L.qr, base + L.kr, base + L.out,
+                   (float*)(base + L.lse), base + L.ws, wsb, stream, tok1 ? &parts : nullptr);
     if (s != DF_OK) return s;
     // O and the LSE are final after the forward: down on the copy stream during the backward
     if (side) {

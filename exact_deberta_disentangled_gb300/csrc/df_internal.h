@@ -41,6 +41,11 @@ struct ProblemDev {
     // it) or nullptr
     int bias_kb, bias_nslot;
     uint16_t* saved_bias;
+    // the forward kernel's batch range: sequences b_base .. b_base + b_count
+    // - 1 (b_count 0: all), so that a caller can run it in parts as inputs
+    // arrive (the host-buffer step); the CTAs of sequences before b_base
+    // exit at once
+    int b_base, b_count;
 };
 
 // Workspace carve-up (device pointers, all 256-byte aligned).
@@ -67,8 +72,9 @@ struct Workspace {
 int launch_delta_table(int L, int span, int nb, int mp, int32_t* out, cudaStream_t st);
 int launch_check_cu(const ProblemDev& p, cudaStream_t st);
 int launch_clear_error(int* err, cudaStream_t st);
+// (tokens tok0 .. tok1 - 1; tok1 < 0: through the last token)
 int launch_relbias(const ProblemDev& p, df_dtype dt, const void* q, const void* k, const void* qr, const void* kr,
-                   float* relb, cudaStream_t st);
+                   float* relb, cudaStream_t st, int tok0 = 0, int tok1 = -1);
 int launch_rowterm(const ProblemDev& p, df_dtype dt, const void* out, const void* dout, float* rowterm,
                    cudaStream_t st);
 int launch_keep_mask(const ProblemDev& p, int b, int h, int form, uint8_t* out, cudaStream_t st);

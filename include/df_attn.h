@@ -192,10 +192,14 @@ df_status df_attn_bwd(const df_attn_params *p, const void *q, const void *k, con
  * p->cu_seqlens, p->query_mask and p->key_mask are HOST pointers (copied
  * too).  Host buffers should be pinned for full copy bandwidth.  The device
  * arena (caller-owned, df_attn_step_host_arena_size bytes) holds the device
- * copies, the band bias the forward saves for the backward and the workspace.  dout is copied up on a per-device copy stream
- * (created on the first call on that device) while the forward runs; out and
- * lse are copied down on it while the backward runs, dv once its kernel has
- * finished and dq, dk once theirs have, while the remaining kernels run.
+ * copies, the band bias the forward saves for the backward and the
+ * workspace.  A per-device copy stream (created on the first call on that
+ * device) overlaps the copies with the kernels: with B >= 2 (16-bit dtypes)
+ * the forward runs in two parts, the first half of the sequences' q, k, v
+ * going up on `stream` and the rest on the copy stream while the first part
+ * runs; dout goes up while the forward runs; out and lse come down while the
+ * backward runs, dq, dv and dk each once it is final, while the remaining
+ * kernels run.
  */
 size_t df_attn_step_host_arena_size(const df_attn_params *p);
 df_status df_attn_step_host(const df_attn_params *p, const void *q, const void *k, const void *v, const void *qr,

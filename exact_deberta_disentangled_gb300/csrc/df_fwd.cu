@@ -27,8 +27,8 @@
 // starts with a barrier of the eight softmax warps).
 // Tensor memory (512 columns): O_0 and O_1 [0, 2D), two S / P buffers and,
 // in [384, 512), two buffers of band-product chunks.  Tile n uses S buffer
-// n & 1: the issuer computes S for tile n + 1 while the softmax works on
-// tile n, band tile or not.  A band tile's two products (own, then cross)
+// n & 1: S of tile n + 1 is computed while the softmax works on tile n, band
+// tile or not.  A band tile's two products (own, then cross)
 // are computed 64 band positions at a time (only the chunks the tile's
 // relative-index range reaches) into the chunk buffers alternately, so that
 // the softmax warps copy one chunk to shared memory while the next one is
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return true;
             };
-            // test-only stall injection: the issuer stops before this tile, so
+            // test-only stall injection: this issuer stops before this tile, so
             // that the other roles' bounded waits run out
             const int stall = p.fault_kernel == 0 ? p.fault_tile : -1;
             // S of every tile, then its band chunks: the first two as soon as
@@ -706,13 +706,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             // P of this half is announced on the barrier of the tile's parity.
-            // The issuer computes S of the next tile before it waits for this
-            // tile's P (and V), so the softmax warps can announce the next tile's
-            // P before the issuer takes this one; on a single barrier the two
-            // phases would be indistinguishable to the issuer's parity wait (a
-            // slow V copy made it wait for good).  The next phase of this tile's
-            // barrier is two tiles on, whose S the issuer computes only after it
-            // has taken this one.
+            // S of the next tile is computed before the P.V issuer waits for
+            // this tile's P (and V), so the softmax warps can announce the next
+            // tile's P before the P.V issuer takes this one; on a single
+            // barrier the two phases would be indistinguishable to its parity
+            // wait (a slow V copy made it wait for good).  The next phase of
+            // this tile's barrier is two tiles on, whose S waits for P.V of
+            // this tile, which the P.V issuer issues only after taking this P.
             if (lane == 0) mbar_arrive(&bars->p_full[2 * hf + (it & 1)]);
         }
         // ------------------------------------------------------------ epilogue

@@ -389,13 +389,14 @@ static df_status bwd_common(const df_attn_params* a, const void* q, const void* 
     cudaStream_t st = (cudaStream_t)stream;
     df_status s = common_prologue(a, p, w, true, workspace, ws_bytes, st);
     if (s != DF_OK) return s;
-    if (launch_rowterm(p, a->dtype, out, dout, w.rowterm, st)) return DF_ERR_CUDA;
-    if (a->dtype == DF_FP32)
+    if (a->dtype == DF_FP32) {
+        if (launch_rowterm(p, a->dtype, out, dout, w.rowterm, st)) return DF_ERR_CUDA;
         return cuda_status(launch_bwd_f32(p, w, (const float*)q, (const float*)k, (const float*)v,
                                           (const float*)qr, (const float*)kr, lse, (const float*)dout, (float*)dq,
                                           (float*)dk, (float*)dv, (float*)dqr, (float*)dkr, st));
-    if (launch_relbias(p, a->dtype, q, k, qr, kr, w.relb, st)) return DF_ERR_CUDA;
-    return cuda_status(launch_bwd_tc(p, w, a->dtype, q, k, v, qr, kr, lse, dout, dq, dk, dv, dqr, dkr, st, hook));
+    }
+    return cuda_status(
+        launch_bwd_tc(p, w, a->dtype, q, k, v, qr, kr, out, lse, dout, dq, dk, dv, dqr, dkr, st, hook));
 }
 
 df_status df_attn_bwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,

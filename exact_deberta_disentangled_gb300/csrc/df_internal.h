@@ -97,9 +97,13 @@ struct BwdHook {
     void (*fn)(void* ctx, int point, cudaStream_t st);
     void* ctx;
 };
+// The tensor-core backward from the forward's O and LSE: row terms, row /
+// column biases, band bias (unless saved), both kernels and both halves of
+// the relative-position gradients.
 int launch_bwd_tc(const ProblemDev& p, const Workspace& ws, df_dtype dt, const void* q, const void* k,
-                  const void* v, const void* qr, const void* kr, const float* lse, const void* dout, void* dq,
-                  void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st, const BwdHook* hook = nullptr);
+                  const void* v, const void* qr, const void* kr, const void* out, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, void* dqr, void* dkr, cudaStream_t st,
+                  const BwdHook* hook = nullptr);
 
 // the two attention-backward kernels (df_bwd_dq.cu, df_bwd_dkv.cu): rows r1 / r2,
 // columns c1 / c2; band tiles read the stored band bias (ws.bias)

@@ -609,7 +609,10 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     if (!side) ok = ok && d2h(out, L.out, tok, st) && d2h(lse, L.lse, lseb, st);
     else ok = ok && cudaEventRecord(ev[3], cs) == cudaSuccess && cudaStreamWaitEvent(st, ev[3], 0) == cudaSuccess;
     if (!ok) return DF_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return DF_ERR_CUDA;
+    // one host round trip: the error word's read (into pageable memory, so the
+    // copy returns only once it and every earlier copy and kernel of the
+    // stream are done) and the stream synchronisation, which reports a
+    // failure of any of them
     return df_get_device_error(base + L.ws, stream);
 }
 

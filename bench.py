@@ -402,10 +402,11 @@ def workload_flops(x, w, H):
     return f, b
 
 
-def time_phases(name, dev, iters, warmup, flush, **make_kw):
+def time_phases(name, dev, iters, warmup, flush, fp32_fast=False, **make_kw):
     """Forward, backward (alone, from the saved forward outputs) and forward +
     backward of one workload through the C ABI: per-iteration CUDA-event
-    times on the launching stream, L2 flushed before every iteration."""
+    times on the launching stream, L2 flushed before every iteration
+    (fp32_fast: fp32 tensors in the fast mode)."""
     import torch
 
     from exact_deberta_disentangled_gb300 import binding as Bd
@@ -415,7 +416,7 @@ def time_phases(name, dev, iters, warmup, flush, **make_kw):
     x = synth.make_inputs(w, **make_kw)
     H = x.q.shape[1]
     g = Bd.Geometry(B=x.B, L=x.L, H=H, D=w.D, span=w.span, nb=w.nb, mp=w.mp, dropout_p=w.dropout_p, seed=11,
-                    offset=0)
+                    offset=0, fp32_fast=fp32_fast)
     if x.packed:
         g.cu_seqlens = x.cu_seqlens.to(dev)
         g.total_tokens = int(x.cu_seqlens[-1])
@@ -456,7 +457,8 @@ def time_phases(name, dev, iters, warmup, flush, **make_kw):
     fl_f, fl_b = workload_flops(x, w, H)
     for phase, fl in (("fwd", fl_f), ("bwd", fl_b), ("fwd_bwd", fl_f + fl_b)):
         res[phase]["tflops_at_median"] = fl / (res[phase]["median"] * 1e-3) / 1e12
-    shape = {"B": x.B, "L": x.L, "H": H, "D": w.D, "R": w.R, "dtype": str(q.dtype).replace("torch.", ""),
+    shape = {"B": x.B, "L": x.L, "H": H, "D": w.D, "R": w.R,
+             "dtype": "float32 (fast mode)" if fp32_fast else str(q.dtype).replace("torch.", ""),
              "dropout_p": w.dropout_p, "packed": x.packed, "masked": x.qmask is not None,
              "tokens": int(x.cu_seqlens[-1]), "fwd_flops": fl_f, "bwd_flops": fl_b}
     return {"shape": shape, **res}
@@ -560,6 +562,9 @@ def run_extras(dev, iters, warmup, flush):
     configs = {}
     for name in ("v3_base", "varlen", "hd128_dropout", "hd32_dropout", "mnli_fp16"):
         configs[name] = time_phases(name, dev, iters, warmup, flush)
+    # fp32 tensors: the fast mode (fp16 tensor-core path) at the L = 8192 sweep shape
+    configs["fast_fp32_L8192"] = time_phases("sweep_L8192", dev, iters, warmup, flush, fp32_fast=True,
+                                             dtype="fp32")
     infer = {f"L{L}": time_inference(dev, L, iters, warmup, flush) for L in (64, 128, 384)}
     side = time_side_steps(dev, iters, warmup, flush)
     return {"sweep": sweep, "configs": configs, "inference_latency": infer, "steps_either_side": side,

@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libdfattn.so")
 
 DF_OK, DF_ERR_INVALID_ARG, DF_ERR_UNSUPPORTED, DF_ERR_WORKSPACE, DF_ERR_CUDA, DF_ERR_TIMEOUT, DF_ERR_DEVICE_ARG = range(7)
 DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+DF_FP32_FAST = 3   # fp32 tensors, inputs rounded to fp16 for the tensor-core path
 
 EXPORTS = ["df_attn_workspace_size", "df_attn_fwd", "df_attn_bwd", "df_attn_step_host_arena_size",
            "df_attn_step_host", "df_rel_index_table", "df_get_device_error", "df_status_string", "df_version",
@@ -180,6 +181,7 @@ class Geometry:
     offset: int = 0
     scale: float = 0.0
     band_bias: Optional[torch.Tensor] = None    # saved band bias (device uint8, band_bias_size bytes)
+    fp32_fast: bool = False   # fp32 tensors: the fast mode (DF_FP32_FAST) instead of strict fp32
 
     @property
     def R(self):
@@ -201,7 +203,7 @@ class Geometry:
         p.philox_seed = self.seed & ((1 << 64) - 1)
         p.philox_offset = self.offset
         p.softmax_scale = self.scale
-        p.dtype = DTYPE_CODE[dtype]
+        p.dtype = DF_FP32_FAST if dtype == torch.float32 and self.fp32_fast else DTYPE_CODE[dtype]
         p.band_bias = None if self.band_bias is None else self.band_bias.data_ptr()
         return p
 

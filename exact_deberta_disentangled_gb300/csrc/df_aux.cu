@@ -1,7 +1,8 @@
 // df_aux.cu -- small kernels around the attention kernels: the relative-
 // position index table, the cu_seqlens consistency check, the per-token
 // relative-position dot products used by tiles whose relative index is
-// clamped (saturated tiles), and the backward row term Dl_i = dO_i . O_i.
+// clamped (saturated tiles), the backward row term Dl_i = dO_i . O_i, and the
+// fp32 <-> fp16 conversions of the fast fp32 mode.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -256,6 +257,47 @@ int launch_rowterm(const ProblemDev& p, df_dtype dt, const void* out, const void
     if (dt == DF_BF16) return rowterm_d<__nv_bfloat16>(p, out, dout, rowterm, st);
     if (dt == DF_FP16) return rowterm_d<__half>(p, out, dout, rowterm, st);
     return rowterm_d<float>(p, out, dout, rowterm, st);
+}
+
+// One segment per blockIdx.y, four elements per thread and step.
+template <bool TO_HALF>
+__global__ void convert_kernel(ConvList cl) {
+    const int sgi = blockIdx.y;
+    const long long n4 = cl.n[sgi] / 4;
+    for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n4; x += (long long)gridDim.x * blockDim.x) {
+        if (TO_HALF) {
+            const float4 v = reinterpret_cast<const float4*>(cl.src[sgi])[x];
+            const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+            uint2 w;
+            w.x = *reinterpret_cast<const uint32_t*>(&a);
+            w.y = *reinterpret_cast<const uint32_t*>(&b);
+            reinterpret_cast<uint2*>(cl.dst[sgi])[x] = w;
+        } else {
+            const uint2 w = reinterpret_cast<const uint2*>(cl.src[sgi])[x];
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+            reinterpret_cast<float4*>(cl.dst[sgi])[x] = make_float4(a.x, a.y, b.x, b.y);
+        }
+    }
+}
+
+int launch_convert(const ConvList& cl, bool to_half, cudaStream_t st) {
+    if (cl.nseg < 1 || cl.nseg > kConvSegs) return (int)cudaErrorInvalidValue;
+    long long most = 0;
+    for (int i = 0; i < cl.nseg; ++i) {
+        if (cl.n[i] % 4 || ((uintptr_t)cl.src[i] | (uintptr_t)cl.dst[i]) & 15u) return (int)cudaErrorInvalidValue;
+        most = cl.n[i] > most ? cl.n[i] : most;
+    }
+    // enough blocks to fill the GPU a few times over across the segments
+    long long bx = (most / 4 + 255) / 256;
+    const long long cap = (4 * 152 + cl.nseg - 1) / cl.nseg;
+    bx = bx < 1 ? 1 : (bx > cap ? cap : bx);
+    const dim3 grid((unsigned)bx, (unsigned)cl.nseg);
+    if (to_half)
+        convert_kernel<true><<<grid, 256, 0, st>>>(cl);
+    else
+        convert_kernel<false><<<grid, 256, 0, st>>>(cl);
+    return (int)cudaGetLastError();
 }
 
 }  // namespace df

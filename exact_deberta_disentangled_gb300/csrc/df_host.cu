@@ -70,7 +70,8 @@ int bias_reach(const ProblemDev& p) {
 df_status resolve(const df_attn_params* a, ProblemDev& out) {
     if (!a) return DF_ERR_INVALID_ARG;
     if (a->B < 1 || a->L < 1 || a->H < 1 || a->D < 1 || a->att_span < 1) return DF_ERR_INVALID_ARG;
-    if (a->dtype != DF_BF16 && a->dtype != DF_FP16 && a->dtype != DF_FP32) return DF_ERR_INVALID_ARG;
+    if (a->dtype != DF_BF16 && a->dtype != DF_FP16 && a->dtype != DF_FP32 && a->dtype != DF_FP32_FAST)
+        return DF_ERR_INVALID_ARG;
     if (!(a->dropout_p >= 0.f && a->dropout_p < 1.f)) return DF_ERR_INVALID_ARG;
     if (!(a->softmax_scale >= 0.f) || !std::isfinite(a->softmax_scale)) return DF_ERR_INVALID_ARG;
     if (a->philox_offset >> 32) return DF_ERR_INVALID_ARG;
@@ -140,7 +141,7 @@ df_status resolve(const df_attn_params* a, ProblemDev& out) {
     return DF_OK;
 }
 
-int elem_bytes(df_dtype d) { return d == DF_FP32 ? 4 : 2; }
+int elem_bytes(df_dtype d) { return d == DF_FP32 || d == DF_FP32_FAST ? 4 : 2; }
 
 int rel_chunks(const ProblemDev& p) {
     // Token chunks of the relative-gradient reduction: enough CTAs to fill
@@ -160,8 +161,49 @@ size_t bias_table_rows(const ProblemDev& p) {
     return nrbg * (size_t)p.H * (size_t)p.bias_nslot * 128;
 }
 
-// Carve the workspace; with base == nullptr only the size is computed.
+// The fast fp32 mode's fp16 copies of the inputs and outputs, placed after
+// the fp16 workspace; with base == nullptr only the size is computed.
+struct FastBufs {
+    char *q, *k, *v, *qr, *kr, *out, *dout, *dq, *dk, *dv, *dqr, *dkr;
+    size_t bytes;
+};
+FastBufs fast_bufs(const ProblemDev& p, bool backward, char* base) {
+    FastBufs f;
+    std::memset(&f, 0, sizeof(f));
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char* {
+        char* r = base ? base + off : nullptr;
+        off += align_up(bytes);
+        return r;
+    };
+    const size_t tok = sizeof(uint16_t) * (size_t)p.T * p.H * p.D, rel = sizeof(uint16_t) * (size_t)p.H * p.R * p.D;
+    f.q = take(tok);
+    f.k = take(tok);
+    f.v = take(tok);
+    f.qr = take(rel);
+    f.kr = take(rel);
+    f.out = take(tok);
+    if (backward) {
+        f.dout = take(tok);
+        f.dq = take(tok);
+        f.dk = take(tok);
+        f.dv = take(tok);
+        f.dqr = take(rel);
+        f.dkr = take(rel);
+    }
+    f.bytes = off;
+    return f;
+}
+
+// Carve the workspace; with base == nullptr only the size is computed.  The
+// fast fp32 mode is the fp16 workspace (error word first, as always) and then
+// the fp16 copies.
 Workspace carve(const ProblemDev& p, df_dtype dt, bool backward, void* base) {
+    if (dt == DF_FP32_FAST) {
+        Workspace w = carve(p, DF_FP16, backward, base);
+        w.bytes += fast_bufs(p, backward, nullptr).bytes;
+        return w;
+    }
     Workspace w;
     std::memset(&w, 0, sizeof(w));
     size_t off = 0;
@@ -321,6 +363,13 @@ static df_status common_prologue(const df_attn_params* a, ProblemDev& p, Workspa
     return DF_OK;
 }
 
+static df_status fast_fwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                          const void* kr, void* out, float* lse, void* workspace, size_t ws_bytes,
+                          df_stream_t stream);
+static df_status fast_bwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                          const void* kr, const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                          void* dv, void* dqr, void* dkr, void* workspace, size_t ws_bytes, df_stream_t stream);
+
 // A forward in two parts (the host-buffer step): sequences [0, b_split),
 // then, once `second_ready` has been recorded, sequences [b_split, B), whose
 // tokens start at tok_split.
@@ -338,6 +387,7 @@ static df_status fwd_common(const df_attn_params* a, const void* q, const void* 
         if (!x || !aligned16(x)) return DF_ERR_INVALID_ARG;
     if (lse && !aligned16(lse)) return DF_ERR_INVALID_ARG;
     if (a && a->cu_seqlens && ((uintptr_t)a->cu_seqlens & 3u)) return DF_ERR_INVALID_ARG;
+    if (a && a->dtype == DF_FP32_FAST) return fast_fwd(a, q, k, v, qr, kr, out, lse, workspace, ws_bytes, stream);
     ProblemDev p;
     Workspace w;
     cudaStream_t st = (cudaStream_t)stream;
@@ -384,6 +434,8 @@ static df_status bwd_common(const df_attn_params* a, const void* q, const void* 
     for (const void* x : ptrs)
         if (!x || !aligned16(x)) return DF_ERR_INVALID_ARG;
     if (a && a->cu_seqlens && ((uintptr_t)a->cu_seqlens & 3u)) return DF_ERR_INVALID_ARG;
+    if (a && a->dtype == DF_FP32_FAST)
+        return fast_bwd(a, q, k, v, qr, kr, out, lse, dout, dq, dk, dv, dqr, dkr, workspace, ws_bytes, stream);
     ProblemDev p;
     Workspace w;
     cudaStream_t st = (cudaStream_t)stream;
@@ -397,6 +449,97 @@ static df_status bwd_common(const df_attn_params* a, const void* q, const void* 
     }
     return cuda_status(
         launch_bwd_tc(p, w, a->dtype, q, k, v, qr, kr, out, lse, dout, dq, dk, dv, dqr, dkr, st, hook));
+}
+
+// ------------------------------------------------------- fast fp32 mode
+// ("DisentangledFlash", section "Status": the optional fast FP32/TF32 mode)
+// fp32 in and out; the inputs are rounded to fp16 (TF32's 10-bit
+// significand) into the workspace, the fp16 tensor-core path runs on them,
+// and its fp16 results are widened to fp32.
+
+namespace {
+struct FastSetup {
+    df_status s;
+    size_t inner;   // bytes of the fp16 workspace at the start
+    FastBufs f;
+    long long tok, rel;   // elements of a token tensor / a relative tensor
+};
+FastSetup fast_setup(const df_attn_params* a, bool backward, void* workspace, size_t ws_bytes) {
+    FastSetup r;
+    std::memset(&r, 0, sizeof(r));
+    ProblemDev p;
+    r.s = resolve(a, p);
+    if (r.s != DF_OK) return r;
+    if (!workspace || !aligned16(workspace)) {
+        r.s = DF_ERR_WORKSPACE;
+        return r;
+    }
+    r.inner = carve(p, DF_FP16, backward, nullptr).bytes;
+    r.f = fast_bufs(p, backward, (char*)workspace + r.inner);
+    if (ws_bytes < r.inner + r.f.bytes) r.s = DF_ERR_WORKSPACE;
+    r.tok = (long long)p.T * p.H * p.D;
+    r.rel = (long long)p.H * p.R * p.D;
+    return r;
+}
+void conv_add(ConvList& cl, const void* src, void* dst, long long n) {
+    cl.src[cl.nseg] = src;
+    cl.dst[cl.nseg] = dst;
+    cl.n[cl.nseg] = n;
+    ++cl.nseg;
+}
+}  // namespace
+
+static df_status fast_fwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                          const void* kr, void* out, float* lse, void* workspace, size_t ws_bytes,
+                          df_stream_t stream) {
+    const FastSetup fs = fast_setup(a, false, workspace, ws_bytes);
+    if (fs.s != DF_OK) return fs.s;
+    const FastBufs& f = fs.f;
+    cudaStream_t st = (cudaStream_t)stream;
+    ConvList in{};
+    conv_add(in, q, f.q, fs.tok);
+    conv_add(in, k, f.k, fs.tok);
+    conv_add(in, v, f.v, fs.tok);
+    conv_add(in, qr, f.qr, fs.rel);
+    conv_add(in, kr, f.kr, fs.rel);
+    if (launch_convert(in, true, st)) return DF_ERR_CUDA;
+    df_attn_params a16 = *a;
+    a16.dtype = DF_FP16;
+    const df_status s = fwd_common(&a16, f.q, f.k, f.v, f.qr, f.kr, f.out, lse, workspace, fs.inner, stream);
+    if (s != DF_OK) return s;
+    ConvList o{};
+    conv_add(o, f.out, out, fs.tok);
+    return cuda_status(launch_convert(o, false, st));
+}
+
+static df_status fast_bwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
+                          const void* kr, const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                          void* dv, void* dqr, void* dkr, void* workspace, size_t ws_bytes, df_stream_t stream) {
+    const FastSetup fs = fast_setup(a, true, workspace, ws_bytes);
+    if (fs.s != DF_OK) return fs.s;
+    const FastBufs& f = fs.f;
+    cudaStream_t st = (cudaStream_t)stream;
+    ConvList in{};
+    conv_add(in, q, f.q, fs.tok);
+    conv_add(in, k, f.k, fs.tok);
+    conv_add(in, v, f.v, fs.tok);
+    conv_add(in, qr, f.qr, fs.rel);
+    conv_add(in, kr, f.kr, fs.rel);
+    conv_add(in, out, f.out, fs.tok);
+    conv_add(in, dout, f.dout, fs.tok);
+    if (launch_convert(in, true, st)) return DF_ERR_CUDA;
+    df_attn_params a16 = *a;
+    a16.dtype = DF_FP16;
+    const df_status s = bwd_common(&a16, f.q, f.k, f.v, f.qr, f.kr, f.out, lse, f.dout, f.dq, f.dk, f.dv, f.dqr,
+                                   f.dkr, workspace, fs.inner, stream, nullptr);
+    if (s != DF_OK) return s;
+    ConvList o{};
+    conv_add(o, f.dq, dq, fs.tok);
+    conv_add(o, f.dk, dk, fs.tok);
+    conv_add(o, f.dv, dv, fs.tok);
+    conv_add(o, f.dqr, dqr, fs.rel);
+    conv_add(o, f.dkr, dkr, fs.rel);
+    return cuda_status(launch_convert(o, false, st));
 }
 
 df_status df_attn_bwd(const df_attn_params* a, const void* q, const void* k, const void* v, const void* qr,
@@ -526,7 +669,7 @@ df_status df_attn_step_host(const df_attn_params* a, const void* q, const void* 
     // the first half of the sequences' Q / K / V go up on the caller's
     // stream, the rest on the copy stream while the first part runs
     FwdParts parts{0, 0, side ? ev[7] : nullptr};
-    if (side && a->dtype != DF_FP32 && p.B >= 2) {
+    if (side && (a->dtype == DF_BF16 || a->dtype == DF_FP16) && p.B >= 2) {
         parts.b_split = p.B / 2;
         parts.tok_split = a->cu_seqlens ? a->cu_seqlens[parts.b_split] : parts.b_split * p.L;
     }

@@ -78,6 +78,17 @@ int launch_relbias(const ProblemDev& p, df_dtype dt, const void* q, const void* 
 int launch_rowterm(const ProblemDev& p, df_dtype dt, const void* out, const void* dout, float* rowterm,
                    cudaStream_t st);
 int launch_keep_mask(const ProblemDev& p, int b, int h, int form, uint8_t* out, cudaStream_t st);
+// Element-wise fp32 <-> fp16 (round to nearest even) of up to kConvSegs
+// arrays in one launch (the fast fp32 mode); every count is a multiple of 4
+// and every pointer 16-byte aligned.
+constexpr int kConvSegs = 8;
+struct ConvList {
+    const void* src[kConvSegs];
+    void* dst[kConvSegs];
+    long long n[kConvSegs];   // elements
+    int nseg;
+};
+int launch_convert(const ConvList& cl, bool to_half, cudaStream_t st);
 
 // strict fp32 path
 int launch_fwd_f32(const ProblemDev& p, const Workspace& ws, const float* q, const float* k, const float* v,

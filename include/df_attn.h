@@ -68,8 +68,23 @@ typedef enum {
 typedef enum {
     DF_BF16 = 0,              /* bf16 storage, fp32 accumulation (tensor cores) */
     DF_FP16 = 1,              /* fp16 storage, fp32 accumulation (tensor cores) */
-    DF_FP32 = 2               /* strict fp32 (CUDA-core fp32 arithmetic)        */
+    DF_FP32 = 2,              /* strict fp32 (CUDA-core fp32 arithmetic)        */
+    DF_FP32_FAST = 3          /* fp32 storage, fast mode (below)                */
 } df_dtype;
+
+/*
+ * Fast fp32 mode (DF_FP32_FAST; "DisentangledFlash", section "Status": an
+ * optional fast FP32/TF32 mode beside the strict fp32 one).  Every tensor is
+ * fp32 as for DF_FP32, the LSE fp32 as always.  The inputs are rounded to
+ * nearest fp16 -- the same 10-bit significand as TF32 -- in the workspace,
+ * the fp16 tensor-core kernels run on them (fp32 accumulation, 16-bit P and
+ * dZ as for DF_FP16), and O and the gradients come back widened to fp32 from
+ * their fp16 results.  Error: that of DF_FP16 plus the input rounding
+ * (relative 2^-11 per element); tensors must stay within the fp16 range
+ * (|x| < 65504, else inf / NaN results).  Same contract as DF_FP16 otherwise
+ * (saved band bias included); the workspace adds the fp16 copies of the
+ * inputs and outputs.
+ */
 
 /*
  * Problem description.
@@ -121,7 +136,7 @@ typedef struct {
  */
 
 /*
- * Saved band bias (bf16 / fp16 only; ignored for DF_FP32).  Near the
+ * Saved band bias (bf16 / fp16 / fast fp32; ignored for DF_FP32).  Near the
  * diagonal every (query, key) pair has its own relative-position term
  * c log2(e) (Q_i . Kr[delta] + K_j . Qr[delta]) ("DisentangledFlash",
  * section "Status": C2P and P2C).  The backward needs it again for every

@@ -60,6 +60,30 @@ def test_workspace_sizes(lib):
     assert b - f >= 2 * 2 * T * H * R
 
 
+def test_fast_fp32_workspace_and_rules(lib):
+    """The fast fp32 mode (fp32 tensors through the fp16 tensor-core path):
+    its workspace is the fp16 one plus fp16 copies of the inputs and outputs
+    (forward: Q, K, V, O and Qr, Kr; backward also dO, dQ, dK, dV and dQr,
+    dKr), its saved band bias is the fp16 one, and the 16-bit kernels'
+    bucketing rule applies to it."""
+    import torch
+    al = lambda x: (x + 255) // 256 * 256
+    for kw in ({}, dict(D=32, L=384, span=64, nb=64, mp=128), dict(D=128, B=3, L=700, span=512, nb=0, mp=0)):
+        g, gf = geom(**kw), geom(fp32_fast=True, **kw)
+        T, H, D, R = g.T, g.H, g.D, g.R
+        tok, rel = al(2 * T * H * D), al(2 * H * R * D)
+        for bwd, ntok, nrel in ((False, 4, 2), (True, 8, 4)):
+            w16 = B.workspace_size(g, torch.float16, bwd)
+            assert w16 > 0
+            assert B.workspace_size(gf, torch.float32, bwd) == w16 + ntok * tok + nrel * rel
+        assert B.band_bias_size(gf, torch.float32) == B.band_bias_size(g, torch.float16) > 0
+        assert B.band_bias_size(g, torch.float32) == 0          # strict fp32 stores none
+    # a bucketing configuration the 16-bit kernels reject (the index jumps by 2)
+    bad = dict(nb=256, mp=300)
+    assert B.workspace_size(geom(fp32_fast=True, **bad), torch.float32, True) == 0
+    assert B.workspace_size(geom(**bad), torch.float32, True) > 0
+
+
 class FakeTensor:
     """An aligned non-null address that is never dereferenced (validation
     fails before any device work)."""

@@ -333,11 +333,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto stage_ofs = [](int s) { return (uint32_t)(s * S::CB); };
             bool ok = mbar_wait_warp(ROWQ ? &bars->a_full : &bars->row_full, 0, wc);
             if (ROWQ) tc_fence_after();
-            // S / dP of tile m
-            auto issue_s = [&](int m) -> bool {
-                const int s = m % S::CST, use = m / S::CST;
-                if (!mbar_wait_warp(&bars->c_full[s], use & 1, wc)) return false;
+            // tile m's column operands in shared memory
+            auto wait_cols = [&](int m) -> bool {
+                if (!mbar_wait_warp(&bars->c_full[m % S::CST], (m / S::CST) & 1, wc)) return false;
                 tc_fence_after();
+                return true;
+            };
+            // S / dP of tile m (its column operands waited for)
+            auto issue_s = [&](int m) -> bool {
+                const int s = m % S::CST;
                 const uint64_t dS = dadd(dC1k0, stage_ofs(s)), dP = dadd(dC2k0, stage_ofs(s));
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -373,10 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // test-only stall injection: the issuer stops before this tile, so
             // that the other roles' bounded waits run out
             const int stall = p.fault_kernel == (ROWQ ? 1 : 2) ? p.fault_tile : -1;
-            if (ok && stall != 0) ok = issue_s(0);
+            if (ok && stall != 0) ok = wait_cols(0) && issue_s(0);
             for (int it = 0; it < ntiles && ok; ++it) {
                 if (stall >= 0 && it + 1 >= stall) break;
                 if (it + 1 < ntiles) {
+                    // tile it + 1's columns, normally in place long before:
+                    // their wait is off the chain from the softmax warps'
+                    // read of tile it to the next S / dP
+                    if (!(ok = wait_cols(it + 1))) break;
                     if (!(ok = mbar_wait_warp(&bars->sread, it & 1, wc))) break;
                     if (!(ok = issue_s(it + 1))) break;
                 }

@@ -44,14 +44,14 @@
 namespace df {
 namespace {
 
-constexpr int kThreads = 320;   // producer, issuer, eight softmax warps
+constexpr int kThreads = 352;   // producer, S / dP issuer, eight softmax warps, product issuer
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Tensor-memory columns (512 per CTA).  The fp32 S and dP of the tile being
 // processed sit in [256, 256 + 2 BN).  The 16-bit dZ and P~ that feed the
-// dK / dQ / dV products have their own columns, so the issuer can compute the
-// next tile's S / dP as soon as the softmax warps have read this tile's into
-// registers.
+// dK / dQ / dV products have their own columns, so the S / dP issuer can
+// compute the next tile's S / dP as soon as the softmax warps have read this
+// tile's into registers.
 template <int D>
 struct BwdTmem {
     using G = Geo<D>;
@@ -110,7 +110,7 @@ struct BwdBars {
     uint64_t c_full[3], c_empty[3];        // column-tile ring
     uint64_t bias_full[1], bias_empty[1];  // stored-bias stage of band tiles
     uint64_t s_full, sread, z_full, zread, mma3_done;
-    uint64_t drain;   // the issuer's last MMAs, before the tensor memory is freed
+    uint64_t drain;   // both issuers' last MMAs, before the tensor memory is freed
     uint32_t tmem_base;
     int abort_flag;
     uint32_t stepw[9];
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->z_full, 8);
         mbar_init(&bars->zread, 8);
         mbar_init(&bars->mma3_done, 1);
-        mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain, 2);   // both issuers' last MMAs
         bars->abort_flag = 0;
         fence_barrier_init();
     }
@@ -311,16 +311,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S::BST; ++s)
                 if (b_cnt[s] > 0) mbar_drain(&bars->bias_full[s], (b_cnt[s] - 1) & 1, wc.limit_ns);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Order per tile m:  S / dP of tile m + 1 (once the softmax warps have
-        // read tile m's into registers), then the dK / dV (dQ) products of tile
-        // m (once its 16-bit dZ / P~ are written).  Band tiles take the same
-        // order: their relative-position part comes from the stored bias.
-        // The whole warp walks the issue loop (its control flow warp-uniform);
-        // the MMAs and commits are the elect.sync forms, issued by one lane.
-        // Operand descriptors are built once (per CTA or per ring stage) and
-        // advanced per k-step by a constant.
+    } else if (warp == 1 || warp == 10) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues S / dP of tile m + 1 once the softmax warps have read
+        // tile m's into registers; warp 10 the dK / dV (dQ) products of tile m
+        // once its 16-bit dZ / P~ are written (sread comes before z_full in
+        // every softmax warp, so S / dP of tile m + 1 normally go first; the
+        // two touch different tensor memory and stages either way).  Band
+        // tiles take the same order: their relative-position part comes from
+        // the stored bias.  Each warp walks its issue loop (control flow
+        // warp-uniform); the MMAs and commits are the elect.sync forms, issued
+        // by one lane.  Operand descriptors are built once (per CTA or per ring
+        // stage) and advanced per k-step by a constant.  The product issuer
+        // reads a column stage only after z_full of its tile, which the softmax
+        // warps arrive on after S / dP of that tile -- issued once the stage
+        // had landed -- completed.
         {
             const uint32_t sR1 = smem_u32(smem + S::R1), sR2 = smem_u32(smem + S::R2);
             constexpr uint32_t idS = idesc_f16(128, BN, BF16, false, false);
@@ -331,8 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dC1k0 = desc_k<G>(sC10, BN, 0), dC2k0 = desc_k<G>(sC20, BN, 0);
             const uint64_t dC1m0 = desc_mn<G>(sC10, BN, 0), dC2m0 = desc_mn<G>(sC20, BN, 0);
             auto stage_ofs = [](int s) { return (uint32_t)(s * S::CB); };
-            bool ok = mbar_wait_warp(ROWQ ? &bars->a_full : &bars->row_full, 0, wc);
-            if (ROWQ) tc_fence_after();
+            bool ok = true;
+            if (warp == 1) {   // the A operands of S / dP: tensor memory (dQ) or shared memory rows
+                ok = mbar_wait_warp(ROWQ ? &bars->a_full : &bars->row_full, 0, wc);
+                if (ROWQ) tc_fence_after();
+            }
             // tile m's column operands in shared memory
             auto wait_cols = [&](int m) -> bool {
                 if (!mbar_wait_warp(&bars->c_full[m % S::CST], (m / S::CST) & 1, wc)) return false;
@@ -374,13 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit_w(&bars->mma3_done);
                 return true;
             };
-            // test-only stall injection: the issuer stops before this tile, so
-            // that the other roles' bounded waits run out
-            const int stall = p.fault_kernel == (ROWQ ? 1 : 2) ? p.fault_tile : -1;
-            if (ok && stall != 0) ok = wait_cols(0) && issue_s(0);
-            for (int it = 0; it < ntiles && ok; ++it) {
-                if (stall >= 0 && it + 1 >= stall) break;
-                if (it + 1 < ntiles) {
+            if (warp == 1) {
+                // test-only stall injection: S / dP stop before this tile, so
+                // that the other roles' bounded waits run out
+                const int stall = p.fault_kernel == (ROWQ ? 1 : 2) ? p.fault_tile : -1;
+                if (ok && stall != 0) ok = wait_cols(0) && issue_s(0);
+                for (int it = 0; it + 1 < ntiles && ok; ++it) {
+                    if (stall >= 0 && it + 1 >= stall) break;
                     // tile it + 1's columns, normally in place long before:
                     // their wait is off the chain from the softmax warps'
                     // read of tile it to the next S / dP
@@ -388,13 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait_warp(&bars->sread, it & 1, wc))) break;
                     if (!(ok = issue_s(it + 1))) break;
                 }
-                if (!(ok = issue_acc(it))) break;
+            } else {
+                for (int it = 0; it < ntiles && ok; ++it) ok = issue_acc(it);
             }
-            // every MMA issued above has completed before the tensor memory is freed
+            // every MMA this warp issued has completed (and, through the
+            // barrier's count of 2, the other issuer's) before the tensor
+            // memory is freed
             tc_commit_w(&bars->drain);
             mbar_drain(&bars->drain, 0, wc.limit_ns);
         }
-    } else {
+    } else {   // warps 2 .. 9
         // ------------------------------------------------------------ softmax / gradient warps
         // Eight warps: warp w owns TMEM lanes 32 (w & 3) .. +31 (rows) and
         // column half hf = (w - 2) / 4 of every tile.  Band-window copies and

@@ -341,10 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dK = s ? dK1 : dK0;
                 for (int g = 0; g < 2 * nch; ++g) {
                     const int tb = bc & 1, r = bc % S::NBS;
-                    if (bc >= 2 && !mbar_wait_warp(&bars->tb_empty[tb], ((bc >> 1) - 1) & 1, wc)) return false;
+                    // the chunk's band rows (normally landed long before; their
+                    // copy needs only chunk bc - NBS's product, issued above)
                     if (!mbar_wait_warp(&bars->band_full[r], (bc / S::NBS) & 1, wc)) return false;
                     // K of tile m stays in its stage until the last cross chunk (S(m) has waited for it)
                     if (g == nch && !mbar_wait_warp(&bars->k_full[s], use & 1, wc)) return false;
+                    // then the gate: the softmax warps have copied chunk bc - 2 out of this slot
+                    if (bc >= 2 && !mbar_wait_warp(&bars->tb_empty[tb], ((bc >> 1) - 1) & 1, wc)) return false;
                     tc_fence_after();
                     const bool cross_pass = g >= nch;
                     const uint64_t dA = cross_pass ? dK : dQ;

@@ -107,3 +107,34 @@ def test_fast_host_buffer_step():
     B.step_host(g, *pin, outs, arena, host_cu=hcu, host_qmask=hqm, host_kmask=hkm)
     for name, got, ref in zip(("out", "lse", "dq", "dk", "dv", "dqr", "dkr"), outs, (out, lse) + tuple(grads)):
         assert torch.equal(got, ref.cpu()), name
+
+
+def test_fast_inference_and_noalloc_forward():
+    """The fast mode through the inference forward (no LSE) and through the
+    no-workspace forward gives the training forward's O bit for bit."""
+    w = synth.WORKLOADS["v3_base"]
+    x = synth.make_inputs(w, B=2, L=256, H=2, dtype="fp32")
+    g = geometry(x, w, 2)
+    g.fp32_fast = True
+    t = [a.to("cuda") for a in (x.q, x.k, x.v, x.qr, x.kr)]
+    out, lse, _ = B.attn_fwd(g, *t)
+    out_inf, _ = B.attn_fwd_inference(g, *t)
+    out_na, lse_na = torch.empty_like(out), torch.empty_like(lse)
+    B.attn_fwd_noalloc(g, *t, out_na, lse_na)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_inf)
+    assert torch.equal(out, out_na) and torch.equal(lse, lse_na)
+
+
+def test_fast_rejects_what_the_16_bit_path_rejects():
+    """A bucketing configuration whose index jumps by two is unsupported for
+    the tensor-core path, hence for the fast mode, and fine in strict fp32."""
+    w = synth.WORKLOADS["v3_base"]
+    x = synth.make_inputs(w, B=1, L=128, H=1, dtype="fp32")
+    g = geometry(x, w, 1)
+    g.nb, g.mp = 256, 300
+    g.fp32_fast = True
+    t = [a.to("cuda") for a in (x.q, x.k, x.v, x.qr, x.kr)]
+    with pytest.raises(B.DfError) as e:
+        B.attn_fwd(g, *t, workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+    assert e.value.code == B.DF_ERR_UNSUPPORTED

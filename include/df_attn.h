@@ -158,7 +158,9 @@ size_t df_attn_band_bias_size(const df_attn_params *p);
  * backward, the row terms Dl_i, the diagonal sums of dZ used for the
  * relative-position gradients ([T, H, R] twice, in the input dtype for bf16 /
  * fp16 and fp32 for strict fp32), fp32 partial sums of dQr / dKr and, for
- * bf16 / fp16 when p->band_bias is NULL, the band bias. */
+ * bf16 / fp16 when p->band_bias is NULL, the band bias.  DF_FP32_FAST: the
+ * fp16 workspace followed by fp16 copies of the inputs and outputs (forward:
+ * Q, K, V, Qr, Kr, O; backward also dO, dQ, dK, dV, dQr, dKr). */
 size_t df_attn_workspace_size(const df_attn_params *p, int backward);
 
 /*

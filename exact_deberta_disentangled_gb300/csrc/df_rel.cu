@@ -103,12 +103,19 @@ __global__ void __launch_bounds__(kRelThreads, 1)
         for (int s = 0; s < 2; ++s)
             if (nload[s] > 0) mbar_drain(&bars->full[s], (nload[s] - 1) & 1, wc.limit_ns);
     }
+    const int row = 32 * warp + lane, tok = tok0 + row;
+    // this row's attention part of the output, loaded while the products run
+    float4 accv[D / 4];
+    {
+        const float4* a4 = reinterpret_cast<const float4*>(acc32 + ((size_t)(tok < p.T ? tok : 0) * p.H + h) * D);
+#pragma unroll
+        for (int v = 0; v < D / 4; ++v) accv[v] = a4[v];
+    }
     __syncthreads();
     ok = __all_sync(0xffffffffu, ok);
     if (ok) ok = mbar_wait_warp(&bars->done, 0, wc);
     if (!ok) mbar_drain(&bars->done, 0, wc.limit_ns);   // the MMAs, before the tensor memory is freed
     tc_fence_after();
-    const int row = 32 * warp + lane, tok = tok0 + row;
     using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     if (ok) {
 #pragma unroll
@@ -117,12 +124,11 @@ __global__ void __launch_bounds__(kRelThreads, 1)
             tc_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * c, r);
             tc_wait_ld();
             if (tok < p.T) {
-                const float* a = acc32 + ((size_t)tok * p.H + h) * D + 32 * c;
                 T16* o = reinterpret_cast<T16*>(out_) + ((size_t)tok * p.H + h) * D + 32 * c;
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    const float4 x0 = reinterpret_cast<const float4*>(a)[2 * v];
-                    const float4 x1 = reinterpret_cast<const float4*>(a)[2 * v + 1];
+                    const float4 x0 = accv[8 * c + 2 * v];
+                    const float4 x1 = accv[8 * c + 2 * v + 1];
                     uint4 w;
                     w.x = pack2<BF16>(x0.x + __uint_as_float(r[8 * v + 0]), x0.y + __uint_as_float(r[8 * v + 1]));
                     w.y = pack2<BF16>(x0.z + __uint_as_float(r[8 * v + 2]), x0.w + __uint_as_float(r[8 * v + 3]));
